@@ -1,0 +1,187 @@
+/*
+ * libmoe — the mixture-of-experts FFN layer of a decoding LLM, with expert
+ * weights in the GGUF IQ4_NL format, for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * What the layer computes (per token t with activation x_t of H values):
+ *   1. Router. s_e = W_r[e,:] . x_t for every routed expert e; p_e = sigmoid(s_e).
+ *      The k experts with the largest p_e + b_e are chosen (ties: lower index);
+ *      their combine weights are w_j = p_{e_j} / sum_i p_{e_i}. The bias b only
+ *      selects. (PocketLLM page "Xing4.0-29B-A4B", Overview: a sigmoid-routed
+ *      MoE with a shared expert, 64 experts activated top-4.)
+ *   2. Experts. Each chosen expert and the always-on shared expert run a SwiGLU
+ *      FFN: h = silu(W_g x) * (W_u x), o = W_d h.
+ *   3. Combine. y_t = sum_j w_j o_{e_j}(x_t) + o_shared(x_t). The order of the
+ *      sum is fixed (the page's "deterministic route reduction"): the shared
+ *      expert first, then the routed experts in ascending id. It does not
+ *      depend on the other tokens of the batch, so y_t is bit-identical
+ *      whatever the batch (Red Lite, "What we learned", section 4: two requests
+ *      in one pass give the answers of serving them in turn).
+ *
+ * IQ4_NL (GGML type 20; the Xing4.0 page's Overview table: "4.5 bits a weight,
+ * 32 weights in 18 bytes"): a block is a little-endian fp16 scale d followed by
+ * 16 bytes; the low nibble of byte j indexes weight j, the high nibble weight
+ * j+16; weight = d * T[nibble] with the format's table
+ * T = {-127,-104,-83,-65,-49,-35,-22,-10,1,13,25,38,53,69,89,113}.
+ * A matrix with R rows and K inputs is R*K/32 consecutive blocks, row-major,
+ * blocks along K (rows = output features), as GGUF stores it. Expert e of a
+ * stacked tensor starts at block e*R*K/32.
+ *
+ * Conventions for every call below
+ *  - Pointers are DEVICE pointers unless the comment says "host".
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream). They allocate nothing, free nothing and never synchronise.
+ *  - Arguments are checked on the host before any launch. A bad argument
+ *    returns a negative moe_status and launches nothing ("refuse, don't
+ *    ignore": the Xing4.0 page's option table refuses unsupported flags).
+ *  - Kernels are launched with programmatic dependent launch: each kernel
+ *    starts streaming constant weights while the previous kernel on the stream
+ *    finishes, and waits for it before it reads any activation, route or
+ *    workspace data. Work enqueued before a call must therefore not trigger
+ *    programmatic completion (griddepcontrol.launch_dependents) before its
+ *    outputs are written. moe_set_pdl(0) turns this off.
+ *  - Nothing on the device traps. Device-side conditions are reported in the
+ *    optional `status` word (device uint32, accumulated with atomicOr/atomicAdd,
+ *    never cleared by libmoe): bits 0..15 count invalid routes (saturating),
+ *    bit 31 (MOE_STATUS_TIMEOUT) means a bounded on-chip wait gave up.
+ */
+#ifndef LIBMOE_MOE_H
+#define LIBMOE_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,   /* NULL pointer, size out of range, shape rule broken */
+  MOE_ERR_UNSUPPORTED = -2,   /* valid for the format but not built here (see limits) */
+  MOE_ERR_WORKSPACE = -3,     /* workspace NULL or smaller than moe_workspace_bytes() */
+  MOE_ERR_MISALIGNED = -4,    /* a pointer breaks the alignment rule of its argument */
+  MOE_ERR_CUDA = -5           /* a CUDA runtime call or launch failed */
+} moe_status;
+
+#define MOE_STATUS_INVALID_ROUTE_MASK 0x0000FFFFu
+#define MOE_STATUS_TIMEOUT 0x80000000u
+
+/* Limits of this build. */
+#define MOE_MAX_EXPERTS 1024
+#define MOE_MAX_TOP_K 16
+#define MOE_MAX_DECODE_TOKENS 16
+#define MOE_MAX_HIDDEN 8192
+#define MOE_MAX_FFN 8192
+
+/* Sizes of one MoE layer. hidden, ffn and ffn_shared are multiples of 64
+ * (IQ4_NL needs 32; the kernels pair blocks) and at most 8192.
+ * 1 <= n_experts <= 1024; 1 <= top_k <= min(n_experts, 16); n_shared is 0 or 1
+ * (ffn_shared is ignored when n_shared == 0). */
+typedef struct {
+  int32_t hidden;      /* H */
+  int32_t ffn;         /* F, width of each routed expert */
+  int32_t ffn_shared;  /* Fs, width of the shared expert */
+  int32_t n_experts;   /* E, routed experts */
+  int32_t top_k;       /* k */
+  int32_t n_shared;    /* 0 or 1 */
+} moe_shape;
+
+/* Expert weights of one layer, IQ4_NL, device memory, each pointer 16-byte
+ * aligned (GGUF aligns tensor data to 32 bytes). Read only; libmoe streams
+ * them while earlier work on the stream finishes, so they must not be written
+ * by work still in flight when a call is enqueued.
+ *   gate, up : [E][F][H/32] blocks     down : [E][H][F/32] blocks
+ *   sh_gate, sh_up : [Fs][H/32]        sh_down : [H][Fs/32]  (NULL when n_shared == 0) */
+typedef struct {
+  const void* gate;
+  const void* up;
+  const void* down;
+  const void* sh_gate;
+  const void* sh_up;
+  const void* sh_down;
+} moe_expert_weights;
+
+/* Router: scores, sigmoid, bias, top-k, renormalised weights.
+ *   router_w : bf16 [E][H] (uint16 bit patterns), 16-byte aligned
+ *   router_bias : fp32 [E] selection bias, or NULL for none
+ *   x        : bf16 [T][H], 16-byte aligned
+ *   T        : 0 <= T <= 1 << 20 (T == 0 launches nothing)
+ *   ids      : out int32 [T][k], per token in descending p+b (ties: lower index)
+ *   weights  : out fp32 [T][k], p_j / sum of the chosen p, same order
+ * Scores accumulate in fp32 and the choice is made in fp32. No workspace. */
+moe_status moe_route_topk(const moe_shape* shape, const uint16_t* router_w,
+                          const float* router_bias, const uint16_t* x, int32_t T,
+                          int32_t* ids, float* weights, void* stream);
+
+/* Bytes of workspace that moe_iq4nl_decode (mode 0) or
+ * moe_iq4nl_prefill_grouped (mode 1) needs for up to max_tokens tokens.
+ * Returns 0 for an invalid shape, mode or max_tokens. The workspace is
+ * caller-owned device memory, 256-byte aligned, and MUST be zero-filled once
+ * after allocation (cudaMemset); every call leaves its counter words at zero
+ * again. One workspace serves any number of layers of the same shape run one
+ * after another on one stream (the wpnews vLLM article's workspace sharing
+ * keyed on shape). Calls that may overlap (other streams) need their own. */
+size_t moe_workspace_bytes(const moe_shape* shape, int32_t max_tokens, int32_t mode);
+
+/* Decode: the whole layer (experts + combine) for 1..16 tokens.
+ *   x        : bf16 [T][H], 16-byte aligned
+ *   ids      : int32 [T][k]; an id outside [0, E) is an invalid route: it is
+ *              treated as expert 0 with weight 0 (wpnews vLLM article, route
+ *              sanitising), i.e. it contributes nothing, and is counted in *status
+ *   weights  : fp32 [T][k]
+ *   y        : out fp32 [T][H], 16-byte aligned
+ *   ws       : workspace of moe_workspace_bytes(shape, >= T, 0) bytes
+ *   status   : device uint32 or NULL
+ * Each distinct expert's weights are read once per call, whatever the number
+ * of tokens routed to it; each IQ4_NL block is decoded once and used for every
+ * such token. Arithmetic: fp32 accumulation of exact integer block dot
+ * products; activations and h enter them as 16-bit integers with one power-of-
+ * two scale per 32 values. */
+moe_status moe_iq4nl_decode(const moe_shape* shape, const moe_expert_weights* w,
+                            const uint16_t* x, int32_t T, const int32_t* ids,
+                            const float* weights, float* y, void* ws, size_t ws_bytes,
+                            uint32_t* status, void* stream);
+
+/* Prefill: the whole layer for a chunk of 1..max_tokens tokens. Tokens are
+ * bucketed by expert with a counting sort (no atomics decide any order), each
+ * expert's tokens run as one grouped tensor-core contraction (tcgen05,
+ * fp16 operands, fp32 accumulation) on weights dequantised on the fly, and a
+ * gather-combine forms y in the fixed order above. Dequantised weights are
+ * round-to-nearest-even fp16 of d*T[q]; x and h also enter as fp16.
+ * Arguments as for moe_iq4nl_decode; ws from moe_workspace_bytes(shape, >= T, 1). */
+moe_status moe_iq4nl_prefill_grouped(const moe_shape* shape, const moe_expert_weights* w,
+                                     const uint16_t* x, int32_t T, const int32_t* ids,
+                                     const float* weights, float* y, void* ws,
+                                     size_t ws_bytes, uint32_t* status, void* stream);
+
+/* Dequantise n_blocks consecutive IQ4_NL blocks (the block layout above).
+ *   blocks : device, 2-byte aligned
+ *   out    : out_fp16 == 0: fp32 [n_blocks*32], the exact product d*T[q]
+ *            out_fp16 == 1: fp16 [n_blocks*32], round-to-nearest-even of d*T[q]
+ *            4-byte aligned */
+moe_status moe_iq4nl_dequantize(const void* blocks, int64_t n_blocks, int32_t out_fp16,
+                                void* out, void* stream);
+
+/* The invalid-route rule on its own (wpnews vLLM article, route sanitising):
+ * ids_out[i] = ids[i] if 0 <= ids[i] < n_experts else 0; weights_out[i] =
+ * weights[i] if the id is valid else 0. Invalid routes are counted in *status.
+ * In-place use (ids_out == ids, weights_out == weights) is allowed. */
+moe_status moe_sanitize_routes(const int32_t* ids, const float* weights, int64_t n,
+                               int32_t n_experts, int32_t* ids_out, float* weights_out,
+                               uint32_t* status, void* stream);
+
+/* 1 (default) launches kernels with programmatic dependent launch; 0 does not.
+ * Host-side, process-wide. Returns the previous setting. */
+int32_t moe_set_pdl(int32_t enable);
+
+/* A static description of a status code (host). */
+const char* moe_status_string(int32_t status);
+
+/* Library version, e.g. "libmoe 0.1 sm_103a" (host, static string). */
+const char* moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBMOE_MOE_H */

@@ -1,0 +1,224 @@
+"""Python binding of libmoe: the IQ4_NL routed-expert MoE layer on one GB300.
+
+Argument marshalling only. Every step of the layer runs in libmoe's CUDA
+kernels (``csrc/``), reached through the C ABI of ``include/moe.h``; PyTorch
+provides device memory and streams. There is no CPU fallback: importing this
+package fails if ``_build/libmoe.so`` has not been built, and every call
+raises ``MoeError`` on a non-zero status.
+
+Functions keep the C names without the ``moe_`` prefix: ``route_topk``,
+``workspace_bytes``, ``iq4nl_decode``, ``iq4nl_prefill_grouped``,
+``iq4nl_dequantize``, ``sanitize_routes``, ``set_pdl``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libmoe.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"libmoe is not built ({LIB_PATH} missing); run "
+        "`python -c 'import __graft_entry__ as g; g.build()'` or "
+        "`python quantized_routed_expert_gb300/build.py`")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = -1
+MOE_ERR_UNSUPPORTED = -2
+MOE_ERR_WORKSPACE = -3
+MOE_ERR_MISALIGNED = -4
+MOE_ERR_CUDA = -5
+STATUS_INVALID_ROUTE_MASK = 0x0000FFFF
+STATUS_TIMEOUT = 0x80000000
+MAX_DECODE_TOKENS = 16
+DECODE, PREFILL = 0, 1
+
+
+class Shape(ctypes.Structure):
+    """moe_shape: hidden, ffn, ffn_shared, n_experts, top_k, n_shared."""
+    _fields_ = [("hidden", ctypes.c_int32), ("ffn", ctypes.c_int32),
+                ("ffn_shared", ctypes.c_int32), ("n_experts", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("n_shared", ctypes.c_int32)]
+
+
+class _Weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("gate", "up", "down", "sh_gate", "sh_up", "sh_down")]
+
+
+_P = ctypes.c_void_p
+_lib.moe_route_topk.argtypes = [ctypes.POINTER(Shape), _P, _P, _P, ctypes.c_int32, _P, _P, _P]
+_lib.moe_route_topk.restype = ctypes.c_int
+_lib.moe_workspace_bytes.argtypes = [ctypes.POINTER(Shape), ctypes.c_int32, ctypes.c_int32]
+_lib.moe_workspace_bytes.restype = ctypes.c_size_t
+for _fn in (_lib.moe_iq4nl_decode, _lib.moe_iq4nl_prefill_grouped):
+    _fn.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(_Weights), _P, ctypes.c_int32, _P, _P,
+                    _P, _P, ctypes.c_size_t, _P, _P]
+    _fn.restype = ctypes.c_int
+_lib.moe_iq4nl_dequantize.argtypes = [_P, ctypes.c_int64, ctypes.c_int32, _P, _P]
+_lib.moe_iq4nl_dequantize.restype = ctypes.c_int
+_lib.moe_sanitize_routes.argtypes = [_P, _P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P, _P]
+_lib.moe_sanitize_routes.restype = ctypes.c_int
+_lib.moe_set_pdl.argtypes = [ctypes.c_int32]
+_lib.moe_set_pdl.restype = ctypes.c_int32
+_lib.moe_status_string.argtypes = [ctypes.c_int32]
+_lib.moe_status_string.restype = ctypes.c_char_p
+_lib.moe_version.restype = ctypes.c_char_p
+
+EXPORTS = ("moe_route_topk", "moe_workspace_bytes", "moe_iq4nl_decode",
+           "moe_iq4nl_prefill_grouped", "moe_iq4nl_dequantize", "moe_sanitize_routes",
+           "moe_set_pdl", "moe_status_string", "moe_version")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {_lib.moe_status_string(status).decode()} ({status})")
+
+
+def _check(status: int, what: str):
+    if status != MOE_OK:
+        raise MoeError(status, what)
+
+
+def version() -> str:
+    return _lib.moe_version().decode()
+
+
+def status_string(status: int) -> str:
+    return _lib.moe_status_string(int(status)).decode()
+
+
+def set_pdl(enable: bool) -> bool:
+    return bool(_lib.moe_set_pdl(1 if enable else 0))
+
+
+def make_shape(hidden, ffn, n_experts, top_k, ffn_shared=None, n_shared=1) -> Shape:
+    return Shape(int(hidden), int(ffn), int(ffn if ffn_shared is None else ffn_shared),
+                 int(n_experts), int(top_k), int(n_shared))
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dev(t, dtype, name):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+class ExpertWeights:
+    """Device tensors (uint8, IQ4_NL blocks) of one layer; keeps them alive."""
+
+    def __init__(self, gate, up, down, sh_gate=None, sh_up=None, sh_down=None):
+        self.tensors = (gate, up, down, sh_gate, sh_up, sh_down)
+        self.c = _Weights(*[_ptr(t) for t in self.tensors])
+
+
+def workspace_bytes(shape: Shape, max_tokens: int, mode: int = DECODE) -> int:
+    return int(_lib.moe_workspace_bytes(ctypes.byref(shape), int(max_tokens), int(mode)))
+
+
+def workspace(shape: Shape, max_tokens: int, mode: int = DECODE, device="cuda"):
+    """A zero-filled workspace (uint8) of the size libmoe asks for."""
+    n = workspace_bytes(shape, max_tokens, mode)
+    if n == 0:
+        raise MoeError(MOE_ERR_INVALID_ARG, "workspace_bytes")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def route_topk(shape: Shape, router_w, router_bias, x, ids=None, weights=None, stream=None):
+    """router_w: bf16 [E,H]; router_bias: fp32 [E] or None; x: bf16 [T,H].
+    Returns (ids int32 [T,k], weights fp32 [T,k])."""
+    _dev(router_w, torch.bfloat16, "router_w")
+    _dev(x, torch.bfloat16, "x")
+    if router_bias is not None:
+        _dev(router_bias, torch.float32, "router_bias")
+    T = x.shape[0]
+    if ids is None:
+        ids = torch.empty((T, shape.top_k), dtype=torch.int32, device=x.device)
+    if weights is None:
+        weights = torch.empty((T, shape.top_k), dtype=torch.float32, device=x.device)
+    _check(_lib.moe_route_topk(ctypes.byref(shape), _ptr(router_w), _ptr(router_bias), _ptr(x),
+                               int(T), _ptr(ids), _ptr(weights), _stream(stream)),
+           "moe_route_topk")
+    return ids, weights
+
+
+def _layer(fn, name, shape, w: ExpertWeights, x, ids, weights, y, ws, status, stream):
+    _dev(x, torch.bfloat16, "x")
+    _dev(ids, torch.int32, "ids")
+    _dev(weights, torch.float32, "weights")
+    T = x.shape[0]
+    if y is None:
+        y = torch.empty((T, shape.hidden), dtype=torch.float32, device=x.device)
+    _dev(y, torch.float32, "y")
+    _check(fn(ctypes.byref(shape), ctypes.byref(w.c), _ptr(x), int(T), _ptr(ids),
+              _ptr(weights), _ptr(y), _ptr(ws), int(ws.numel() if ws is not None else 0),
+              _ptr(status), _stream(stream)), name)
+    return y
+
+
+def iq4nl_decode(shape: Shape, w: ExpertWeights, x, ids, weights, ws, y=None, status=None,
+                 stream=None):
+    """Decode 1..16 tokens: y fp32 [T,H]."""
+    return _layer(_lib.moe_iq4nl_decode, "moe_iq4nl_decode", shape, w, x, ids, weights, y, ws,
+                  status, stream)
+
+
+def iq4nl_prefill_grouped(shape: Shape, w: ExpertWeights, x, ids, weights, ws, y=None,
+                          status=None, stream=None):
+    """Prefill a chunk of tokens: y fp32 [T,H]."""
+    return _layer(_lib.moe_iq4nl_prefill_grouped, "moe_iq4nl_prefill_grouped", shape, w, x, ids,
+                  weights, y, ws, status, stream)
+
+
+def iq4nl_dequantize(blocks, fp16: bool = False, out=None, stream=None):
+    """blocks: uint8 device tensor of 18-byte blocks -> fp32 (exact) or fp16 [n*32]."""
+    _dev(blocks, torch.uint8, "blocks")
+    if blocks.numel() % 18:
+        raise ValueError("blocks must hold a whole number of 18-byte blocks")
+    n = blocks.numel() // 18
+    if out is None:
+        out = torch.empty(n * 32, dtype=torch.float16 if fp16 else torch.float32,
+                          device=blocks.device)
+    _check(_lib.moe_iq4nl_dequantize(_ptr(blocks), n, 1 if fp16 else 0, _ptr(out),
+                                     _stream(stream)), "moe_iq4nl_dequantize")
+    return out
+
+
+def sanitize_routes(ids, weights, n_experts: int, ids_out=None, weights_out=None, status=None,
+                    stream=None):
+    _dev(ids, torch.int32, "ids")
+    _dev(weights, torch.float32, "weights")
+    ids_out = torch.empty_like(ids) if ids_out is None else ids_out
+    weights_out = torch.empty_like(weights) if weights_out is None else weights_out
+    _check(_lib.moe_sanitize_routes(_ptr(ids), _ptr(weights), ids.numel(), int(n_experts),
+                                    _ptr(ids_out), _ptr(weights_out), _ptr(status),
+                                    _stream(stream)), "moe_sanitize_routes")
+    return ids_out, weights_out

@@ -1,0 +1,182 @@
+// Device helpers shared by the libmoe kernels (sm_103a).
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "moe.h"
+
+namespace moe {
+
+constexpr int kBlockW = 32;       // weights per IQ4_NL block
+constexpr int kBlockB = 18;       // bytes per IQ4_NL block
+constexpr int kPairB = 36;        // bytes per pair of consecutive blocks
+constexpr int kThreads = 288;     // 8 consumer warps + 1 producer warp
+constexpr int kConsumers = 256;
+constexpr int kProducerWarp = 8;
+
+// ---------------------------------------------------------------------------
+// The IQ4_NL table as packed int8 (bytes T[0..3], T[4..7], T[8..11], T[12..15]).
+// T = {-127,-104,-83,-65,-49,-35,-22,-10,1,13,25,38,53,69,89,113}.
+constexpr uint32_t kTab0 = 0xBFAD9881u;
+constexpr uint32_t kTab1 = 0xF6EADDCFu;
+constexpr uint32_t kTab2 = 0x26190D01u;
+constexpr uint32_t kTab3 = 0x71594535u;
+
+// Eight 4-bit codes (one 32-bit word of a block's index bytes) to eight int8
+// table values. Bytes of r0: T[c0], T[c1], T[c2], T[c3]; r1: T[c4..c7], where c
+// are the nibbles from least significant up. Each byte_perm picks from one half
+// of the table; a third byte_perm keeps, per byte, the half that bit 3 names.
+__device__ __forceinline__ void iq4_lookup8(uint32_t q, uint32_t& r0, uint32_t& r1) {
+  const uint32_t sel = 0x32103210u | ((q & 0x88888888u) >> 1);
+  const uint32_t lo0 = __byte_perm(kTab0, kTab1, q);
+  const uint32_t hi0 = __byte_perm(kTab2, kTab3, q);
+  r0 = __byte_perm(lo0, hi0, sel);
+  const uint32_t q1 = q >> 16;
+  const uint32_t lo1 = __byte_perm(kTab0, kTab1, q1);
+  const uint32_t hi1 = __byte_perm(kTab2, kTab3, q1);
+  r1 = __byte_perm(lo1, hi1, sel >> 16);
+}
+
+// Exact integer dot product of one block's 32 table values (8 words from
+// iq4_lookup8 over the 4 index words) with a 32-vector in "pair" layout:
+// word j holds (v_j, v_{j+16}) as two int16. Byte order of the looked-up words
+// is (c_j, c_{j+16}, c_{j+1}, c_{j+17}), which dp2a.lo/.hi consume in place.
+__device__ __forceinline__ int iq4_dot_block(const uint32_t (&t)[8], const uint32_t* v) {
+  int acc = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc = __dp2a_lo((int)v[4 * i + 0], (int)t[2 * i], acc);
+    acc = __dp2a_hi((int)v[4 * i + 1], (int)t[2 * i], acc);
+    acc = __dp2a_lo((int)v[4 * i + 2], (int)t[2 * i + 1], acc);
+    acc = __dp2a_hi((int)v[4 * i + 3], (int)t[2 * i + 1], acc);
+  }
+  return acc;
+}
+
+// Decode one block pair (36 bytes, 4-byte aligned, as 9 words) into two fp16
+// scales and the 8 index words of each block.
+__device__ __forceinline__ void split_pair(const uint32_t (&w)[9], float& d0, float& d1,
+                                           uint32_t (&q0)[4], uint32_t (&q1)[4]) {
+  d0 = __half2float(__ushort_as_half((unsigned short)(w[0] & 0xFFFFu)));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) q0[i] = __byte_perm(w[i], w[i + 1], 0x5432);
+  d1 = __half2float(__ushort_as_half((unsigned short)(w[4] >> 16)));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) q1[i] = w[5 + i];
+}
+
+__device__ __forceinline__ void load_pair_smem(const uint8_t* p, uint32_t (&w)[9]) {
+  const uint32_t* p32 = reinterpret_cast<const uint32_t*>(p);
+#pragma unroll
+  for (int i = 0; i < 9; ++i) w[i] = p32[i];
+}
+
+// ---------------------------------------------------------------------------
+// 16-bit block quantisation of an activation vector (x or h).
+// For 32 values with largest biased fp32 exponent e: M_i = rint(v_i 2^(141-e))
+// clamped to 32767 (so |M_i| <= 2^15 - 1), scale = 2^(e-141). Blocks whose
+// largest exponent is <= 14 (|v| < 2^-112) are zero; an inf/NaN gives a NaN
+// scale so that it propagates to the output.
+__device__ __forceinline__ float quant_factor(uint32_t emax) {
+  return __uint_as_float((268u - emax) << 23);
+}
+__device__ __forceinline__ float quant_scale(uint32_t emax) {
+  if (emax <= 14u) return 0.0f;
+  if (emax >= 255u) return __uint_as_float(0x7FC00000u);
+  return __uint_as_float((emax - 14u) << 23);
+}
+__device__ __forceinline__ int quant_one(float v, uint32_t emax) {
+  if (emax <= 14u || emax >= 255u) return 0;
+  int m = __float2int_rn(v * quant_factor(emax));
+  return m > 32767 ? 32767 : m;
+}
+
+// ---------------------------------------------------------------------------
+// PTX wrappers: mbarrier, 1D bulk copy (TMA), programmatic dependent launch.
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait: gives up after ~kWaitLimitNs, records MOE_STATUS_TIMEOUT and
+// returns false. Nothing in libmoe waits without a limit.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (status) atomicOr(status, MOE_STATUS_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Global -> shared bulk copy that completes `bytes` of transaction on `bar`.
+// src and dst 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Named barrier among the 256 consumer threads (id 1); id 2 adds the producer warp.
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+}
+__device__ __forceinline__ void all_sync_named() {
+  asm volatile("bar.sync 2, 288;" ::: "memory");
+}
+
+// Host: raise a kernel's dynamic shared memory limit once per (kernel, device),
+// so that launches made during stream capture issue nothing but the launch.
+cudaError_t ensure_smem_attr(const void* kernel, size_t bytes);
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return g / (1.0f + expf(-g)) * u;
+}
+
+}  // namespace moe

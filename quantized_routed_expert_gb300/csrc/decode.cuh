@@ -1,0 +1,86 @@
+// Decode path of libmoe: parameters, workspace layout and launch helpers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "moe.h"
+
+namespace moe {
+
+constexpr int kMaxPairs = MOE_MAX_DECODE_TOKENS * MOE_MAX_TOP_K;  // T*k
+constexpr int kChunkRows = 8;     // f-rows (gate + up) per gate/up stage
+constexpr int kPairsPerStage = 4; // h vectors per down stage
+
+inline int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+
+// Bytes of one IQ4_NL row with K inputs.
+inline int64_t row_bytes(int64_t K) { return K / 32 * 18; }
+// Rows per alignment granule: the smallest g with g*row_bytes(K) % 16 == 0.
+inline int row_granule(int64_t K) {
+  const int64_t rb = row_bytes(K);
+  int g = 1;
+  while ((g * rb) % 16) g *= 2;
+  return g;
+}
+// Lanes per row in the down kernel (and the h layout): one lane per block pair.
+inline int lanes_per_row(int64_t K) { return K / 64 >= 32 ? 32 : (int)(K / 64); }
+// Words of one quantised vector record (int16 pairs + fp32 scales), 16-byte padded.
+inline int64_t qvec_words(int64_t K) {
+  const int64_t lpr = lanes_per_row(K);
+  const int64_t groups = (K / 64 + lpr - 1) / lpr;
+  return groups * lpr * 32 + align_up(K / 32, 4);
+}
+
+struct DecodeLayout {
+  int64_t h_r, h_s, rec_r, rec_s, cnt, total;  // byte offsets
+};
+
+inline DecodeLayout decode_layout(const moe_shape& s, int64_t T) {
+  DecodeLayout L{};
+  int64_t off = 0;
+  auto take = [&](int64_t bytes) {
+    const int64_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  const int64_t Fs = s.n_shared ? s.ffn_shared : 0;
+  L.h_r = take(T * s.top_k * s.ffn * 4);
+  L.h_s = take(T * Fs * 4);
+  L.rec_r = take(T * s.top_k * qvec_words(s.ffn) * 4);
+  L.rec_s = take(Fs ? T * qvec_words(Fs) * 4 : 0);
+  const int64_t fmax = s.ffn > Fs ? s.ffn : Fs;
+  L.cnt = take((int64_t)(s.n_experts + 1) * (fmax / 32) * 4);
+  L.total = off;
+  return L;
+}
+
+struct DecodeParams {
+  int H, F, Fs, E, k, n_shared, T;
+  const uint8_t* gate;
+  const uint8_t* up;
+  const uint8_t* down;
+  const uint8_t* sh_gate;
+  const uint8_t* sh_up;
+  const uint8_t* sh_down;
+  const uint16_t* x;
+  const int32_t* ids;
+  const float* weights;
+  float* y;
+  float* h_r;        // [T*k][F]
+  float* h_s;        // [T][Fs]
+  uint32_t* rec_r;   // [T*k][qvec_words(F)]
+  uint32_t* rec_s;   // [T][qvec_words(Fs)]
+  uint32_t* cnt;     // [(E+1)][max(F,Fs)/32]
+  uint32_t* status;
+  // launch-derived
+  int gu_stages;     // gate/up ring depth
+  int dn_stages;     // down ring depth
+  int dn_rows_max;   // max output rows per down CTA
+};
+
+size_t gateup_smem_bytes(const DecodeParams& p, int stages);
+size_t down_smem_bytes(const DecodeParams& p, int stages);
+cudaError_t launch_decode(const DecodeParams& p, int num_sms, bool pdl, cudaStream_t stream);
+
+}  // namespace moe

@@ -1,0 +1,222 @@
+"""Parity of the CUDA router, dequantiser and decode path with the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _gpu import (DEV, check_close, check_route, gapped_rows, lib, moe_shape, oracle_layer,
+                  run_decode, weights_of)
+from _util import golden_kv
+
+pytestmark = pytest.mark.gpu
+
+_layers = {}
+
+
+def layer_of(cfg_or_shape, layer=0, seed=None):
+    from synth.layers import Layer
+    s = synth.SHAPES[cfg_or_shape] if isinstance(cfg_or_shape, int) else cfg_or_shape
+    seed = synth.seed_of(cfg_or_shape) if seed is None else seed
+    key = (s.name, s.H, s.F, s.E, s.k, s.n_shared, seed, layer)
+    if key not in _layers:
+        if len(_layers) > 6:
+            _layers.clear()
+            torch.cuda.empty_cache()
+        _layers[key] = Layer(s, seed, layer, device=DEV)
+    return _layers[key]
+
+
+# ---------------------------------------------------------------- inputs, dequant
+
+def test_device_generator_matches_host():
+    from synth import device as sdev
+    for (layer, tensor, e, nb) in [(0, synth.GATE, 0, 300), (3, synth.DOWN, 7, 1000),
+                                   (17, synth.SH_UP, 0, 64)]:
+        t = torch.empty((e + 1) * nb * 18, dtype=torch.uint8, device=DEV)
+        sdev.fill_iq4nl(t, e + 1, nb, 1235, layer, tensor)
+        got = t.view(e + 1, nb, 18)[e].cpu().numpy()
+        ref = synth.iq4nl_blocks(1235, layer, tensor, e, nb)
+        assert np.array_equal(got, ref)
+
+
+def _edge_blocks():
+    rng = np.random.default_rng(5)
+    blocks = synth.iq4nl_blocks(77, 0, synth.GATE, 0, 512)
+    edge = [0x0001, 0x03FF, 0x0400, 0x7BFF, 0x8000, 0x0000, 0xFBFF, 0x8001, 0x3C00, 0xBC00,
+            0x7C00, 0xFC00]
+    extra = np.zeros((len(edge), 18), np.uint8)
+    for i, d in enumerate(edge):
+        extra[i, 0] = d & 0xFF
+        extra[i, 1] = d >> 8
+        extra[i, 2:] = rng.integers(0, 256, 16, dtype=np.uint8)
+    return np.concatenate([blocks, extra])
+
+
+def test_dequant_fp32_bit_exact():
+    moe = lib()
+    b = _edge_blocks()
+    out = moe.iq4nl_dequantize(torch.from_numpy(b.reshape(-1)).to(DEV)).cpu().numpy()
+    ref = oracle.dequant(b, oracle.EXACT).astype(np.float32)      # exact in fp32
+    assert np.array_equal(out.view(np.uint32), ref.view(np.uint32))
+
+
+def test_dequant_fp16_bit_exact():
+    moe = lib()
+    b = _edge_blocks()
+    out = moe.iq4nl_dequantize(torch.from_numpy(b.reshape(-1)).to(DEV), fp16=True)
+    out = out.cpu().numpy()
+    ref = oracle.dequant(b, oracle.MMA16).astype(np.float16)      # already fp16 values
+    assert np.array_equal(out.view(np.uint16), ref.view(np.uint16))
+
+
+def test_sanitize_worked_example():
+    moe = lib()
+    g = golden_kv("route_sanitizer.txt")
+    ids = torch.tensor([int(v) for v in g["ids_in"]], dtype=torch.int32, device=DEV)
+    w = torch.tensor([float(v) for v in g["w_in"]], dtype=torch.float32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    io, wo = moe.sanitize_routes(ids, w, int(g["n_experts"][0]), status=status)
+    assert io.cpu().tolist() == [int(v) for v in g["ids_out"]]
+    assert wo.cpu().tolist() == [float(v) for v in g["w_out"]]
+    assert int(status.item()) == 2
+
+
+# ---------------------------------------------------------------- router
+
+@pytest.mark.parametrize("cfg,T", [(0, 4), (1, 1), (2, 2), (3, 1), (3, 16)])
+def test_route_parity(cfg, T):
+    moe = lib()
+    from synth.layers import bf16_tensor
+    L = layer_of(cfg)
+    x_host = gapped_rows(L, T)
+    ids, w = moe.route_topk(moe_shape(L.shape), L.router_w, L.bias, bf16_tensor(x_host, DEV))
+    torch.cuda.synchronize()
+    check_route(ids.cpu().numpy(), w.cpu().numpy(), L, x_host)
+
+
+def test_route_token_tiles_ragged():
+    # a prefill-sized chunk with a ragged last tile, on the Xing router shape
+    moe = lib()
+    from synth.layers import bf16_tensor
+    L = layer_of(4)
+    x_host = gapped_rows(L, 83)
+    ids, w = moe.route_topk(moe_shape(L.shape), L.router_w, L.bias, bf16_tensor(x_host, DEV))
+    torch.cuda.synchronize()
+    check_route(ids.cpu().numpy(), w.cpu().numpy(), L, x_host)
+
+
+# ---------------------------------------------------------------- decode
+
+@pytest.mark.parametrize("cfg,T,layer", [(0, 4, 0), (0, 1, 0), (1, 1, 0), (1, 1, 37), (2, 2, 0),
+                                         (2, 2, 47), (3, 1, 0), (3, 4, 1), (3, 16, 3)])
+def test_decode_parity(cfg, T, layer):
+    L = layer_of(cfg, layer)
+    x_host = gapped_rows(L, T)
+    ids, w, y = run_decode(L, x_host)
+    check_route(ids, w, L, x_host)
+    ref = oracle_layer(L, x_host, ids, w)
+    check_close(y, ref, f"decode cfg{cfg} T{T} layer{layer}")
+
+
+def test_decode_batch_invariance_and_determinism():
+    L = layer_of(3, 1)
+    x_host = gapped_rows(L, 4)
+    ids, w, y = run_decode(L, x_host)
+    _, _, y2 = run_decode(L, x_host, ids, w)
+    assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
+    for t in range(4):
+        _, _, yt = run_decode(L, x_host[t:t + 1], ids[t:t + 1], w[t:t + 1])
+        assert np.array_equal(yt[0].view(np.uint32), y[t].view(np.uint32)), t
+
+
+def test_decode_paired_tokens_share_experts():
+    # the same token twice (a guess equal to the token): union of experts = k
+    L = layer_of(2, 5)
+    x1 = gapped_rows(L, 1)
+    x_host = np.concatenate([x1, x1])
+    ids, w, y = run_decode(L, x_host)
+    assert np.array_equal(ids[0], ids[1])
+    assert np.array_equal(y[0].view(np.uint32), y[1].view(np.uint32))
+    check_close(y, oracle_layer(L, x_host, ids, w), "paired identical tokens")
+
+
+def test_decode_invalid_and_duplicate_routes():
+    L = layer_of(0)
+    s = L.shape
+    x_host = gapped_rows(L, 4)
+    ids, w, _ = run_decode(L, x_host)
+    bad = ids.copy()
+    bad[0, 1] = -1
+    bad[2, 0] = s.E + 5
+    bad[3, 1] = bad[3, 0]               # duplicate expert in one token
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    _, _, y = run_decode(L, x_host, bad, w, status=status)
+    assert int(status.item()) & 0xFFFF == 2
+    ref = oracle_layer(L, x_host, bad, w)
+    check_close(y, ref, "invalid/duplicate routes")
+
+
+def test_workspace_reused_across_layers():
+    moe = lib()
+    s = synth.SHAPES[0]
+    L0, L1 = layer_of(0, 0), layer_of(0, 1)
+    x0, x1 = gapped_rows(L0, 4), gapped_rows(L1, 4)
+    ws = moe.workspace(moe_shape(s), 4, moe.DECODE, DEV)
+    ids0, w0, ya = run_decode(L0, x0, ws=ws)
+    ids1, w1, yb = run_decode(L1, x1, ws=ws)
+    _, _, ya2 = run_decode(L0, x0, ids0, w0)
+    _, _, yb2 = run_decode(L1, x1, ids1, w1)
+    assert np.array_equal(ya.view(np.uint32), ya2.view(np.uint32))
+    assert np.array_equal(yb.view(np.uint32), yb2.view(np.uint32))
+
+
+@pytest.mark.parametrize("H,F,E,k,T,ns", [
+    (64, 64, 1, 1, 1, 0),          # one expert, no shared: a dense SwiGLU
+    (64, 64, 1024, 16, 16, 1),     # largest E, k, T: 256 routed pairs
+    (128, 192, 5, 3, 7, 1),        # ragged: 3 block pairs per F row, odd T
+    (256, 128, 8, 2, 16, 1),       # tiny down rows (72 B, 8-byte multiples)
+    (8192, 64, 4, 2, 2, 1),        # widest hidden
+])
+def test_decode_edge_shapes(H, F, E, k, T, ns):
+    s = synth.Shape("edge", H, F, E, k, T, 1, n_shared=ns)
+    L = layer_of(s, 0, seed=99)
+    rng = np.random.default_rng(H + F + E)
+    x_host = synth.to_bf16_bits(rng.standard_normal((T, H)))
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    w = rng.random((T, k)).astype(np.float32)
+    _, _, y = run_decode(L, x_host, ids, w)
+    ref = oracle_layer(L, x_host, ids, w.astype(np.float64))
+    check_close(y, ref, f"edge H{H} F{F} E{E} k{k} T{T}")
+
+
+def test_decode_argument_errors():
+    moe = lib()
+    from synth.layers import bf16_tensor
+    L = layer_of(0)
+    s = L.shape
+    shape = moe_shape(s)
+    x = bf16_tensor(gapped_rows(L, 4), DEV)
+    ids, w = moe.route_topk(shape, L.router_w, L.bias, x)
+    ws = moe.workspace(shape, 4, moe.DECODE, DEV)
+    wts = weights_of(L)
+    with pytest.raises(moe.MoeError) as e:       # workspace too small
+        moe.iq4nl_decode(shape, wts, x, ids, w, ws[:1024])
+    assert e.value.status == moe.MOE_ERR_WORKSPACE
+    with pytest.raises(moe.MoeError) as e:       # misaligned activations
+        xb = torch.empty(4 * s.H + 1, dtype=torch.bfloat16, device=DEV)[1:].view(4, s.H)
+        moe.iq4nl_decode(shape, wts, xb, ids, w, ws)
+    assert e.value.status == moe.MOE_ERR_MISALIGNED
+    big = torch.zeros((17, s.H), dtype=torch.bfloat16, device=DEV)
+    ids17 = torch.zeros((17, s.k), dtype=torch.int32, device=DEV)
+    w17 = torch.zeros((17, s.k), dtype=torch.float32, device=DEV)
+    with pytest.raises(moe.MoeError) as e:       # more than 16 decode tokens
+        moe.iq4nl_decode(shape, wts, big, ids17, w17, ws)
+    assert e.value.status == moe.MOE_ERR_INVALID_ARG
+    bad_shape = moe.make_shape(s.H, s.F, s.E, s.E + 1)
+    with pytest.raises(moe.MoeError) as e:
+        moe.iq4nl_decode(bad_shape, wts, x, ids, w, ws)
+    assert e.value.status == moe.MOE_ERR_INVALID_ARG
+    empty = torch.zeros((0, s.H), dtype=torch.bfloat16, device=DEV)
+    y0 = moe.iq4nl_decode(shape, wts, empty, ids[:0], w[:0], ws)   # T == 0: nothing to do
+    assert y0.shape == (0, s.H)
