@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--impl", default="libmoe", choices=["libmoe", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="run only the first N layers (small profiling cases)")
     return ap.parse_args()
 
 
@@ -62,9 +64,14 @@ def peaks():
         return FALLBACK_HBM_GBS, 1900.0, "fallback"
 
 
-def workload(cfg: int, tokens):
+def workload(cfg: int, tokens, layers=None):
+    import copy
     import synth
     s = synth.SHAPES[cfg]
+    if layers is not None and layers < s.L:
+        s = copy.copy(s)
+        s.L = int(layers)
+        s.name = f"{s.name} (first {s.L} layers)"
     T = s.T if tokens is None else int(tokens)
     if cfg != 4 and T > 16:
         T = 16
@@ -209,7 +216,7 @@ def run_libmoe(args):
     import synth
     from synth.layers import Layer, x_sets
 
-    s, T = workload(args.config, args.tokens)
+    s, T = workload(args.config, args.tokens, args.layers)
     seed = synth.seed_of(args.config)
     prefill = args.config == 4
     shape = moe.make_shape(s.H, s.F, s.E, s.k, s.Fs, s.n_shared)
@@ -227,8 +234,18 @@ def run_libmoe(args):
 
     def step(xin):
         for l in range(s.L):
-            moe.route_topk(shape, layers[l].router_w, layers[l].bias, xin[l], ids[l], w[l])
-            layer_fn(shape, wts[l], xin[l], ids[l], w[l], ws, y=y[l], status=status)
+            if prefill:
+                moe.route_topk(shape, layers[l].router_w, layers[l].bias, xin[l], ids[l], w[l])
+                layer_fn(shape, wts[l], xin[l], ids[l], w[l], ws, y=y[l], status=status)
+            else:
+                moe.iq4nl_decode_routed(shape, layers[l].router_w, layers[l].bias, wts[l], xin[l],
+                                        ws, ids=ids[l], weights=w[l], y=y[l], status=status)
+
+    if prefill:
+        launches_per_layer = (moe.launches_per_call(shape, T, moe.CALL_ROUTE) +
+                              moe.launches_per_call(shape, T, moe.CALL_PREFILL))
+    else:
+        launches_per_layer = moe.launches_per_call(shape, T, moe.CALL_DECODE_ROUTED)
 
     # capture one graph per input set
     stream = torch.cuda.Stream(device=dev)
@@ -293,15 +310,21 @@ def run_libmoe(args):
     ms = float(t_max.item())
     st = int(status.item())
 
-    # ---- per-call durations (same buffers, same stream, back-to-back launches)
-    def time_calls(fn, reps=3):
+    # ---- per-call durations: one graph per kind of call over all layers (the
+    # routes of input set 0 in place), replayed on the same stream
+    def graph_ms(fn, reps=5):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for l in range(s.L):
+                fn(l)
+        torch.cuda.synchronize()
+        g.replay()
         torch.cuda.synchronize()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(cur)
-        for r in range(reps):
-            for l in range(s.L):
-                fn(l, r)
+        for _ in range(reps):
+            g.replay()
         b.record(cur)
         torch.cuda.synchronize()
         return a.elapsed_time(b) / (reps * s.L)
@@ -309,10 +332,10 @@ def run_libmoe(args):
     xin0 = xs[0]
     graphs[0].replay()
     torch.cuda.synchronize()
-    layer_ms = time_calls(lambda l, r: layer_fn(shape, wts[l], xin0[l], ids[l], w[l], ws,
-                                                y=y[l], status=status))
-    route_ms = time_calls(lambda l, r: moe.route_topk(shape, layers[l].router_w,
-                                                      layers[l].bias, xin0[l], ids[l], w[l]))
+    layer_ms = graph_ms(lambda l: layer_fn(shape, wts[l], xin0[l], ids[l], w[l], ws, y=y[l],
+                                           status=status))
+    route_ms = graph_ms(lambda l: moe.route_topk(shape, layers[l].router_w, layers[l].bias,
+                                                 xin0[l], ids[l], w[l]))
     layer_bytes = (bytes_set[0] - s.L * router_bytes) / s.L
 
     hbm, bf16, peak_kind = peaks()
@@ -374,13 +397,16 @@ def run_libmoe(args):
             "bytes_per_step": bytes_per_step,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "traffic": traffic,
-                         "kernel": "moe_iq4nl_decode (gate/up + down kernels), per layer call"
+                         "kernel": "moe_iq4nl_decode (the layer without routing), per call"
                                    if not prefill else "moe_iq4nl_prefill_grouped",
                          "peak_kind": peak_kind, "avg_call_ms": layer_ms,
                          "algorithmic_bytes_per_call": layer_bytes},
             "route_call_ms": route_ms,
+            "step_call": "moe_iq4nl_prefill_grouped after moe_route_topk" if prefill else
+                         "moe_iq4nl_decode_routed (route + layer in one call)",
+            "launches_per_layer": launches_per_layer,
             "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
-            "gpu_launches": args.steps * s.L * 3,
+            "gpu_launches": args.steps * s.L * launches_per_layer,
             "status_word": st,
         }
         print(json.dumps(line), flush=True)

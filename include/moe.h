@@ -142,6 +142,21 @@ moe_status moe_iq4nl_decode(const moe_shape* shape, const moe_expert_weights* w,
                             const float* weights, float* y, void* ws, size_t ws_bytes,
                             uint32_t* status, void* stream);
 
+/* Route + decode in one call: what moe_route_topk followed by moe_iq4nl_decode
+ * computes, for 1..16 tokens, with the same outputs (ids, weights, y) and the
+ * same arithmetic. For 1..4 tokens and hidden, ffn, ffn_shared multiples of 256
+ * it is a single persistent launch: the router runs inside the layer kernel
+ * (each CTA scores a slice of the experts, a grid-wide barrier, then every CTA
+ * takes the top-k itself), which removes one kernel boundary per layer from the
+ * critical path. The ids written here are always valid.
+ *   router_w, router_bias, x: as for moe_route_topk;  w, y, ws, status: as for
+ *   moe_iq4nl_decode;  ids, weights: out [T][k], as moe_route_topk writes them. */
+moe_status moe_iq4nl_decode_routed(const moe_shape* shape, const uint16_t* router_w,
+                                   const float* router_bias, const moe_expert_weights* w,
+                                   const uint16_t* x, int32_t T, int32_t* ids, float* weights,
+                                   float* y, void* ws, size_t ws_bytes, uint32_t* status,
+                                   void* stream);
+
 /* Prefill: the whole layer for a chunk of 1..max_tokens tokens. Tokens are
  * bucketed by expert with a counting sort (no atomics decide any order), each
  * expert's tokens run as one grouped tensor-core contraction (tcgen05,
@@ -169,6 +184,12 @@ moe_status moe_iq4nl_dequantize(const void* blocks, int64_t n_blocks, int32_t ou
 moe_status moe_sanitize_routes(const int32_t* ids, const float* weights, int64_t n,
                                int32_t n_experts, int32_t* ids_out, float* weights_out,
                                uint32_t* status, void* stream);
+
+/* Kernel launches one call makes for this shape and token count (host, no
+ * device work): call 0 = moe_route_topk, 1 = moe_iq4nl_decode,
+ * 2 = moe_iq4nl_decode_routed, 3 = moe_iq4nl_prefill_grouped. Returns a
+ * negative moe_status for bad arguments. */
+int32_t moe_launches_per_call(const moe_shape* shape, int32_t T, int32_t call);
 
 /* 1 (default) launches kernels with programmatic dependent launch; 0 does not.
  * Host-side, process-wide. Returns the previous setting. */

@@ -61,19 +61,25 @@ for _fn in (_lib.moe_iq4nl_decode, _lib.moe_iq4nl_prefill_grouped):
     _fn.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(_Weights), _P, ctypes.c_int32, _P, _P,
                     _P, _P, ctypes.c_size_t, _P, _P]
     _fn.restype = ctypes.c_int
+_lib.moe_iq4nl_decode_routed.argtypes = [ctypes.POINTER(Shape), _P, _P, ctypes.POINTER(_Weights),
+                                         _P, ctypes.c_int32, _P, _P, _P, _P, ctypes.c_size_t, _P,
+                                         _P]
+_lib.moe_iq4nl_decode_routed.restype = ctypes.c_int
 _lib.moe_iq4nl_dequantize.argtypes = [_P, ctypes.c_int64, ctypes.c_int32, _P, _P]
 _lib.moe_iq4nl_dequantize.restype = ctypes.c_int
 _lib.moe_sanitize_routes.argtypes = [_P, _P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P, _P]
 _lib.moe_sanitize_routes.restype = ctypes.c_int
+_lib.moe_launches_per_call.argtypes = [ctypes.POINTER(Shape), ctypes.c_int32, ctypes.c_int32]
+_lib.moe_launches_per_call.restype = ctypes.c_int32
 _lib.moe_set_pdl.argtypes = [ctypes.c_int32]
 _lib.moe_set_pdl.restype = ctypes.c_int32
 _lib.moe_status_string.argtypes = [ctypes.c_int32]
 _lib.moe_status_string.restype = ctypes.c_char_p
 _lib.moe_version.restype = ctypes.c_char_p
 
-EXPORTS = ("moe_route_topk", "moe_workspace_bytes", "moe_iq4nl_decode",
+EXPORTS = ("moe_route_topk", "moe_workspace_bytes", "moe_iq4nl_decode", "moe_iq4nl_decode_routed",
            "moe_iq4nl_prefill_grouped", "moe_iq4nl_dequantize", "moe_sanitize_routes",
-           "moe_set_pdl", "moe_status_string", "moe_version")
+           "moe_launches_per_call", "moe_set_pdl", "moe_status_string", "moe_version")
 
 
 class MoeError(RuntimeError):
@@ -93,6 +99,17 @@ def version() -> str:
 
 def status_string(status: int) -> str:
     return _lib.moe_status_string(int(status)).decode()
+
+
+CALL_ROUTE, CALL_DECODE, CALL_DECODE_ROUTED, CALL_PREFILL = 0, 1, 2, 3
+
+
+def launches_per_call(shape: Shape, T: int, call: int) -> int:
+    """Kernel launches one call makes (host query)."""
+    n = int(_lib.moe_launches_per_call(ctypes.byref(shape), int(T), int(call)))
+    if n < 0:
+        raise MoeError(n, "moe_launches_per_call")
+    return n
 
 
 def set_pdl(enable: bool) -> bool:
@@ -189,6 +206,31 @@ def iq4nl_decode(shape: Shape, w: ExpertWeights, x, ids, weights, ws, y=None, st
     """Decode 1..16 tokens: y fp32 [T,H]."""
     return _layer(_lib.moe_iq4nl_decode, "moe_iq4nl_decode", shape, w, x, ids, weights, y, ws,
                   status, stream)
+
+
+def iq4nl_decode_routed(shape: Shape, router_w, router_bias, w: ExpertWeights, x, ws, ids=None,
+                        weights=None, y=None, status=None, stream=None):
+    """Route and decode 1..16 tokens in one call. Returns (ids, weights, y)."""
+    _dev(router_w, torch.bfloat16, "router_w")
+    if router_bias is not None:
+        _dev(router_bias, torch.float32, "router_bias")
+    _dev(x, torch.bfloat16, "x")
+    T = x.shape[0]
+    if ids is None:
+        ids = torch.empty((T, shape.top_k), dtype=torch.int32, device=x.device)
+    if weights is None:
+        weights = torch.empty((T, shape.top_k), dtype=torch.float32, device=x.device)
+    if y is None:
+        y = torch.empty((T, shape.hidden), dtype=torch.float32, device=x.device)
+    _dev(ids, torch.int32, "ids")
+    _dev(weights, torch.float32, "weights")
+    _dev(y, torch.float32, "y")
+    _check(_lib.moe_iq4nl_decode_routed(ctypes.byref(shape), _ptr(router_w), _ptr(router_bias),
+                                        ctypes.byref(w.c), _ptr(x), int(T), _ptr(ids),
+                                        _ptr(weights), _ptr(y), _ptr(ws),
+                                        int(ws.numel() if ws is not None else 0), _ptr(status),
+                                        _stream(stream)), "moe_iq4nl_decode_routed")
+    return ids, weights, y
 
 
 def iq4nl_prefill_grouped(shape: Shape, w: ExpertWeights, x, ids, weights, ws, y=None,

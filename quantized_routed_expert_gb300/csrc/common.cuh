@@ -45,15 +45,15 @@ __device__ __forceinline__ void iq4_lookup8(uint32_t q, uint32_t& r0, uint32_t& 
 // word j holds (v_j, v_{j+16}) as two int16. Byte order of the looked-up words
 // is (c_j, c_{j+16}, c_{j+1}, c_{j+17}), which dp2a.lo/.hi consume in place.
 __device__ __forceinline__ int iq4_dot_block(const uint32_t (&t)[8], const uint32_t* v) {
-  int acc = 0;
+  int a0 = 0, a1 = 0;                  // two chains: half the dependent dp2a depth
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    acc = __dp2a_lo((int)v[4 * i + 0], (int)t[2 * i], acc);
-    acc = __dp2a_hi((int)v[4 * i + 1], (int)t[2 * i], acc);
-    acc = __dp2a_lo((int)v[4 * i + 2], (int)t[2 * i + 1], acc);
-    acc = __dp2a_hi((int)v[4 * i + 3], (int)t[2 * i + 1], acc);
+    a0 = __dp2a_lo((int)v[4 * i + 0], (int)t[2 * i], a0);
+    a1 = __dp2a_hi((int)v[4 * i + 1], (int)t[2 * i], a1);
+    a0 = __dp2a_lo((int)v[4 * i + 2], (int)t[2 * i + 1], a0);
+    a1 = __dp2a_hi((int)v[4 * i + 3], (int)t[2 * i + 1], a1);
   }
-  return acc;
+  return a0 + a1;
 }
 
 // Decode one block pair (36 bytes, 4-byte aligned, as 9 words) into two fp16
@@ -114,14 +114,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                "r"(bytes)
                : "memory");
 }
+// The suspend-time hint lets the hardware park the waiting thread until the
+// phase completes (or the hint's time passes) instead of returning at once,
+// so waiting warps do not spin and take issue slots from computing warps.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n .reg .pred p;\n"
-      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u)
       : "memory");
   return ok != 0;
 }
@@ -138,8 +141,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (;;) {
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if (global_timer_ns() - t0 > kWaitLimitNs) {
       if (status) atomicOr(status, MOE_STATUS_TIMEOUT);
       return false;

@@ -11,168 +11,10 @@
 
 #include "common.cuh"
 #include "decode.cuh"
+#include "decode_common.cuh"
+#include "route.cuh"
 
 namespace moe {
-
-// ---------------------------------------------------------------------------
-// Route table built in shared memory from ids (route sanitising: an id outside
-// [0, E) is dropped, i.e. routed to expert 0 with weight 0).
-struct RouteTable {
-  int n_slots;                 // distinct routed experts, ascending
-  int n_valid;
-  int invalid;
-  uint32_t bitmap[MOE_MAX_EXPERTS / 32];
-  int word_off[MOE_MAX_EXPERTS / 32];
-  int sid[kMaxPairs];          // sanitised expert id per pair, -1 if invalid
-  float wt[kMaxPairs];         // weight per pair
-  int slot_expert[kMaxPairs];
-  int slot_off[kMaxPairs + 1]; // CSR offsets into list
-  int list[kMaxPairs];         // pair indices grouped by slot, ascending within a slot
-};
-
-__device__ __forceinline__ int slot_of_expert(const RouteTable& rt, int e) {
-  const uint32_t w = rt.bitmap[e >> 5];
-  return rt.word_off[e >> 5] + __popc(w & ((1u << (e & 31)) - 1u));
-}
-
-// Called by the 256 consumer threads. P = T*k <= 256.
-__device__ void build_route_table(RouteTable& rt, const int32_t* __restrict__ ids,
-                                  const float* __restrict__ wts, int P, int E) {
-  const int tid = threadIdx.x;
-  if (tid < MOE_MAX_EXPERTS / 32) rt.bitmap[tid] = 0u;
-  if (tid == 0) rt.invalid = 0;
-  consumers_sync();
-  for (int i = tid; i < P; i += kConsumers) {
-    const int id = ids[i];
-    const bool ok = id >= 0 && id < E;
-    rt.sid[i] = ok ? id : -1;
-    rt.wt[i] = ok ? wts[i] : 0.0f;
-    if (ok) atomicOr(&rt.bitmap[id >> 5], 1u << (id & 31));
-    else atomicAdd(&rt.invalid, 1);
-  }
-  consumers_sync();
-  if (tid < 32) {
-    const int nw = (E + 31) >> 5;
-    const int c = tid < nw ? __popc(rt.bitmap[tid]) : 0;
-    int incl = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (tid >= o) incl += v;
-    }
-    const int excl = incl - c;
-    if (tid < nw) {
-      rt.word_off[tid] = excl;
-      uint32_t bits = rt.bitmap[tid];
-      int pos = excl;
-      while (bits) {
-        const int b = __ffs(bits) - 1;
-        bits &= bits - 1u;
-        rt.slot_expert[pos++] = tid * 32 + b;
-      }
-    }
-    if (tid == 31) rt.n_slots = incl;
-  }
-  consumers_sync();
-  // stable counting sort of the valid pairs by expert: rank = #smaller experts
-  // + #earlier pairs of the same expert
-  for (int p = tid; p < P; p += kConsumers) {
-    const int e = rt.sid[p];
-    if (e < 0) continue;
-    int rank = 0;
-    bool first = true;
-    for (int q = 0; q < P; ++q) {
-      const int eq = rt.sid[q];
-      if (eq < 0) continue;
-      rank += (eq < e) || (eq == e && q < p);
-      first = first && !(eq == e && q < p);
-    }
-    rt.list[rank] = p;
-    if (first) rt.slot_off[slot_of_expert(rt, e)] = rank;
-  }
-  if (tid == 0) {
-    rt.n_valid = P - rt.invalid;
-    rt.slot_off[rt.n_slots] = rt.n_valid;
-  }
-  consumers_sync();
-}
-
-__host__ __device__ __forceinline__ size_t align_up_dev(size_t v, size_t a) {
-  return (v + a - 1) / a * a;
-}
-__host__ __device__ __forceinline__ int row_granule_dev(int K) {
-  const int rb = K / 32 * kBlockB;
-  int g = 1;
-  while ((g * rb) % 16) g *= 2;
-  return g;
-}
-
-// ---------------------------------------------------------------------------
-// Quantised vector layout: the int16 pair words of block pair q, 16-byte chunk
-// c (0..7), live at uint4 index ((q / lpr) * 8 + c) * lpr + q % lpr, so that
-// lanes reading consecutive pairs read consecutive 16-byte chunks. Scales
-// (one fp32 per 32 values) follow the pair words.
-__device__ __forceinline__ int qv_u4(int q, int c, int lpr) {
-  return ((q / lpr) * 8 + c) * lpr + (q % lpr);
-}
-__host__ __device__ __forceinline__ int dlanes_per_row(int K) { return K / 64 >= 32 ? 32 : K / 64; }
-__host__ __device__ __forceinline__ int dqvec_pair_words(int K) {
-  const int lpr = dlanes_per_row(K);
-  return (K / 64 + lpr - 1) / lpr * lpr * 32;
-}
-__host__ __device__ __forceinline__ int dqvec_words(int K) {
-  return dqvec_pair_words(K) + ((K / 32 + 3) & ~3);
-}
-
-// Quantise 32 consecutive values (one per lane) of block b of a K-vector into
-// the record `rec` (shared or global). All 32 lanes participate.
-__device__ __forceinline__ void quant_block_store(float v, int b, int K, uint32_t* rec) {
-  const int lane = threadIdx.x & 31;
-  const uint32_t e = (__float_as_uint(v) >> 23) & 0xFFu;
-  const uint32_t emax = __reduce_max_sync(0xFFFFFFFFu, e);
-  const int m = quant_one(v, emax);
-  const int hi = __shfl_down_sync(0xFFFFFFFFu, m, 16);
-  const int lpr = dlanes_per_row(K);
-  if (lane < 16) {
-    const int q = b >> 1;
-    const int w = 16 * (b & 1) + lane;          // word within the pair
-    const uint32_t word = (uint32_t)(m & 0xFFFF) | ((uint32_t)hi << 16);
-    rec[qv_u4(q, w >> 2, lpr) * 4 + (w & 3)] = word;
-  }
-  if (lane == 0) reinterpret_cast<float*>(rec + dqvec_pair_words(K))[b] = quant_scale(emax);
-}
-
-// ---------------------------------------------------------------------------
-// Gate/up work: shared-expert rows are split evenly over the CTAs (known before
-// the routes are), routed rows (slots x F, slot-major) likewise after.
-struct Chunk {
-  int slot;   // -1 = shared expert, else routed slot index
-  int f0;
-  int rows;
-};
-
-struct RowRange {
-  int a, b;   // [a, b) in flattened rows
-};
-
-__device__ __forceinline__ RowRange split_rows(int total, int g, int cta, int ncta) {
-  const int units = total / g;
-  const long long ua = (long long)units * cta / ncta;
-  const long long ub = (long long)units * (cta + 1) / ncta;
-  return RowRange{(int)ua * g, (int)ub * g};
-}
-
-// The next chunk of [row, end) of a slot-major space with rows_per_slot rows.
-__device__ __forceinline__ Chunk next_chunk(int row, int end, int rows_per_slot, bool shared) {
-  Chunk c;
-  const int s = row / rows_per_slot;
-  c.slot = shared ? -1 : s;
-  c.f0 = row - s * rows_per_slot;
-  int n = rows_per_slot - c.f0;
-  if (end - row < n) n = end - row;
-  c.rows = n < kChunkRows ? n : kChunkRows;
-  return c;
-}
 
 template <int MAXT>
 __device__ __forceinline__ void gateup_rows(const DecodeParams& p, const RouteTable& rt,
@@ -208,6 +50,7 @@ __device__ __forceinline__ void gateup_rows(const DecodeParams& p, const RouteTa
     for (int j = 0; j < MAXT; ++j) ag[j] = au[j] = 0.0f;
 
     for (int q = lane; q < npairs; q += 32) {
+      const int qbase = qv_base(q, lpr);
       uint32_t w[9];
       float dg0, dg1, du0, du1;
       uint32_t a0[4], a1[4];
@@ -230,11 +73,11 @@ __device__ __forceinline__ void gateup_rows(const DecodeParams& p, const RouteTa
       for (int j = 0; j < MAXT; ++j) {
         if (j < ng) {
           const uint32_t* rec = xq + (size_t)tok[j] * xq_words;
-          const uint4* r4 = reinterpret_cast<const uint4*>(rec);
+          const uint4* r4 = reinterpret_cast<const uint4*>(rec) + qbase;
           uint32_t v[32];
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            const uint4 u = r4[qv_u4(q, c, lpr)];
+            const uint4 u = r4[c * lpr];
             v[4 * c] = u.x; v[4 * c + 1] = u.y; v[4 * c + 2] = u.z; v[4 * c + 3] = u.w;
           }
           const float* xs = reinterpret_cast<const float*>(rec + xs_off);
@@ -268,39 +111,7 @@ __device__ __forceinline__ void gateup_rows(const DecodeParams& p, const RouteTa
     }
   }
 
-  // Arrival on this F-block; the 32nd arrival quantises the block for every
-  // token of the slot and resets the counter. Every lane fences its own h
-  // stores before lane 0 arrives.
-  __threadfence();
-  __syncwarp();
-  const int cid = shared ? p.E : rt.slot_expert[ch.slot];
-  const int fmax = p.F > p.Fs ? p.F : p.Fs;
-  uint32_t* cnt = p.cnt + (size_t)cid * (fmax / 32) + f / 32;
-  uint32_t old = 0;
-  if (lane == 0) old = atomicAdd(cnt, 1u);
-  old = __shfl_sync(0xFFFFFFFFu, old, 0);
-  if (old == 31u) {
-    __threadfence();
-    const int b = f / 32;
-    const int words = dqvec_words(F);
-    for (int j = 0; j < ntok; ++j) {
-      const float* hp;
-      uint32_t* rec;
-      if (shared) {
-        hp = p.h_s + (size_t)j * p.Fs;
-        rec = p.rec_s + (size_t)j * words;
-      } else {
-        const int pr = rt.list[lbase + j];
-        hp = p.h_r + (size_t)pr * p.F;
-        rec = p.rec_r + (size_t)pr * words;
-      }
-      const float v = __ldcg(hp + b * 32 + lane);
-      quant_block_store(v, b, F, rec);
-    }
-    if (lane == 0) *cnt = 0u;
-  }
 }
-
 
 // ---------------------------------------------------------------------------
 // Shared-memory layouts (host and device agree on them).
@@ -409,19 +220,13 @@ __global__ void __launch_bounds__(kThreads, 2) gateup_kernel(const DecodeParams 
 
   // Consumers. Quantise x first: the inputs of this call are complete (the
   // router that precedes this kernel read them after its own dependency wait).
-  {
-    const int nb = H / 32;
-    for (int i = warp; i < p.T * nb; i += kConsumers / 32) {
-      const int t = i / nb, b = i - t * nb;
-      const float v = __bfloat162float(
-          __ushort_as_bfloat16(p.x[(size_t)t * H + b * 32 + lane]));
-      quant_block_store(v, b, H, xq + (size_t)t * xq_words);
-    }
-  }
+  quant_x_to_smem(p.x, p.T, H, xq, xq_words, warp, kConsumers / 32);
   consumers_sync();
 
   int it = 0;
   bool ok = true;
+  Pending pd;
+  pd.n = 0;
   auto consume = [&](const Chunk& c) {
     const int s = it % NST;
     const uint32_t par = (it / NST) & 1;
@@ -430,6 +235,11 @@ __global__ void __launch_bounds__(kThreads, 2) gateup_kernel(const DecodeParams 
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
     ++it;
+    if (warp < c.rows) {
+      pd.slot[pd.n] = c.slot;
+      pd.f[pd.n] = c.f0 + warp;
+      if (++pd.n == kPendMax) flush_arrivals(p, rt, pd);
+    }
     return true;
   };
   for (int r = shr.a; ok && r < shr.b;) {
@@ -439,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 2) gateup_kernel(const DecodeParams 
   }
   pdl_wait();
   pdl_trigger();
-  build_route_table(rt, p.ids, p.weights, p.T * p.k, p.E);
+  build_route_table<kConsumers, 1>(rt, p.ids, p.weights, p.T * p.k, p.E);
   if (blockIdx.x == 0 && threadIdx.x == 0 && p.status && rt.invalid)
     atomicAdd(p.status, (uint32_t)(rt.invalid < 0xFFFF ? rt.invalid : 0xFFFF));
   all_sync_named();
@@ -449,6 +259,7 @@ __global__ void __launch_bounds__(kThreads, 2) gateup_kernel(const DecodeParams 
     ok = consume(c);
     r += c.rows;
   }
+  if (pd.n) flush_arrivals(p, rt, pd);
 }
 
 // ---------------------------------------------------------------------------
@@ -571,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 2) down_kernel(const DecodeParams p)
   }
 
   // Consumers.
-  build_route_table(rt, p.ids, p.weights, p.T * p.k, p.E);
+  build_route_table<kConsumers, 1>(rt, p.ids, p.weights, p.T * p.k, p.E);
   for (int i = threadIdx.x; i < nrows * p.T; i += kConsumers) yacc[i] = 0.0f;
   consumers_sync();
   all_sync_named();
@@ -618,6 +429,7 @@ __global__ void __launch_bounds__(kThreads, 2) down_kernel(const DecodeParams p)
       if (active) {
         const uint8_t* row = wst + (size_t)r * rbK;
         for (int q = q0; q < npq; q += lpr) {
+          const int qbase = qv_base(q, lpr);
           uint32_t w[9];
           float d0, d1;
           uint32_t a0[4], a1[4];
@@ -633,11 +445,11 @@ __global__ void __launch_bounds__(kThreads, 2) down_kernel(const DecodeParams p)
           for (int j = 0; j < NPS; ++j) {
             if (j < np) {
               const uint32_t* rec = recs + (size_t)j * words;
-              const uint4* r4 = reinterpret_cast<const uint4*>(rec);
+              const uint4* r4 = reinterpret_cast<const uint4*>(rec) + qbase;
               uint32_t v[32];
 #pragma unroll
               for (int c = 0; c < 8; ++c) {
-                const uint4 u = r4[qv_u4(q, c, lpr)];
+                const uint4 u = r4[c * lpr];
                 v[4 * c] = u.x; v[4 * c + 1] = u.y; v[4 * c + 2] = u.z; v[4 * c + 3] = u.w;
               }
               const float* sc = reinterpret_cast<const float*>(rec + pw);
@@ -709,6 +521,16 @@ int pick_stages(size_t fixed, size_t stage, int lo, int hi) {
 
 cudaError_t launch_decode(const DecodeParams& p0, int num_sms, bool pdl, cudaStream_t stream) {
   DecodeParams p = p0;
+  p.route = 0;
+  {
+    size_t fsm = 0;
+    int rg = 0, rmax = 0;
+    if (fused_decode_supported(p, num_sms, &fsm, &rg, &rmax)) {
+      p.fz_rg = rg;
+      p.dn_rows_max = rmax;
+      return launch_decode_fused(p, num_sms, fsm, pdl, stream);
+    }
+  }
   // gate/up
   const GuSmem g1 = gu_smem(p.H, p.T, 1);
   p.gu_stages = pick_stages(g1.ring, g1.stage, 2, 6);
@@ -734,6 +556,28 @@ cudaError_t launch_decode(const DecodeParams& p0, int num_sms, bool pdl, cudaStr
   else e = launch(gateup_kernel<16>, num_sms, gsm, pdl, stream, p);
   if (e != cudaSuccess) return e;
   return launch(down_kernel<kPairsPerStage>, grid_dn, dsm, pdl, stream, p);
+}
+
+// Route + layer in one call: one fused launch when the shape allows, else the
+// router kernel followed by the decode kernels.
+cudaError_t launch_decode_routed(const DecodeParams& p0, int num_sms, bool pdl,
+                                 cudaStream_t stream) {
+  DecodeParams p = p0;
+  p.route = 1;
+  size_t fsm = 0;
+  int rg = 0, rmax = 0;
+  if (fused_decode_supported(p, num_sms, &fsm, &rg, &rmax)) {
+    p.fz_rg = rg;
+    p.dn_rows_max = rmax;
+    return launch_decode_fused(p, num_sms, fsm, pdl, stream);
+  }
+  RouteParams rp{p.H, p.E, p.k, p.T, p.Wr, p.bias, p.x, p.ids_out, p.w_out};
+  cudaError_t e = launch_route(rp, pdl, stream);
+  if (e != cudaSuccess) return e;
+  p.route = 0;
+  p.ids = p.ids_out;
+  p.weights = p.w_out;
+  return launch_decode(p, num_sms, pdl, stream);
 }
 
 }  // namespace moe

@@ -23,8 +23,13 @@ inline int row_granule(int64_t K) {
   while ((g * rb) % 16) g *= 2;
   return g;
 }
-// Lanes per row in the down kernel (and the h layout): one lane per block pair.
-inline int lanes_per_row(int64_t K) { return K / 64 >= 32 ? 32 : (int)(K / 64); }
+// Lanes per row in the down kernels (and the quantised vector layout): a power
+// of two, at most 8 and at most the number of block pairs of the row.
+inline int lanes_per_row(int64_t K) {
+  int l = 8;
+  while (l > K / 64) l >>= 1;
+  return l;
+}
 // Words of one quantised vector record (int16 pairs + fp32 scales), 16-byte padded.
 inline int64_t qvec_words(int64_t K) {
   const int64_t lpr = lanes_per_row(K);
@@ -33,7 +38,7 @@ inline int64_t qvec_words(int64_t K) {
 }
 
 struct DecodeLayout {
-  int64_t h_r, h_s, rec_r, rec_s, cnt, total;  // byte offsets
+  int64_t h_r, h_s, rec_r, rec_s, cnt, sync, scores, total;  // byte offsets
 };
 
 inline DecodeLayout decode_layout(const moe_shape& s, int64_t T) {
@@ -51,6 +56,8 @@ inline DecodeLayout decode_layout(const moe_shape& s, int64_t T) {
   L.rec_s = take(Fs ? T * qvec_words(Fs) * 4 : 0);
   const int64_t fmax = s.ffn > Fs ? s.ffn : Fs;
   L.cnt = take((int64_t)(s.n_experts + 1) * (fmax / 32) * 4);
+  L.sync = take(64);                       // grid-barrier counters of the fused kernel
+  L.scores = take(T * s.n_experts * 4);    // router scores of the routed fused kernel
   L.total = off;
   return L;
 }
@@ -72,15 +79,30 @@ struct DecodeParams {
   uint32_t* rec_r;   // [T*k][qvec_words(F)]
   uint32_t* rec_s;   // [T][qvec_words(Fs)]
   uint32_t* cnt;     // [(E+1)][max(F,Fs)/32]
+  uint32_t* sync;    // [4]: h arrivals, departures, score arrivals (fused kernel)
   uint32_t* status;
+  // routing inside the fused kernel (route != 0)
+  int route;
+  const uint16_t* Wr;    // bf16 [E][H]
+  const float* bias;     // [E] or NULL
+  int32_t* ids_out;      // [T][k]
+  float* w_out;          // [T][k]
+  float* scores;         // workspace [T][E]
   // launch-derived
   int gu_stages;     // gate/up ring depth
   int dn_stages;     // down ring depth
   int dn_rows_max;   // max output rows per down CTA
+  int fz_rg;         // fused kernel: output rows per down unit
 };
 
 size_t gateup_smem_bytes(const DecodeParams& p, int stages);
 size_t down_smem_bytes(const DecodeParams& p, int stages);
 cudaError_t launch_decode(const DecodeParams& p, int num_sms, bool pdl, cudaStream_t stream);
+bool fused_decode_supported(const DecodeParams& p, int num_sms, size_t* smem, int* rg,
+                            int* rows_max);
+cudaError_t launch_decode_routed(const DecodeParams& p, int num_sms, bool pdl,
+                                 cudaStream_t stream);
+cudaError_t launch_decode_fused(const DecodeParams& p, int num_sms, size_t smem, bool pdl,
+                                cudaStream_t stream);
 
 }  // namespace moe

@@ -1,0 +1,645 @@
+// Fused decode kernel of libmoe (sm_103a): gate/up + SwiGLU, a grid barrier,
+// then down + combine, in one persistent launch (one CTA per SM).
+//
+// Every warp streams its own work units: it issues 1D bulk copies (TMA) of
+// the IQ4_NL rows of its next units into two private shared-memory slots and
+// computes each unit as it lands, with no barrier between warps. Units:
+//   gate/up: one f-row of one expert (its gate row and its up row);
+//   down:    a group of output rows of one expert's W_d.
+// Each IQ4_NL block is decoded once (byte_perm table lookup) and dotted with
+// every token routed to the expert by dp2a against 16-bit block-quantised
+// activations (Red Lite, "What we learned", section 4: decode each weight
+// block once for both tokens of a paired pass). Down-phase weights are fetched
+// before the grid barrier, so they stream while the gate/up phase finishes.
+// Each output is the sum, in a fixed order, of per-(pair, row) partials: the
+// shared expert first, then the routed experts in ascending id.
+#include "common.cuh"
+#include "decode.cuh"
+#include "decode_common.cuh"
+
+namespace moe {
+
+constexpr int kFW = 16;            // warps per CTA
+constexpr int kFT = kFW * 32;      // threads per CTA
+constexpr int kFSlots = 2;         // bulk-copy slots per warp
+
+struct FusedSmem {
+  size_t xq, slots, bars, recs, part, total, slot_bytes;
+  // router scratch (routed kernel), overlaying the records area, which is used
+  // only after the h barrier
+  size_t r_wr, r_x, r_part, r_keys, r_ids, r_w;
+};
+
+// Experts whose scores CTA c computes: a balanced split of E over the grid.
+__host__ __device__ inline int route_e0(int E, int c, int G) { return (int)((long long)E * c / G); }
+
+__host__ __device__ inline FusedSmem fused_smem(int H, int F, int Fs, int ns, int T, int k,
+                                                int rows_max, int rg, int route, int E, int G) {
+  FusedSmem m;
+  const size_t rbH = (size_t)(H / 32) * kBlockB;
+  size_t rbK = (size_t)(F / 32) * kBlockB;
+  if (ns) {
+    const size_t rbs = (size_t)(Fs / 32) * kBlockB;
+    rbK = rbK > rbs ? rbK : rbs;
+  }
+  const size_t gu = 2 * rbH;
+  const size_t dn = (size_t)rg * rbK;
+  m.slot_bytes = align_up_dev(gu > dn ? gu : dn, 128);
+  m.xq = align_up_dev(sizeof(RouteTable), 128);
+  m.slots = align_up_dev(m.xq + (size_t)T * dqvec_words(H) * 4, 128);
+  m.bars = m.slots + (size_t)kFW * kFSlots * m.slot_bytes;
+  m.recs = align_up_dev(m.bars + (size_t)(kFW * kFSlots + 4) * 8, 128);
+  const size_t recs = (size_t)T * k * dqvec_words(F) * 4 + (ns ? (size_t)T * dqvec_words(Fs) * 4 : 0);
+  m.part = align_up_dev(m.recs + recs, 16);
+  size_t end = m.part + (size_t)(T * k + (ns ? T : 0)) * rows_max * 4;
+  m.r_wr = m.r_x = m.r_part = m.r_keys = m.r_ids = m.r_w = 0;
+  if (route) {
+    const int epc = (E + G - 1) / G + 1;             // most experts any CTA scores
+    m.r_wr = m.recs;
+    m.r_x = align_up_dev(m.r_wr + (size_t)epc * H * 2, 128);
+    m.r_part = align_up_dev(m.r_x + (size_t)T * H * 2, 16);
+    m.r_keys = align_up_dev(m.r_part + (size_t)epc * 16 * T * 4, 16);
+    m.r_ids = align_up_dev(m.r_keys + (size_t)T * E * 4, 16);
+    m.r_w = align_up_dev(m.r_ids + (size_t)T * k * 4, 16);
+    const size_t rend = m.r_w + (size_t)T * k * 4;
+    end = end > rend ? end : rend;
+  }
+  m.total = end;
+  return m;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// One gate/up unit: the warp's f-row (gate row at `g`, up row at `u`) for every
+// token of the slot; writes h (fp32) for each (token, slot) pair.
+template <int MAXT>
+__device__ __forceinline__ void gateup_unit(const DecodeParams& p, const RouteTable& rt,
+                                            const uint8_t* g, const uint8_t* u, int slot, int f,
+                                            const uint32_t* xq, int xq_words) {
+  const int lane = threadIdx.x & 31;
+  const int H = p.H;
+  const int npairs = H / 64;
+  const int lpr = dlanes_per_row(H);
+  const bool shared = slot < 0;
+  const int ntok = shared ? p.T : rt.slot_off[slot + 1] - rt.slot_off[slot];
+  const int lbase = shared ? 0 : rt.slot_off[slot];
+  const int xs_off = dqvec_pair_words(H);
+  for (int g0 = 0; g0 < ntok; g0 += MAXT) {
+    const int ng = ntok - g0 < MAXT ? ntok - g0 : MAXT;
+    int tok[MAXT];
+#pragma unroll
+    for (int j = 0; j < MAXT; ++j) {
+      const int jj = g0 + (j < ng ? j : 0);
+      tok[j] = shared ? jj : rt.list[lbase + jj] / p.k;
+    }
+    float ag[MAXT], au[MAXT];
+#pragma unroll
+    for (int j = 0; j < MAXT; ++j) ag[j] = au[j] = 0.0f;
+    for (int q = lane; q < npairs; q += 32) {
+      const int qbase = qv_base(q, lpr);
+      uint32_t w[9];
+      float dg0, dg1, du0, du1;
+      uint32_t a0[4], a1[4];
+      uint32_t tg0[8], tg1[8], tu0[8], tu1[8];
+      load_pair_smem(g + q * kPairB, w);
+      split_pair(w, dg0, dg1, a0, a1);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        iq4_lookup8(a0[i], tg0[2 * i], tg0[2 * i + 1]);
+        iq4_lookup8(a1[i], tg1[2 * i], tg1[2 * i + 1]);
+      }
+      load_pair_smem(u + q * kPairB, w);
+      split_pair(w, du0, du1, a0, a1);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        iq4_lookup8(a0[i], tu0[2 * i], tu0[2 * i + 1]);
+        iq4_lookup8(a1[i], tu1[2 * i], tu1[2 * i + 1]);
+      }
+#pragma unroll
+      for (int j = 0; j < MAXT; ++j) {
+        if (j < ng) {
+          const uint32_t* rec = xq + (size_t)tok[j] * xq_words;
+          const uint4* r4 = reinterpret_cast<const uint4*>(rec) + qbase;
+          uint32_t v[32];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 t4 = r4[c * lpr];
+            v[4 * c] = t4.x; v[4 * c + 1] = t4.y; v[4 * c + 2] = t4.z; v[4 * c + 3] = t4.w;
+          }
+          const float* xs = reinterpret_cast<const float*>(rec + xs_off);
+          const float s0 = xs[2 * q], s1 = xs[2 * q + 1];
+          const int ig0 = iq4_dot_block(tg0, v);
+          const int ig1 = iq4_dot_block(tg1, v + 16);
+          const int iu0 = iq4_dot_block(tu0, v);
+          const int iu1 = iq4_dot_block(tu1, v + 16);
+          ag[j] = fmaf((float)ig0, dg0 * s0, ag[j]);
+          ag[j] = fmaf((float)ig1, dg1 * s1, ag[j]);
+          au[j] = fmaf((float)iu0, du0 * s0, au[j]);
+          au[j] = fmaf((float)iu1, du1 * s1, au[j]);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < MAXT; ++j) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        ag[j] += __shfl_xor_sync(0xFFFFFFFFu, ag[j], o);
+        au[j] += __shfl_xor_sync(0xFFFFFFFFu, au[j], o);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < MAXT; ++j) {
+      if (j < ng && lane == j) {
+        const float hv = silu_mul(ag[j], au[j]);
+        if (shared) p.h_s[(size_t)tok[j] * p.Fs + f] = hv;
+        else p.h_r[(size_t)rt.list[lbase + g0 + j] * p.F + f] = hv;
+      }
+    }
+  }
+}
+
+// One down unit: rows [r0, r0 + nrows) (CTA-local indices) of the slot's W_d at
+// `wrows`; for every pair of the slot, the row dot products into `part`.
+__device__ __forceinline__ void down_unit(const DecodeParams& p, const RouteTable& rt,
+                                          const uint8_t* wrows, int slot, int r0, int nrows,
+                                          const uint32_t* recs, float* part, int rows_max) {
+  constexpr int NPS = 4;
+  const int lane = threadIdx.x & 31;
+  const bool shared = slot < 0;
+  const int K = shared ? p.Fs : p.F;
+  const int rbK = K / 32 * kBlockB;
+  const int lpr = dlanes_per_row(K);
+  const int rpw = 32 / lpr;
+  const int npq = K / 64;
+  const int words = dqvec_words(K);
+  const int pw = dqvec_pair_words(K);
+  const int P = p.T * p.k;
+  const int ntok = shared ? p.T : rt.slot_off[slot + 1] - rt.slot_off[slot];
+  const int lbase = shared ? 0 : rt.slot_off[slot];
+  const uint32_t* rec_sh = recs + (size_t)P * dqvec_words(p.F);
+  const int q0 = lane % lpr;
+  for (int g0 = 0; g0 < ntok; g0 += NPS) {
+    const int np = ntok - g0 < NPS ? ntok - g0 : NPS;
+    int pidx[NPS];
+    const uint32_t* rp[NPS];
+#pragma unroll
+    for (int j = 0; j < NPS; ++j) {
+      const int jj = g0 + (j < np ? j : 0);
+      if (shared) {
+        pidx[j] = P + jj;
+        rp[j] = rec_sh + (size_t)jj * words;
+      } else {
+        pidx[j] = rt.list[lbase + jj];
+        rp[j] = recs + (size_t)pidx[j] * words;
+      }
+    }
+    for (int rb = 0; rb < nrows; rb += rpw) {
+      const int rl = rb + lane / lpr;
+      const bool active = rl < nrows;
+      float acc[NPS];
+#pragma unroll
+      for (int j = 0; j < NPS; ++j) acc[j] = 0.0f;
+      if (active) {
+        const uint8_t* row = wrows + (size_t)rl * rbK;
+        for (int q = q0; q < npq; q += lpr) {
+          const int qbase = qv_base(q, lpr);
+          uint32_t w[9];
+          float d0, d1;
+          uint32_t a0[4], a1[4];
+          uint32_t t0[8], t1[8];
+          load_pair_smem(row + q * kPairB, w);
+          split_pair(w, d0, d1, a0, a1);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            iq4_lookup8(a0[i], t0[2 * i], t0[2 * i + 1]);
+            iq4_lookup8(a1[i], t1[2 * i], t1[2 * i + 1]);
+          }
+#pragma unroll
+          for (int j = 0; j < NPS; ++j) {
+            if (j < np) {
+              const uint4* r4 = reinterpret_cast<const uint4*>(rp[j]) + qbase;
+              uint32_t v[32];
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                const uint4 t4 = r4[c * lpr];
+                v[4 * c] = t4.x; v[4 * c + 1] = t4.y; v[4 * c + 2] = t4.z; v[4 * c + 3] = t4.w;
+              }
+              const float* sc = reinterpret_cast<const float*>(rp[j] + pw);
+              const int i0 = iq4_dot_block(t0, v);
+              const int i1 = iq4_dot_block(t1, v + 16);
+              acc[j] = fmaf((float)i0, d0 * sc[2 * q], acc[j]);
+              acc[j] = fmaf((float)i1, d1 * sc[2 * q + 1], acc[j]);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < NPS; ++j)
+        if (j < np)
+          for (int o = lpr >> 1; o > 0; o >>= 1)
+            acc[j] += __shfl_xor_sync(0xFFFFFFFFu, acc[j], o);
+      if (active && q0 == 0) {
+#pragma unroll
+        for (int j = 0; j < NPS; ++j)
+          if (j < np) part[(size_t)pidx[j] * rows_max + r0 + rl] = acc[j];
+      }
+    }
+  }
+}
+
+template <int MAXT, bool ROUTE>
+__global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int H = p.H;
+  const int rows_max = p.dn_rows_max;
+  const int RG = p.fz_rg;
+  const FusedSmem L = fused_smem(H, p.F, p.Fs, p.n_shared, p.T, p.k, rows_max, RG, ROUTE ? 1 : 0,
+                                 p.E, gridDim.x);
+  RouteTable& rt = *reinterpret_cast<RouteTable*>(smem);
+  uint32_t* xq = reinterpret_cast<uint32_t*>(smem + L.xq);
+  uint8_t* slots = smem + L.slots;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* recs_bar = bars + kFW * kFSlots;
+  uint64_t* rwr_bar = recs_bar + 1;            // router rows of this CTA
+  uint64_t* rx_bar = recs_bar + 2;             // activations for the router
+  uint32_t* recs = reinterpret_cast<uint32_t*>(smem + L.recs);
+  float* part = reinterpret_cast<float*>(smem + L.part);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int xq_words = dqvec_words(H);
+  const int rbH = H / 32 * kBlockB;
+  uint8_t* myslots = slots + (size_t)warp * kFSlots * L.slot_bytes;
+  uint64_t* mybar = bars + warp * kFSlots;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kFW * kFSlots + 3; ++i) mbar_init(&bars[i], 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  // ---- this CTA's work
+  const RowRange shr = p.n_shared ? split_rows(p.Fs, 1, blockIdx.x, gridDim.x) : RowRange{0, 0};
+  const RowRange dn = split_rows(H, 1, blockIdx.x, gridDim.x);
+  const int nrows_cta = dn.b - dn.a;
+  const int ngroups = (nrows_cta + RG - 1) / RG;
+  auto count = [&](int a, int b) { return a + warp < b ? (b - a - warp + kFW - 1) / kFW : 0; };
+  const int n_sh = count(shr.a, shr.b);
+  int n_rt = 0, n_tot = n_sh;      // known once the route table exists
+  RowRange rr{0, 0};
+  int n_dslots = 0;
+
+  int issued = 0, consumed = 0;
+  bool ok = true;
+  // Issue unit j of this warp's sequence (lane 0 issues; all lanes count).
+  auto issue = [&](int j) {
+    const int s = j % kFSlots;
+    uint8_t* dst = myslots + (size_t)s * L.slot_bytes;
+    if (j < n_sh) {
+      const int f = shr.a + warp + kFW * j;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&mybar[s], 2 * rbH);
+        bulk_g2s(dst, p.sh_gate + (size_t)f * rbH, rbH, &mybar[s]);
+        bulk_g2s(dst + rbH, p.sh_up + (size_t)f * rbH, rbH, &mybar[s]);
+      }
+    } else if (j < n_sh + n_rt) {
+      const int r = rr.a + warp + kFW * (j - n_sh);
+      const int sl = r / p.F, f = r - sl * p.F;
+      const size_t row = (size_t)rt.slot_expert[sl] * p.F + f;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&mybar[s], 2 * rbH);
+        bulk_g2s(dst, p.gate + row * rbH, rbH, &mybar[s]);
+        bulk_g2s(dst + rbH, p.up + row * rbH, rbH, &mybar[s]);
+      }
+    } else {
+      const int u = warp + kFW * (j - n_sh - n_rt);
+      const int su = u / ngroups, gi = u - su * ngroups;
+      const bool sh = p.n_shared && su == 0;
+      const int sl = su - p.n_shared;
+      const int K = sh ? p.Fs : p.F;
+      const int rbK = K / 32 * kBlockB;
+      const int r0 = gi * RG;
+      const int nr = nrows_cta - r0 < RG ? nrows_cta - r0 : RG;
+      const uint8_t* src = sh ? p.sh_down + (size_t)(dn.a + r0) * rbK
+                              : p.down + ((size_t)rt.slot_expert[sl] * H + dn.a + r0) * rbK;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&mybar[s], (uint32_t)(nr * rbK));
+        bulk_g2s(dst, src, (uint32_t)(nr * rbK), &mybar[s]);
+      }
+    }
+  };
+  auto issue_upto = [&](int limit) {
+    while (issued < limit && issued - consumed < kFSlots) issue(issued++);
+  };
+  auto wait_unit = [&](int j) {
+    return mbar_wait(&mybar[j % kFSlots], (uint32_t)((j / kFSlots) & 1), p.status);
+  };
+
+  // Router rows of this CTA's experts (constant): fetch them while the previous
+  // kernel on the stream finishes.
+  const int re0 = ROUTE ? route_e0(p.E, blockIdx.x, gridDim.x) : 0;
+  const int re1 = ROUTE ? route_e0(p.E, blockIdx.x + 1, gridDim.x) : 0;
+  if (ROUTE && threadIdx.x == 0 && re1 > re0) {
+    const uint32_t bytes = (uint32_t)((re1 - re0) * H * 2);
+    mbar_arrive_expect_tx(rwr_bar, bytes);
+    bulk_g2s(smem + L.r_wr, p.Wr + (size_t)re0 * H, bytes, rwr_bar);
+  }
+  // Shared-expert rows do not depend on the routes: start fetching them too.
+  issue_upto(n_sh);
+  pdl_wait();
+  pdl_trigger();
+  if (ROUTE && threadIdx.x == 0 && re1 > re0) {
+    const uint32_t bytes = (uint32_t)(p.T * H * 2);
+    mbar_arrive_expect_tx(rx_bar, bytes);
+    bulk_g2s(smem + L.r_x, p.x, bytes, rx_bar);
+  }
+  quant_x_to_smem(p.x, p.T, H, xq, xq_words, warp, kFW);
+
+  if (ROUTE) {
+    // Scores of this CTA's experts: 16 chunks of H per expert, one warp per
+    // (expert, chunk), chunk partials summed in a fixed order.
+    const int ne = re1 - re0;
+    float* rpart = reinterpret_cast<float*>(smem + L.r_part);
+    if (ne > 0) {
+      ok = mbar_wait(rwr_bar, 0, p.status) && mbar_wait(rx_bar, 0, p.status);
+      const uint16_t* wr_s = reinterpret_cast<const uint16_t*>(smem + L.r_wr);
+      const uint16_t* x_s = reinterpret_cast<const uint16_t*>(smem + L.r_x);
+      const int hc = H / 16;                     // chunk length, a multiple of 16
+      for (int it = warp; it < ne * 16; it += kFW) {
+        const int el = it >> 4, c = it & 15;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int g8 = lane; g8 < hc / 8; g8 += 32) {
+          const uint4 wv = reinterpret_cast<const uint4*>(wr_s + (size_t)el * H + c * hc)[g8];
+          const uint32_t wr[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            if (t < p.T) {
+              const uint4 xv = reinterpret_cast<const uint4*>(x_s + (size_t)t * H + c * hc)[g8];
+              const uint32_t xr[4] = {xv.x, xv.y, xv.z, xv.w};
+              float a = acc[t];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                a = fmaf(__uint_as_float(wr[i] << 16), __uint_as_float(xr[i] << 16), a);
+                a = fmaf(__uint_as_float(wr[i] & 0xFFFF0000u), __uint_as_float(xr[i] & 0xFFFF0000u), a);
+              }
+              acc[t] = a;
+            }
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xFFFFFFFFu, acc[t], o);
+        if (lane == 0)
+          for (int t = 0; t < p.T; ++t) rpart[(el * 16 + c) * p.T + t] = acc[t];
+      }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < ne * p.T; i += kFT) {
+      const int el = i / p.T, t = i - el * p.T;
+      float sc = 0.f;
+      for (int c = 0; c < 16; ++c) sc += rpart[(el * 16 + c) * p.T + t];
+      p.scores[(size_t)t * p.E + re0 + el] = sc;
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) atomicAdd(&p.sync[2], 1u);
+  }
+  __syncthreads();
+
+  Pending pd;
+  pd.n = 0;
+  for (int j = 0; ok && j < n_sh; ++j) {
+    ok = wait_unit(j);
+    if (!ok) break;
+    const uint8_t* d = myslots + (size_t)(j % kFSlots) * L.slot_bytes;
+    const int f = shr.a + warp + kFW * j;
+    gateup_unit<MAXT>(p, rt, d, d + rbH, -1, f, xq, xq_words);
+    __syncwarp();
+    ++consumed;
+    pd.slot[pd.n] = -1;
+    pd.f[pd.n] = f;
+    if (++pd.n == kPendMax) flush_arrivals(p, rt, pd);
+    issue_upto(n_sh);
+  }
+
+  const int32_t* ids_src = p.ids;
+  const float* w_src = p.weights;
+  if (ROUTE) {
+    // all scores of this call -> top-k, redundantly in every CTA
+    if (threadIdx.x == 0) {
+      const uint64_t t0 = global_timer_ns();
+      while (ld_acquire_u32(&p.sync[2]) < gridDim.x) {
+        __nanosleep(32);
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+          if (p.status) atomicOr(p.status, MOE_STATUS_TIMEOUT);
+          break;
+        }
+      }
+      __threadfence();
+    }
+    __syncthreads();
+    float* keys = reinterpret_cast<float*>(smem + L.r_keys);
+    int32_t* ids_s = reinterpret_cast<int32_t*>(smem + L.r_ids);
+    float* w_s = reinterpret_cast<float*>(smem + L.r_w);
+    for (int i = threadIdx.x; i < p.T * p.E; i += kFT) {
+      const int e = i % p.E;
+      const float pr = 1.0f / (1.0f + expf(-__ldcg(p.scores + i)));
+      keys[i] = pr + (p.bias ? p.bias[e] : 0.0f);
+    }
+    __syncthreads();
+    if (warp < p.T) {
+      float* kk = keys + (size_t)warp * p.E;
+      const int t = warp;
+      float psum = 0.0f, psel = 0.0f;
+      int isel = 0;
+      for (int j = 0; j < p.k; ++j) {
+        float best = -INFINITY;
+        int bi = 0x7FFFFFFF;
+        for (int e = lane; e < p.E; e += 32) {
+          const float kv = kk[e];
+          if (kv > best) { best = kv; bi = e; }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+          const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+          if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
+        }
+        if (bi >= p.E) bi = 0;
+        const float pr = 1.0f / (1.0f + expf(-__ldcg(p.scores + (size_t)t * p.E + bi)));
+        psum += pr;
+        if (lane == j) { psel = pr; isel = bi; }
+        __syncwarp();
+        if (lane == 0) kk[bi] = -INFINITY;
+        __syncwarp();
+      }
+      if (lane < p.k) {
+        ids_s[t * p.k + lane] = isel;
+        w_s[t * p.k + lane] = psel / psum;
+        if (blockIdx.x == 0) {
+          p.ids_out[(size_t)t * p.k + lane] = isel;
+          p.w_out[(size_t)t * p.k + lane] = psel / psum;
+        }
+      }
+    }
+    __syncthreads();
+    ids_src = ids_s;
+    w_src = w_s;
+  }
+  build_route_table<kFT, 0>(rt, ids_src, w_src, p.T * p.k, p.E);
+  if (blockIdx.x == 0 && threadIdx.x == 0 && p.status && rt.invalid)
+    atomicAdd(p.status, (uint32_t)(rt.invalid < 0xFFFF ? rt.invalid : 0xFFFF));
+  for (int i = threadIdx.x; i < (p.T * p.k + (p.n_shared ? p.T : 0)) * rows_max; i += kFT)
+    part[i] = 0.0f;
+  rr = split_rows(rt.n_slots * p.F, 1, blockIdx.x, gridDim.x);
+  n_rt = count(rr.a, rr.b);
+  n_dslots = rt.n_slots + p.n_shared;
+  const int n_dn_units = n_dslots * ngroups;
+  const int n_dn = warp < n_dn_units ? (n_dn_units - warp + kFW - 1) / kFW : 0;
+  n_tot = n_sh + n_rt + n_dn;
+  issue_upto(n_tot);
+
+  for (int j = n_sh; ok && j < n_sh + n_rt; ++j) {
+    ok = wait_unit(j);
+    if (!ok) break;
+    const uint8_t* d = myslots + (size_t)(j % kFSlots) * L.slot_bytes;
+    const int r = rr.a + warp + kFW * (j - n_sh);
+    const int sl = r / p.F, f = r - sl * p.F;
+    gateup_unit<MAXT>(p, rt, d, d + rbH, sl, f, xq, xq_words);
+    __syncwarp();
+    ++consumed;
+    pd.slot[pd.n] = sl;
+    pd.f[pd.n] = f;
+    if (++pd.n == kPendMax) flush_arrivals(p, rt, pd);
+    issue_upto(n_tot);
+  }
+  if (pd.n) flush_arrivals(p, rt, pd);
+
+  // ---- grid barrier: every h block is quantised once every CTA has arrived
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(&p.sync[0], 1u);
+    const uint64_t t0 = global_timer_ns();
+    while (ld_acquire_u32(&p.sync[0]) < gridDim.x) {
+      __nanosleep(64);
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        if (p.status) atomicOr(p.status, MOE_STATUS_TIMEOUT);
+        break;
+      }
+    }
+    __threadfence();
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    // all quantised h records of this call -> shared memory
+    const int P = p.T * p.k;
+    const uint32_t rb = (uint32_t)dqvec_words(p.F) * 4;
+    const uint32_t rbs = p.n_shared ? (uint32_t)dqvec_words(p.Fs) * 4 : 0u;
+    mbar_arrive_expect_tx(recs_bar, P * rb + p.T * rbs);
+    bulk_g2s(recs, p.rec_r, P * rb, recs_bar);
+    if (p.n_shared)
+      bulk_g2s(reinterpret_cast<uint8_t*>(recs) + (size_t)P * rb, p.rec_s, p.T * rbs, recs_bar);
+  }
+  __syncthreads();
+  ok = ok && mbar_wait(recs_bar, 0, p.status);
+
+  for (int j = n_sh + n_rt; ok && j < n_tot; ++j) {
+    ok = wait_unit(j);
+    if (!ok) break;
+    const uint8_t* d = myslots + (size_t)(j % kFSlots) * L.slot_bytes;
+    const int u = warp + kFW * (j - n_sh - n_rt);
+    const int su = u / ngroups, gi = u - su * ngroups;
+    const bool sh = p.n_shared && su == 0;
+    const int r0 = gi * RG;
+    const int nr = nrows_cta - r0 < RG ? nrows_cta - r0 : RG;
+    down_unit(p, rt, d, sh ? -1 : su - p.n_shared, r0, nr, recs, part, rows_max);
+    __syncwarp();
+    ++consumed;
+    issue_upto(n_tot);
+  }
+  __syncthreads();
+
+  // ---- combine in the fixed order: shared expert, then routed experts ascending
+  for (int i = threadIdx.x; i < nrows_cta * p.T; i += kFT) {
+    const int t = i / nrows_cta, r = i - t * nrows_cta;
+    float acc = 0.0f;
+    if (p.n_shared) acc = part[(size_t)(p.T * p.k + t) * rows_max + r];
+    for (int e = 0; e < rt.n_valid; ++e) {
+      const int pr = rt.list[e];
+      if (pr / p.k == t) acc += rt.wt[pr] * part[(size_t)pr * rows_max + r];
+    }
+    p.y[(size_t)t * H + dn.a + r] = acc;
+  }
+
+  // ---- leave: the last CTA out resets the barrier counters for the next call
+  if (threadIdx.x == 0) {
+    const uint32_t old = atomicAdd(&p.sync[1], 1u);
+    if (old == gridDim.x - 1) {
+      p.sync[0] = 0u;
+      p.sync[1] = 0u;
+      p.sync[2] = 0u;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+bool fused_decode_supported(const DecodeParams& p, int num_sms, size_t* smem, int* rg,
+                            int* rows_max) {
+  if (p.T < 1 || p.T > 4) return false;
+  if (p.H % 256 || p.F % 256 || (p.n_shared && p.Fs % 256)) return false;
+  const int grid = num_sms;
+  const int rmax = (p.H + grid - 1) / grid;
+  // down rows per unit: the rows one pass of a warp covers (finer units
+  // balance the down phase over the warps)
+  int K = p.F;
+  if (p.n_shared && p.Fs > K) K = p.Fs;
+  int r = 32 / lanes_per_row(K);
+  if (r > rmax) r = rmax;
+  const FusedSmem m = fused_smem(p.H, p.F, p.Fs, p.n_shared, p.T, p.k, rmax, r, p.route, p.E,
+                                 grid);
+  if (m.total > 227 * 1024) return false;
+  *smem = m.total;
+  *rg = r;
+  *rows_max = rmax;
+  return true;
+}
+
+namespace {
+template <int MAXT, bool ROUTE>
+cudaError_t launch_fused_t(const DecodeParams& p, const cudaLaunchConfig_t& cfg, size_t smem) {
+  const cudaError_t e =
+      ensure_smem_attr(reinterpret_cast<const void*>(decode_fused_kernel<MAXT, ROUTE>), smem);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, decode_fused_kernel<MAXT, ROUTE>, p);
+}
+}  // namespace
+
+cudaError_t launch_decode_fused(const DecodeParams& p, int num_sms, size_t smem, bool pdl,
+                                cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms);
+  cfg.blockDim = dim3(kFT);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (p.route) {
+    switch (p.T) {
+      case 1: return launch_fused_t<1, true>(p, cfg, smem);
+      case 2: return launch_fused_t<2, true>(p, cfg, smem);
+      default: return launch_fused_t<4, true>(p, cfg, smem);
+    }
+  }
+  switch (p.T) {
+    case 1: return launch_fused_t<1, false>(p, cfg, smem);
+    case 2: return launch_fused_t<2, false>(p, cfg, smem);
+    default: return launch_fused_t<4, false>(p, cfg, smem);
+  }
+}
+
+}  // namespace moe

@@ -78,6 +78,39 @@ moe_status layer_args(const moe_shape* s, const moe_expert_weights* w, const uin
   return MOE_OK;
 }
 
+moe::DecodeParams decode_params(const moe_shape* shape, const moe_expert_weights* w,
+                                const uint16_t* x, int32_t T, const int32_t* ids,
+                                const float* weights, float* y, void* ws,
+                                const moe::DecodeLayout& L, uint32_t* status) {
+  uint8_t* base = reinterpret_cast<uint8_t*>(ws);
+  moe::DecodeParams p{};
+  p.H = shape->hidden;
+  p.F = shape->ffn;
+  p.Fs = shape->n_shared ? shape->ffn_shared : 0;
+  p.E = shape->n_experts;
+  p.k = shape->top_k;
+  p.n_shared = shape->n_shared;
+  p.T = T;
+  p.gate = reinterpret_cast<const uint8_t*>(w->gate);
+  p.up = reinterpret_cast<const uint8_t*>(w->up);
+  p.down = reinterpret_cast<const uint8_t*>(w->down);
+  p.sh_gate = reinterpret_cast<const uint8_t*>(w->sh_gate);
+  p.sh_up = reinterpret_cast<const uint8_t*>(w->sh_up);
+  p.sh_down = reinterpret_cast<const uint8_t*>(w->sh_down);
+  p.x = x;
+  p.ids = ids;
+  p.weights = weights;
+  p.y = y;
+  p.h_r = reinterpret_cast<float*>(base + L.h_r);
+  p.h_s = reinterpret_cast<float*>(base + L.h_s);
+  p.rec_r = reinterpret_cast<uint32_t*>(base + L.rec_r);
+  p.rec_s = reinterpret_cast<uint32_t*>(base + L.rec_s);
+  p.cnt = reinterpret_cast<uint32_t*>(base + L.cnt);
+  p.sync = reinterpret_cast<uint32_t*>(base + L.sync);
+  p.status = status;
+  return p;
+}
+
 }  // namespace
 
 extern "C" {
@@ -123,33 +156,34 @@ moe_status moe_iq4nl_decode(const moe_shape* shape, const moe_expert_weights* w,
   if (ws_bytes < (size_t)L.total) return MOE_ERR_WORKSPACE;
   const int sms = num_sms();
   if (sms <= 0) return MOE_ERR_CUDA;
-  uint8_t* base = reinterpret_cast<uint8_t*>(ws);
-  moe::DecodeParams p{};
-  p.H = shape->hidden;
-  p.F = shape->ffn;
-  p.Fs = shape->n_shared ? shape->ffn_shared : 0;
-  p.E = shape->n_experts;
-  p.k = shape->top_k;
-  p.n_shared = shape->n_shared;
-  p.T = T;
-  p.gate = reinterpret_cast<const uint8_t*>(w->gate);
-  p.up = reinterpret_cast<const uint8_t*>(w->up);
-  p.down = reinterpret_cast<const uint8_t*>(w->down);
-  p.sh_gate = reinterpret_cast<const uint8_t*>(w->sh_gate);
-  p.sh_up = reinterpret_cast<const uint8_t*>(w->sh_up);
-  p.sh_down = reinterpret_cast<const uint8_t*>(w->sh_down);
-  p.x = x;
-  p.ids = ids;
-  p.weights = weights;
-  p.y = y;
-  p.h_r = reinterpret_cast<float*>(base + L.h_r);
-  p.h_s = reinterpret_cast<float*>(base + L.h_s);
-  p.rec_r = reinterpret_cast<uint32_t*>(base + L.rec_r);
-  p.rec_s = reinterpret_cast<uint32_t*>(base + L.rec_s);
-  p.cnt = reinterpret_cast<uint32_t*>(base + L.cnt);
-  p.status = status;
+  moe::DecodeParams p = decode_params(shape, w, x, T, ids, weights, y, ws, L, status);
   const cudaError_t e = moe::launch_decode(p, sms, g_pdl.load() != 0,
                                            reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_iq4nl_decode_routed(const moe_shape* shape, const uint16_t* router_w,
+                                   const float* router_bias, const moe_expert_weights* w,
+                                   const uint16_t* x, int32_t T, int32_t* ids, float* weights,
+                                   float* y, void* ws, size_t ws_bytes, uint32_t* status,
+                                   void* stream) {
+  moe_status st = layer_args(shape, w, x, T, MOE_MAX_DECODE_TOKENS, ids, weights, y, ws, status);
+  if (st != MOE_OK || T == 0) return st;
+  if (!router_w) return MOE_ERR_INVALID_ARG;
+  if (!aligned(router_w, 16) || (router_bias && !aligned(router_bias, 4)))
+    return MOE_ERR_MISALIGNED;
+  const moe::DecodeLayout L = moe::decode_layout(*shape, T);
+  if (ws_bytes < (size_t)L.total) return MOE_ERR_WORKSPACE;
+  const int sms = num_sms();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  moe::DecodeParams p = decode_params(shape, w, x, T, ids, weights, y, ws, L, status);
+  p.Wr = router_w;
+  p.bias = router_bias;
+  p.ids_out = ids;
+  p.w_out = weights;
+  p.scores = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + L.scores);
+  const cudaError_t e = moe::launch_decode_routed(p, sms, g_pdl.load() != 0,
+                                                  reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -198,6 +232,34 @@ moe_status moe_sanitize_routes(const int32_t* ids, const float* weights, int64_t
   const cudaError_t e = moe::launch_sanitize(ids, weights, n, n_experts, ids_out, weights_out,
                                              status, sms, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int32_t moe_launches_per_call(const moe_shape* shape, int32_t T, int32_t call) {
+  const moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return 0;
+  const int sms = num_sms();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  if (call == 0) return 1;
+  if (call == 1 || call == 2) {
+    if (T > MOE_MAX_DECODE_TOKENS) return MOE_ERR_INVALID_ARG;
+    moe::DecodeParams p{};
+    p.H = shape->hidden;
+    p.F = shape->ffn;
+    p.Fs = shape->n_shared ? shape->ffn_shared : 0;
+    p.E = shape->n_experts;
+    p.k = shape->top_k;
+    p.n_shared = shape->n_shared;
+    p.T = T;
+    p.route = call == 2 ? 1 : 0;
+    size_t sm = 0;
+    int rg = 0, rmax = 0;
+    if (moe::fused_decode_supported(p, sms, &sm, &rg, &rmax)) return 1;
+    return call == 2 ? 3 : 2;
+  }
+  if (call == 3) return moe::prefill_launches(*shape, T);
+  return MOE_ERR_INVALID_ARG;
 }
 
 int32_t moe_set_pdl(int32_t enable) { return g_pdl.exchange(enable ? 1 : 0); }

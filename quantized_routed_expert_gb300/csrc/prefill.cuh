@@ -15,6 +15,7 @@ struct PrefillLayout {
 };
 
 PrefillLayout prefill_layout(const moe_shape& s, int64_t T);
+int prefill_launches(const moe_shape& s, int T);
 
 cudaError_t launch_prefill(const moe_shape& s, const moe_expert_weights& w, const uint16_t* x,
                            int T, const int32_t* ids, const float* weights, float* y,

@@ -18,10 +18,10 @@ namespace cg = cooperative_groups;
 namespace moe {
 
 __host__ __device__ inline size_t route_smem(int H, int E, int C, int TT) {
-  const int epc = (E + C - 1) / C;
+  (void)C;
   size_t off = (size_t)TT * H * 2;                       // x tile, bf16
   off = (off + 15) & ~size_t(15);
-  off += (size_t)TT * epc * 4;                           // scores of this CTA's experts
+  off += (size_t)TT * E * 4;                             // scores of the tokens this CTA owns
   off = (off + 15) & ~size_t(15);
   off += (size_t)8 * E * 4;                              // per-warp key scratch
   return off;
@@ -40,8 +40,8 @@ __global__ void __launch_bounds__(256) route_kernel(RouteParams p) {
   const int epc = (E + C - 1) / C;
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
   size_t off = ((size_t)TT * H * 2 + 15) & ~size_t(15);
-  float* sc = reinterpret_cast<float*>(smem + off);
-  off = (off + (size_t)TT * epc * 4 + 15) & ~size_t(15);
+  float* sc = reinterpret_cast<float*>(smem + off);      // [TT][E], rows of owned tokens
+  off = (off + (size_t)TT * E * 4 + 15) & ~size_t(15);
   float* keys = reinterpret_cast<float*>(smem + off);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -52,10 +52,10 @@ __global__ void __launch_bounds__(256) route_kernel(RouteParams p) {
   const int e1 = e0 + epc < E ? e0 + epc : E;
 
   // Router weights are constant: warm L2 with this CTA's rows while the
-  // previous kernel finishes.
+  // previous kernel on the stream finishes.
   if (threadIdx.x == 0 && e1 > e0) {
     const char* base = reinterpret_cast<const char*>(p.Wr + (size_t)e0 * H);
-    size_t bytes = (size_t)(e1 - e0) * H * 2;
+    const size_t bytes = (size_t)(e1 - e0) * H * 2;
     for (size_t o = 0; o < bytes; o += 65536) {
       const uint32_t n = (uint32_t)(bytes - o < 65536 ? bytes - o : 65536);
       asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + o), "r"(n & ~15u)
@@ -74,14 +74,16 @@ __global__ void __launch_bounds__(256) route_kernel(RouteParams p) {
   }
   __syncthreads();
 
-  // scores: one warp per expert, lanes over H in 8-element chunks
+  // Scores: one warp per expert, lanes over H in 8-element chunks (many loads
+  // in flight), then each score is stored straight into the shared memory of
+  // the CTA that owns its token (token i of the tile belongs to rank i % C).
   const int h8 = H / 8;
   for (int e = e0 + warp; e < e1; e += 8) {
     const uint4* wr = reinterpret_cast<const uint4*>(p.Wr + (size_t)e * H);
     float acc[TT];
 #pragma unroll
     for (int t = 0; t < TT; ++t) acc[t] = 0.0f;
-#pragma unroll 4
+#pragma unroll 8
     for (int c = lane; c < h8; c += 32) {
       const uint4 w = __ldg(wr + c);
       const float w0 = bf16_lo(w.x), w1 = bf16_hi(w.x), w2 = bf16_lo(w.y), w3 = bf16_hi(w.y);
@@ -108,27 +110,28 @@ __global__ void __launch_bounds__(256) route_kernel(RouteParams p) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xFFFFFFFFu, acc[t], o);
     }
-    if (lane == 0) {
 #pragma unroll
-      for (int t = 0; t < TT; ++t)
-        if (t < nt) sc[t * epc + (e - e0)] = acc[t];
+    for (int t = 0; t < TT; ++t) {
+      if (t < nt && lane == (t & 31)) {
+        float* dst = cluster.map_shared_rank(sc, t % C);
+        dst[t * E + e] = acc[t];
+      }
     }
   }
   cluster.sync();
 
-  // top-k: token i of the tile is handled by CTA i % C, warp (i / C) % 8
+  // top-k for the tokens this CTA owns; only local shared memory from here on
   float* mykeys = keys + (size_t)warp * E;
   for (int i = rank + C * warp; i < nt; i += C * 8) {
+    const float* srow = sc + (size_t)i * E;
     for (int e = lane; e < E; e += 32) {
-      const float* rs = cluster.map_shared_rank(sc, e / epc);
-      const float s = rs[i * epc + (e % epc)];
-      const float pr = 1.0f / (1.0f + expf(-s));
+      const float pr = 1.0f / (1.0f + expf(-srow[e]));
       mykeys[e] = pr + (p.bias ? p.bias[e] : 0.0f);
     }
     __syncwarp();
     float psum = 0.0f;
-    float psel[MOE_MAX_TOP_K];
-    int isel[MOE_MAX_TOP_K];
+    float psel = 0.0f;
+    int isel = 0;
     for (int j = 0; j < p.k; ++j) {
       float best = -INFINITY;
       int bi = 0x7FFFFFFF;
@@ -143,26 +146,56 @@ __global__ void __launch_bounds__(256) route_kernel(RouteParams p) {
         if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
       }
       if (bi >= E) bi = 0;            // only with NaN keys
-      const float* rs = cluster.map_shared_rank(sc, bi / epc);
-      const float s = rs[i * epc + (bi % epc)];
-      const float pr = 1.0f / (1.0f + expf(-s));
-      if (j < MOE_MAX_TOP_K) { psel[j] = pr; isel[j] = bi; }
+      const float pr = 1.0f / (1.0f + expf(-srow[bi]));
       psum += pr;
+      if (lane == j) { psel = pr; isel = bi; }
       __syncwarp();
       if (lane == 0) mykeys[bi] = -INFINITY;
       __syncwarp();
     }
-    if (lane == 0) {
-      const int t = t0 + i;
-      for (int j = 0; j < p.k; ++j) {
-        p.ids[(size_t)t * p.k + j] = isel[j];
-        p.w[(size_t)t * p.k + j] = psel[j] / psum;
-      }
+    if (lane < p.k) {
+      const size_t t = (size_t)(t0 + i);
+      p.ids[t * p.k + lane] = isel;
+      p.w[t * p.k + lane] = psel / psum;
     }
     __syncwarp();
   }
-  cluster.sync();
 }
+
+namespace {
+// Permits clusters of more than 8 CTAs for a kernel, once; an error means the
+// device does not offer them and the caller falls back to 8.
+cudaError_t allow_wide_clusters(const void* kernel) {
+  static const void* done[8];
+  static int n = 0;
+  for (int i = 0; i < n; ++i)
+    if (done[i] == kernel) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return e;
+  }
+  if (n < 8) done[n++] = kernel;
+  return cudaSuccess;
+}
+// Whether 16-CTA clusters can run for (token tile, shared memory size); -1 = not asked yet.
+struct WideEntry {
+  int tt;
+  size_t sm;
+  int ok;
+};
+WideEntry g_wide[32];
+int g_nwide = 0;
+int wide_cluster_cache(int tt, size_t sm) {
+  for (int i = 0; i < g_nwide; ++i)
+    if (g_wide[i].tt == tt && g_wide[i].sm == sm) return g_wide[i].ok;
+  return -1;
+}
+void wide_cluster_store(int tt, size_t sm, int ok) {
+  if (g_nwide < 32) g_wide[g_nwide++] = WideEntry{tt, sm, ok};
+}
+}  // namespace
 
 cudaError_t launch_route(const RouteParams& p, bool pdl, cudaStream_t stream) {
   // token tile: x tile <= 128 KB; cluster: split experts for small T
@@ -174,8 +207,10 @@ cudaError_t launch_route(const RouteParams& p, bool pdl, cudaStream_t stream) {
     TT = t;
   }
   const int ntiles = (p.T + TT - 1) / TT;
-  int C = ntiles >= 32 ? 1 : (ntiles >= 8 ? 4 : 8);
-  if (C > p.E) C = 1;
+  // Split the experts of a tile over a cluster when there are few tiles: 16
+  // CTAs (a non-portable cluster size) where allowed, else 8.
+  int C = ntiles >= 32 ? 1 : (ntiles >= 8 ? 4 : 16);
+  while (C > 1 && C > p.E) C >>= 1;
   const size_t sm = route_smem(p.H, p.E, C, TT);
   if (sm > 200 * 1024) return cudaErrorInvalidConfiguration;
 
@@ -199,6 +234,22 @@ cudaError_t launch_route(const RouteParams& p, bool pdl, cudaStream_t stream) {
   case N:                                                                                  \
     e = ensure_smem_attr(reinterpret_cast<const void*>(route_kernel<N>), sm);             \
     if (e != cudaSuccess) return e;                                                        \
+    if (C > 8) {                                                                           \
+      int ok16 = wide_cluster_cache(N, sm);                                                \
+      if (ok16 < 0) {                                                                      \
+        e = allow_wide_clusters(reinterpret_cast<const void*>(route_kernel<N>));           \
+        int ncl = 0;                                                                       \
+        if (e == cudaSuccess &&                                                            \
+            cudaOccupancyMaxActiveClusters(&ncl, route_kernel<N>, &cfg) != cudaSuccess)    \
+          ncl = 0;                                                                         \
+        cudaGetLastError();                                                                \
+        ok16 = (e == cudaSuccess && ncl >= 1) ? 1 : 0;                                     \
+        wide_cluster_store(N, sm, ok16);                                                   \
+      }                                                                                    \
+      if (!ok16) C = 8;                                                                    \
+      attr[0].val.clusterDim.x = C;                                                        \
+      cfg.gridDim = dim3(ntiles * C);                                                      \
+    }                                                                                      \
     return cudaLaunchKernelEx(&cfg, route_kernel<N>, p);
   switch (TT) {
     MOE_ROUTE_CASE(1)

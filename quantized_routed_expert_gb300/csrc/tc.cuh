@@ -1,0 +1,139 @@
+// tcgen05 (5th-generation tensor core), TMEM and tensor-map TMA wrappers (sm_100 family).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+// Shared-memory matrix descriptor for a K-major operand stored in the 128-byte
+// swizzled canonical layout: 8-row atoms of 8 x 128 B, atoms 1024 B apart
+// (stride byte offset), the 16-byte chunk c of row r stored at chunk c ^ (r % 8).
+// The tile base is 1024-byte aligned. Advancing K by 16 fp16 elements adds 32 B
+// to the start address.
+__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address, 16-byte units
+  d |= (uint64_t)1 << 16;                     // leading byte offset (unused here)
+  d |= (uint64_t)(1024 >> 4) << 32;           // stride byte offset: 8-row atoms
+  d |= (uint64_t)1 << 46;                     // descriptor version (sm_100)
+  d |= (uint64_t)2 << 61;                     // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp16 A and B (both K-major), fp32 D.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Whole warp: allocate `ncols` TMEM columns, address written to *dst (shared).
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns: thread i of the warp gets TMEM lane
+// (lane base + i), columns [col, col + 32).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+        "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
+        "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
+        "=r"(v[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 2D tiled TMA load (box given by the tensor map) completing on `bar`.
+// x (innermost coordinate, elements) must make x * elsize a multiple of 16.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Offset table for fp16 dequantisation: byte j holds T[j] + 128 (1..241), so
+// that the half with bits 0x6400 | byte is exactly 1024 + T + 128.
+constexpr uint32_t kTabU0 = 0x3F2D1801u;   // T[0..3]+128  = 1, 24, 45, 63
+constexpr uint32_t kTabU1 = 0x766A5D4Fu;   // T[4..7]+128  = 79, 93, 106, 118
+constexpr uint32_t kTabU2 = 0xA6998D81u;   // T[8..11]+128 = 129, 141, 153, 166
+constexpr uint32_t kTabU3 = 0xF1D9C5B5u;   // T[12..15]+128 = 181, 197, 217, 241
+
+// Eight codes (4 index bytes) -> the 8 offset table values in K order:
+// lo = (U[lo nibble of byte 0..3]), hi = (U[hi nibble of byte 0..3]).
+__device__ __forceinline__ void iq4_lookup8_split(uint32_t q, uint32_t& lo, uint32_t& hi) {
+  const uint32_t sel = 0x32103210u | ((q & 0x88888888u) >> 1);
+  const uint32_t a0 = __byte_perm(kTabU0, kTabU1, q);
+  const uint32_t b0 = __byte_perm(kTabU2, kTabU3, q);
+  const uint32_t r0 = __byte_perm(a0, b0, sel);          // L0 H0 L1 H1
+  const uint32_t q1 = q >> 16;
+  const uint32_t a1 = __byte_perm(kTabU0, kTabU1, q1);
+  const uint32_t b1 = __byte_perm(kTabU2, kTabU3, q1);
+  const uint32_t r1 = __byte_perm(a1, b1, sel >> 16);    // L2 H2 L3 H3
+  lo = __byte_perm(r0, r1, 0x6420);
+  hi = __byte_perm(r0, r1, 0x7531);
+}
+
+// Four offset-table bytes -> four fp16 d*T, each the round-to-nearest-even of
+// the exact product (T is exact in fp16; one multiply rounds once).
+__device__ __forceinline__ void offsets_to_half4(uint32_t u, __half2 d2, uint32_t& o01,
+                                                 uint32_t& o23) {
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+  uint32_t h01 = __byte_perm(u, 0x64646464u, 0x4140);
+  uint32_t h23 = __byte_perm(u, 0x64646464u, 0x4342);
+  __half2 t01 = __hsub2(*reinterpret_cast<__half2*>(&h01), bias);
+  __half2 t23 = __hsub2(*reinterpret_cast<__half2*>(&h23), bias);
+  __half2 w01 = __hmul2(t01, d2);
+  __half2 w23 = __hmul2(t23, d2);
+  o01 = *reinterpret_cast<uint32_t*>(&w01);
+  o23 = *reinterpret_cast<uint32_t*>(&w23);
+}
+
+}  // namespace moe

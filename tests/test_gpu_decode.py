@@ -177,6 +177,9 @@ def test_workspace_reused_across_layers():
     (128, 192, 5, 3, 7, 1),        # ragged: 3 block pairs per F row, odd T
     (256, 128, 8, 2, 16, 1),       # tiny down rows (72 B, 8-byte multiples)
     (8192, 64, 4, 2, 2, 1),        # widest hidden
+    (256, 256, 8, 3, 3, 1),        # single-launch fused path, odd T
+    (4096, 512, 2, 2, 4, 0),       # fused path without a shared expert
+    (2048, 768, 33, 5, 2, 1),      # fused path, F not a power of two
 ])
 def test_decode_edge_shapes(H, F, E, k, T, ns):
     s = synth.Shape("edge", H, F, E, k, T, 1, n_shared=ns)
@@ -220,3 +223,45 @@ def test_decode_argument_errors():
     empty = torch.zeros((0, s.H), dtype=torch.bfloat16, device=DEV)
     y0 = moe.iq4nl_decode(shape, wts, empty, ids[:0], w[:0], ws)   # T == 0: nothing to do
     assert y0.shape == (0, s.H)
+
+
+def test_fused_and_two_kernel_paths_agree_bitwise():
+    # 1..4 tokens run the fused single-launch kernel, 5..16 the two-kernel
+    # path; per token both do the same arithmetic in the same order.
+    s = synth.Shape("paths", 512, 256, 16, 4, 6, 1)
+    L = layer_of(s, 0, seed=7)
+    rng = np.random.default_rng(3)
+    x_host = synth.to_bf16_bits(rng.standard_normal((6, s.H)))
+    ids = np.stack([rng.choice(s.E, s.k, replace=False) for _ in range(6)]).astype(np.int32)
+    w = rng.random((6, s.k)).astype(np.float32)
+    _, _, y6 = run_decode(L, x_host, ids, w)
+    for t in range(6):
+        _, _, y1 = run_decode(L, x_host[t:t + 1], ids[t:t + 1], w[t:t + 1])
+        assert np.array_equal(y1[0].view(np.uint32), y6[t].view(np.uint32)), t
+    check_close(y6, oracle_layer(L, x_host, ids, w.astype(np.float64)), "paths shape")
+
+
+@pytest.mark.parametrize("cfg,T,layer", [(1, 1, 3), (2, 2, 7), (3, 1, 2), (3, 4, 0), (0, 4, 0)])
+def test_decode_routed_matches_route_then_decode(cfg, T, layer):
+    # one call (fused routing where the shape allows) == moe_route_topk + moe_iq4nl_decode
+    moe = lib()
+    from synth.layers import bf16_tensor
+    L = layer_of(cfg, layer)
+    s = L.shape
+    shape = moe_shape(s)
+    x_host = gapped_rows(L, T)
+    x = bf16_tensor(x_host, DEV)
+    ws = moe.workspace(shape, T, moe.DECODE, DEV)
+    ids, w, y = moe.iq4nl_decode_routed(shape, L.router_w, L.bias, weights_of(L), x, ws)
+    torch.cuda.synchronize()
+    ids, w, y = ids.cpu().numpy(), w.cpu().numpy(), y.cpu().numpy()
+    check_route(ids, w, L, x_host)
+    ids2, _, _ = run_decode(L, x_host)            # moe_route_topk + moe_iq4nl_decode
+    assert np.array_equal(np.sort(ids, 1), np.sort(ids2, 1))
+    check_close(y, oracle_layer(L, x_host, ids, w), f"decode_routed cfg{cfg} T{T}")
+    # a second call on the same workspace (barrier counters reset) gives the same bits
+    ids3, w3, y3 = moe.iq4nl_decode_routed(shape, L.router_w, L.bias, weights_of(L), x, ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(y3.cpu().numpy().view(np.uint32), y.view(np.uint32))
+    n = moe.launches_per_call(shape, T, moe.CALL_DECODE_ROUTED)
+    assert n >= 1
