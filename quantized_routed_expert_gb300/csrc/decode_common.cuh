@@ -284,36 +284,53 @@ inline __device__ void flush_arrivals(const DecodeParams& p, const RouteTable& r
     old = atomicAdd(p.cnt + (size_t)cid * (fmax / 32) + pd.f[lane] / 32, 1u);
   }
   const uint32_t last = __ballot_sync(0xFFFFFFFFu, lane < pd.n && old == 31u);
+  if (last) __threadfence();
+  // (entry, token) blocks to quantise, gathered in batches so that their loads
+  // are all in flight before the first block is reduced
+  constexpr int kBatch = 8;
+  int ent[kBatch], tokj[kBatch];
+  int nb = 0;
+  auto drain = [&]() {
+    const float* src[kBatch];
+    uint32_t* dst[kBatch];
+    int Fb[kBatch], blk[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = ent[u < nb ? u : 0], j = tokj[u < nb ? u : 0];
+      const int slot = pd.slot[i];
+      const bool shared = slot < 0;
+      const int F = shared ? p.Fs : p.F;
+      const int words = dqvec_words(F);
+      const int pr = shared ? j : rt.list[rt.slot_off[slot] + j];
+      src[u] = shared ? p.h_s + (size_t)j * p.Fs : p.h_r + (size_t)pr * p.F;
+      dst[u] = shared ? p.rec_s + (size_t)j * words : p.rec_r + (size_t)pr * words;
+      Fb[u] = F;
+      blk[u] = pd.f[i] / 32;
+    }
+    float v[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) v[u] = u < nb ? __ldcg(src[u] + blk[u] * 32 + lane) : 0.f;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u)
+      if (u < nb) quant_block_store(v[u], blk[u], Fb[u], dst[u]);
+    nb = 0;
+  };
   for (int i = 0; i < pd.n; ++i) {
     if (!((last >> i) & 1u)) continue;
     const int slot = pd.slot[i];
-    const int f = pd.f[i];
-    const bool shared = slot < 0;
-    const int cid = shared ? p.E : rt.slot_expert[slot];
-    uint32_t* cnt = p.cnt + (size_t)cid * (fmax / 32) + f / 32;
-    {
-      __threadfence();
-      const int b = f / 32;
-      const int F = shared ? p.Fs : p.F;
-      const int words = dqvec_words(F);
-      const int ntok = shared ? p.T : rt.slot_off[slot + 1] - rt.slot_off[slot];
-      const int lbase = shared ? 0 : rt.slot_off[slot];
-      for (int j = 0; j < ntok; ++j) {
-        const float* hp;
-        uint32_t* rec;
-        if (shared) {
-          hp = p.h_s + (size_t)j * p.Fs;
-          rec = p.rec_s + (size_t)j * words;
-        } else {
-          const int pr = rt.list[lbase + j];
-          hp = p.h_r + (size_t)pr * p.F;
-          rec = p.rec_r + (size_t)pr * words;
-        }
-        const float v = __ldcg(hp + b * 32 + lane);
-        quant_block_store(v, b, F, rec);
-      }
-      if (lane == 0) *cnt = 0u;
+    const int ntok = slot < 0 ? p.T : rt.slot_off[slot + 1] - rt.slot_off[slot];
+    for (int j = 0; j < ntok; ++j) {
+      ent[nb] = i;
+      tokj[nb] = j;
+      if (++nb == kBatch) drain();
     }
+  }
+  if (nb) drain();
+  // reset the counters of the blocks this warp completed
+  if (lane < pd.n && old == 31u) {
+    const int slot = pd.slot[lane];
+    const int cid = slot < 0 ? p.E : rt.slot_expert[slot];
+    p.cnt[(size_t)cid * (fmax / 32) + pd.f[lane] / 32] = 0u;
   }
   __syncwarp();
   pd.n = 0;

@@ -59,7 +59,7 @@ __host__ __device__ inline FusedSmem fused_smem(int H, int F, int Fs, int ns, in
     m.r_x = align_up_dev(m.r_wr + (size_t)epc * H * 2, 128);
     m.r_part = align_up_dev(m.r_x + (size_t)T * H * 2, 16);
     m.r_keys = align_up_dev(m.r_part + (size_t)epc * 16 * T * 4, 16);
-    m.r_ids = align_up_dev(m.r_keys + (size_t)T * E * 4, 16);
+    m.r_ids = align_up_dev(m.r_keys + (size_t)2 * T * E * 4, 16);   // keys, then sigmoids
     m.r_w = align_up_dev(m.r_ids + (size_t)T * k * 4, 16);
     const size_t rend = m.r_w + (size_t)T * k * 4;
     end = end > rend ? end : rend;
@@ -444,9 +444,11 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const DecodeParams
     float* keys = reinterpret_cast<float*>(smem + L.r_keys);
     int32_t* ids_s = reinterpret_cast<int32_t*>(smem + L.r_ids);
     float* w_s = reinterpret_cast<float*>(smem + L.r_w);
+    float* probs = keys + (size_t)p.T * p.E;
     for (int i = threadIdx.x; i < p.T * p.E; i += kFT) {
       const int e = i % p.E;
       const float pr = 1.0f / (1.0f + expf(-__ldcg(p.scores + i)));
+      probs[i] = pr;
       keys[i] = pr + (p.bias ? p.bias[e] : 0.0f);
     }
     __syncthreads();
@@ -469,7 +471,7 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const DecodeParams
           if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
         }
         if (bi >= p.E) bi = 0;
-        const float pr = 1.0f / (1.0f + expf(-__ldcg(p.scores + (size_t)t * p.E + bi)));
+        const float pr = probs[(size_t)t * p.E + bi];
         psum += pr;
         if (lane == j) { psel = pr; isel = bi; }
         __syncwarp();
