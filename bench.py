@@ -134,7 +134,7 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- oracle timing
 
-def oracle_sample(cfg: int, T: int, budget_s: float = 20.0, threads=None):
+def oracle_sample(cfg: int, T: int, budget_s: float = 20.0, threads=None, max_tokens: int = 16):
     """Time the oracle on the host cores: route + layer for T tokens of the
     workload, layer by layer, until the layers are done or the budget is spent.
     Returns (tokens/s through the whole layer stack, cores, description)."""
@@ -143,6 +143,8 @@ def oracle_sample(cfg: int, T: int, budget_s: float = 20.0, threads=None):
     s = synth.SHAPES[cfg]
     seed = synth.seed_of(cfg)
     threads = threads or (os.cpu_count() or 1)
+    T_full = T
+    T = min(T, max_tokens)                       # a bounded sample of the chunk's tokens
     pairs = T * (s.k + s.n_shared)
     cores = max(1, min(threads, pairs))
     spent, layers = 0.0, 0
@@ -163,8 +165,8 @@ def oracle_sample(cfg: int, T: int, budget_s: float = 20.0, threads=None):
             break
     # tokens/s through all L layers, scaled from the layers done
     tps = T * layers / s.L / spent
-    desc = (f"{T} token(s) through {layers} of {s.L} layers (route + layer, exact fp64), "
-            f"{spent:.1f} s, scaled to the full stack")
+    desc = (f"{T} of {T_full} token(s) through {layers} of {s.L} layers (route + layer, exact "
+            f"fp64), {spent:.1f} s, scaled to the full stack")
     return tps, cores, desc
 
 
@@ -271,6 +273,10 @@ def run_libmoe(args):
         ids_by_set.append(ids.cpu().numpy().copy())
     eb = s.expert_bytes()
     router_bytes = s.E * s.H * 2
+    # algorithmic FLOPs per layer: 3 matrices x 2 x H x F per (token, expert)
+    valid_pairs = [(a[l] >= 0).sum() for a in ids_by_set for l in range(s.L)]
+    flops_layer = 2.0 * 3.0 * s.H * (float(np.mean(valid_pairs)) * s.F +
+                                     (T * s.Fs if s.n_shared else 0))
     bytes_set = []
     for a in ids_by_set:
         tot = 0
@@ -343,6 +349,7 @@ def run_libmoe(args):
     value = tokens * 1000.0 / ms
     step_gbs = bytes_per_step / (ms * 1e-3) / 1e9
     achieved = layer_bytes / (layer_ms * 1e-3) / 1e9
+    tflops = flops_layer / (layer_ms * 1e-3) / 1e12
 
     # ---- end to end through the public API with host buffers
     e2e = None
@@ -385,7 +392,8 @@ def run_libmoe(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "iq4_nl weights x int16 activations, exact int dot, f32 accumulate",
+            "dtype": ("iq4_nl weights x int16 activations, exact int dot, f32 accumulate"
+                      if not prefill else "fp16 x fp16 -> f32 (tcgen05 kind::f16)"),
             "data": "synthetic (seeded; shapes of the pages' models)",
             "config": {"workload": s.name, "tokens_per_step": T, "layers": s.L,
                        "input_sets": N_SETS, "graph": "one CUDA graph per step, PDL between "
@@ -395,12 +403,19 @@ def run_libmoe(args):
                        "parallelism": f"replicas x{world}"},
             "hbm_gbs": step_gbs, "hbm_frac_of_measured": step_gbs / hbm,
             "bytes_per_step": bytes_per_step,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                         "frac": achieved / hbm, "traffic": traffic,
-                         "kernel": "moe_iq4nl_decode (the layer without routing), per call"
-                                   if not prefill else "moe_iq4nl_prefill_grouped",
-                         "peak_kind": peak_kind, "avg_call_ms": layer_ms,
-                         "algorithmic_bytes_per_call": layer_bytes},
+            "roofline": ({"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                          "frac": achieved / hbm, "traffic": traffic,
+                          "kernel": "moe_iq4nl_decode (the layer without routing), per call",
+                          "peak_kind": peak_kind, "avg_call_ms": layer_ms,
+                          "algorithmic_bytes_per_call": layer_bytes}
+                         if not prefill else
+                         {"bound": "tensor", "achieved": tflops, "peak": bf16, "unit": "TFLOP/s",
+                          "frac": tflops / bf16, "traffic": traffic,
+                          "kernel": "moe_iq4nl_prefill_grouped (bucket, gather, tcgen05 gate/up "
+                                    "and down GEMMs, combine), per call",
+                          "peak_kind": peak_kind + " (cuBLAS bf16 dense; kind::f16 fp16 has the "
+                                       "same rate)",
+                          "avg_call_ms": layer_ms, "algorithmic_flops_per_call": flops_layer}),
             "route_call_ms": route_ms,
             "step_call": "moe_iq4nl_prefill_grouped after moe_route_topk" if prefill else
                          "moe_iq4nl_decode_routed (route + layer in one call)",

@@ -433,20 +433,39 @@ pf_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
       if (GATEUP) mat = sh ? (part ? p.s1 : p.s0) : (part ? p.a1 : p.a0);
       else mat = sh ? p.s0 : p.a0;
       const uint8_t* row = mat + ((sh ? 0 : (size_t)ti.bucket * M) + ti.m0 + r) * rb;
-      uint32_t wnext[9];
-      {
-        const uint32_t* src = reinterpret_cast<const uint32_t*>(row);
+      // Raw IQ4_NL bytes of this thread's row, four K-steps (144 bytes) per
+      // load group, double-buffered in registers; rows whose length is not a
+      // multiple of four pairs use 4-byte loads.
+      const int nks = K / kTK;
+      const bool vec = (nks & 3) == 0;
+      uint4 cur[9], nxt[9];
+      auto load_group = [&](int g, uint4 (&dst)[9]) {
+        const uint4* src = reinterpret_cast<const uint4*>(row + (size_t)g * 4 * kPairB);
 #pragma unroll
-        for (int i = 0; i < 9; ++i) wnext[i] = __ldg(src + i);
-      }
-      for (int ks = 0; ks < K / kTK; ++ks, ++it) {
+        for (int i = 0; i < 9; ++i) dst[i] = __ldg(src + i);
+      };
+      if (vec) load_group(0, nxt);
+      for (int ks = 0; ks < nks; ++ks, ++it) {
         uint32_t w[9];
+        if (vec) {
+          const int j = ks & 3;
+          if (j == 0) {
 #pragma unroll
-        for (int i = 0; i < 9; ++i) w[i] = wnext[i];
-        if (ks + 1 < K / kTK) {
-          const uint32_t* src = reinterpret_cast<const uint32_t*>(row + (size_t)(ks + 1) * kPairB);
+            for (int i = 0; i < 9; ++i) cur[i] = nxt[i];
+            if (ks + 4 < nks) load_group((ks >> 2) + 1, nxt);
+          }
+          const uint32_t* cw = reinterpret_cast<const uint32_t*>(cur);
 #pragma unroll
-          for (int i = 0; i < 9; ++i) wnext[i] = __ldg(src + i);
+          for (int i = 0; i < 9; ++i) {
+            // word 9j+i of the 36-word group, with j only known at run time:
+            // select among the four compile-time candidates
+            const uint32_t c0 = cw[i], c1 = cw[9 + i], c2 = cw[18 + i], c3 = cw[27 + i];
+            w[i] = j == 0 ? c0 : (j == 1 ? c1 : (j == 2 ? c2 : c3));
+          }
+        } else {
+          const uint32_t* src = reinterpret_cast<const uint32_t*>(row + (size_t)ks * kPairB);
+#pragma unroll
+          for (int i = 0; i < 9; ++i) w[i] = __ldg(src + i);
         }
         const int s = it % S::kStages;
         if (!mbar_wait(&empty[s], ((it / S::kStages) & 1) ^ 1, p.status)) { ok = false; break; }
