@@ -157,6 +157,38 @@ moe_status moe_iq4nl_decode_routed(const moe_shape* shape, const uint16_t* route
                                    float* y, void* ws, size_t ws_bytes, uint32_t* status,
                                    void* stream);
 
+/* Decode without a caller-provided workspace. This call has no counterpart on
+ * the pages; it is a convenience of this library. It exists for callers that
+ * cannot allocate device memory at the point where they run the layer: code
+ * that runs while another component captures the stream into a CUDA graph
+ * with its own memory pool, hosts that embed the library behind an allocator
+ * they do not control, and runtimes that plan all device memory up front.
+ *
+ * It computes exactly what moe_iq4nl_decode computes (same arguments minus the
+ * workspace, same outputs, same arithmetic), on a scratch area that is part of
+ * the library: a fixed device array of MOE_STATIC_SCRATCH_BYTES (8 MiB) on
+ * every GPU that loads the library, held until the process exits. It allocates
+ * and frees nothing. A shape and token count whose
+ * moe_workspace_bytes(shape, T, 0) exceeds that size is refused with
+ * MOE_ERR_UNSUPPORTED (use moe_iq4nl_decode with your own workspace instead).
+ *
+ *  - Set-up: the first call on each device (with that device current) looks
+ *    up the scratch's device address once (cudaGetSymbolAddress) and keeps it;
+ *    a failure there returns MOE_ERR_CUDA. Make that first call before any
+ *    stream capture begins.
+ *  - Each call first clears the scratch's counter words on `stream` (a
+ *    stream-ordered memset), then launches the decode kernels.
+ *  - There is ONE scratch per device, shared by every caller in the process.
+ *    Calls whose work may overlap on the GPU (other streams, other threads
+ *    without ordering between their streams) race on it and give wrong
+ *    results. Order them on one stream, or use moe_iq4nl_decode with a
+ *    workspace each. */
+#define MOE_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
+moe_status moe_iq4nl_decode_static(const moe_shape* shape, const moe_expert_weights* w,
+                                   const uint16_t* x, int32_t T, const int32_t* ids,
+                                   const float* weights, float* y, uint32_t* status,
+                                   void* stream);
+
 /* Prefill: the whole layer for a chunk of 1..max_tokens tokens. Tokens are
  * bucketed by expert with a counting sort (no atomics decide any order), each
  * expert's tokens run as one grouped tensor-core contraction (tcgen05,

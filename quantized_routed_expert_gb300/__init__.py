@@ -37,6 +37,7 @@ MOE_ERR_CUDA = -5
 STATUS_INVALID_ROUTE_MASK = 0x0000FFFF
 STATUS_TIMEOUT = 0x80000000
 MAX_DECODE_TOKENS = 16
+STATIC_SCRATCH_BYTES = 8 << 20
 DECODE, PREFILL = 0, 1
 
 
@@ -65,6 +66,9 @@ _lib.moe_iq4nl_decode_routed.argtypes = [ctypes.POINTER(Shape), _P, _P, ctypes.P
                                          _P, ctypes.c_int32, _P, _P, _P, _P, ctypes.c_size_t, _P,
                                          _P]
 _lib.moe_iq4nl_decode_routed.restype = ctypes.c_int
+_lib.moe_iq4nl_decode_static.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(_Weights), _P,
+                                         ctypes.c_int32, _P, _P, _P, _P, _P]
+_lib.moe_iq4nl_decode_static.restype = ctypes.c_int
 _lib.moe_iq4nl_dequantize.argtypes = [_P, ctypes.c_int64, ctypes.c_int32, _P, _P]
 _lib.moe_iq4nl_dequantize.restype = ctypes.c_int
 _lib.moe_sanitize_routes.argtypes = [_P, _P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P, _P]
@@ -78,7 +82,7 @@ _lib.moe_status_string.restype = ctypes.c_char_p
 _lib.moe_version.restype = ctypes.c_char_p
 
 EXPORTS = ("moe_route_topk", "moe_workspace_bytes", "moe_iq4nl_decode", "moe_iq4nl_decode_routed",
-           "moe_iq4nl_prefill_grouped", "moe_iq4nl_dequantize", "moe_sanitize_routes",
+           "moe_iq4nl_decode_static", "moe_iq4nl_prefill_grouped", "moe_iq4nl_dequantize", "moe_sanitize_routes",
            "moe_launches_per_call", "moe_set_pdl", "moe_status_string", "moe_version")
 
 
@@ -206,6 +210,27 @@ def iq4nl_decode(shape: Shape, w: ExpertWeights, x, ids, weights, ws, y=None, st
     """Decode 1..16 tokens: y fp32 [T,H]."""
     return _layer(_lib.moe_iq4nl_decode, "moe_iq4nl_decode", shape, w, x, ids, weights, y, ws,
                   status, stream)
+
+
+def iq4nl_decode_static(shape: Shape, w: ExpertWeights, x, ids, weights, y=None, status=None,
+                        stream=None):
+    """Decode 1..16 tokens on the library's own fixed scratch (no workspace
+    argument, nothing allocated by libmoe). For callers that cannot allocate
+    device memory where they run the layer. One scratch per device: calls that
+    may overlap on the GPU race, so keep them on one stream. The first call on
+    a device sets the scratch up and should come before any stream capture.
+    Pass ``y`` to keep this wrapper from allocating the output itself."""
+    _dev(x, torch.bfloat16, "x")
+    _dev(ids, torch.int32, "ids")
+    _dev(weights, torch.float32, "weights")
+    T = x.shape[0]
+    if y is None:
+        y = torch.empty((T, shape.hidden), dtype=torch.float32, device=x.device)
+    _dev(y, torch.float32, "y")
+    _check(_lib.moe_iq4nl_decode_static(ctypes.byref(shape), ctypes.byref(w.c), _ptr(x), int(T),
+                                        _ptr(ids), _ptr(weights), _ptr(y), _ptr(status),
+                                        _stream(stream)), "moe_iq4nl_decode_static")
+    return y
 
 
 def iq4nl_decode_routed(shape: Shape, router_w, router_bias, w: ExpertWeights, x, ws, ids=None,

@@ -69,3 +69,23 @@ def test_pdl_switch_round_trips(lib):
     import quantized_routed_expert_gb300 as moe
     prev = moe.set_pdl(False)
     assert moe.set_pdl(prev) is False
+
+
+def test_static_decode_checks_on_the_host(lib):
+    # Refusals happen before any CUDA call, so they answer without a GPU.
+    import quantized_routed_expert_gb300 as moe
+    P = ctypes.c_void_p
+    fn = lib.moe_iq4nl_decode_static
+    fn.argtypes = [ctypes.POINTER(moe.Shape), P, P, ctypes.c_int32, P, P, P, P, P]
+    fn.restype = ctypes.c_int
+    big = moe.make_shape(8192, 8192, 64, 16)                     # 16 tokens need > 8 MiB
+    assert moe.workspace_bytes(big, 16, moe.DECODE) > moe.STATIC_SCRATCH_BYTES
+    assert fn(ctypes.byref(big), None, None, 16, None, None, None, None, None) == \
+        moe.MOE_ERR_UNSUPPORTED
+    small = moe.make_shape(3584, 1024, 64, 4)
+    assert fn(ctypes.byref(small), None, None, 1, None, None, None, None, None) == \
+        moe.MOE_ERR_INVALID_ARG
+    assert fn(ctypes.byref(small), None, None, 17, None, None, None, None, None) == \
+        moe.MOE_ERR_INVALID_ARG
+    assert fn(ctypes.byref(small), None, None, 0, None, None, None, None, None) == \
+        moe.MOE_ERR_INVALID_ARG                                  # T == 0 still wants weights
