@@ -27,17 +27,22 @@ constexpr uint32_t kTab3 = 0x71594535u;
 
 // Eight 4-bit codes (one 32-bit word of a block's index bytes) to eight int8
 // table values. Bytes of r0: T[c0], T[c1], T[c2], T[c3]; r1: T[c4..c7], where c
-// are the nibbles from least significant up. Each byte_perm picks from one half
-// of the table; a third byte_perm keeps, per byte, the half that bit 3 names.
+// are the nibbles from least significant up. One prmt picks from the lower half
+// of the table (T[0..7]) and one from the upper half (T[8..15]) by the low three
+// bits of each code; a third keeps, per byte, the half that bit 3 names. The
+// selector nibbles handed to prmt have bit 3 clear (prmt's sign-replicate mode
+// stays off).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
 __device__ __forceinline__ void iq4_lookup8(uint32_t q, uint32_t& r0, uint32_t& r1) {
-  const uint32_t sel = 0x32103210u | ((q & 0x88888888u) >> 1);
-  const uint32_t lo0 = __byte_perm(kTab0, kTab1, q);
-  const uint32_t hi0 = __byte_perm(kTab2, kTab3, q);
-  r0 = __byte_perm(lo0, hi0, sel);
-  const uint32_t q1 = q >> 16;
-  const uint32_t lo1 = __byte_perm(kTab0, kTab1, q1);
-  const uint32_t hi1 = __byte_perm(kTab2, kTab3, q1);
-  r1 = __byte_perm(lo1, hi1, sel >> 16);
+  const uint32_t qm = q & 0x77777777u;
+  const uint32_t sel = 0x32103210u | ((q >> 1) & 0x44444444u);
+  r0 = prmt(prmt(kTab0, kTab1, qm), prmt(kTab2, kTab3, qm), sel);
+  const uint32_t qm1 = qm >> 16;
+  r1 = prmt(prmt(kTab0, kTab1, qm1), prmt(kTab2, kTab3, qm1), sel >> 16);
 }
 
 // Exact integer dot product of one block's 32 table values (8 words from
@@ -157,6 +162,24 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
           "r"(smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// An L2 policy that marks lines evict-first: for data read once per call
+// (streamed expert weights), so that it does not push out what is reused (the
+// kernel's own instructions, activations, routes, h).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// bulk_g2s with an L2 cache policy on the global reads.
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
 

@@ -181,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, 2) gateup_kernel(const DecodeParams 
   if (warp == kProducerWarp) {
     // Producer: one lane issues the bulk copies; shared-expert rows first (they
     // do not depend on the routes), then this CTA's share of the routed rows.
+    const uint64_t pol = l2_evict_first_policy();   // weights: read once per call
     int it = 0;
     bool ok = true;
     auto issue = [&](const Chunk& c, const uint8_t* gbase, const uint8_t* ubase, int64_t row0) {
@@ -190,8 +191,8 @@ __global__ void __launch_bounds__(kThreads, 2) gateup_kernel(const DecodeParams 
       const uint32_t bytes = (uint32_t)(c.rows * rb);
       uint8_t* dst = ring + (size_t)s * L.stage;
       mbar_arrive_expect_tx(&full[s], 2 * bytes);
-      bulk_g2s(dst, gbase + (row0 + c.f0) * rb, bytes, &full[s]);
-      bulk_g2s(dst + bytes, ubase + (row0 + c.f0) * rb, bytes, &full[s]);
+      bulk_g2s_hint(dst, gbase + (row0 + c.f0) * rb, bytes, &full[s], pol);
+      bulk_g2s_hint(dst + bytes, ubase + (row0 + c.f0) * rb, bytes, &full[s], pol);
       ++it;
       return true;
     };
@@ -347,6 +348,7 @@ __global__ void __launch_bounds__(kThreads, 2) down_kernel(const DecodeParams p)
           bulk_g2s(dst + (size_t)j * rbytes, src, rbytes, &full[s]);
         }
       };
+      const uint64_t pol = l2_evict_first_policy();   // weights: read once per call
       int it = 0;
       bool waited = false;
       StageIt si = stage_first(p, rt);
@@ -359,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 2) down_kernel(const DecodeParams p)
         int np;
         desc(si, wsrc, wbytes, np, rbytes);
         mbar_arrive_expect_tx(&full[s], wbytes + np * rbytes);
-        if (wbytes) bulk_g2s(ring + (size_t)s * L.stage, wsrc, wbytes, &full[s]);
+        if (wbytes) bulk_g2s_hint(ring + (size_t)s * L.stage, wsrc, wbytes, &full[s], pol);
         if (waited) issue_recs(si, s);
         ++it;
         stage_next(p, rt, si);

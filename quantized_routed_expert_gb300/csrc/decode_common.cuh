@@ -15,6 +15,11 @@ __device__ __forceinline__ void bar_sync() {
   asm volatile("bar.sync %0, %1;" ::"n"(BAR), "n"(NT) : "memory");
 }
 
+// A named barrier over n threads (n a multiple of 32), id and n at run time.
+__device__ __forceinline__ void bar_sync_n(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Route table built in shared memory from ids (route sanitising: an id outside
 // [0, E) is dropped, i.e. routed to expert 0 with weight 0).
@@ -99,6 +104,123 @@ __device__ void build_route_table(RouteTable& rt, const int32_t* __restrict__ id
   bar_sync<BAR, NT>();
 }
 
+// The same table built by one warp, for P <= 64 pairs (T <= 4 tokens): two
+// pairs per lane, ranks by shuffles, slot boundaries by ballots. No CTA
+// barrier; the caller synchronises before other warps read the table.
+// (bitmap and word_off are not filled.)
+__device__ __forceinline__ void build_route_table_warp(RouteTable& rt,
+                                                       const int32_t* __restrict__ ids,
+                                                       const float* __restrict__ wts, int P,
+                                                       int E) {
+  const int lane = threadIdx.x & 31;
+  const int p1 = lane + 32;
+  int e0 = -1, e1 = -1;
+  if (lane < P) {
+    const int id = ids[lane];
+    e0 = id >= 0 && id < E ? id : -1;
+    rt.sid[lane] = e0;
+    rt.wt[lane] = e0 >= 0 ? wts[lane] : 0.0f;
+  }
+  if (p1 < P) {
+    const int id = ids[p1];
+    e1 = id >= 0 && id < E ? id : -1;
+    rt.sid[p1] = e1;
+    rt.wt[p1] = e1 >= 0 ? wts[p1] : 0.0f;
+  }
+  const int inv = __popc(__ballot_sync(0xFFFFFFFFu, lane < P && e0 < 0)) +
+                  __popc(__ballot_sync(0xFFFFFFFFu, p1 < P && e1 < 0));
+  // stable rank by (expert, pair index) among the valid pairs
+  int r0 = 0, r1 = 0;
+#pragma unroll 1
+  for (int q = 0; q < P; ++q) {
+    const int eq = __shfl_sync(0xFFFFFFFFu, q < 32 ? e0 : e1, q & 31);
+    if (eq >= 0) {
+      r0 += (eq < e0) || (eq == e0 && q < lane);
+      r1 += (eq < e1) || (eq == e1 && q < p1);
+    }
+  }
+  if (lane < P && e0 >= 0) rt.list[r0] = lane;
+  if (p1 < P && e1 >= 0) rt.list[r1] = p1;
+  __syncwarp();
+  const int nv = P - inv;
+  int es0 = -1, es1 = -1;
+  bool f0 = false, f1 = false;
+  if (lane < nv) {
+    es0 = rt.sid[rt.list[lane]];
+    f0 = lane == 0 || rt.sid[rt.list[lane - 1]] != es0;
+  }
+  if (p1 < nv) {
+    es1 = rt.sid[rt.list[p1]];
+    f1 = rt.sid[rt.list[p1 - 1]] != es1;
+  }
+  const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, f0);
+  const uint32_t b1 = __ballot_sync(0xFFFFFFFFu, f1);
+  const uint32_t below = (1u << lane) - 1u;
+  if (f0) {
+    const int sl = __popc(b0 & below);
+    rt.slot_expert[sl] = es0;
+    rt.slot_off[sl] = lane;
+  }
+  if (f1) {
+    const int sl = __popc(b0) + __popc(b1 & below);
+    rt.slot_expert[sl] = es1;
+    rt.slot_off[sl] = p1;
+  }
+  if (lane == 0) {
+    const int ns = __popc(b0) + __popc(b1);
+    rt.n_slots = ns;
+    rt.slot_off[ns] = nv;
+    rt.n_valid = nv;
+    rt.invalid = inv;
+  }
+  __syncwarp();
+}
+
+// Top-k of one token by one warp. keys[E] (shared memory) are p + b and are
+// consumed: each chosen entry is set to -inf. probs[E] are the sigmoids.
+// The choice: the largest key, ties to the lower index; a NaN key is never
+// chosen (if no key is left, expert 0). Lane j < k returns the j-th id and
+// its renormalised weight; the sum of the chosen p runs in choice order.
+__device__ __forceinline__ uint32_t ordered_key_bits(float k) {
+  const uint32_t u = __float_as_uint(k + 0.0f);       // -0 -> +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+// Lane-local best key over e = lane, lane + 32, ... (strict >: the lowest
+// index among equal keys; NaN never wins). Returns E when none is left.
+__device__ __forceinline__ int lane_best(const float* keys, int E, float& best) {
+  best = -INFINITY;
+  int be = E;
+#pragma unroll 1
+  for (int e = (int)(threadIdx.x & 31); e < E; e += 32) {
+    const float kv = keys[e];
+    if (kv > best) { best = kv; be = e; }
+  }
+  return be;
+}
+__device__ __forceinline__ int2 warp_topk(float* keys, const float* probs, int E, int k) {
+  const int lane = threadIdx.x & 31;
+  float best;
+  int be = lane_best(keys, E, best);
+  float psum = 0.0f, psel = 0.0f;
+  int isel = 0;
+#pragma unroll 1
+  for (int j = 0; j < k; ++j) {
+    const uint32_t ok = be < E ? ordered_key_bits(best) : 0u;
+    const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, ok);
+    const uint32_t cand = (mx != 0u && ok == mx) ? (uint32_t)be : 0xFFFFFFFFu;
+    uint32_t bi = __reduce_min_sync(0xFFFFFFFFu, cand);
+    if (bi >= (uint32_t)E) bi = 0;
+    const float pr = probs[bi];
+    psum += pr;
+    if (lane == j) { psel = pr; isel = (int)bi; }
+    if ((int)(bi & 31u) == lane) {
+      keys[bi] = -INFINITY;
+      be = lane_best(keys, E, best);
+    }
+  }
+  return make_int2(isel, __float_as_int(psel / psum));
+}
+
 __host__ __device__ __forceinline__ size_t align_up_dev(size_t v, size_t a) {
   return (v + a - 1) / a * a;
 }
@@ -124,9 +246,14 @@ __device__ __forceinline__ int qv_u4(int q, int c, int lpr) { return qv_base(q, 
 // butterfly), at most 8 (a lane then walks several block pairs of its row) and
 // at most the number of block pairs in the row.
 __host__ __device__ __forceinline__ int dlanes_per_row(int K) {
+#ifdef __CUDA_ARCH__
+  const int m = (K >> 6) < 8 ? (K >> 6) : 8;      // K is a multiple of 64
+  return 1 << (31 - __clz(m));
+#else
   int l = 8;
   while (l > K / 64) l >>= 1;
   return l;
+#endif
 }
 __host__ __device__ __forceinline__ int dqvec_pair_words(int K) {
   const int lpr = dlanes_per_row(K);
@@ -154,6 +281,80 @@ __device__ __forceinline__ void quant_block_store(float v, int b, int K, uint32_
   if (lane == 0) reinterpret_cast<float*>(rec + dqvec_pair_words(K))[b] = quant_scale(emax);
 }
 
+
+// The same quantisation of one 32-value block done by a single lane (the 32
+// values in registers): the largest exponent, the 16 pair words as four
+// 16-byte stores, the scale. rec 16-byte aligned.
+__device__ __forceinline__ void quant_store_lane(const float (&v)[32], int b, int K,
+                                                 uint32_t* rec) {
+  uint32_t emax = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const uint32_t e = (__float_as_uint(v[i]) >> 23) & 0xFFu;
+    emax = e > emax ? e : emax;
+  }
+  const int lpr = dlanes_per_row(K);
+  const int q = b >> 1, c0 = 4 * (b & 1);
+  uint4* r4 = reinterpret_cast<uint4*>(rec);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int j = 4 * c + i;
+      w[i] = (uint32_t)(quant_one(v[j], emax) & 0xFFFF) |
+             ((uint32_t)quant_one(v[j + 16], emax) << 16);
+    }
+    r4[qv_u4(q, c0 + c, lpr)] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  reinterpret_cast<float*>(rec + dqvec_pair_words(K))[b] = quant_scale(emax);
+}
+
+// Lane-per-block quantisation of fp32 data in global memory (read through L2:
+// written by other CTAs of this grid). src 16-byte aligned.
+static __device__ __noinline__ void quant_f32_block_lane(const float* src, int b, int K,
+                                                  uint32_t* rec) {
+  float v[32];
+  const float4* s4 = reinterpret_cast<const float4*>(src);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 f = __ldcg(s4 + i);
+    v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+  }
+  quant_store_lane(v, b, K, rec);
+}
+
+// Lane-per-block quantisation of 32 bf16 values (16-byte aligned) in global memory.
+static __device__ __noinline__ void quant_bf16_block_lane(const uint16_t* src, int b, int K,
+                                                   uint32_t* rec) {
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  uint4 r[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) r[u] = __ldcg(s4 + u);
+  float v[32];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const uint32_t w4[4] = {r[u].x, r[u].y, r[u].z, r[u].w};
+#pragma unroll
+    for (int i2 = 0; i2 < 4; ++i2) {
+      v[8 * u + 2 * i2] = __uint_as_float(w4[i2] << 16);
+      v[8 * u + 2 * i2 + 1] = __uint_as_float(w4[i2] & 0xFFFF0000u);
+    }
+  }
+  quant_store_lane(v, b, K, rec);
+}
+
+// Quantise T bf16 rows of K values (16-byte aligned) into records in shared
+// memory, one 32-value block per thread; threads tid, tid + nt, ... of the CTA.
+__device__ __forceinline__ void quant_x_lanes(const uint16_t* __restrict__ x, int T, int K,
+                                              uint32_t* xq, int xq_words, int tid, int nt) {
+  const int nb = K / 32;
+#pragma unroll 1
+  for (int i = tid; i < T * nb; i += nt) {
+    const int t = i / nb, b = i - t * nb;
+    quant_bf16_block_lane(x + (size_t)t * K + b * 32, b, K, xq + (size_t)t * xq_words);
+  }
+}
 
 // Quantise T bf16 rows of K values into records in shared memory. Each lane
 // loads 8 consecutive values (16 bytes); four lanes form one 32-value block, so
@@ -336,5 +537,40 @@ inline __device__ void flush_arrivals(const DecodeParams& p, const RouteTable& r
   pd.n = 0;
 }
 
+
+// Quantise every h row of this call from global memory into records in
+// shared memory, in the layout the down units read: the routed pairs' records
+// (indexed by pair), then the shared expert's (by token). One 32-value block
+// per thread, all of the CTA's threads at once.
+__device__ __forceinline__ void quant_h_to_smem(const DecodeParams& p, const RouteTable& rt,
+                                                uint32_t* recs, int tid, int nt) {
+  const int nbF = p.F / 32;
+  const int nbS = p.n_shared ? p.Fs / 32 : 1;
+  const int wF = dqvec_words(p.F);
+  const int wS = p.n_shared ? dqvec_words(p.Fs) : 0;
+  uint32_t* rec_sh = recs + (size_t)p.T * p.k * wF;
+  const int nr = rt.n_valid * nbF;
+  const int total = nr + (p.n_shared ? p.T * nbS : 0);
+#pragma unroll 1
+  for (int i = tid; i < total; i += nt) {
+    const float* src;
+    uint32_t* dst;
+    int b, K;
+    if (i < nr) {
+      const int e = i / nbF;
+      b = i - e * nbF;
+      K = p.F;
+      src = p.h_r + (size_t)rt.list[e] * p.F + b * 32;
+      dst = recs + (size_t)rt.list[e] * wF;
+    } else {
+      const int j = (i - nr) / nbS;
+      b = (i - nr) - j * nbS;
+      K = p.Fs;
+      src = p.h_s + (size_t)j * p.Fs + b * 32;
+      dst = rec_sh + (size_t)j * wS;
+    }
+    quant_f32_block_lane(src, b, K, dst);
+  }
+}
 
 }  // namespace moe

@@ -75,26 +75,30 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
 }
 
 // One gate/up unit: the warp's f-row (gate row at `g`, up row at `u`) for every
-// token of the slot; writes h (fp32) for each (token, slot) pair.
-template <int MAXT>
-__device__ __forceinline__ void gateup_unit(const DecodeParams& p, const RouteTable& rt,
-                                            const uint8_t* g, const uint8_t* u, int slot, int f,
-                                            const uint32_t* xq, int xq_words) {
+// token of the slot; writes h (fp32) for each (token, slot) pair. LPR is the
+// interleave width of the quantised x records (dlanes_per_row(H)); 0 = known
+// only at run time.
+template <int MAXT, int LPR>
+__device__ __noinline__ void gateup_unit_t(const DecodeParams& p, const RouteTable& rt,
+                                           const uint8_t* g, const uint8_t* u, int slot, int f,
+                                           const uint32_t* xq, int xq_words) {
   const int lane = threadIdx.x & 31;
   const int H = p.H;
-  const int npairs = H / 64;
-  const int lpr = dlanes_per_row(H);
+  const int npairs = H >> 6;
+  const int lpr = LPR ? LPR : dlanes_per_row(H);
   const bool shared = slot < 0;
   const int ntok = shared ? p.T : rt.slot_off[slot + 1] - rt.slot_off[slot];
   const int lbase = shared ? 0 : rt.slot_off[slot];
   const int xs_off = dqvec_pair_words(H);
+#pragma unroll 1
   for (int g0 = 0; g0 < ntok; g0 += MAXT) {
     const int ng = ntok - g0 < MAXT ? ntok - g0 : MAXT;
-    int tok[MAXT];
+    const uint32_t* rec[MAXT];
 #pragma unroll
     for (int j = 0; j < MAXT; ++j) {
       const int jj = g0 + (j < ng ? j : 0);
-      tok[j] = shared ? jj : rt.list[lbase + jj] / p.k;
+      const int tok = shared ? jj : rt.list[lbase + jj] / p.k;
+      rec[j] = xq + (size_t)tok * xq_words;
     }
     float ag[MAXT], au[MAXT];
 #pragma unroll
@@ -122,24 +126,22 @@ __device__ __forceinline__ void gateup_unit(const DecodeParams& p, const RouteTa
 #pragma unroll
       for (int j = 0; j < MAXT; ++j) {
         if (j < ng) {
-          const uint32_t* rec = xq + (size_t)tok[j] * xq_words;
-          const uint4* r4 = reinterpret_cast<const uint4*>(rec) + qbase;
+          const uint4* r4 = reinterpret_cast<const uint4*>(rec[j]) + qbase;
           uint32_t v[32];
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const uint4 t4 = r4[c * lpr];
             v[4 * c] = t4.x; v[4 * c + 1] = t4.y; v[4 * c + 2] = t4.z; v[4 * c + 3] = t4.w;
           }
-          const float* xs = reinterpret_cast<const float*>(rec + xs_off);
-          const float s0 = xs[2 * q], s1 = xs[2 * q + 1];
+          const float2 sc = reinterpret_cast<const float2*>(rec[j] + xs_off)[q];
           const int ig0 = iq4_dot_block(tg0, v);
           const int ig1 = iq4_dot_block(tg1, v + 16);
           const int iu0 = iq4_dot_block(tu0, v);
           const int iu1 = iq4_dot_block(tu1, v + 16);
-          ag[j] = fmaf((float)ig0, dg0 * s0, ag[j]);
-          ag[j] = fmaf((float)ig1, dg1 * s1, ag[j]);
-          au[j] = fmaf((float)iu0, du0 * s0, au[j]);
-          au[j] = fmaf((float)iu1, du1 * s1, au[j]);
+          ag[j] = fmaf((float)ig0, dg0 * sc.x, ag[j]);
+          ag[j] = fmaf((float)ig1, dg1 * sc.y, ag[j]);
+          au[j] = fmaf((float)iu0, du0 * sc.x, au[j]);
+          au[j] = fmaf((float)iu1, du1 * sc.y, au[j]);
         }
       }
     }
@@ -155,33 +157,42 @@ __device__ __forceinline__ void gateup_unit(const DecodeParams& p, const RouteTa
     for (int j = 0; j < MAXT; ++j) {
       if (j < ng && lane == j) {
         const float hv = silu_mul(ag[j], au[j]);
-        if (shared) p.h_s[(size_t)tok[j] * p.Fs + f] = hv;
+        if (shared) p.h_s[(size_t)(g0 + j) * p.Fs + f] = hv;
         else p.h_r[(size_t)rt.list[lbase + g0 + j] * p.F + f] = hv;
       }
     }
   }
 }
+template <int MAXT>
+__device__ __forceinline__ void gateup_unit(const DecodeParams& p, const RouteTable& rt,
+                                            const uint8_t* g, const uint8_t* u, int slot, int f,
+                                            const uint32_t* xq, int xq_words) {
+  if (dlanes_per_row(p.H) == 8) gateup_unit_t<MAXT, 8>(p, rt, g, u, slot, f, xq, xq_words);
+  else gateup_unit_t<MAXT, 0>(p, rt, g, u, slot, f, xq, xq_words);
+}
 
 // One down unit: rows [r0, r0 + nrows) (CTA-local indices) of the slot's W_d at
 // `wrows`; for every pair of the slot, the row dot products into `part`.
-__device__ __forceinline__ void down_unit(const DecodeParams& p, const RouteTable& rt,
-                                          const uint8_t* wrows, int slot, int r0, int nrows,
-                                          const uint32_t* recs, float* part, int rows_max) {
-  constexpr int NPS = 4;
+// NPS pairs share each decoded block; LPR as for gate/up (0 = run time).
+template <int NPS, int LPR>
+__device__ __noinline__ void down_unit_t(const DecodeParams& p, const RouteTable& rt,
+                                         const uint8_t* wrows, int slot, int r0, int nrows,
+                                         const uint32_t* recs, float* part, int rows_max) {
   const int lane = threadIdx.x & 31;
   const bool shared = slot < 0;
   const int K = shared ? p.Fs : p.F;
-  const int rbK = K / 32 * kBlockB;
-  const int lpr = dlanes_per_row(K);
+  const int rbK = (K >> 5) * kBlockB;
+  const int lpr = LPR ? LPR : dlanes_per_row(K);
   const int rpw = 32 / lpr;
-  const int npq = K / 64;
+  const int npq = K >> 6;
   const int words = dqvec_words(K);
   const int pw = dqvec_pair_words(K);
   const int P = p.T * p.k;
   const int ntok = shared ? p.T : rt.slot_off[slot + 1] - rt.slot_off[slot];
   const int lbase = shared ? 0 : rt.slot_off[slot];
   const uint32_t* rec_sh = recs + (size_t)P * dqvec_words(p.F);
-  const int q0 = lane % lpr;
+  const int q0 = lane & (lpr - 1);
+#pragma unroll 1
   for (int g0 = 0; g0 < ntok; g0 += NPS) {
     const int np = ntok - g0 < NPS ? ntok - g0 : NPS;
     int pidx[NPS];
@@ -197,6 +208,7 @@ __device__ __forceinline__ void down_unit(const DecodeParams& p, const RouteTabl
         rp[j] = recs + (size_t)pidx[j] * words;
       }
     }
+#pragma unroll 1
     for (int rb = 0; rb < nrows; rb += rpw) {
       const int rl = rb + lane / lpr;
       const bool active = rl < nrows;
@@ -228,20 +240,22 @@ __device__ __forceinline__ void down_unit(const DecodeParams& p, const RouteTabl
                 const uint4 t4 = r4[c * lpr];
                 v[4 * c] = t4.x; v[4 * c + 1] = t4.y; v[4 * c + 2] = t4.z; v[4 * c + 3] = t4.w;
               }
-              const float* sc = reinterpret_cast<const float*>(rp[j] + pw);
+              const float2 sc = reinterpret_cast<const float2*>(rp[j] + pw)[q];
               const int i0 = iq4_dot_block(t0, v);
               const int i1 = iq4_dot_block(t1, v + 16);
-              acc[j] = fmaf((float)i0, d0 * sc[2 * q], acc[j]);
-              acc[j] = fmaf((float)i1, d1 * sc[2 * q + 1], acc[j]);
+              acc[j] = fmaf((float)i0, d0 * sc.x, acc[j]);
+              acc[j] = fmaf((float)i1, d1 * sc.y, acc[j]);
             }
           }
         }
       }
 #pragma unroll
       for (int j = 0; j < NPS; ++j)
-        if (j < np)
-          for (int o = lpr >> 1; o > 0; o >>= 1)
-            acc[j] += __shfl_xor_sync(0xFFFFFFFFu, acc[j], o);
+        if (j < np) {
+#pragma unroll
+          for (int o = (LPR ? LPR : 8) >> 1; o > 0; o >>= 1)
+            if (LPR || o < lpr) acc[j] += __shfl_xor_sync(0xFFFFFFFFu, acc[j], o);
+        }
       if (active && q0 == 0) {
 #pragma unroll
         for (int j = 0; j < NPS; ++j)
@@ -250,9 +264,67 @@ __device__ __forceinline__ void down_unit(const DecodeParams& p, const RouteTabl
     }
   }
 }
+template <int NPS>
+__device__ __forceinline__ void down_unit(const DecodeParams& p, const RouteTable& rt,
+                                          const uint8_t* wrows, int slot, int r0, int nrows,
+                                          const uint32_t* recs, float* part, int rows_max) {
+  const int K = slot < 0 ? p.Fs : p.F;
+  if (dlanes_per_row(K) == 8) down_unit_t<NPS, 8>(p, rt, wrows, slot, r0, nrows, recs, part, rows_max);
+  else down_unit_t<NPS, 0>(p, rt, wrows, slot, r0, nrows, recs, part, rows_max);
+}
+
+// What one warp needs to issue the bulk copies of its units: the warp's unit
+// sequence is its shared-expert gate/up rows, then its routed gate/up rows,
+// then its down-row groups (shared expert first, then the routed slots).
+struct UnitPlan {
+  uint8_t* myslots;
+  size_t slot_bytes;
+  uint64_t* mybar;
+  uint64_t pol;
+  int warp, n_sh, n_rt, sh_a, rr_a, ngroups, nrows_cta, dn_a, rg;
+};
+
+// Issue unit j of a warp's sequence into slot j % kFSlots (one lane calls).
+__device__ __noinline__ void issue_unit(const DecodeParams& p, const RouteTable& rt,
+                                        const UnitPlan& u, int j) {
+  const int s = j % kFSlots;
+  uint8_t* dst = u.myslots + (size_t)s * u.slot_bytes;
+  uint64_t* bar = &u.mybar[s];
+  const uint32_t rbH = (uint32_t)(p.H / 32 * kBlockB);
+  if (j < u.n_sh + u.n_rt) {
+    const uint8_t *g, *up;
+    if (j < u.n_sh) {
+      const size_t f = (size_t)(u.sh_a + u.warp + kFW * j);
+      g = p.sh_gate + f * rbH;
+      up = p.sh_up + f * rbH;
+    } else {
+      const int r = u.rr_a + u.warp + kFW * (j - u.n_sh);
+      const int sl = r / p.F, f = r - sl * p.F;
+      const size_t row = (size_t)rt.slot_expert[sl] * p.F + f;
+      g = p.gate + row * rbH;
+      up = p.up + row * rbH;
+    }
+    mbar_arrive_expect_tx(bar, 2 * rbH);
+    bulk_g2s_hint(dst, g, rbH, bar, u.pol);
+    bulk_g2s_hint(dst + rbH, up, rbH, bar, u.pol);
+  } else {
+    const int un = u.warp + kFW * (j - u.n_sh - u.n_rt);
+    const int su = un / u.ngroups, gi = un - su * u.ngroups;
+    const bool sh = p.n_shared && su == 0;
+    const int sl = su - p.n_shared;
+    const int K = sh ? p.Fs : p.F;
+    const int rbK = K / 32 * kBlockB;
+    const int r0 = gi * u.rg;
+    const int nr = u.nrows_cta - r0 < u.rg ? u.nrows_cta - r0 : u.rg;
+    const uint8_t* src = sh ? p.sh_down + (size_t)(u.dn_a + r0) * rbK
+                            : p.down + ((size_t)rt.slot_expert[sl] * p.H + u.dn_a + r0) * rbK;
+    mbar_arrive_expect_tx(bar, (uint32_t)(nr * rbK));
+    bulk_g2s_hint(dst, src, (uint32_t)(nr * rbK), bar, u.pol);
+  }
+}
 
 template <int MAXT, bool ROUTE>
-__global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int H = p.H;
   const int rows_max = p.dn_rows_max;
@@ -275,6 +347,7 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const DecodeParams
   uint64_t* mybar = bars + warp * kFSlots;
 
   if (threadIdx.x == 0) {
+    #pragma unroll 1
     for (int i = 0; i < kFW * kFSlots + 3; ++i) mbar_init(&bars[i], 1);
     mbar_fence_init();
   }
@@ -293,45 +366,26 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const DecodeParams
 
   int issued = 0, consumed = 0;
   bool ok = true;
-  // Issue unit j of this warp's sequence (lane 0 issues; all lanes count).
-  auto issue = [&](int j) {
-    const int s = j % kFSlots;
-    uint8_t* dst = myslots + (size_t)s * L.slot_bytes;
-    if (j < n_sh) {
-      const int f = shr.a + warp + kFW * j;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&mybar[s], 2 * rbH);
-        bulk_g2s(dst, p.sh_gate + (size_t)f * rbH, rbH, &mybar[s]);
-        bulk_g2s(dst + rbH, p.sh_up + (size_t)f * rbH, rbH, &mybar[s]);
-      }
-    } else if (j < n_sh + n_rt) {
-      const int r = rr.a + warp + kFW * (j - n_sh);
-      const int sl = r / p.F, f = r - sl * p.F;
-      const size_t row = (size_t)rt.slot_expert[sl] * p.F + f;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&mybar[s], 2 * rbH);
-        bulk_g2s(dst, p.gate + row * rbH, rbH, &mybar[s]);
-        bulk_g2s(dst + rbH, p.up + row * rbH, rbH, &mybar[s]);
-      }
-    } else {
-      const int u = warp + kFW * (j - n_sh - n_rt);
-      const int su = u / ngroups, gi = u - su * ngroups;
-      const bool sh = p.n_shared && su == 0;
-      const int sl = su - p.n_shared;
-      const int K = sh ? p.Fs : p.F;
-      const int rbK = K / 32 * kBlockB;
-      const int r0 = gi * RG;
-      const int nr = nrows_cta - r0 < RG ? nrows_cta - r0 : RG;
-      const uint8_t* src = sh ? p.sh_down + (size_t)(dn.a + r0) * rbK
-                              : p.down + ((size_t)rt.slot_expert[sl] * H + dn.a + r0) * rbK;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&mybar[s], (uint32_t)(nr * rbK));
-        bulk_g2s(dst, src, (uint32_t)(nr * rbK), &mybar[s]);
-      }
-    }
-  };
+  const uint64_t pol = l2_evict_first_policy();   // weights are read once per call
+  UnitPlan up;
+  up.myslots = myslots;
+  up.slot_bytes = L.slot_bytes;
+  up.mybar = mybar;
+  up.warp = warp;
+  up.n_sh = n_sh;
+  up.n_rt = 0;
+  up.sh_a = shr.a;
+  up.rr_a = 0;
+  up.ngroups = ngroups;
+  up.nrows_cta = nrows_cta;
+  up.dn_a = dn.a;
+  up.rg = RG;
+  up.pol = pol;
   auto issue_upto = [&](int limit) {
-    while (issued < limit && issued - consumed < kFSlots) issue(issued++);
+    while (issued < limit && issued - consumed < kFSlots) {
+      if (lane == 0) issue_unit(p, rt, up, issued);
+      ++issued;
+    }
   };
   auto wait_unit = [&](int j) {
     return mbar_wait(&mybar[j % kFSlots], (uint32_t)((j / kFSlots) & 1), p.status);
@@ -344,7 +398,8 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const DecodeParams
   if (ROUTE && threadIdx.x == 0 && re1 > re0) {
     const uint32_t bytes = (uint32_t)((re1 - re0) * H * 2);
     mbar_arrive_expect_tx(rwr_bar, bytes);
-    bulk_g2s(smem + L.r_wr, p.Wr + (size_t)re0 * H, bytes, rwr_bar);
+    bulk_g2s_hint(smem + L.r_wr, p.Wr + (size_t)re0 * H, bytes, rwr_bar,
+                  l2_evict_first_policy());
   }
   // Shared-expert rows do not depend on the routes: start fetching them too.
   issue_upto(n_sh);
@@ -355,7 +410,7 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const DecodeParams
     mbar_arrive_expect_tx(rx_bar, bytes);
     bulk_g2s(smem + L.r_x, p.x, bytes, rx_bar);
   }
-  quant_x_to_smem(p.x, p.T, H, xq, xq_words, warp, kFW);
+  quant_x_lanes(p.x, p.T, H, xq, xq_words, threadIdx.x, kFT);
 
   if (ROUTE) {
     // Scores of this CTA's experts: 16 chunks of H per expert, one warp per
@@ -367,9 +422,11 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const DecodeParams
       const uint16_t* wr_s = reinterpret_cast<const uint16_t*>(smem + L.r_wr);
       const uint16_t* x_s = reinterpret_cast<const uint16_t*>(smem + L.r_x);
       const int hc = H / 16;                     // chunk length, a multiple of 16
+      #pragma unroll 1
       for (int it = warp; it < ne * 16; it += kFW) {
         const int el = it >> 4, c = it & 15;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        #pragma unroll 1
         for (int g8 = lane; g8 < hc / 8; g8 += 32) {
           const uint4 wv = reinterpret_cast<const uint4*>(wr_s + (size_t)el * H + c * hc)[g8];
           const uint32_t wr[4] = {wv.x, wv.y, wv.z, wv.w};
@@ -392,11 +449,15 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const DecodeParams
         for (int t = 0; t < 4; ++t)
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xFFFFFFFFu, acc[t], o);
-        if (lane == 0)
-          for (int t = 0; t < p.T; ++t) rpart[(el * 16 + c) * p.T + t] = acc[t];
+        if (lane == 0) {
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            if (t < p.T) rpart[(el * 16 + c) * p.T + t] = acc[t];
+        }
       }
     }
     __syncthreads();
+    #pragma unroll 1
     for (int i = threadIdx.x; i < ne * p.T; i += kFT) {
       const int el = i / p.T, t = i - el * p.T;
       float sc = 0.f;
@@ -409,8 +470,7 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const DecodeParams
   }
   __syncthreads();
 
-  Pending pd;
-  pd.n = 0;
+  #pragma unroll 1
   for (int j = 0; ok && j < n_sh; ++j) {
     ok = wait_unit(j);
     if (!ok) break;
@@ -419,16 +479,15 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const DecodeParams
     gateup_unit<MAXT>(p, rt, d, d + rbH, -1, f, xq, xq_words);
     __syncwarp();
     ++consumed;
-    pd.slot[pd.n] = -1;
-    pd.f[pd.n] = f;
-    if (++pd.n == kPendMax) flush_arrivals(p, rt, pd);
     issue_upto(n_sh);
   }
 
   const int32_t* ids_src = p.ids;
   const float* w_src = p.weights;
   if (ROUTE) {
-    // all scores of this call -> top-k, redundantly in every CTA
+    // all scores of this call -> top-k: warp t takes token t, in every CTA
+    int32_t* ids_s = reinterpret_cast<int32_t*>(smem + L.r_ids);
+    float* w_s = reinterpret_cast<float*>(smem + L.r_w);
     if (threadIdx.x == 0) {
       const uint64_t t0 = global_timer_ns();
       while (ld_acquire_u32(&p.sync[2]) < gridDim.x) {
@@ -441,69 +500,53 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const DecodeParams
       __threadfence();
     }
     __syncthreads();
-    float* keys = reinterpret_cast<float*>(smem + L.r_keys);
-    int32_t* ids_s = reinterpret_cast<int32_t*>(smem + L.r_ids);
-    float* w_s = reinterpret_cast<float*>(smem + L.r_w);
-    float* probs = keys + (size_t)p.T * p.E;
+    float* keys_all = reinterpret_cast<float*>(smem + L.r_keys);
+    #pragma unroll 1
     for (int i = threadIdx.x; i < p.T * p.E; i += kFT) {
       const int e = i % p.E;
       const float pr = 1.0f / (1.0f + expf(-__ldcg(p.scores + i)));
-      probs[i] = pr;
-      keys[i] = pr + (p.bias ? p.bias[e] : 0.0f);
+      keys_all[(size_t)p.T * p.E + i] = pr;
+      keys_all[i] = pr + (p.bias ? p.bias[e] : 0.0f);
     }
     __syncthreads();
     if (warp < p.T) {
-      float* kk = keys + (size_t)warp * p.E;
       const int t = warp;
-      float psum = 0.0f, psel = 0.0f;
-      int isel = 0;
-      for (int j = 0; j < p.k; ++j) {
-        float best = -INFINITY;
-        int bi = 0x7FFFFFFF;
-        for (int e = lane; e < p.E; e += 32) {
-          const float kv = kk[e];
-          if (kv > best) { best = kv; bi = e; }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-          const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-          if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
-        }
-        if (bi >= p.E) bi = 0;
-        const float pr = probs[(size_t)t * p.E + bi];
-        psum += pr;
-        if (lane == j) { psel = pr; isel = bi; }
-        __syncwarp();
-        if (lane == 0) kk[bi] = -INFINITY;
-        __syncwarp();
-      }
+      float* keys = keys_all + (size_t)t * p.E;
+      float* probs = keys + (size_t)p.T * p.E;
+      const int2 r = warp_topk(keys, probs, p.E, p.k);
+      const int id = r.x;
+      const float wv = __int_as_float(r.y);
       if (lane < p.k) {
-        ids_s[t * p.k + lane] = isel;
-        w_s[t * p.k + lane] = psel / psum;
+        ids_s[t * p.k + lane] = id;
+        w_s[t * p.k + lane] = wv;
         if (blockIdx.x == 0) {
-          p.ids_out[(size_t)t * p.k + lane] = isel;
-          p.w_out[(size_t)t * p.k + lane] = psel / psum;
+          p.ids_out[(size_t)t * p.k + lane] = id;
+          p.w_out[(size_t)t * p.k + lane] = wv;
         }
       }
+      if (p.T > 1) bar_sync_n(1, p.T * 32);     // the token warps only
     }
-    __syncthreads();
     ids_src = ids_s;
     w_src = w_s;
   }
-  build_route_table<kFT, 0>(rt, ids_src, w_src, p.T * p.k, p.E);
+  if (warp == 0) build_route_table_warp(rt, ids_src, w_src, p.T * p.k, p.E);
+  __syncthreads();
   if (blockIdx.x == 0 && threadIdx.x == 0 && p.status && rt.invalid)
     atomicAdd(p.status, (uint32_t)(rt.invalid < 0xFFFF ? rt.invalid : 0xFFFF));
+  #pragma unroll 1
   for (int i = threadIdx.x; i < (p.T * p.k + (p.n_shared ? p.T : 0)) * rows_max; i += kFT)
     part[i] = 0.0f;
   rr = split_rows(rt.n_slots * p.F, 1, blockIdx.x, gridDim.x);
   n_rt = count(rr.a, rr.b);
+  up.n_rt = n_rt;
+  up.rr_a = rr.a;
   n_dslots = rt.n_slots + p.n_shared;
   const int n_dn_units = n_dslots * ngroups;
   const int n_dn = warp < n_dn_units ? (n_dn_units - warp + kFW - 1) / kFW : 0;
   n_tot = n_sh + n_rt + n_dn;
   issue_upto(n_tot);
 
+  #pragma unroll 1
   for (int j = n_sh; ok && j < n_sh + n_rt; ++j) {
     ok = wait_unit(j);
     if (!ok) break;
@@ -513,14 +556,10 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const DecodeParams
     gateup_unit<MAXT>(p, rt, d, d + rbH, sl, f, xq, xq_words);
     __syncwarp();
     ++consumed;
-    pd.slot[pd.n] = sl;
-    pd.f[pd.n] = f;
-    if (++pd.n == kPendMax) flush_arrivals(p, rt, pd);
     issue_upto(n_tot);
   }
-  if (pd.n) flush_arrivals(p, rt, pd);
 
-  // ---- grid barrier: every h block is quantised once every CTA has arrived
+  // ---- grid barrier: every h row of this call is in global memory
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
@@ -534,19 +573,13 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const DecodeParams
       }
     }
     __threadfence();
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-    // all quantised h records of this call -> shared memory
-    const int P = p.T * p.k;
-    const uint32_t rb = (uint32_t)dqvec_words(p.F) * 4;
-    const uint32_t rbs = p.n_shared ? (uint32_t)dqvec_words(p.Fs) * 4 : 0u;
-    mbar_arrive_expect_tx(recs_bar, P * rb + p.T * rbs);
-    bulk_g2s(recs, p.rec_r, P * rb, recs_bar);
-    if (p.n_shared)
-      bulk_g2s(reinterpret_cast<uint8_t*>(recs) + (size_t)P * rb, p.rec_s, p.T * rbs, recs_bar);
   }
   __syncthreads();
-  ok = ok && mbar_wait(recs_bar, 0, p.status);
+  // every CTA quantises all of h into its own records
+  quant_h_to_smem(p, rt, recs, threadIdx.x, kFT);
+  __syncthreads();
 
+  #pragma unroll 1
   for (int j = n_sh + n_rt; ok && j < n_tot; ++j) {
     ok = wait_unit(j);
     if (!ok) break;
@@ -556,7 +589,7 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const DecodeParams
     const bool sh = p.n_shared && su == 0;
     const int r0 = gi * RG;
     const int nr = nrows_cta - r0 < RG ? nrows_cta - r0 : RG;
-    down_unit(p, rt, d, sh ? -1 : su - p.n_shared, r0, nr, recs, part, rows_max);
+    down_unit<MAXT>(p, rt, d, sh ? -1 : su - p.n_shared, r0, nr, recs, part, rows_max);
     __syncwarp();
     ++consumed;
     issue_upto(n_tot);
@@ -564,10 +597,12 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const DecodeParams
   __syncthreads();
 
   // ---- combine in the fixed order: shared expert, then routed experts ascending
+  #pragma unroll 1
   for (int i = threadIdx.x; i < nrows_cta * p.T; i += kFT) {
     const int t = i / nrows_cta, r = i - t * nrows_cta;
     float acc = 0.0f;
     if (p.n_shared) acc = part[(size_t)(p.T * p.k + t) * rows_max + r];
+    #pragma unroll 1
     for (int e = 0; e < rt.n_valid; ++e) {
       const int pr = rt.list[e];
       if (pr / p.k == t) acc += rt.wt[pr] * part[(size_t)pr * rows_max + r];
