@@ -45,6 +45,70 @@ __device__ __forceinline__ void iq4_lookup8(uint32_t q, uint32_t& r0, uint32_t& 
   r1 = prmt(prmt(kTab0, kTab1, qm1), prmt(kTab2, kTab3, qm1), sel >> 16);
 }
 
+// The table split for single-token dot products, with no per-byte merge:
+// prmt over the lower half T[0..7] with the raw code gives T[c] for c < 8 and
+// -1 for c >= 8 (prmt's sign-replicate mode on a negative entry); prmt over
+// the upper half stored as T[8..15] + 1, with bit 3 of each code flipped, gives
+// T[c] + 1 for c >= 8 and 0 for c < 8 (sign of a positive entry). The two
+// signed bytes sum to T[c] for every code, so a dot product may take both.
+constexpr uint32_t kTabP2 = 0x271A0E02u;   // T[8..11] + 1 = 2, 14, 26, 39
+constexpr uint32_t kTabP3 = 0x725A4636u;   // T[12..15] + 1 = 54, 70, 90, 114
+__device__ __forceinline__ uint32_t iq4_lo4(uint32_t codes) {      // low 16 bits used
+  return prmt(kTab0, kTab1, codes);
+}
+__device__ __forceinline__ uint32_t iq4_hi4(uint32_t flipped) {    // codes ^ 0x8888
+  return prmt(kTabP2, kTabP3, flipped);
+}
+
+// Exact integer dot products of both blocks of a pair (its 36 bytes as nine
+// words, straight from shared memory) with one token's pair-layout vector v[32]
+// (words 0..15 for block 0, 16..31 for block 1), on the split table: no byte
+// realignment and no merge step; each code's value enters as its two parts.
+// Block 0's index bytes are pair bytes 2..17 (aligned word i: the high half of
+// w[i], then the low half of w[i+1]); block 1's are w[5..8].
+__device__ __forceinline__ void iq4_pair_dot1(const uint32_t (&w)[9], const uint32_t* v,
+                                              int& dot0, int& dot1) {
+  int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t lo0 = w[i] >> 16, hi0 = w[i + 1];
+    const uint32_t f0 = lo0 ^ 0x8888u, f1 = hi0 ^ 0x8888u;
+    const uint32_t l0 = iq4_lo4(lo0), l1 = iq4_lo4(hi0);
+    const uint32_t h0 = iq4_hi4(f0), h1 = iq4_hi4(f1);
+    a0 = __dp2a_lo((int)v[4 * i + 0], (int)l0, a0);
+    a1 = __dp2a_hi((int)v[4 * i + 1], (int)l0, a1);
+    a2 = __dp2a_lo((int)v[4 * i + 0], (int)h0, a2);
+    a3 = __dp2a_hi((int)v[4 * i + 1], (int)h0, a3);
+    a0 = __dp2a_lo((int)v[4 * i + 2], (int)l1, a0);
+    a1 = __dp2a_hi((int)v[4 * i + 3], (int)l1, a1);
+    a2 = __dp2a_lo((int)v[4 * i + 2], (int)h1, a2);
+    a3 = __dp2a_hi((int)v[4 * i + 3], (int)h1, a3);
+  }
+  dot0 = (a0 + a1) + (a2 + a3);
+  a0 = a1 = a2 = a3 = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t q = w[5 + i];
+    const uint32_t qf = q ^ 0x88888888u;
+    const uint32_t l0 = iq4_lo4(q), l1 = iq4_lo4(q >> 16);
+    const uint32_t h0 = iq4_hi4(qf), h1 = iq4_hi4(qf >> 16);
+    a0 = __dp2a_lo((int)v[16 + 4 * i + 0], (int)l0, a0);
+    a1 = __dp2a_hi((int)v[16 + 4 * i + 1], (int)l0, a1);
+    a2 = __dp2a_lo((int)v[16 + 4 * i + 0], (int)h0, a2);
+    a3 = __dp2a_hi((int)v[16 + 4 * i + 1], (int)h0, a3);
+    a0 = __dp2a_lo((int)v[16 + 4 * i + 2], (int)l1, a0);
+    a1 = __dp2a_hi((int)v[16 + 4 * i + 3], (int)l1, a1);
+    a2 = __dp2a_lo((int)v[16 + 4 * i + 2], (int)h1, a2);
+    a3 = __dp2a_hi((int)v[16 + 4 * i + 3], (int)h1, a3);
+  }
+  dot1 = (a0 + a1) + (a2 + a3);
+}
+// The two fp16 scales of a pair (as fp32).
+__device__ __forceinline__ void pair_scales(const uint32_t (&w)[9], float& d0, float& d1) {
+  d0 = __half2float(__ushort_as_half((unsigned short)(w[0] & 0xFFFFu)));
+  d1 = __half2float(__ushort_as_half((unsigned short)(w[4] >> 16)));
+}
+
 // Exact integer dot product of one block's 32 table values (8 words from
 // iq4_lookup8 over the 4 index words) with a 32-vector in "pair" layout:
 // word j holds (v_j, v_{j+16}) as two int16. Byte order of the looked-up words
@@ -93,9 +157,13 @@ __device__ __forceinline__ float quant_scale(uint32_t emax) {
   if (emax >= 255u) return __uint_as_float(0x7FC00000u);
   return __uint_as_float((emax - 14u) << 23);
 }
+// Round to nearest even by adding 1.5 * 2^23: |v * factor| <= 2^15, so the sum
+// lies in [2^23, 2^24), where the float spacing is 1 (an FMA and an integer
+// subtract instead of a float-to-int conversion; the same value). v * factor
+// is exact (factor is a power of two), so fusing the multiply changes nothing.
 __device__ __forceinline__ int quant_one(float v, uint32_t emax) {
   if (emax <= 14u || emax >= 255u) return 0;
-  int m = __float2int_rn(v * quant_factor(emax));
+  const int m = __float_as_int(fmaf(v, quant_factor(emax), 12582912.0f)) - 0x4B400000;
   return m > 32767 ? 32767 : m;
 }
 

@@ -185,29 +185,46 @@ __device__ __forceinline__ uint32_t ordered_key_bits(float k) {
   const uint32_t u = __float_as_uint(k + 0.0f);       // -0 -> +0
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
-// Lane-local best key over e = lane, lane + 32, ... (strict >: the lowest
-// index among equal keys; NaN never wins). Returns E when none is left.
-__device__ __forceinline__ int lane_best(const float* keys, int E, float& best) {
-  best = -INFINITY;
-  int be = E;
-#pragma unroll 1
-  for (int e = (int)(threadIdx.x & 31); e < E; e += 32) {
+// Best and second-best key of one lane over e = lane, lane + 32, ... below
+// E32 (keys padded with -inf up to a multiple of 32). Strict >: among equal
+// keys the lower index ranks first; NaN never ranks. e = E means none.
+__device__ __forceinline__ void lane_best2(const float* keys, int E32, int E, float& b1, int& e1,
+                                           float& b2, int& e2) {
+  b1 = -INFINITY;
+  b2 = -INFINITY;
+  e1 = E;
+  e2 = E;
+#pragma unroll 4
+  for (int e = (int)(threadIdx.x & 31); e < E32; e += 32) {
     const float kv = keys[e];
-    if (kv > best) { best = kv; be = e; }
+    if (kv > b1) {
+      b2 = b1; e2 = e1; b1 = kv; e1 = e;
+    } else if (kv > b2) {
+      b2 = kv; e2 = e;
+    }
   }
-  return be;
 }
+// Top-k of one token by one warp. keys (E values, padded with -inf to a
+// multiple of 32, in shared memory) are p + b and are consumed: each chosen
+// entry is set to -inf. probs[E] are the sigmoids. The choice: the largest
+// key, ties to the lower index; a NaN key is never chosen (if no key is left,
+// expert 0). Each round takes the warp's best by two reductions; the winning
+// lane moves up its cached second best and rescans only when it has none.
+// Lane j < k returns the j-th id and its renormalised weight; the sum of the
+// chosen p runs in choice order.
 __device__ __forceinline__ int2 warp_topk(float* keys, const float* probs, int E, int k) {
   const int lane = threadIdx.x & 31;
-  float best;
-  int be = lane_best(keys, E, best);
+  const int E32 = (E + 31) & ~31;
+  float b1, b2;
+  int e1, e2;
+  lane_best2(keys, E32, E, b1, e1, b2, e2);
+  bool have2 = true;
   float psum = 0.0f, psel = 0.0f;
   int isel = 0;
-#pragma unroll 1
   for (int j = 0; j < k; ++j) {
-    const uint32_t ok = be < E ? ordered_key_bits(best) : 0u;
+    const uint32_t ok = e1 < E ? ordered_key_bits(b1) : 0u;
     const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, ok);
-    const uint32_t cand = (mx != 0u && ok == mx) ? (uint32_t)be : 0xFFFFFFFFu;
+    const uint32_t cand = (mx != 0u && ok == mx) ? (uint32_t)e1 : 0xFFFFFFFFu;
     uint32_t bi = __reduce_min_sync(0xFFFFFFFFu, cand);
     if (bi >= (uint32_t)E) bi = 0;
     const float pr = probs[bi];
@@ -215,7 +232,12 @@ __device__ __forceinline__ int2 warp_topk(float* keys, const float* probs, int E
     if (lane == j) { psel = pr; isel = (int)bi; }
     if ((int)(bi & 31u) == lane) {
       keys[bi] = -INFINITY;
-      be = lane_best(keys, E, best);
+      if (have2) {
+        b1 = b2; e1 = e2; have2 = false;
+      } else {
+        lane_best2(keys, E32, E, b1, e1, b2, e2);
+        have2 = true;
+      }
     }
   }
   return make_int2(isel, __float_as_int(psel / psum));
@@ -282,77 +304,65 @@ __device__ __forceinline__ void quant_block_store(float v, int b, int K, uint32_
 }
 
 
-// The same quantisation of one 32-value block done by a single lane (the 32
-// values in registers): the largest exponent, the 16 pair words as four
-// 16-byte stores, the scale. rec 16-byte aligned.
-__device__ __forceinline__ void quant_store_lane(const float (&v)[32], int b, int K,
-                                                 uint32_t* rec) {
-  uint32_t emax = 0;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const uint32_t e = (__float_as_uint(v[i]) >> 23) & 0xFFu;
-    emax = e > emax ? e : emax;
-  }
-  const int lpr = dlanes_per_row(K);
-  const int q = b >> 1, c0 = 4 * (b & 1);
-  uint4* r4 = reinterpret_cast<uint4*>(rec);
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int j = 4 * c + i;
-      w[i] = (uint32_t)(quant_one(v[j], emax) & 0xFFFF) |
-             ((uint32_t)quant_one(v[j + 16], emax) << 16);
-    }
-    r4[qv_u4(q, c0 + c, lpr)] = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-  reinterpret_cast<float*>(rec + dqvec_pair_words(K))[b] = quant_scale(emax);
-}
-
-// Lane-per-block quantisation of fp32 data in global memory (read through L2:
-// written by other CTAs of this grid). src 16-byte aligned.
-static __device__ __noinline__ void quant_f32_block_lane(const float* src, int b, int K,
-                                                  uint32_t* rec) {
-  float v[32];
-  const float4* s4 = reinterpret_cast<const float4*>(src);
+// Four lanes per 32-value block: lane s = lane & 3 holds values 8s..8s+7 of
+// block b. The largest exponent is combined over the four lanes by two
+// shuffles; lanes 0 and 1 of the group write the pair words (value j with
+// value j + 16, taken from lane s + 2), lane 0 the scale. All 32 lanes of the
+// warp call it (ok = false: a lane without a block).
+__device__ __forceinline__ void quant_group8(const float (&v)[8], bool ok, int b, int K,
+                                             uint32_t* rec) {
+  const int s = threadIdx.x & 3;
+  uint32_t e = 0;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const float4 f = __ldcg(s4 + i);
-    v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+    const uint32_t ei = (__float_as_uint(v[i]) >> 23) & 0xFFu;
+    e = ei > e ? ei : e;
   }
-  quant_store_lane(v, b, K, rec);
-}
-
-// Lane-per-block quantisation of 32 bf16 values (16-byte aligned) in global memory.
-static __device__ __noinline__ void quant_bf16_block_lane(const uint16_t* src, int b, int K,
-                                                   uint32_t* rec) {
-  const uint4* s4 = reinterpret_cast<const uint4*>(src);
-  uint4 r[4];
+  uint32_t o = __shfl_xor_sync(0xFFFFFFFFu, e, 1);
+  e = o > e ? o : e;
+  o = __shfl_xor_sync(0xFFFFFFFFu, e, 2);
+  e = o > e ? o : e;
+  int m[8], m2[8];
 #pragma unroll
-  for (int u = 0; u < 4; ++u) r[u] = __ldcg(s4 + u);
-  float v[32];
+  for (int i = 0; i < 8; ++i) m[i] = quant_one(v[i], e);
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const uint32_t w4[4] = {r[u].x, r[u].y, r[u].z, r[u].w};
+  for (int i = 0; i < 8; ++i) m2[i] = __shfl_down_sync(0xFFFFFFFFu, m[i], 2);
+  if (ok && s < 2) {
+    const int lpr = dlanes_per_row(K);
+    uint32_t w[8];
 #pragma unroll
-    for (int i2 = 0; i2 < 4; ++i2) {
-      v[8 * u + 2 * i2] = __uint_as_float(w4[i2] << 16);
-      v[8 * u + 2 * i2 + 1] = __uint_as_float(w4[i2] & 0xFFFF0000u);
-    }
+    for (int i = 0; i < 8; ++i) w[i] = (uint32_t)(m[i] & 0xFFFF) | ((uint32_t)m2[i] << 16);
+    const int q = b >> 1;
+    const int c0 = 4 * (b & 1) + 2 * s;
+    uint4* r4 = reinterpret_cast<uint4*>(rec);
+    r4[qv_u4(q, c0, lpr)] = make_uint4(w[0], w[1], w[2], w[3]);
+    r4[qv_u4(q, c0 + 1, lpr)] = make_uint4(w[4], w[5], w[6], w[7]);
   }
-  quant_store_lane(v, b, K, rec);
+  if (ok && s == 0) reinterpret_cast<float*>(rec + dqvec_pair_words(K))[b] = quant_scale(e);
 }
 
 // Quantise T bf16 rows of K values (16-byte aligned) into records in shared
-// memory, one 32-value block per thread; threads tid, tid + nt, ... of the CTA.
+// memory, four lanes per 32-value block (16 bytes each); all threads tid, tid +
+// nt, ... of the CTA (nt a multiple of 32).
 __device__ __forceinline__ void quant_x_lanes(const uint16_t* __restrict__ x, int T, int K,
                                               uint32_t* xq, int xq_words, int tid, int nt) {
   const int nb = K / 32;
 #pragma unroll 1
-  for (int i = tid; i < T * nb; i += nt) {
-    const int t = i / nb, b = i - t * nb;
-    quant_bf16_block_lane(x + (size_t)t * K + b * 32, b, K, xq + (size_t)t * xq_words);
+  for (int i0 = tid & ~31; i0 < T * nb * 4; i0 += nt) {
+    const int i = i0 + (tid & 31);
+    const bool ok = i < T * nb * 4;
+    const int blk = ok ? i >> 2 : 0;
+    const int t = blk / nb, b = blk - t * nb;
+    uint4 raw = make_uint4(0, 0, 0, 0);
+    if (ok) raw = __ldcg(reinterpret_cast<const uint4*>(x + (size_t)t * K + b * 32) + (i & 3));
+    const uint32_t r[4] = {raw.x, raw.y, raw.z, raw.w};
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[2 * j] = __uint_as_float(r[j] << 16);
+      v[2 * j + 1] = __uint_as_float(r[j] & 0xFFFF0000u);
+    }
+    quant_group8(v, ok, b, K, xq + (size_t)t * xq_words);
   }
 }
 
@@ -538,12 +548,15 @@ inline __device__ void flush_arrivals(const DecodeParams& p, const RouteTable& r
 }
 
 
-// Quantise every h row of this call from global memory into records in
-// shared memory, in the layout the down units read: the routed pairs' records
-// (indexed by pair), then the shared expert's (by token). One 32-value block
-// per thread, all of the CTA's threads at once.
-__device__ __forceinline__ void quant_h_to_smem(const DecodeParams& p, const RouteTable& rt,
-                                                uint32_t* recs, int tid, int nt) {
+// h rows of this call into records in shared memory, in the layout the down
+// units read: the routed pairs' records (indexed by pair), then the shared
+// expert's (by token). Four lanes per 32-value block. STAGED: the rows sit in
+// shared memory in list order (the valid routed pairs as rt.list orders them,
+// F values each, then the shared expert's rows, Fs values each); otherwise
+// they are read from global memory through L2 (written by other CTAs).
+template <bool STAGED>
+__device__ __forceinline__ void quant_h(const DecodeParams& p, const RouteTable& rt,
+                                        const float* stage, uint32_t* recs, int tid, int nt) {
   const int nbF = p.F / 32;
   const int nbS = p.n_shared ? p.Fs / 32 : 1;
   const int wF = dqvec_words(p.F);
@@ -552,24 +565,37 @@ __device__ __forceinline__ void quant_h_to_smem(const DecodeParams& p, const Rou
   const int nr = rt.n_valid * nbF;
   const int total = nr + (p.n_shared ? p.T * nbS : 0);
 #pragma unroll 1
-  for (int i = tid; i < total; i += nt) {
-    const float* src;
+  for (int i0 = tid & ~31; i0 < total * 4; i0 += nt) {
+    const int i = i0 + (tid & 31);
+    const bool ok = i < total * 4;
+    const int blk = ok ? i >> 2 : 0;
     uint32_t* dst;
     int b, K;
-    if (i < nr) {
-      const int e = i / nbF;
-      b = i - e * nbF;
+    if (blk < nr) {
+      const int e = blk / nbF;
+      b = blk - e * nbF;
       K = p.F;
-      src = p.h_r + (size_t)rt.list[e] * p.F + b * 32;
       dst = recs + (size_t)rt.list[e] * wF;
     } else {
-      const int j = (i - nr) / nbS;
-      b = (i - nr) - j * nbS;
+      const int j = (blk - nr) / nbS;
+      b = (blk - nr) - j * nbS;
       K = p.Fs;
-      src = p.h_s + (size_t)j * p.Fs + b * 32;
       dst = rec_sh + (size_t)j * wS;
     }
-    quant_f32_block_lane(src, b, K, dst);
+    float4 f0 = make_float4(0.f, 0.f, 0.f, 0.f), f1 = f0;
+    if (STAGED) {
+      const float4* s4 = reinterpret_cast<const float4*>(stage + (size_t)blk * 32 + 8 * (i & 3));
+      f0 = s4[0];
+      f1 = s4[1];
+    } else if (ok) {
+      const float* row = blk < nr ? p.h_r + (size_t)rt.list[blk / nbF] * p.F
+                                  : p.h_s + (size_t)((blk - nr) / nbS) * p.Fs;
+      const float4* s4 = reinterpret_cast<const float4*>(row + b * 32 + 8 * (i & 3));
+      f0 = __ldcg(s4);
+      f1 = __ldcg(s4 + 1);
+    }
+    const float v[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+    quant_group8(v, ok, b, K, dst);
   }
 }
 

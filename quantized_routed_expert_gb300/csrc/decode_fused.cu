@@ -28,6 +28,8 @@ struct FusedSmem {
   // router scratch (routed kernel), overlaying the records area, which is used
   // only after the h barrier
   size_t r_wr, r_x, r_part, r_keys, r_ids, r_w;
+  // h staging for the local quantisation (0 bytes: h is read from L2 instead)
+  size_t stage, stage_bytes;
 };
 
 // Experts whose scores CTA c computes: a balanced split of E over the grid.
@@ -59,10 +61,21 @@ __host__ __device__ inline FusedSmem fused_smem(int H, int F, int Fs, int ns, in
     m.r_x = align_up_dev(m.r_wr + (size_t)epc * H * 2, 128);
     m.r_part = align_up_dev(m.r_x + (size_t)T * H * 2, 16);
     m.r_keys = align_up_dev(m.r_part + (size_t)epc * 16 * T * 4, 16);
-    m.r_ids = align_up_dev(m.r_keys + (size_t)2 * T * E * 4, 16);   // keys, then sigmoids
+    m.r_ids = align_up_dev(m.r_keys + (size_t)2 * T * ((E + 31) & ~31) * 4, 16);  // keys, sigmoids
     m.r_w = align_up_dev(m.r_ids + (size_t)T * k * 4, 16);
     const size_t rend = m.r_w + (size_t)T * k * 4;
     end = end > rend ? end : rend;
+  }
+  // stage every h row of the call in shared memory when it fits
+  const size_t hb = ((size_t)T * k * F + (ns ? (size_t)T * Fs : 0)) * 4;
+  const size_t st = align_up_dev(end, 128);
+  if (st + hb <= (size_t)227 * 1024) {
+    m.stage = st;
+    m.stage_bytes = hb;
+    end = st + hb;
+  } else {
+    m.stage = 0;
+    m.stage_bytes = 0;
   }
   m.total = end;
   return m;
@@ -79,7 +92,7 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
 // interleave width of the quantised x records (dlanes_per_row(H)); 0 = known
 // only at run time.
 template <int MAXT, int LPR>
-__device__ __noinline__ void gateup_unit_t(const DecodeParams& p, const RouteTable& rt,
+__device__ __forceinline__ void gateup_unit_t(const DecodeParams& p, const RouteTable& rt,
                                            const uint8_t* g, const uint8_t* u, int slot, int f,
                                            const uint32_t* xq, int xq_words) {
   const int lane = threadIdx.x & 31;
@@ -103,6 +116,33 @@ __device__ __noinline__ void gateup_unit_t(const DecodeParams& p, const RouteTab
     float ag[MAXT], au[MAXT];
 #pragma unroll
     for (int j = 0; j < MAXT; ++j) ag[j] = au[j] = 0.0f;
+    if constexpr (MAXT == 1) {
+      // one token: the split-table dot products (fewer ALU-pipe operations)
+      for (int q = lane; q < npairs; q += 32) {
+        const int qbase = qv_base(q, lpr);
+        uint32_t wg[9], wu[9];
+        load_pair_smem(g + q * kPairB, wg);
+        load_pair_smem(u + q * kPairB, wu);
+        float dg0, dg1, du0, du1;
+        pair_scales(wg, dg0, dg1);
+        pair_scales(wu, du0, du1);
+        const uint4* r4 = reinterpret_cast<const uint4*>(rec[0]) + qbase;
+        uint32_t v[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 t4 = r4[c * lpr];
+          v[4 * c] = t4.x; v[4 * c + 1] = t4.y; v[4 * c + 2] = t4.z; v[4 * c + 3] = t4.w;
+        }
+        const float2 sc = reinterpret_cast<const float2*>(rec[0] + xs_off)[q];
+        int ig0, ig1, iu0, iu1;
+        iq4_pair_dot1(wg, v, ig0, ig1);
+        iq4_pair_dot1(wu, v, iu0, iu1);
+        ag[0] = fmaf((float)ig0, dg0 * sc.x, ag[0]);
+        ag[0] = fmaf((float)ig1, dg1 * sc.y, ag[0]);
+        au[0] = fmaf((float)iu0, du0 * sc.x, au[0]);
+        au[0] = fmaf((float)iu1, du1 * sc.y, au[0]);
+      }
+    } else {
     for (int q = lane; q < npairs; q += 32) {
       const int qbase = qv_base(q, lpr);
       uint32_t w[9];
@@ -145,6 +185,7 @@ __device__ __noinline__ void gateup_unit_t(const DecodeParams& p, const RouteTab
         }
       }
     }
+    }
 #pragma unroll
     for (int j = 0; j < MAXT; ++j) {
 #pragma unroll
@@ -163,19 +204,12 @@ __device__ __noinline__ void gateup_unit_t(const DecodeParams& p, const RouteTab
     }
   }
 }
-template <int MAXT>
-__device__ __forceinline__ void gateup_unit(const DecodeParams& p, const RouteTable& rt,
-                                            const uint8_t* g, const uint8_t* u, int slot, int f,
-                                            const uint32_t* xq, int xq_words) {
-  if (dlanes_per_row(p.H) == 8) gateup_unit_t<MAXT, 8>(p, rt, g, u, slot, f, xq, xq_words);
-  else gateup_unit_t<MAXT, 0>(p, rt, g, u, slot, f, xq, xq_words);
-}
 
 // One down unit: rows [r0, r0 + nrows) (CTA-local indices) of the slot's W_d at
 // `wrows`; for every pair of the slot, the row dot products into `part`.
 // NPS pairs share each decoded block; LPR as for gate/up (0 = run time).
 template <int NPS, int LPR>
-__device__ __noinline__ void down_unit_t(const DecodeParams& p, const RouteTable& rt,
+__device__ __forceinline__ void down_unit_t(const DecodeParams& p, const RouteTable& rt,
                                          const uint8_t* wrows, int slot, int r0, int nrows,
                                          const uint32_t* recs, float* part, int rows_max) {
   const int lane = threadIdx.x & 31;
@@ -217,6 +251,28 @@ __device__ __noinline__ void down_unit_t(const DecodeParams& p, const RouteTable
       for (int j = 0; j < NPS; ++j) acc[j] = 0.0f;
       if (active) {
         const uint8_t* row = wrows + (size_t)rl * rbK;
+        if constexpr (NPS == 1) {
+          // one token: the split-table dot products
+          for (int q = q0; q < npq; q += lpr) {
+            const int qbase = qv_base(q, lpr);
+            uint32_t w[9];
+            load_pair_smem(row + q * kPairB, w);
+            float d0, d1;
+            pair_scales(w, d0, d1);
+            const uint4* r4 = reinterpret_cast<const uint4*>(rp[0]) + qbase;
+            uint32_t v[32];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint4 t4 = r4[c * lpr];
+              v[4 * c] = t4.x; v[4 * c + 1] = t4.y; v[4 * c + 2] = t4.z; v[4 * c + 3] = t4.w;
+            }
+            const float2 sc = reinterpret_cast<const float2*>(rp[0] + pw)[q];
+            int i0, i1;
+            iq4_pair_dot1(w, v, i0, i1);
+            acc[0] = fmaf((float)i0, d0 * sc.x, acc[0]);
+            acc[0] = fmaf((float)i1, d1 * sc.y, acc[0]);
+          }
+        } else {
         for (int q = q0; q < npq; q += lpr) {
           const int qbase = qv_base(q, lpr);
           uint32_t w[9];
@@ -248,6 +304,7 @@ __device__ __noinline__ void down_unit_t(const DecodeParams& p, const RouteTable
             }
           }
         }
+        }
       }
 #pragma unroll
       for (int j = 0; j < NPS; ++j)
@@ -263,14 +320,6 @@ __device__ __noinline__ void down_unit_t(const DecodeParams& p, const RouteTable
       }
     }
   }
-}
-template <int NPS>
-__device__ __forceinline__ void down_unit(const DecodeParams& p, const RouteTable& rt,
-                                          const uint8_t* wrows, int slot, int r0, int nrows,
-                                          const uint32_t* recs, float* part, int rows_max) {
-  const int K = slot < 0 ? p.Fs : p.F;
-  if (dlanes_per_row(K) == 8) down_unit_t<NPS, 8>(p, rt, wrows, slot, r0, nrows, recs, part, rows_max);
-  else down_unit_t<NPS, 0>(p, rt, wrows, slot, r0, nrows, recs, part, rows_max);
 }
 
 // What one warp needs to issue the bulk copies of its units: the warp's unit
@@ -323,7 +372,7 @@ __device__ __noinline__ void issue_unit(const DecodeParams& p, const RouteTable&
   }
 }
 
-template <int MAXT, bool ROUTE>
+template <int MAXT, bool ROUTE, int LPR>
 __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int H = p.H;
@@ -470,93 +519,104 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
   }
   __syncthreads();
 
-  #pragma unroll 1
-  for (int j = 0; ok && j < n_sh; ++j) {
-    ok = wait_unit(j);
-    if (!ok) break;
-    const uint8_t* d = myslots + (size_t)(j % kFSlots) * L.slot_bytes;
-    const int f = shr.a + warp + kFW * j;
-    gateup_unit<MAXT>(p, rt, d, d + rbH, -1, f, xq, xq_words);
-    __syncwarp();
-    ++consumed;
-    issue_upto(n_sh);
-  }
-
-  const int32_t* ids_src = p.ids;
-  const float* w_src = p.weights;
-  if (ROUTE) {
-    // all scores of this call -> top-k: warp t takes token t, in every CTA
-    int32_t* ids_s = reinterpret_cast<int32_t*>(smem + L.r_ids);
-    float* w_s = reinterpret_cast<float*>(smem + L.r_w);
-    if (threadIdx.x == 0) {
-      const uint64_t t0 = global_timer_ns();
-      while (ld_acquire_u32(&p.sync[2]) < gridDim.x) {
-        __nanosleep(32);
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
-          if (p.status) atomicOr(p.status, MOE_STATUS_TIMEOUT);
-          break;
+  // gate/up: the shared expert's rows first (known before the routes), then,
+  // after the routing step, the routed rows. One loop, one unit call site.
+  int j = 0;
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    if (pass == 1) {
+      const int32_t* ids_src = p.ids;
+      const float* w_src = p.weights;
+      if (ROUTE) {
+        // all scores of this call -> top-k: warp t takes token t, in every CTA
+        int32_t* ids_s = reinterpret_cast<int32_t*>(smem + L.r_ids);
+        float* w_s = reinterpret_cast<float*>(smem + L.r_w);
+        if (threadIdx.x == 0) {
+          const uint64_t t0 = global_timer_ns();
+          while (ld_acquire_u32(&p.sync[2]) < gridDim.x) {
+            __nanosleep(32);
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+              if (p.status) atomicOr(p.status, MOE_STATUS_TIMEOUT);
+              break;
+            }
+          }
+          __threadfence();
         }
-      }
-      __threadfence();
-    }
-    __syncthreads();
-    float* keys_all = reinterpret_cast<float*>(smem + L.r_keys);
-    #pragma unroll 1
-    for (int i = threadIdx.x; i < p.T * p.E; i += kFT) {
-      const int e = i % p.E;
-      const float pr = 1.0f / (1.0f + expf(-__ldcg(p.scores + i)));
-      keys_all[(size_t)p.T * p.E + i] = pr;
-      keys_all[i] = pr + (p.bias ? p.bias[e] : 0.0f);
-    }
-    __syncthreads();
-    if (warp < p.T) {
-      const int t = warp;
-      float* keys = keys_all + (size_t)t * p.E;
-      float* probs = keys + (size_t)p.T * p.E;
-      const int2 r = warp_topk(keys, probs, p.E, p.k);
-      const int id = r.x;
-      const float wv = __int_as_float(r.y);
-      if (lane < p.k) {
-        ids_s[t * p.k + lane] = id;
-        w_s[t * p.k + lane] = wv;
-        if (blockIdx.x == 0) {
-          p.ids_out[(size_t)t * p.k + lane] = id;
-          p.w_out[(size_t)t * p.k + lane] = wv;
+        __syncthreads();
+        // keys p + b and sigmoids p, rows padded to E32 with -inf (keys)
+        float* keys_all = reinterpret_cast<float*>(smem + L.r_keys);
+        const int E32 = (p.E + 31) & ~31;
+#pragma unroll 1
+        for (int i = threadIdx.x; i < p.T * E32; i += kFT) {
+          const int t = i / E32, e = i - t * E32;
+          float key = -INFINITY, pr = 0.0f;
+          if (e < p.E) {
+            pr = 1.0f / (1.0f + expf(-__ldcg(p.scores + (size_t)t * p.E + e)));
+            key = pr + (p.bias ? p.bias[e] : 0.0f);
+          }
+          keys_all[(size_t)p.T * E32 + i] = pr;
+          keys_all[i] = key;
         }
+        __syncthreads();
+        if (warp < p.T) {
+          const int t = warp;
+          float* keys = keys_all + (size_t)t * E32;
+          float* probs = keys + (size_t)p.T * E32;
+          const int2 r = warp_topk(keys, probs, p.E, p.k);
+          const int id = r.x;
+          const float wv = __int_as_float(r.y);
+          if (lane < p.k) {
+            ids_s[t * p.k + lane] = id;
+            w_s[t * p.k + lane] = wv;
+            if (blockIdx.x == 0) {
+              p.ids_out[(size_t)t * p.k + lane] = id;
+              p.w_out[(size_t)t * p.k + lane] = wv;
+            }
+          }
+          if (p.T > 1) bar_sync_n(1, p.T * 32);     // the token warps only
+        }
+        ids_src = ids_s;
+        w_src = w_s;
       }
-      if (p.T > 1) bar_sync_n(1, p.T * 32);     // the token warps only
-    }
-    ids_src = ids_s;
-    w_src = w_s;
-  }
-  if (warp == 0) build_route_table_warp(rt, ids_src, w_src, p.T * p.k, p.E);
-  __syncthreads();
-  if (blockIdx.x == 0 && threadIdx.x == 0 && p.status && rt.invalid)
-    atomicAdd(p.status, (uint32_t)(rt.invalid < 0xFFFF ? rt.invalid : 0xFFFF));
-  #pragma unroll 1
-  for (int i = threadIdx.x; i < (p.T * p.k + (p.n_shared ? p.T : 0)) * rows_max; i += kFT)
-    part[i] = 0.0f;
-  rr = split_rows(rt.n_slots * p.F, 1, blockIdx.x, gridDim.x);
-  n_rt = count(rr.a, rr.b);
-  up.n_rt = n_rt;
-  up.rr_a = rr.a;
-  n_dslots = rt.n_slots + p.n_shared;
-  const int n_dn_units = n_dslots * ngroups;
-  const int n_dn = warp < n_dn_units ? (n_dn_units - warp + kFW - 1) / kFW : 0;
-  n_tot = n_sh + n_rt + n_dn;
-  issue_upto(n_tot);
+      if (warp == 0) build_route_table_warp(rt, ids_src, w_src, p.T * p.k, p.E);
+      __syncthreads();
+      if (blockIdx.x == 0 && threadIdx.x == 0 && p.status && rt.invalid)
+        atomicAdd(p.status, (uint32_t)(rt.invalid < 0xFFFF ? rt.invalid : 0xFFFF));
+      #pragma unroll 1
+      for (int i = threadIdx.x; i < (p.T * p.k + (p.n_shared ? p.T : 0)) * rows_max; i += kFT)
+        part[i] = 0.0f;
+      rr = split_rows(rt.n_slots * p.F, 1, blockIdx.x, gridDim.x);
+      n_rt = count(rr.a, rr.b);
+      up.n_rt = n_rt;
+      up.rr_a = rr.a;
+      n_dslots = rt.n_slots + p.n_shared;
+      const int n_dn_units = n_dslots * ngroups;
+      const int n_dn = warp < n_dn_units ? (n_dn_units - warp + kFW - 1) / kFW : 0;
+      n_tot = n_sh + n_rt + n_dn;
+      issue_upto(n_tot);
 
-  #pragma unroll 1
-  for (int j = n_sh; ok && j < n_sh + n_rt; ++j) {
-    ok = wait_unit(j);
-    if (!ok) break;
-    const uint8_t* d = myslots + (size_t)(j % kFSlots) * L.slot_bytes;
-    const int r = rr.a + warp + kFW * (j - n_sh);
-    const int sl = r / p.F, f = r - sl * p.F;
-    gateup_unit<MAXT>(p, rt, d, d + rbH, sl, f, xq, xq_words);
-    __syncwarp();
-    ++consumed;
-    issue_upto(n_tot);
+    }
+    const int jend = pass == 0 ? n_sh : n_sh + n_rt;
+    const int ilim = pass == 0 ? n_sh : n_tot;
+#pragma unroll 1
+    for (; ok && j < jend; ++j) {
+      ok = wait_unit(j);
+      if (!ok) break;
+      const uint8_t* d = myslots + (size_t)(j % kFSlots) * L.slot_bytes;
+      int sl, f;
+      if (j < n_sh) {
+        sl = -1;
+        f = shr.a + warp + kFW * j;
+      } else {
+        const int r = rr.a + warp + kFW * (j - n_sh);
+        sl = r / p.F;
+        f = r - sl * p.F;
+      }
+      gateup_unit_t<MAXT, LPR>(p, rt, d, d + rbH, sl, f, xq, xq_words);
+      __syncwarp();
+      ++consumed;
+      issue_upto(ilim);
+    }
   }
 
   // ---- grid barrier: every h row of this call is in global memory
@@ -575,8 +635,29 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
     __threadfence();
   }
   __syncthreads();
-  // every CTA quantises all of h into its own records
-  quant_h_to_smem(p, rt, recs, threadIdx.x, kFT);
+  // every CTA quantises all of h into its own records: staged in shared
+  // memory by bulk copies when there is room, else read through L2
+  if (L.stage_bytes) {
+    float* stage = reinterpret_cast<float*>(smem + L.stage);
+    if (threadIdx.x == 0) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      const uint32_t rbF = (uint32_t)p.F * 4, rbS = (uint32_t)p.Fs * 4;
+      const uint32_t total = rt.n_valid * rbF + (p.n_shared ? p.T * rbS : 0u);
+      mbar_arrive_expect_tx(recs_bar, total);
+      uint8_t* dst = reinterpret_cast<uint8_t*>(stage);
+      for (int e = 0; e < rt.n_valid; ++e, dst += rbF)
+        bulk_g2s(dst, p.h_r + (size_t)rt.list[e] * p.F, rbF, recs_bar);
+      if (p.n_shared)
+        for (int j = 0; j < p.T; ++j, dst += rbS)
+          bulk_g2s(dst, p.h_s + (size_t)j * p.Fs, rbS, recs_bar);
+    }
+    // wait even after an earlier timeout: no copy of this CTA stays in flight
+    const bool landed = mbar_wait(recs_bar, 0, p.status);
+    ok = ok && landed;
+    if (ok) quant_h<true>(p, rt, stage, recs, threadIdx.x, kFT);
+  } else {
+    quant_h<false>(p, rt, nullptr, recs, threadIdx.x, kFT);
+  }
   __syncthreads();
 
   #pragma unroll 1
@@ -589,7 +670,7 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
     const bool sh = p.n_shared && su == 0;
     const int r0 = gi * RG;
     const int nr = nrows_cta - r0 < RG ? nrows_cta - r0 : RG;
-    down_unit<MAXT>(p, rt, d, sh ? -1 : su - p.n_shared, r0, nr, recs, part, rows_max);
+    down_unit_t<MAXT, LPR>(p, rt, d, sh ? -1 : su - p.n_shared, r0, nr, recs, part, rows_max);
     __syncwarp();
     ++consumed;
     issue_upto(n_tot);
@@ -608,6 +689,12 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
       if (pr / p.k == t) acc += rt.wt[pr] * part[(size_t)pr * rows_max + r];
     }
     p.y[(size_t)t * H + dn.a + r] = acc;
+  }
+
+  // ---- after a timeout, drain this warp's bulk copies still in flight
+  while (consumed < issued) {
+    wait_unit(consumed);
+    ++consumed;
   }
 
   // ---- leave: the last CTA out resets the barrier counters for the next call
@@ -644,12 +731,20 @@ bool fused_decode_supported(const DecodeParams& p, int num_sms, size_t* smem, in
 }
 
 namespace {
-template <int MAXT, bool ROUTE>
+template <int MAXT, bool ROUTE, int LPR>
 cudaError_t launch_fused_t(const DecodeParams& p, const cudaLaunchConfig_t& cfg, size_t smem) {
-  const cudaError_t e =
-      ensure_smem_attr(reinterpret_cast<const void*>(decode_fused_kernel<MAXT, ROUTE>), smem);
+  const cudaError_t e = ensure_smem_attr(
+      reinterpret_cast<const void*>(decode_fused_kernel<MAXT, ROUTE, LPR>), smem);
   if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, decode_fused_kernel<MAXT, ROUTE>, p);
+  return cudaLaunchKernelEx(&cfg, decode_fused_kernel<MAXT, ROUTE, LPR>, p);
+}
+template <bool ROUTE, int LPR>
+cudaError_t launch_fused_tt(const DecodeParams& p, const cudaLaunchConfig_t& cfg, size_t smem) {
+  switch (p.T) {
+    case 1: return launch_fused_t<1, ROUTE, LPR>(p, cfg, smem);
+    case 2: return launch_fused_t<2, ROUTE, LPR>(p, cfg, smem);
+    default: return launch_fused_t<4, ROUTE, LPR>(p, cfg, smem);
+  }
 }
 }  // namespace
 
@@ -665,18 +760,13 @@ cudaError_t launch_decode_fused(const DecodeParams& p, int num_sms, size_t smem,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  if (p.route) {
-    switch (p.T) {
-      case 1: return launch_fused_t<1, true>(p, cfg, smem);
-      case 2: return launch_fused_t<2, true>(p, cfg, smem);
-      default: return launch_fused_t<4, true>(p, cfg, smem);
-    }
-  }
-  switch (p.T) {
-    case 1: return launch_fused_t<1, false>(p, cfg, smem);
-    case 2: return launch_fused_t<2, false>(p, cfg, smem);
-    default: return launch_fused_t<4, false>(p, cfg, smem);
-  }
+  // the record interleave width is 8 for every width of 512 and more; the
+  // kernels built for it use immediate offsets, the others compute them
+  const bool w8 = lanes_per_row(p.H) == 8 && lanes_per_row(p.F) == 8 &&
+                  (!p.n_shared || lanes_per_row(p.Fs) == 8);
+  if (p.route)
+    return w8 ? launch_fused_tt<true, 8>(p, cfg, smem) : launch_fused_tt<true, 0>(p, cfg, smem);
+  return w8 ? launch_fused_tt<false, 8>(p, cfg, smem) : launch_fused_tt<false, 0>(p, cfg, smem);
 }
 
 }  // namespace moe
