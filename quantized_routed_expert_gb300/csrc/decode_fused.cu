@@ -519,104 +519,98 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
   }
   __syncthreads();
 
-  // gate/up: the shared expert's rows first (known before the routes), then,
-  // after the routing step, the routed rows. One loop, one unit call site.
+  // ---- routing (this CTA's experts' scores were published above)
+  const int32_t* ids_src = p.ids;
+  const float* w_src = p.weights;
+  if (ROUTE) {
+    // all scores of this call -> top-k: warp t takes token t, in every CTA
+    int32_t* ids_s = reinterpret_cast<int32_t*>(smem + L.r_ids);
+    float* w_s = reinterpret_cast<float*>(smem + L.r_w);
+    if (threadIdx.x == 0) {
+      const uint64_t t0 = global_timer_ns();
+      while (ld_acquire_u32(&p.sync[2]) < gridDim.x) {
+        __nanosleep(32);
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+          if (p.status) atomicOr(p.status, MOE_STATUS_TIMEOUT);
+          break;
+        }
+      }
+      __threadfence();
+    }
+    __syncthreads();
+    // keys p + b and sigmoids p, rows padded to E32 with -inf (keys)
+    float* keys_all = reinterpret_cast<float*>(smem + L.r_keys);
+    const int E32 = (p.E + 31) & ~31;
+#pragma unroll 1
+    for (int i = threadIdx.x; i < p.T * E32; i += kFT) {
+      const int t = i / E32, e = i - t * E32;
+      float key = -INFINITY, pr = 0.0f;
+      if (e < p.E) {
+        pr = 1.0f / (1.0f + expf(-__ldcg(p.scores + (size_t)t * p.E + e)));
+        key = pr + (p.bias ? p.bias[e] : 0.0f);
+      }
+      keys_all[(size_t)p.T * E32 + i] = pr;
+      keys_all[i] = key;
+    }
+    __syncthreads();
+    if (warp < p.T) {
+      const int t = warp;
+      float* keys = keys_all + (size_t)t * E32;
+      float* probs = keys + (size_t)p.T * E32;
+      const int2 r = warp_topk(keys, probs, p.E, p.k);
+      const int id = r.x;
+      const float wv = __int_as_float(r.y);
+      if (lane < p.k) {
+        ids_s[t * p.k + lane] = id;
+        w_s[t * p.k + lane] = wv;
+        if (blockIdx.x == 0) {
+          p.ids_out[(size_t)t * p.k + lane] = id;
+          p.w_out[(size_t)t * p.k + lane] = wv;
+        }
+      }
+      if (p.T > 1) bar_sync_n(1, p.T * 32);     // the token warps only
+    }
+    ids_src = ids_s;
+    w_src = w_s;
+  }
+  if (warp == 0) build_route_table_warp(rt, ids_src, w_src, p.T * p.k, p.E);
+  __syncthreads();
+  if (blockIdx.x == 0 && threadIdx.x == 0 && p.status && rt.invalid)
+    atomicAdd(p.status, (uint32_t)(rt.invalid < 0xFFFF ? rt.invalid : 0xFFFF));
+  #pragma unroll 1
+  for (int i = threadIdx.x; i < (p.T * p.k + (p.n_shared ? p.T : 0)) * rows_max; i += kFT)
+    part[i] = 0.0f;
+  rr = split_rows(rt.n_slots * p.F, 1, blockIdx.x, gridDim.x);
+  n_rt = count(rr.a, rr.b);
+  up.n_rt = n_rt;
+  up.rr_a = rr.a;
+  n_dslots = rt.n_slots + p.n_shared;
+  const int n_dn_units = n_dslots * ngroups;
+  const int n_dn = warp < n_dn_units ? (n_dn_units - warp + kFW - 1) / kFW : 0;
+  n_tot = n_sh + n_rt + n_dn;
+  issue_upto(n_tot);
+
+  // the routed rows' copies are in flight: compute the shared expert's rows
+  // (landed long ago) while they arrive, then the routed rows
   int j = 0;
 #pragma unroll 1
-  for (int pass = 0; pass < 2; ++pass) {
-    if (pass == 1) {
-      const int32_t* ids_src = p.ids;
-      const float* w_src = p.weights;
-      if (ROUTE) {
-        // all scores of this call -> top-k: warp t takes token t, in every CTA
-        int32_t* ids_s = reinterpret_cast<int32_t*>(smem + L.r_ids);
-        float* w_s = reinterpret_cast<float*>(smem + L.r_w);
-        if (threadIdx.x == 0) {
-          const uint64_t t0 = global_timer_ns();
-          while (ld_acquire_u32(&p.sync[2]) < gridDim.x) {
-            __nanosleep(32);
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
-              if (p.status) atomicOr(p.status, MOE_STATUS_TIMEOUT);
-              break;
-            }
-          }
-          __threadfence();
-        }
-        __syncthreads();
-        // keys p + b and sigmoids p, rows padded to E32 with -inf (keys)
-        float* keys_all = reinterpret_cast<float*>(smem + L.r_keys);
-        const int E32 = (p.E + 31) & ~31;
-#pragma unroll 1
-        for (int i = threadIdx.x; i < p.T * E32; i += kFT) {
-          const int t = i / E32, e = i - t * E32;
-          float key = -INFINITY, pr = 0.0f;
-          if (e < p.E) {
-            pr = 1.0f / (1.0f + expf(-__ldcg(p.scores + (size_t)t * p.E + e)));
-            key = pr + (p.bias ? p.bias[e] : 0.0f);
-          }
-          keys_all[(size_t)p.T * E32 + i] = pr;
-          keys_all[i] = key;
-        }
-        __syncthreads();
-        if (warp < p.T) {
-          const int t = warp;
-          float* keys = keys_all + (size_t)t * E32;
-          float* probs = keys + (size_t)p.T * E32;
-          const int2 r = warp_topk(keys, probs, p.E, p.k);
-          const int id = r.x;
-          const float wv = __int_as_float(r.y);
-          if (lane < p.k) {
-            ids_s[t * p.k + lane] = id;
-            w_s[t * p.k + lane] = wv;
-            if (blockIdx.x == 0) {
-              p.ids_out[(size_t)t * p.k + lane] = id;
-              p.w_out[(size_t)t * p.k + lane] = wv;
-            }
-          }
-          if (p.T > 1) bar_sync_n(1, p.T * 32);     // the token warps only
-        }
-        ids_src = ids_s;
-        w_src = w_s;
-      }
-      if (warp == 0) build_route_table_warp(rt, ids_src, w_src, p.T * p.k, p.E);
-      __syncthreads();
-      if (blockIdx.x == 0 && threadIdx.x == 0 && p.status && rt.invalid)
-        atomicAdd(p.status, (uint32_t)(rt.invalid < 0xFFFF ? rt.invalid : 0xFFFF));
-      #pragma unroll 1
-      for (int i = threadIdx.x; i < (p.T * p.k + (p.n_shared ? p.T : 0)) * rows_max; i += kFT)
-        part[i] = 0.0f;
-      rr = split_rows(rt.n_slots * p.F, 1, blockIdx.x, gridDim.x);
-      n_rt = count(rr.a, rr.b);
-      up.n_rt = n_rt;
-      up.rr_a = rr.a;
-      n_dslots = rt.n_slots + p.n_shared;
-      const int n_dn_units = n_dslots * ngroups;
-      const int n_dn = warp < n_dn_units ? (n_dn_units - warp + kFW - 1) / kFW : 0;
-      n_tot = n_sh + n_rt + n_dn;
-      issue_upto(n_tot);
-
+  for (; ok && j < n_sh + n_rt; ++j) {
+    ok = wait_unit(j);
+    if (!ok) break;
+    const uint8_t* d = myslots + (size_t)(j % kFSlots) * L.slot_bytes;
+    int sl, f;
+    if (j < n_sh) {
+      sl = -1;
+      f = shr.a + warp + kFW * j;
+    } else {
+      const int r = rr.a + warp + kFW * (j - n_sh);
+      sl = r / p.F;
+      f = r - sl * p.F;
     }
-    const int jend = pass == 0 ? n_sh : n_sh + n_rt;
-    const int ilim = pass == 0 ? n_sh : n_tot;
-#pragma unroll 1
-    for (; ok && j < jend; ++j) {
-      ok = wait_unit(j);
-      if (!ok) break;
-      const uint8_t* d = myslots + (size_t)(j % kFSlots) * L.slot_bytes;
-      int sl, f;
-      if (j < n_sh) {
-        sl = -1;
-        f = shr.a + warp + kFW * j;
-      } else {
-        const int r = rr.a + warp + kFW * (j - n_sh);
-        sl = r / p.F;
-        f = r - sl * p.F;
-      }
-      gateup_unit_t<MAXT, LPR>(p, rt, d, d + rbH, sl, f, xq, xq_words);
-      __syncwarp();
-      ++consumed;
-      issue_upto(ilim);
-    }
+    gateup_unit_t<MAXT, LPR>(p, rt, d, d + rbH, sl, f, xq, xq_words);
+    __syncwarp();
+    ++consumed;
+    issue_upto(n_tot);
   }
 
   // ---- grid barrier: every h row of this call is in global memory
