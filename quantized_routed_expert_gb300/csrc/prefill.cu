@@ -291,9 +291,20 @@ struct TileInfo {
   int bucket, m0, n0, nvalid, row0;
 };
 
+// Token tiles are loaded with the smallest of four box heights that covers
+// the tile's tokens, and the MMA runs with N = tokens rounded up to 16: with
+// skewed routing most buckets hold far fewer than 256 tokens.
+constexpr int kNumBoxes = 4;                 // 32, 64, 128, 256 rows
+struct TmapSet {
+  CUtensorMap m[kNumBoxes];
+};
+__device__ __forceinline__ int box_index(int n) {
+  return n <= 32 ? 0 : (n <= 64 ? 1 : (n <= 128 ? 2 : 3));
+}
+
 template <bool GATEUP>
 __global__ void __launch_bounds__(kGThreads, 1)
-pf_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
+pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
   using S = GemmSmem<GATEUP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -376,19 +387,20 @@ pf_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
             break;
           }
           uint8_t* b = stages + (size_t)s * S::kStage + (GATEUP ? 2 : 1) * S::kA;
-          mbar_arrive_expect_tx(&full_b[s], S::kB);
-          tma_load_2d(b, &tmap_b, ks * kTK, ti.row0 + ti.n0, &full_b[s]);
+          const int bx = box_index(ti.nvalid);
+          mbar_arrive_expect_tx(&full_b[s], (uint32_t)((32 << bx) * kTK * 2));
+          tma_load_2d(b, &tmaps.m[bx], ks * kTK, ti.row0 + ti.n0, &full_b[s]);
         }
       }
     }
   } else if (warp == 1) {
     // ---- MMA issue (one thread)
     if (lane == 0) {
-      const uint32_t idesc = idesc_f16_f32(kTM, kTN);
       int it = 0, tc = 0;
       for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tc) {
         const TileInfo ti = tile_info(t);
         const int K = ti.bucket < p.E ? p.K : p.Ks;
+        const uint32_t idesc = idesc_f16_f32(kTM, (ti.nvalid + 15) & ~15);
         if (!mbar_wait(acc_empty, (tc & 1) ^ 1, p.status)) break;
         tc_fence_after();
         for (int ks = 0; ks < K / kTK; ++ks, ++it) {
@@ -581,12 +593,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // fp16 [rows][cols] row-major, box 64 columns x 256 rows, 128-byte swizzle.
-bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t cols) {
+bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {(cuuint32_t)kTK, (cuuint32_t)kTN};
+  cuuint32_t box[2] = {(cuuint32_t)kTK, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -648,9 +660,11 @@ cudaError_t launch_prefill(const moe_shape& s, const moe_expert_weights& w, cons
                 (const int32_t*)boff, (const int32_t*)row_tok, E, H, x16);
   if (e != cudaSuccess) return e;
 
-  CUtensorMap tm_x, tm_h;
-  if (!make_tmap(&tm_x, x16, rows, H) || !make_tmap(&tm_h, h16, rows, fmax))
-    return cudaErrorInvalidValue;
+  TmapSet tm_x, tm_h;
+  for (int b = 0; b < kNumBoxes; ++b)
+    if (!make_tmap(&tm_x.m[b], x16, rows, H, 32 << b) ||
+        !make_tmap(&tm_h.m[b], h16, rows, fmax, 32 << b))
+      return cudaErrorInvalidValue;
   GemmParams g1{};
   g1.E = E;
   g1.n_shared = s.n_shared;
