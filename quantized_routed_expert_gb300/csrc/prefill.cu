@@ -449,42 +449,15 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
       // load group, double-buffered in registers; rows whose length is not a
       // multiple of four pairs use 4-byte loads.
       const int nks = K / kTK;
-      const bool vec = (nks & 3) == 0;
-      uint4 cur[9], nxt[9];
-      auto load_group = [&](int g, uint4 (&dst)[9]) {
-        const uint4* src = reinterpret_cast<const uint4*>(row + (size_t)g * 4 * kPairB);
-#pragma unroll
-        for (int i = 0; i < 9; ++i) dst[i] = __ldg(src + i);
-      };
-      if (vec) load_group(0, nxt);
-      for (int ks = 0; ks < nks; ++ks, ++it) {
-        uint32_t w[9];
-        if (vec) {
-          const int j = ks & 3;
-          if (j == 0) {
-#pragma unroll
-            for (int i = 0; i < 9; ++i) cur[i] = nxt[i];
-            if (ks + 4 < nks) load_group((ks >> 2) + 1, nxt);
-          }
-          const uint32_t* cw = reinterpret_cast<const uint32_t*>(cur);
-#pragma unroll
-          for (int i = 0; i < 9; ++i) {
-            // word 9j+i of the 36-word group, with j only known at run time:
-            // select among the four compile-time candidates
-            const uint32_t c0 = cw[i], c1 = cw[9 + i], c2 = cw[18 + i], c3 = cw[27 + i];
-            w[i] = j == 0 ? c0 : (j == 1 ? c1 : (j == 2 ? c2 : c3));
-          }
-        } else {
-          const uint32_t* src = reinterpret_cast<const uint32_t*>(row + (size_t)ks * kPairB);
-#pragma unroll
-          for (int i = 0; i < 9; ++i) w[i] = __ldg(src + i);
-        }
+      // One K-step: wait for the stage, dequantise this thread's 64 weights
+      // (one block pair, nine words w) into the swizzled A tile, publish.
+      auto step = [&](const uint32_t (&w)[9]) -> bool {
         const int s = it % S::kStages;
-        if (!mbar_wait(&empty[s], ((it / S::kStages) & 1) ^ 1, p.status)) { ok = false; break; }
+        if (!mbar_wait(&empty[s], ((it / S::kStages) & 1) ^ 1, p.status)) return false;
         uint8_t* st = stages + (size_t)s * S::kStage;
         uint32_t q0[4], q1[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) q0[i] = __byte_perm(w[i], w[i + 1], 0x5432);
+        for (int i = 0; i < 4; ++i) q0[i] = prmt(w[i], w[i + 1], 0x5432u);
 #pragma unroll
         for (int i = 0; i < 4; ++i) q1[i] = w[5 + i];
         const uint16_t d0 = (uint16_t)(w[0] & 0xFFFFu), d1 = (uint16_t)(w[4] >> 16);
@@ -499,6 +472,43 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&full_a[s]);
+        ++it;
+        return true;
+      };
+      if ((nks & 3) == 0) {
+        // raw bytes four K-steps (144 bytes) at a time, double-buffered in
+        // registers; the four steps of a group are unrolled so that every
+        // word comes from a fixed register
+        uint4 cur[9], nxt[9];
+        auto load_group = [&](int g, uint4 (&dst)[9]) {
+          const uint4* src = reinterpret_cast<const uint4*>(row + (size_t)g * 4 * kPairB);
+#pragma unroll
+          for (int i = 0; i < 9; ++i) dst[i] = __ldg(src + i);
+        };
+        load_group(0, nxt);
+#pragma unroll 1
+        for (int g = 0; ok && g < nks / 4; ++g) {
+#pragma unroll
+          for (int i = 0; i < 9; ++i) cur[i] = nxt[i];
+          if (g + 1 < nks / 4) load_group(g + 1, nxt);
+          const uint32_t* cw = reinterpret_cast<const uint32_t*>(cur);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t w[9];
+#pragma unroll
+            for (int i = 0; i < 9; ++i) w[i] = cw[9 * j + i];
+            if (!step(w)) { ok = false; break; }
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int ks = 0; ok && ks < nks; ++ks) {
+          const uint32_t* src = reinterpret_cast<const uint32_t*>(row + (size_t)ks * kPairB);
+          uint32_t w[9];
+#pragma unroll
+          for (int i = 0; i < 9; ++i) w[i] = __ldg(src + i);
+          if (!step(w)) ok = false;
+        }
       }
       if (!ok) break;
       // epilogue: TMEM lanes of this warp's quarter, half of the token columns

@@ -108,17 +108,17 @@ constexpr uint32_t kTabU3 = 0xF1D9C5B5u;   // T[12..15]+128 = 181, 197, 217, 241
 
 // Eight codes (4 index bytes) -> the 8 offset table values in K order:
 // lo = (U[lo nibble of byte 0..3]), hi = (U[hi nibble of byte 0..3]).
+// prmt with selector nibbles whose bit 3 is clear (one instruction; the
+// __byte_perm intrinsic masks a run-time selector itself).
 __device__ __forceinline__ void iq4_lookup8_split(uint32_t q, uint32_t& lo, uint32_t& hi) {
-  const uint32_t sel = 0x32103210u | ((q & 0x88888888u) >> 1);
-  const uint32_t a0 = __byte_perm(kTabU0, kTabU1, q);
-  const uint32_t b0 = __byte_perm(kTabU2, kTabU3, q);
-  const uint32_t r0 = __byte_perm(a0, b0, sel);          // L0 H0 L1 H1
-  const uint32_t q1 = q >> 16;
-  const uint32_t a1 = __byte_perm(kTabU0, kTabU1, q1);
-  const uint32_t b1 = __byte_perm(kTabU2, kTabU3, q1);
-  const uint32_t r1 = __byte_perm(a1, b1, sel >> 16);    // L2 H2 L3 H3
-  lo = __byte_perm(r0, r1, 0x6420);
-  hi = __byte_perm(r0, r1, 0x7531);
+  const uint32_t qm = q & 0x77777777u;
+  const uint32_t sel = 0x32103210u | ((q >> 1) & 0x44444444u);
+  const uint32_t r0 = prmt(prmt(kTabU0, kTabU1, qm), prmt(kTabU2, kTabU3, qm), sel);  // L0 H0 L1 H1
+  const uint32_t qm1 = qm >> 16;
+  const uint32_t r1 =
+      prmt(prmt(kTabU0, kTabU1, qm1), prmt(kTabU2, kTabU3, qm1), sel >> 16);         // L2 H2 L3 H3
+  lo = prmt(r0, r1, 0x6420u);
+  hi = prmt(r0, r1, 0x7531u);
 }
 
 // Four offset-table bytes -> four fp16 d*T, each the round-to-nearest-even of
@@ -126,8 +126,8 @@ __device__ __forceinline__ void iq4_lookup8_split(uint32_t q, uint32_t& lo, uint
 __device__ __forceinline__ void offsets_to_half4(uint32_t u, __half2 d2, uint32_t& o01,
                                                  uint32_t& o23) {
   const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-  uint32_t h01 = __byte_perm(u, 0x64646464u, 0x4140);
-  uint32_t h23 = __byte_perm(u, 0x64646464u, 0x4342);
+  uint32_t h01 = prmt(u, 0x64646464u, 0x4140u);
+  uint32_t h23 = prmt(u, 0x64646464u, 0x4342u);
   __half2 t01 = __hsub2(*reinterpret_cast<__half2*>(&h01), bias);
   __half2 t23 = __hsub2(*reinterpret_cast<__half2*>(&h23), bias);
   __half2 w01 = __hmul2(t01, d2);
