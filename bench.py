@@ -78,6 +78,25 @@ def workload(cfg: int, tokens, layers=None):
     return s, T
 
 
+# ---------------------------------------------------------------- replicas
+
+def max_over_ranks(value: float, dist=None, device="cpu") -> float:
+    """The largest of every rank's value (the step time of the slowest
+    replica); the value itself on one process."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, world: int, seconds: float) -> float:
+    """Units all ranks processed per second of the slowest rank (replicas:
+    every rank runs its own copy of the workload)."""
+    return units_per_rank * world / seconds
+
+
 # ---------------------------------------------------------------- ncu traffic
 
 PROFILE_DECODE_FUSED = "decode_fused_xing_decode.md"
@@ -401,11 +420,7 @@ def run_libmoe(args):
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1) / args.steps
-    t_max = torch.tensor([ms], device=dev)
-    if dist is not None:
-        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
-    ms = float(t_max.item())
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev)
     st = int(status.item())
 
     # ---- per-call durations: one graph per kind of call over all layers (the
@@ -438,7 +453,7 @@ def run_libmoe(args):
 
     hbm, bf16, peak_kind = peaks()
     tokens = T * world
-    value = tokens * 1000.0 / ms
+    value = whole_job_rate(T, world, ms * 1e-3)
     step_gbs = bytes_per_step / (ms * 1e-3) / 1e9
     achieved = layer_bytes / (layer_ms * 1e-3) / 1e9
     layer_call_ms = layer_ms
@@ -465,12 +480,8 @@ def run_libmoe(args):
             g2.replay()
             host_y.copy_(y, non_blocking=True)
         torch.cuda.synchronize()
-        dt = (time.perf_counter() - t0) / args.steps
-        tmx = torch.tensor([dt], device=dev)
-        if dist is not None:
-            dist.all_reduce(tmx, op=dist.ReduceOp.MAX)
-        dt = float(tmx.item())
-        e2e = {"value": tokens / dt, "unit": UNIT,
+        dt = max_over_ranks((time.perf_counter() - t0) / args.steps, dist, dev)
+        e2e = {"value": whole_job_rate(T, world, dt), "unit": UNIT,
                "h2d_bytes_per_step": int(xin.numel() * xin.element_size()),
                "d2h_bytes_per_step": int(y.numel() * y.element_size())}
 
