@@ -554,48 +554,87 @@ inline __device__ void flush_arrivals(const DecodeParams& p, const RouteTable& r
 // shared memory in list order (the valid routed pairs as rt.list orders them,
 // F values each, then the shared expert's rows, Fs values each); otherwise
 // they are read from global memory through L2 (written by other CTAs).
+// Two lanes per 32-value block: lane s = lane & 1 quantises values 8s..8s+7
+// and 16+8s..16+8s+7, i.e. exactly the pair words 8s..8s+7 (value j with
+// value j + 16); the block's largest exponent is combined by one shuffle.
+__device__ __forceinline__ void quant_half_block(const float4 (&f)[4], bool ok, int b, int K,
+                                                 uint32_t* rec) {
+  const int s = threadIdx.x & 1;
+  const float v[16] = {f[0].x, f[0].y, f[0].z, f[0].w, f[1].x, f[1].y, f[1].z, f[1].w,
+                       f[2].x, f[2].y, f[2].z, f[2].w, f[3].x, f[3].y, f[3].z, f[3].w};
+  uint32_t e = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t ei = (__float_as_uint(v[i]) >> 23) & 0xFFu;
+    e = ei > e ? ei : e;
+  }
+  const uint32_t o = __shfl_xor_sync(0xFFFFFFFFu, e, 1);
+  e = o > e ? o : e;
+  if (ok) {
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      w[i] = (uint32_t)(quant_one(v[i], e) & 0xFFFF) | ((uint32_t)quant_one(v[8 + i], e) << 16);
+    const int lpr = dlanes_per_row(K);
+    const int q = b >> 1;
+    const int c0 = 4 * (b & 1) + 2 * s;
+    uint4* r4 = reinterpret_cast<uint4*>(rec);
+    r4[qv_u4(q, c0, lpr)] = make_uint4(w[0], w[1], w[2], w[3]);
+    r4[qv_u4(q, c0 + 1, lpr)] = make_uint4(w[4], w[5], w[6], w[7]);
+    if (s == 0) reinterpret_cast<float*>(rec + dqvec_pair_words(K))[b] = quant_scale(e);
+  }
+}
+
+// floor(n / d) for 0 <= n < 2^16 and 1 <= d < 2^16 with inv = ceil(2^32 / d).
+__device__ __forceinline__ int div_by_inv(int n, uint32_t inv) {
+  return (int)__umulhi((uint32_t)n, inv);
+}
+
 template <bool STAGED>
 __device__ __forceinline__ void quant_h(const DecodeParams& p, const RouteTable& rt,
                                         const float* stage, uint32_t* recs, int tid, int nt) {
   const int nbF = p.F / 32;
   const int nbS = p.n_shared ? p.Fs / 32 : 1;
+  const uint32_t invF = 0xFFFFFFFFu / (uint32_t)nbF + 1u;
+  const uint32_t invS = 0xFFFFFFFFu / (uint32_t)nbS + 1u;
   const int wF = dqvec_words(p.F);
   const int wS = p.n_shared ? dqvec_words(p.Fs) : 0;
   uint32_t* rec_sh = recs + (size_t)p.T * p.k * wF;
   const int nr = rt.n_valid * nbF;
   const int total = nr + (p.n_shared ? p.T * nbS : 0);
 #pragma unroll 1
-  for (int i0 = tid & ~31; i0 < total * 4; i0 += nt) {
+  for (int i0 = tid & ~31; i0 < total * 2; i0 += nt) {
     const int i = i0 + (tid & 31);
-    const bool ok = i < total * 4;
-    const int blk = ok ? i >> 2 : 0;
+    const bool ok = i < total * 2;
+    const int blk = ok ? i >> 1 : 0;
+    const int s = i & 1;
     uint32_t* dst;
+    const float* row;
     int b, K;
     if (blk < nr) {
-      const int e = blk / nbF;
+      const int e = div_by_inv(blk, invF);
       b = blk - e * nbF;
       K = p.F;
       dst = recs + (size_t)rt.list[e] * wF;
+      row = p.h_r + (size_t)rt.list[e] * p.F;
     } else {
-      const int j = (blk - nr) / nbS;
+      const int j = div_by_inv(blk - nr, invS);
       b = (blk - nr) - j * nbS;
       K = p.Fs;
       dst = rec_sh + (size_t)j * wS;
+      row = p.h_s + (size_t)j * p.Fs;
     }
-    float4 f0 = make_float4(0.f, 0.f, 0.f, 0.f), f1 = f0;
+    float4 f[4];
+    const float* src = STAGED ? stage + (size_t)blk * 32 : row + b * 32;
+    const float4* s4 = reinterpret_cast<const float4*>(src + 8 * s);
     if (STAGED) {
-      const float4* s4 = reinterpret_cast<const float4*>(stage + (size_t)blk * 32 + 8 * (i & 3));
-      f0 = s4[0];
-      f1 = s4[1];
+      f[0] = s4[0]; f[1] = s4[1]; f[2] = s4[4]; f[3] = s4[5];
     } else if (ok) {
-      const float* row = blk < nr ? p.h_r + (size_t)rt.list[blk / nbF] * p.F
-                                  : p.h_s + (size_t)((blk - nr) / nbS) * p.Fs;
-      const float4* s4 = reinterpret_cast<const float4*>(row + b * 32 + 8 * (i & 3));
-      f0 = __ldcg(s4);
-      f1 = __ldcg(s4 + 1);
+      f[0] = __ldcg(s4); f[1] = __ldcg(s4 + 1); f[2] = __ldcg(s4 + 4); f[3] = __ldcg(s4 + 5);
+    } else {
+      f[0] = f[1] = f[2] = f[3] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    const float v[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
-    quant_group8(v, ok, b, K, dst);
+    quant_half_block(f, ok, b, K, dst);
   }
 }
 
