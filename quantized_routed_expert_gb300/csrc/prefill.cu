@@ -235,8 +235,6 @@ __global__ void pf_gather_kernel(const uint16_t* __restrict__ x, const int32_t* 
 constexpr int kTM = 128;
 constexpr int kTN = 256;
 constexpr int kTK = 64;
-constexpr int kGThreads = 320;
-constexpr int kDqWarps = 8;
 
 struct GemmParams {
   int E, n_shared;
@@ -254,14 +252,28 @@ struct GemmParams {
   uint32_t* status;
 };
 
-template <bool GATEUP>
-struct GemmSmem {
-  static constexpr int kA = kTM * kTK * 2;                     // 16 KB
-  static constexpr int kB = kTN * kTK * 2;                     // 32 KB
+// Shared memory and warp roles of the GEMM kernels. RAW: the IQ4_NL rows of the
+// weight tile arrive by 2D bulk copies, four K-steps (144 bytes) per row per
+// copy, into a ring the dequantising warps read (the reduction length is a
+// multiple of 256 so the row pitch is a multiple of 16 bytes); otherwise each
+// dequantising thread loads its own row from global memory.
+template <bool GATEUP, bool RAW>
+struct GemmCfg {
+  static constexpr int kCtl = RAW ? 3 : 2;                        // control warps
+  static constexpr int kDq = (RAW && GATEUP) ? 16 : 8;            // dequantising warps
+  static constexpr int kThreads = (kCtl + kDq) * 32;
+  static constexpr int kA = kTM * kTK * 2;                        // 16 KB
+  static constexpr int kB = kTN * kTK * 2;                        // 32 KB
   static constexpr int kStage = (GATEUP ? 2 : 1) * kA + kB;
-  static constexpr int kStages = GATEUP ? 3 : 4;
-  static constexpr int kBars = 3 * kStages + 2;
-  static constexpr size_t kTotal = 1024 /*align slack*/ + (size_t)kStages * kStage + 4096;
+  static constexpr int kStages = RAW ? (GATEUP ? 2 : 3) : (GATEUP ? 3 : 4);
+  static constexpr int kRawGroup = 4;                             // K-steps per raw copy
+  static constexpr int kRawMat = kTM * kRawGroup * kPairB;        // 18 KB per matrix
+  static constexpr int kRawStage = (GATEUP ? 2 : 1) * kRawMat;
+  static constexpr int kRawRing = 2;                              // raw ring depth
+  static constexpr int kRawStages = RAW ? kRawRing : 0;           // raw stages allocated
+  static constexpr int kBars = 3 * kStages + 2 + 2 * kRawStages;
+  static constexpr size_t kTotal =
+      1024 /*align slack*/ + (size_t)kStages * kStage + (size_t)kRawStages * kRawStage + 4096;
 };
 
 __device__ __forceinline__ void sw128_store_chunk(uint8_t* tile, int r, int c, uint4 v) {
@@ -296,26 +308,30 @@ struct TileInfo {
 // skewed routing most buckets hold far fewer than 256 tokens.
 constexpr int kNumBoxes = 4;                 // 32, 64, 128, 256 rows
 struct TmapSet {
-  CUtensorMap m[kNumBoxes];
+  CUtensorMap m[kNumBoxes];   // token rows, by box height
+  CUtensorMap raw[4];         // IQ4_NL rows (bytes): routed gate|down, routed up, shared gate|down, shared up
 };
 __device__ __forceinline__ int box_index(int n) {
   return n <= 32 ? 0 : (n <= 64 ? 1 : (n <= 128 ? 2 : 3));
 }
 
-template <bool GATEUP>
-__global__ void __launch_bounds__(kGThreads, 1)
+template <bool GATEUP, bool RAW>
+__global__ void __launch_bounds__(GemmCfg<GATEUP, RAW>::kThreads, 1)
 pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
-  using S = GemmSmem<GATEUP>;
+  using S = GemmCfg<GATEUP, RAW>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S::kStages * S::kStage);
+  uint8_t* raw = smem + (size_t)S::kStages * S::kStage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(raw + (size_t)S::kRawStages * S::kRawStage);
   uint64_t* full_a = bars;
   uint64_t* full_b = bars + S::kStages;
   uint64_t* empty = bars + 2 * S::kStages;
   uint64_t* acc_full = bars + 3 * S::kStages;
   uint64_t* acc_empty = acc_full + 1;
+  uint64_t* full_raw = acc_empty + 1;
+  uint64_t* empty_raw = full_raw + S::kRawStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + S::kBars);
   int* boff = reinterpret_cast<int*>(tmem_slot + 4);           // [E+2] bucket offsets
   int* tpre = boff + (p.E + 2);                                 // [E+2] tile prefix
@@ -323,12 +339,16 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S::kStages; ++s) {
-      mbar_init(&full_a[s], kDqWarps);
+      mbar_init(&full_a[s], S::kDq);
       mbar_init(&full_b[s], 1);
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, kDqWarps);
+    mbar_init(acc_empty, S::kDq);
+    for (int s = 0; s < S::kRawStages; ++s) {
+      mbar_init(&full_raw[s], 1);
+      mbar_init(&empty_raw[s], S::kDq);
+    }
     mbar_fence_init();
   }
   if (warp == 1) tmem_alloc(tmem_slot, 512);
@@ -336,7 +356,7 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
   pdl_trigger();
   // bucket offsets and the tile prefix (tiles of a bucket: weight tiles x token tiles)
   const int nb = p.E + p.n_shared;
-  for (int i = threadIdx.x; i < p.E + 2; i += kGThreads) boff[i] = p.bucket_off[i];
+  for (int i = threadIdx.x; i < p.E + 2; i += S::kThreads) boff[i] = p.bucket_off[i];
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -427,98 +447,162 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
         tc_commit(acc_full);
       }
     }
+  } else if (RAW && warp == 2) {
+    // ---- IQ4_NL rows of the weight tiles by TMA, four K-steps per copy
+    if (lane == 0) {
+      int it = 0;
+      for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+        const TileInfo ti = tile_info(t);
+        const bool sh = ti.bucket >= p.E;
+        const int K = sh ? p.Ks : p.K;
+        const int row = (sh ? 0 : ti.bucket * p.M) + ti.m0;
+        bool ok = true;
+        for (int g = 0; g < K / (kTK * S::kRawGroup); ++g, ++it) {
+          const int s = it % S::kRawRing;
+          if (!mbar_wait(&empty_raw[s], ((it / S::kRawRing) & 1) ^ 1, p.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* dst = raw + (size_t)s * S::kRawStage;
+          mbar_arrive_expect_tx(&full_raw[s], (uint32_t)S::kRawStage);
+          tma_load_2d(dst, &tmaps.raw[sh ? 2 : 0], g * S::kRawGroup * kPairB, row, &full_raw[s]);
+          if (GATEUP)
+            tma_load_2d(dst + S::kRawMat, &tmaps.raw[sh ? 3 : 1], g * S::kRawGroup * kPairB, row,
+                        &full_raw[s]);
+        }
+        if (!ok) break;
+      }
+    }
   } else {
     // ---- dequantise weight tiles, then the epilogue of each tile
-    const int d = threadIdx.x - 64;             // 0..255
-    const int dw = warp - 2;                    // 0..7
+    const int d = threadIdx.x - S::kCtl * 32;
+    const int dw = warp - S::kCtl;
     const int r = d & (kTM - 1);
-    const int part = d >> 7;                    // gate/up: matrix; down: block of the pair
-    int it = 0, tc = 0;
+    // RAW gate/up: (row, matrix, block of the pair) per thread; otherwise
+    // gate/up: (row, matrix), a whole pair per K-step; down: (row, block).
+    const int part = (RAW && GATEUP) ? ((d >> 7) & 1) : (d >> 7);
+    const int blkh = (RAW && GATEUP) ? (d >> 8) : part;
+    int it = 0, itr = 0, tc = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++tc) {
       const TileInfo ti = tile_info(t);
       const bool sh = ti.bucket >= p.E;
       const int K = sh ? p.Ks : p.K;
-      const int M = sh ? p.Ms : p.M;
-      const size_t rb = (size_t)(K / 32) * kBlockB;
-      const uint8_t* mat;
-      if (GATEUP) mat = sh ? (part ? p.s1 : p.s0) : (part ? p.a1 : p.a0);
-      else mat = sh ? p.s0 : p.a0;
-      const uint8_t* row = mat + ((sh ? 0 : (size_t)ti.bucket * M) + ti.m0 + r) * rb;
-      // Raw IQ4_NL bytes of this thread's row, four K-steps (144 bytes) per
-      // load group, double-buffered in registers; rows whose length is not a
-      // multiple of four pairs use 4-byte loads.
       const int nks = K / kTK;
-      // One K-step: wait for the stage, dequantise this thread's 64 weights
-      // (one block pair, nine words w) into the swizzled A tile, publish.
-      auto step = [&](const uint32_t (&w)[9]) -> bool {
-        const int s = it % S::kStages;
-        if (!mbar_wait(&empty[s], ((it / S::kStages) & 1) ^ 1, p.status)) return false;
-        uint8_t* st = stages + (size_t)s * S::kStage;
-        uint32_t q0[4], q1[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) q0[i] = prmt(w[i], w[i + 1], 0x5432u);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) q1[i] = w[5 + i];
-        const uint16_t d0 = (uint16_t)(w[0] & 0xFFFFu), d1 = (uint16_t)(w[4] >> 16);
-        if (GATEUP) {
-          uint8_t* tile = st + part * S::kA;
-          dequant_block_to_tile(q0, d0, tile, r, 0);
-          dequant_block_to_tile(q1, d1, tile, r, 4);
-        } else {
-          if (part == 0) dequant_block_to_tile(q0, d0, st, r, 0);
-          else dequant_block_to_tile(q1, d1, st, r, 4);
-        }
+      // publish one dequantised K-step of this thread
+      auto publish = [&](int s) {
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&full_a[s]);
         ++it;
-        return true;
       };
-      if ((nks & 3) == 0) {
-        // raw bytes four K-steps (144 bytes) at a time, double-buffered in
-        // registers; the four steps of a group are unrolled so that every
-        // word comes from a fixed register
-        uint4 cur[9], nxt[9];
-        auto load_group = [&](int g, uint4 (&dst)[9]) {
-          const uint4* src = reinterpret_cast<const uint4*>(row + (size_t)g * 4 * kPairB);
+      if constexpr (RAW) {
+        for (int g = 0; ok && g < nks / S::kRawGroup; ++g, ++itr) {
+          const int sr = itr % S::kRawRing;
+          if (!mbar_wait(&full_raw[sr], (itr / S::kRawRing) & 1, p.status)) { ok = false; break; }
+          const uint8_t* rrow = raw + (size_t)sr * S::kRawStage + (GATEUP ? part * S::kRawMat : 0) +
+                                (size_t)r * S::kRawGroup * kPairB;
 #pragma unroll
-          for (int i = 0; i < 9; ++i) dst[i] = __ldg(src + i);
-        };
-        load_group(0, nxt);
-#pragma unroll 1
-        for (int g = 0; ok && g < nks / 4; ++g) {
-#pragma unroll
-          for (int i = 0; i < 9; ++i) cur[i] = nxt[i];
-          if (g + 1 < nks / 4) load_group(g + 1, nxt);
-          const uint32_t* cw = reinterpret_cast<const uint32_t*>(cur);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint32_t w[9];
-#pragma unroll
-            for (int i = 0; i < 9; ++i) w[i] = cw[9 * j + i];
-            if (!step(w)) { ok = false; break; }
+          for (int j = 0; j < S::kRawGroup; ++j) {
+            const int s = it % S::kStages;
+            if (!mbar_wait(&empty[s], ((it / S::kStages) & 1) ^ 1, p.status)) { ok = false; break; }
+            uint8_t* tile = stages + (size_t)s * S::kStage + (GATEUP ? part * S::kA : 0);
+            const uint32_t* w = reinterpret_cast<const uint32_t*>(rrow + j * kPairB + (blkh ? 16 : 0));
+            uint32_t q[4];
+            uint16_t dbits;
+            if (blkh == 0) {
+              const uint32_t w0 = w[0], w1 = w[1], w2 = w[2], w3 = w[3], w4 = w[4];
+              dbits = (uint16_t)(w0 & 0xFFFFu);
+              q[0] = prmt(w0, w1, 0x5432u);
+              q[1] = prmt(w1, w2, 0x5432u);
+              q[2] = prmt(w2, w3, 0x5432u);
+              q[3] = prmt(w3, w4, 0x5432u);
+            } else {
+              dbits = (uint16_t)(w[0] >> 16);
+              q[0] = w[1]; q[1] = w[2]; q[2] = w[3]; q[3] = w[4];
+            }
+            dequant_block_to_tile(q, dbits, tile, r, 4 * blkh);
+            publish(s);
           }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty_raw[sr]);
         }
       } else {
-#pragma unroll 1
-        for (int ks = 0; ok && ks < nks; ++ks) {
-          const uint32_t* src = reinterpret_cast<const uint32_t*>(row + (size_t)ks * kPairB);
-          uint32_t w[9];
+        const size_t rb = (size_t)(K / 32) * kBlockB;
+        const int M = sh ? p.Ms : p.M;
+        const uint8_t* mat;
+        if (GATEUP) mat = sh ? (part ? p.s1 : p.s0) : (part ? p.a1 : p.a0);
+        else mat = sh ? p.s0 : p.a0;
+        const uint8_t* row = mat + ((sh ? 0 : (size_t)ti.bucket * M) + ti.m0 + r) * rb;
+        // One K-step: wait for the stage, dequantise this thread's weights
+        // (one block pair, nine words w) into the swizzled A tile, publish.
+        auto step = [&](const uint32_t (&w)[9]) -> bool {
+          const int s = it % S::kStages;
+          if (!mbar_wait(&empty[s], ((it / S::kStages) & 1) ^ 1, p.status)) return false;
+          uint8_t* st = stages + (size_t)s * S::kStage;
+          uint32_t q0[4], q1[4];
 #pragma unroll
-          for (int i = 0; i < 9; ++i) w[i] = __ldg(src + i);
-          if (!step(w)) ok = false;
+          for (int i = 0; i < 4; ++i) q0[i] = prmt(w[i], w[i + 1], 0x5432u);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) q1[i] = w[5 + i];
+          const uint16_t d0 = (uint16_t)(w[0] & 0xFFFFu), d1 = (uint16_t)(w[4] >> 16);
+          if (GATEUP) {
+            uint8_t* tile = st + part * S::kA;
+            dequant_block_to_tile(q0, d0, tile, r, 0);
+            dequant_block_to_tile(q1, d1, tile, r, 4);
+          } else {
+            if (part == 0) dequant_block_to_tile(q0, d0, st, r, 0);
+            else dequant_block_to_tile(q1, d1, st, r, 4);
+          }
+          publish(s);
+          return true;
+        };
+        if ((nks & 3) == 0) {
+          // raw bytes four K-steps (144 bytes) at a time, double-buffered in
+          // registers; the four steps of a group are unrolled so that every
+          // word comes from a fixed register
+          uint4 cur[9], nxt[9];
+          auto load_group = [&](int g, uint4 (&dst)[9]) {
+            const uint4* src = reinterpret_cast<const uint4*>(row + (size_t)g * 4 * kPairB);
+#pragma unroll
+            for (int i = 0; i < 9; ++i) dst[i] = __ldg(src + i);
+          };
+          load_group(0, nxt);
+#pragma unroll 1
+          for (int g = 0; ok && g < nks / 4; ++g) {
+#pragma unroll
+            for (int i = 0; i < 9; ++i) cur[i] = nxt[i];
+            if (g + 1 < nks / 4) load_group(g + 1, nxt);
+            const uint32_t* cw = reinterpret_cast<const uint32_t*>(cur);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint32_t w[9];
+#pragma unroll
+              for (int i = 0; i < 9; ++i) w[i] = cw[9 * j + i];
+              if (!step(w)) { ok = false; break; }
+            }
+          }
+        } else {
+#pragma unroll 1
+          for (int ks = 0; ok && ks < nks; ++ks) {
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(row + (size_t)ks * kPairB);
+            uint32_t w[9];
+#pragma unroll
+            for (int i = 0; i < 9; ++i) w[i] = __ldg(src + i);
+            if (!step(w)) ok = false;
+          }
         }
       }
       if (!ok) break;
-      // epilogue: TMEM lanes of this warp's quarter, half of the token columns
+      // epilogue: TMEM lanes of this warp's quarter, a share of the token columns
       if (!mbar_wait(acc_full, tc & 1, p.status)) { ok = false; break; }
       tc_fence_after();
       const int q = warp & 3;
-      const int ch = dw >> 2;                   // column half
+      constexpr int kCols = kTN / (S::kDq / 4);
+      const int ch = dw >> 2;                   // column share
       const int mrow = ti.m0 + q * 32 + lane;   // weight row of this thread
-      for (int c = 0; c < kTN / 2; c += 32) {
-        const int col = ch * (kTN / 2) + c;
+      for (int c = 0; c < kCols; c += 32) {
+        const int col = ch * kCols + c;
         if (col >= ti.nvalid) break;            // warp-uniform
         uint32_t g[32];
         tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + col, g);
@@ -617,6 +701,24 @@ bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, i
   return r == CUDA_SUCCESS;
 }
 
+// IQ4_NL rows (bytes) of a stacked weight matrix: rows x (K/32 * 18) bytes;
+// boxes of 144 bytes (four block pairs) x 128 rows. Needs the row pitch to be
+// a multiple of 16 bytes (K a multiple of 256).
+bool make_raw_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t K) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const int64_t rb = K / 32 * kBlockB;
+  cuuint64_t dims[2] = {(cuuint64_t)rb, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)rb};
+  cuuint32_t box[2] = {(cuuint32_t)(4 * kPairB), (cuuint32_t)kTM};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <typename Kern, typename... Args>
 cudaError_t launch_ex(Kern kernel, dim3 grid, dim3 block, size_t smem, bool pdl,
                       cudaStream_t stream, Args... args) {
@@ -631,6 +733,18 @@ cudaError_t launch_ex(Kern kernel, dim3 grid, dim3 block, size_t smem, bool pdl,
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+template <bool GATEUP, bool RAW>
+cudaError_t launch_gemm(int num_sms, int E, bool pdl, cudaStream_t stream, const TmapSet& tm,
+                        const GemmParams& g) {
+  using S = GemmCfg<GATEUP, RAW>;
+  const size_t sm = S::kTotal + (size_t)(E + 2) * 8;
+  const cudaError_t e =
+      ensure_smem_attr(reinterpret_cast<const void*>(pf_gemm_kernel<GATEUP, RAW>), sm);
+  if (e != cudaSuccess) return e;
+  return launch_ex(pf_gemm_kernel<GATEUP, RAW>, dim3(num_sms), dim3(S::kThreads), sm, pdl, stream,
+                   tm, g);
 }
 
 }  // namespace
@@ -690,10 +804,19 @@ cudaError_t launch_prefill(const moe_shape& s, const moe_expert_weights& w, cons
   g1.h = h16;
   g1.ldh = fmax;
   g1.status = status;
-  const size_t sm1 = GemmSmem<true>::kTotal + (size_t)(E + 2) * 8;
-  e = ensure_smem_attr(reinterpret_cast<const void*>(pf_gemm_kernel<true>), sm1);
-  if (e != cudaSuccess) return e;
-  e = launch_ex(pf_gemm_kernel<true>, dim3(num_sms), dim3(kGThreads), sm1, pdl, stream, tm_x, g1);
+  // raw-weight copies when the reduction lengths keep row pitches 16-byte aligned
+  const bool raw1 = H % 256 == 0;
+  const bool raw2 = F % 256 == 0 && (!s.n_shared || Fs % 256 == 0);
+  if (raw1 && (!make_raw_tmap(&tm_x.raw[0], w.gate, (int64_t)E * F, H) ||
+               !make_raw_tmap(&tm_x.raw[1], w.up, (int64_t)E * F, H) ||
+               (s.n_shared && (!make_raw_tmap(&tm_x.raw[2], w.sh_gate, Fs, H) ||
+                               !make_raw_tmap(&tm_x.raw[3], w.sh_up, Fs, H)))))
+    return cudaErrorInvalidValue;
+  if (raw2 && (!make_raw_tmap(&tm_h.raw[0], w.down, (int64_t)E * H, F) ||
+               (s.n_shared && !make_raw_tmap(&tm_h.raw[2], w.sh_down, H, Fs))))
+    return cudaErrorInvalidValue;
+  e = raw1 ? launch_gemm<true, true>(num_sms, E, pdl, stream, tm_x, g1)
+           : launch_gemm<true, false>(num_sms, E, pdl, stream, tm_x, g1);
   if (e != cudaSuccess) return e;
 
   GemmParams g2 = g1;
@@ -708,10 +831,8 @@ cudaError_t launch_prefill(const moe_shape& s, const moe_expert_weights& w, cons
   g2.h = nullptr;
   g2.o = o;
   g2.ldo = H;
-  const size_t sm2 = GemmSmem<false>::kTotal + (size_t)(E + 2) * 8;
-  e = ensure_smem_attr(reinterpret_cast<const void*>(pf_gemm_kernel<false>), sm2);
-  if (e != cudaSuccess) return e;
-  e = launch_ex(pf_gemm_kernel<false>, dim3(num_sms), dim3(kGThreads), sm2, pdl, stream, tm_h, g2);
+  e = raw2 ? launch_gemm<false, true>(num_sms, E, pdl, stream, tm_h, g2)
+           : launch_gemm<false, false>(num_sms, E, pdl, stream, tm_h, g2);
   if (e != cudaSuccess) return e;
 
   const int64_t total = (int64_t)T * (H / 4);
