@@ -222,6 +222,27 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   }
 }
 
+// Bounded wait, by the whole warp, until a shared-memory counter that other
+// warps of the CTA raise reaches `target` (acquire at CTA scope: what they
+// wrote before raising it is visible after). false after ~kWaitLimitNs.
+__device__ __forceinline__ uint32_t ld_acquire_cta_shared(const uint32_t* a) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(a)) : "memory");
+  return v;
+}
+__device__ __forceinline__ bool wait_count_cta(const uint32_t* a, uint32_t target,
+                                               uint32_t* status) {
+  if (ld_acquire_cta_shared(a) >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (ld_acquire_cta_shared(a) >= target) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (status) atomicOr(status, MOE_STATUS_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // Global -> shared bulk copy that completes `bytes` of transaction on `bar`.
 // src and dst 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,

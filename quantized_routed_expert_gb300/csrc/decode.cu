@@ -16,116 +16,322 @@
 
 namespace moe {
 
-template <int MAXT>
-__device__ __forceinline__ void gateup_rows(const DecodeParams& p, const RouteTable& rt,
-                                            const uint8_t* stage, const Chunk& ch,
-                                            const uint32_t* xq, int xq_words) {
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  if (warp >= ch.rows) return;
-  const int H = p.H;
-  const int rb = H / 32 * kBlockB;
-  const int npairs = H / 64;
-  const int lpr = dlanes_per_row(H);
-  const int f = ch.f0 + warp;
-  const bool shared = ch.slot < 0;
-  const int F = shared ? p.Fs : p.F;
-  const uint8_t* grow = stage + (size_t)warp * rb;
-  const uint8_t* urow = stage + (size_t)(ch.rows + warp) * rb;
-  // tokens of this slot
-  const int ntok = shared ? p.T : rt.slot_off[ch.slot + 1] - rt.slot_off[ch.slot];
-  const int lbase = shared ? 0 : rt.slot_off[ch.slot];
-  const int xs_off = dqvec_pair_words(H);
+// ---------------------------------------------------------------------------
+// Gate/up + SwiGLU for the shapes and token counts the fused kernel does not
+// take. Every warp streams its own units as the fused kernel does (g
+// consecutive f-rows of one expert per unit, g the rows that make a copy a
+// multiple of 16 bytes; two bulk-copy slots per warp) and computes each row
+// with the same per-row code, so every h value is bitwise the fused kernel's.
+//
+// Work goes to CTAs in whole 32-row blocks (the quantisation blocks of h), so
+// each block of h is completed inside one CTA: a shared-memory counter per
+// block collects the rows, and the warp that adds the last row quantises the
+// block for every token of its expert into the records the down kernel reads.
+// The shared expert's blocks go one each to the last CTAs (evenly, if there
+// are more blocks than CTAs); the routed blocks (slot-major) are then split so
+// that every CTA gets about the same compute, by the measured cost of a row
+// for n tokens (gu_cost, in tenths of a one-token row).
+constexpr int kGuSlots = 2;
+constexpr int kGuMaxT = 4;        // tokens per pass over a row (more: several passes)
 
-  for (int g0 = 0; g0 < ntok; g0 += MAXT) {
-    const int ng = ntok - g0 < MAXT ? ntok - g0 : MAXT;
-    int tok[MAXT];
-#pragma unroll
-    for (int j = 0; j < MAXT; ++j) {
-      const int jj = g0 + (j < ng ? j : 0);
-      tok[j] = shared ? jj : rt.list[lbase + jj] / p.k;
-    }
-    float ag[MAXT], au[MAXT];
-#pragma unroll
-    for (int j = 0; j < MAXT; ++j) ag[j] = au[j] = 0.0f;
-
-    for (int q = lane; q < npairs; q += 32) {
-      const int qbase = qv_base(q, lpr);
-      uint32_t w[9];
-      float dg0, dg1, du0, du1;
-      uint32_t a0[4], a1[4];
-      uint32_t tg0[8], tg1[8], tu0[8], tu1[8];
-      load_pair_smem(grow + q * kPairB, w);
-      split_pair(w, dg0, dg1, a0, a1);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        iq4_lookup8(a0[i], tg0[2 * i], tg0[2 * i + 1]);
-        iq4_lookup8(a1[i], tg1[2 * i], tg1[2 * i + 1]);
-      }
-      load_pair_smem(urow + q * kPairB, w);
-      split_pair(w, du0, du1, a0, a1);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        iq4_lookup8(a0[i], tu0[2 * i], tu0[2 * i + 1]);
-        iq4_lookup8(a1[i], tu1[2 * i], tu1[2 * i + 1]);
-      }
-#pragma unroll
-      for (int j = 0; j < MAXT; ++j) {
-        if (j < ng) {
-          const uint32_t* rec = xq + (size_t)tok[j] * xq_words;
-          const uint4* r4 = reinterpret_cast<const uint4*>(rec) + qbase;
-          uint32_t v[32];
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint4 u = r4[c * lpr];
-            v[4 * c] = u.x; v[4 * c + 1] = u.y; v[4 * c + 2] = u.z; v[4 * c + 3] = u.w;
-          }
-          const float* xs = reinterpret_cast<const float*>(rec + xs_off);
-          const float s0 = xs[2 * q], s1 = xs[2 * q + 1];
-          const int ig0 = iq4_dot_block(tg0, v);
-          const int ig1 = iq4_dot_block(tg1, v + 16);
-          const int iu0 = iq4_dot_block(tu0, v);
-          const int iu1 = iq4_dot_block(tu1, v + 16);
-          ag[j] = fmaf((float)ig0, dg0 * s0, ag[j]);
-          ag[j] = fmaf((float)ig1, dg1 * s1, ag[j]);
-          au[j] = fmaf((float)iu0, du0 * s0, au[j]);
-          au[j] = fmaf((float)iu1, du1 * s1, au[j]);
-        }
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < MAXT; ++j) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        ag[j] += __shfl_xor_sync(0xFFFFFFFFu, ag[j], o);
-        au[j] += __shfl_xor_sync(0xFFFFFFFFu, au[j], o);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < MAXT; ++j) {
-      if (j < ng && lane == j) {
-        const float hv = silu_mul(ag[j], au[j]);
-        if (shared) p.h_s[(size_t)tok[j] * p.Fs + f] = hv;
-        else p.h_r[(size_t)rt.list[lbase + g0 + j] * p.F + f] = hv;
-      }
-    }
-  }
-
+// Cost of a row with n tokens: one token 10 (its own code path); otherwise
+// passes of up to 4 tokens, a full pass 24 and a last pass of 1, 2 or 3
+// tokens 12, 18, 21 (rates of the unit code on the GPU).
+__host__ __device__ inline int gu_cost(int n) {
+  if (n <= 1) return 10;
+  const int r = n & 3;
+  return (n >> 2) * 24 + (r == 0 ? 0 : r == 1 ? 12 : r == 2 ? 18 : 21);
 }
 
-// ---------------------------------------------------------------------------
-// Shared-memory layouts (host and device agree on them).
+__host__ __device__ inline int gu_shared_cum(int S, int c, int G) {
+  return S <= G ? (c > G - S ? c - (G - S) : 0) : S * c / G;
+}
+// Routed blocks of CTAs 0..c-1 (non-decreasing in c; all routed blocks at
+// c = G). bps: blocks per slot. All 32 lanes of a warp call it and get the
+// same value. 32-bit arithmetic suffices: the total cost is below 2^22 (at
+// most 256 slots x 256 blocks x cost 12 per token) and G below 2^9.
+__device__ __forceinline__ int gu_routed_cum(const RouteTable& rt, int bps, int S, int T, int c,
+                                             int G) {
+  const int lane = threadIdx.x & 31;
+  const int ns = rt.n_slots;
+  // slot costs: lane l sums slots 8l .. 8l+7; exclusive scan over lanes
+  int mine = 0;
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const int sl = lane * 8 + m;
+    if (sl < ns) mine += bps * gu_cost(rt.slot_off[sl + 1] - rt.slot_off[sl]);
+  }
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const int rcost = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  const int ws = gu_cost(T);
+  const int tot = S * ws + rcost;
+  // the routed cost that CTAs 0..c-1 take, made non-decreasing
+  int best = 0;
+#pragma unroll 1
+  for (int i = 1 + lane; i <= c; i += 32) {
+    int v = tot * i / G - ws * gu_shared_cum(S, i, G);
+    v = v > rcost ? rcost : v;
+    best = v > best ? v : best;
+  }
+  const int X = (int)__reduce_max_sync(0xFFFFFFFFu, (unsigned)best);
+  if (X >= rcost) return ns * bps;
+  // the slot holding cost X, and the whole blocks of it below X
+  int res = 0;
+  const int start = incl - mine;
+  const bool here = start <= X && X < incl;
+  if (here) {
+    int pc = start;
+#pragma unroll 1
+    for (int m = 0; m < 8; ++m) {
+      const int sl = lane * 8 + m;
+      const int cs = gu_cost(rt.slot_off[sl + 1] - rt.slot_off[sl]);
+      if (X < pc + bps * cs) {
+        res = sl * bps + (X - pc) / cs;
+        break;
+      }
+      pc += bps * cs;
+    }
+  }
+  const unsigned who = __ballot_sync(0xFFFFFFFFu, here);
+  return __shfl_sync(0xFFFFFFFFu, res, __ffs(who) - 1);
+}
+// Most 32-row blocks any CTA can get (slots_max routed experts, P pairs): a
+// CTA takes about tot / G of the cost, a routed block costs at least 10 and
+// all of them at most 12 per pair, and the floors and the block granularity
+// add a few.
+inline int gu_blocks_max(int S, int bps, int slots_max, int P, int T, int G) {
+  const int rmax = bps * (10 * slots_max > 12 * P ? 10 * slots_max : 12 * P);
+  const int tot = S * gu_cost(T) + rmax;
+  const int sh = S <= G ? (S > 0 ? 1 : 0) : (S + G - 1) / G;
+  return tot / (10 * G) + 4 + gu_cost(T) / 10 + sh;
+}
+
 struct GuSmem {
-  size_t xq, bar, ring, stage, total;
+  size_t xq, slots, bars, cnt, total, slot_bytes;
 };
-__host__ __device__ inline GuSmem gu_smem(int H, int T, int nst) {
+// xs: the quantised x records sit in shared memory; otherwise the kernel reads
+// them from the workspace, where quant_x_kernel wrote them. nblk: the block
+// counters a CTA needs.
+__host__ __device__ inline GuSmem gu_smem(int H, int T, int nw, bool xs, int g, int nblk) {
   GuSmem m;
+  m.slot_bytes = align_up_dev((size_t)2 * g * (H / 32) * kBlockB, 128);
   m.xq = align_up_dev(sizeof(RouteTable), 128);
-  m.bar = align_up_dev(m.xq + (size_t)T * dqvec_words(H) * 4, 16);
-  m.ring = align_up_dev(m.bar + (size_t)16 * nst, 128);
-  m.stage = align_up_dev((size_t)2 * kChunkRows * (H / 32) * kBlockB, 128);
-  m.total = m.ring + (size_t)nst * m.stage;
+  m.slots = align_up_dev(m.xq + (xs ? (size_t)T * dqvec_words(H) * 4 : 0), 128);
+  m.bars = m.slots + (size_t)nw * kGuSlots * m.slot_bytes;
+  m.cnt = m.bars + (size_t)nw * kGuSlots * 8;
+  m.total = m.cnt + (size_t)nblk * 4;
   return m;
+}
+
+// x -> quantised records in the workspace.
+__global__ void __launch_bounds__(256) quant_x_kernel(const __grid_constant__ DecodeParams p) {
+  pdl_wait();
+  pdl_trigger();
+  quant_x_lanes(p.x, p.T, p.H, p.xrec, dqvec_words(p.H), blockIdx.x * blockDim.x + threadIdx.x,
+                gridDim.x * blockDim.x);
+}
+
+// Block fb (32 h values) of a slot -> its records, for every token of the slot
+// (one warp; the values were written by warps of this CTA).
+__device__ __noinline__ void quant_h_block(const DecodeParams& p, const RouteTable& rt, int slot,
+                                           int fb) {
+  const int lane = threadIdx.x & 31;
+  const bool shared = slot < 0;
+  const int F = shared ? p.Fs : p.F;
+  const int words = dqvec_words(F);
+  const int ntok = shared ? p.T : rt.slot_off[slot + 1] - rt.slot_off[slot];
+  const int lbase = shared ? 0 : rt.slot_off[slot];
+  constexpr int kBatch = 8;      // loads in flight before the first reduction
+#pragma unroll 1
+  for (int j0 = 0; j0 < ntok; j0 += kBatch) {
+    float v[kBatch];
+    uint32_t* dst[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int j = j0 + u < ntok ? j0 + u : j0;
+      const int pr = shared ? j : rt.list[lbase + j];
+      const float* src = shared ? p.h_s + (size_t)j * p.Fs : p.h_r + (size_t)pr * p.F;
+      dst[u] = shared ? p.rec_s + (size_t)j * words : p.rec_r + (size_t)pr * words;
+      v[u] = src[fb * 32 + lane];
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u)
+      if (j0 + u < ntok) quant_block_store(v[u], fb, F, dst[u]);
+  }
+}
+
+template <int LPR, bool XS>
+__global__ void __launch_bounds__(512, 1) gu_kernel(const __grid_constant__ DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int H = p.H;
+  const int nw = blockDim.x >> 5;
+  const int g = row_granule_dev(H);
+  const GuSmem L = gu_smem(H, p.T, nw, XS, g, p.gu_nblk);
+  RouteTable& rt = *reinterpret_cast<RouteTable*>(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int xq_words = dqvec_words(H);
+  const size_t rbH = (size_t)(H / 32) * kBlockB;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint32_t* bcnt = reinterpret_cast<uint32_t*>(smem + L.cnt);
+  uint8_t* myslots = smem + L.slots + (size_t)warp * kGuSlots * L.slot_bytes;
+  uint64_t* mybar = bars + warp * kGuSlots;
+
+  if (threadIdx.x == 0) {
+#pragma unroll 1
+    for (int i = 0; i < nw * kGuSlots; ++i) mbar_init(&bars[i], 1);
+    mbar_fence_init();
+  }
+#pragma unroll 1
+  for (int i = threadIdx.x; i < p.gu_nblk; i += blockDim.x) bcnt[i] = 0u;
+  __syncthreads();
+
+  // this CTA's blocks: shared [sb0, sb1) of the shared expert, then routed
+  // [rb0, rb1) of the slot-major routed rows; its units (g rows each) are
+  // numbered in that order and dealt round-robin to the warps
+  const int G = gridDim.x, c = blockIdx.x;
+  const int S = p.n_shared ? p.Fs / 32 : 0;
+  const int sb0 = gu_shared_cum(S, c, G), sb1 = gu_shared_cum(S, c + 1, G);
+  const int upb = 32 / g;                      // units per block
+  const int n_sh_u = (sb1 - sb0) * upb;
+  int rb0 = 0, n_u = n_sh_u;
+  auto count = [&](int nu) { return warp < nu ? (nu - warp + nw - 1) / nw : 0; };
+  const int n_sh = count(n_sh_u);
+  int n_tot = n_sh;
+  int issued = 0, consumed = 0;
+  bool ok = true;
+  const uint64_t pol = l2_evict_first_policy();   // weights: read once per call
+  // a warp's units, in order: u = warp, warp + nw, ... of the CTA's units;
+  // slot (-1 shared) and first f-row, kept up to date without divisions
+  const int lg_upb = 5 - (31 - __clz(g));        // log2 of the units per block
+  struct Cursor {
+    int u, sl, f;
+  };
+  auto cur_get = [&](Cursor& k, int& sl, int& f) {
+    if (k.u < n_sh_u) {
+      sl = -1;
+      f = sb0 * 32 + k.u * g;
+      return;
+    }
+    if (k.sl < 0) {
+      const int r = rb0 * 32 + (k.u - n_sh_u) * g;
+      k.sl = r / p.F;
+      k.f = r - k.sl * p.F;
+    }
+    sl = k.sl;
+    f = k.f;
+  };
+  auto cur_next = [&](Cursor& k) {
+    if (k.sl >= 0) {
+      k.f += nw * g;
+      while (k.f >= p.F) {
+        k.f -= p.F;
+        ++k.sl;
+      }
+    }
+    k.u += nw;
+  };
+  Cursor ci{warp, -1, 0}, cc{warp, -1, 0};        // next unit to issue, to compute
+  const uint32_t ubytes = (uint32_t)(g * rbH);     // a multiple of 16
+  auto issue_upto = [&](int limit) {
+    while (issued < limit && issued - consumed < kGuSlots) {
+      int sl, f;
+      cur_get(ci, sl, f);
+      if (lane == 0) {
+        const size_t row = sl < 0 ? (size_t)f : (size_t)rt.slot_expert[sl] * p.F + f;
+        const int s = issued % kGuSlots;
+        uint8_t* dst = myslots + (size_t)s * L.slot_bytes;
+        mbar_arrive_expect_tx(&mybar[s], 2 * ubytes);
+        bulk_g2s_hint(dst, (sl < 0 ? p.sh_gate : p.gate) + row * rbH, ubytes, &mybar[s], pol);
+        bulk_g2s_hint(dst + ubytes, (sl < 0 ? p.sh_up : p.up) + row * rbH, ubytes, &mybar[s],
+                      pol);
+      }
+      cur_next(ci);
+      ++issued;
+    }
+  };
+
+  issue_upto(n_sh);
+  pdl_wait();
+  pdl_trigger();
+  uint32_t* xq = XS ? reinterpret_cast<uint32_t*>(smem + L.xq) : p.xrec;
+  if (XS) quant_x_lanes(p.x, p.T, H, xq, xq_words, threadIdx.x, blockDim.x);
+  if (p.T * p.k <= 64) {
+    if (warp == 0) build_route_table_warp(rt, p.ids, p.weights, p.T * p.k, p.E);
+    __syncthreads();
+  } else {
+    build_route_table<0>(rt, p.ids, p.weights, p.T * p.k, p.E, blockDim.x);
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0 && p.status && rt.invalid)
+    atomicAdd(p.status, (uint32_t)(rt.invalid < 0xFFFF ? rt.invalid : 0xFFFF));
+  int rb1 = 0;
+  {
+    rb0 = gu_routed_cum(rt, p.F / 32, S, p.T, c, G);
+    rb1 = gu_routed_cum(rt, p.F / 32, S, p.T, c + 1, G);
+    // never more blocks than the counters the launch provided (only a route
+    // table the host bound did not foresee could ask for more)
+    if (rb1 - rb0 + (sb1 - sb0) > p.gu_nblk) {
+      rb1 = rb0 + (p.gu_nblk - (sb1 - sb0));
+      if (blockIdx.x == 0 && threadIdx.x == 0 && p.status) atomicOr(p.status, MOE_STATUS_TIMEOUT);
+    }
+    n_u = n_sh_u + (rb1 - rb0) * upb;
+  }
+  n_tot = count(n_u);
+  issue_upto(n_tot);
+
+#pragma unroll 1
+  for (int j = 0; ok && j < n_tot; ++j) {
+    ok = mbar_wait(&mybar[j % kGuSlots], (uint32_t)((j / kGuSlots) & 1), p.status);
+    if (!ok) break;
+    const uint8_t* d = myslots + (size_t)(j % kGuSlots) * L.slot_bytes;
+    int sl, f;
+    cur_get(cc, sl, f);
+    const int blk = cc.u >> lg_upb;
+    cur_next(cc);
+    // one-token experts (most of them) take the code built for one token
+    const int ntok = sl < 0 ? p.T : rt.slot_off[sl + 1] - rt.slot_off[sl];
+#pragma unroll 1
+    for (int i = 0; i < g; ++i) {
+      if (ntok == 1)
+        gateup_unit_t<1, LPR>(p, rt, d + i * rbH, d + (g + i) * rbH, sl, f + i, xq, xq_words);
+      else
+        gateup_unit_t<kGuMaxT, LPR>(p, rt, d + i * rbH, d + (g + i) * rbH, sl, f + i, xq,
+                                    xq_words);
+    }
+    __syncwarp();
+    ++consumed;
+    issue_upto(n_tot);
+    // this warp's h stores, then its rows' arrival on the block
+    __threadfence_block();
+    __syncwarp();
+    if (lane == 0) atomicAdd(&bcnt[blk], (uint32_t)g);
+  }
+  // after a timeout: no bulk copy of this warp stays in flight
+  while (consumed < issued) {
+    mbar_wait(&mybar[consumed % kGuSlots], (uint32_t)((consumed / kGuSlots) & 1), p.status);
+    ++consumed;
+  }
+  // Quantise the CTA's blocks of h, block b by warp b % nw once all 32 of its
+  // rows have arrived (spread evenly: the warp that happens to add the last
+  // row would otherwise collect most of them and fall behind).
+  const int nsb = sb1 - sb0, nb = nsb + (rb1 - rb0);
+  const int bps = p.F / 32;
+#pragma unroll 1
+  for (int b = warp; ok && b < nb; b += nw) {
+    ok = wait_count_cta(&bcnt[b], 32u, p.status);
+    if (!ok) break;
+    if (b < nsb) {
+      quant_h_block(p, rt, -1, sb0 + b);
+    } else {
+      const int rb = rb0 + b - nsb;
+      const int sl = rb / bps;
+      quant_h_block(p, rt, sl, rb - sl * bps);
+    }
+  }
 }
 
 struct DnSmem {
@@ -148,119 +354,6 @@ __host__ __device__ inline DnSmem dn_smem(int F, int Fs, int n_shared, int T, in
   m.stage = align_up_dev(align_up_dev((size_t)rows_max * rb, 16) + kPairsPerStage * rec, 128);
   m.total = m.ring + (size_t)nst * m.stage;
   return m;
-}
-
-template <int MAXT>
-__global__ void __launch_bounds__(kThreads, 2) gateup_kernel(const DecodeParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int H = p.H;
-  const int NST = p.gu_stages;
-  const GuSmem L = gu_smem(H, p.T, NST);
-  RouteTable& rt = *reinterpret_cast<RouteTable*>(smem);
-  uint32_t* xq = reinterpret_cast<uint32_t*>(smem + L.xq);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar);
-  uint64_t* empty = full + NST;
-  uint8_t* ring = smem + L.ring;
-  const int xq_words = dqvec_words(H);
-  const int rb = H / 32 * kBlockB;
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int g = row_granule_dev(H);
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < NST; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumers / 32);
-    }
-    mbar_fence_init();
-  }
-  __syncthreads();
-
-  const RowRange shr = p.n_shared ? split_rows(p.Fs, g, blockIdx.x, gridDim.x) : RowRange{0, 0};
-
-  if (warp == kProducerWarp) {
-    // Producer: one lane issues the bulk copies; shared-expert rows first (they
-    // do not depend on the routes), then this CTA's share of the routed rows.
-    const uint64_t pol = l2_evict_first_policy();   // weights: read once per call
-    int it = 0;
-    bool ok = true;
-    auto issue = [&](const Chunk& c, const uint8_t* gbase, const uint8_t* ubase, int64_t row0) {
-      const int s = it % NST;
-      const uint32_t par = ((it / NST) & 1) ^ 1;
-      if (!mbar_wait(&empty[s], par, p.status)) return false;
-      const uint32_t bytes = (uint32_t)(c.rows * rb);
-      uint8_t* dst = ring + (size_t)s * L.stage;
-      mbar_arrive_expect_tx(&full[s], 2 * bytes);
-      bulk_g2s_hint(dst, gbase + (row0 + c.f0) * rb, bytes, &full[s], pol);
-      bulk_g2s_hint(dst + bytes, ubase + (row0 + c.f0) * rb, bytes, &full[s], pol);
-      ++it;
-      return true;
-    };
-    if (lane == 0) {
-      for (int r = shr.a; ok && r < shr.b;) {
-        const Chunk c = next_chunk(r, shr.b, p.Fs, true);
-        ok = issue(c, p.sh_gate, p.sh_up, 0);
-        r += c.rows;
-      }
-    }
-    __syncwarp();
-    pdl_wait();
-    pdl_trigger();
-    all_sync_named();                      // route table ready
-    if (lane == 0 && ok) {
-      const RowRange rr = split_rows(rt.n_slots * p.F, g, blockIdx.x, gridDim.x);
-      for (int r = rr.a; ok && r < rr.b;) {
-        const Chunk c = next_chunk(r, rr.b, p.F, false);
-        const int64_t row0 = (int64_t)rt.slot_expert[c.slot] * p.F;
-        ok = issue(c, p.gate, p.up, row0);
-        r += c.rows;
-      }
-    }
-    return;
-  }
-
-  // Consumers. Quantise x first: the inputs of this call are complete (the
-  // router that precedes this kernel read them after its own dependency wait).
-  quant_x_to_smem(p.x, p.T, H, xq, xq_words, warp, kConsumers / 32);
-  consumers_sync();
-
-  int it = 0;
-  bool ok = true;
-  Pending pd;
-  pd.n = 0;
-  auto consume = [&](const Chunk& c) {
-    const int s = it % NST;
-    const uint32_t par = (it / NST) & 1;
-    if (!mbar_wait(&full[s], par, p.status)) return false;
-    gateup_rows<MAXT>(p, rt, ring + (size_t)s * L.stage, c, xq, xq_words);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-    ++it;
-    if (warp < c.rows) {
-      pd.slot[pd.n] = c.slot;
-      pd.f[pd.n] = c.f0 + warp;
-      if (++pd.n == kPendMax) flush_arrivals(p, rt, pd);
-    }
-    return true;
-  };
-  for (int r = shr.a; ok && r < shr.b;) {
-    const Chunk c = next_chunk(r, shr.b, p.Fs, true);
-    ok = consume(c);
-    r += c.rows;
-  }
-  pdl_wait();
-  pdl_trigger();
-  build_route_table<kConsumers, 1>(rt, p.ids, p.weights, p.T * p.k, p.E);
-  if (blockIdx.x == 0 && threadIdx.x == 0 && p.status && rt.invalid)
-    atomicAdd(p.status, (uint32_t)(rt.invalid < 0xFFFF ? rt.invalid : 0xFFFF));
-  all_sync_named();
-  const RowRange rr = split_rows(rt.n_slots * p.F, g, blockIdx.x, gridDim.x);
-  for (int r = rr.a; ok && r < rr.b;) {
-    const Chunk c = next_chunk(r, rr.b, p.F, false);
-    ok = consume(c);
-    r += c.rows;
-  }
-  if (pd.n) flush_arrivals(p, rt, pd);
 }
 
 // ---------------------------------------------------------------------------
@@ -384,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 2) down_kernel(const DecodeParams p)
   }
 
   // Consumers.
-  build_route_table<kConsumers, 1>(rt, p.ids, p.weights, p.T * p.k, p.E);
+  build_route_table<1>(rt, p.ids, p.weights, p.T * p.k, p.E, kConsumers);
   for (int i = threadIdx.x; i < nrows * p.T; i += kConsumers) yacc[i] = 0.0f;
   consumers_sync();
   all_sync_named();
@@ -428,8 +521,32 @@ __global__ void __launch_bounds__(kThreads, 2) down_kernel(const DecodeParams p)
       float acc[NPS];
 #pragma unroll
       for (int j = 0; j < NPS; ++j) acc[j] = 0.0f;
-      if (active) {
+      if (active && np == 1) {
+        // one token: the split-table dot products (same integers as below)
         const uint8_t* row = wst + (size_t)r * rbK;
+        const float* sc = reinterpret_cast<const float*>(recs + pw);
+#pragma unroll 1
+        for (int q = q0; q < npq; q += lpr) {
+          const int qbase = qv_base(q, lpr);
+          uint32_t w[9];
+          load_pair_smem(row + q * kPairB, w);
+          float d0, d1;
+          pair_scales(w, d0, d1);
+          const uint4* r4 = reinterpret_cast<const uint4*>(recs) + qbase;
+          uint32_t v[32];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 u = r4[c * lpr];
+            v[4 * c] = u.x; v[4 * c + 1] = u.y; v[4 * c + 2] = u.z; v[4 * c + 3] = u.w;
+          }
+          int i0, i1;
+          iq4_pair_dot1(w, v, i0, i1);
+          acc[0] = fmaf((float)i0, d0 * sc[2 * q], acc[0]);
+          acc[0] = fmaf((float)i1, d1 * sc[2 * q + 1], acc[0]);
+        }
+      } else if (active) {
+        const uint8_t* row = wst + (size_t)r * rbK;
+#pragma unroll 1
         for (int q = q0; q < npq; q += lpr) {
           const int qbase = qv_base(q, lpr);
           uint32_t w[9];
@@ -465,7 +582,8 @@ __global__ void __launch_bounds__(kThreads, 2) down_kernel(const DecodeParams p)
       }
 #pragma unroll
       for (int j = 0; j < NPS; ++j)
-        for (int o = lpr >> 1; o > 0; o >>= 1) acc[j] += __shfl_xor_sync(0xFFFFFFFFu, acc[j], o);
+        if (j < np)
+          for (int o = lpr >> 1; o > 0; o >>= 1) acc[j] += __shfl_xor_sync(0xFFFFFFFFu, acc[j], o);
       if (active && q0 == 0) {
 #pragma unroll
         for (int j = 0; j < NPS; ++j)
@@ -484,25 +602,17 @@ __global__ void __launch_bounds__(kThreads, 2) down_kernel(const DecodeParams p)
 
 // ---------------------------------------------------------------------------
 // Host side.
-size_t gateup_smem_bytes(const DecodeParams& p, int stages) {
-  return gu_smem(p.H, p.T, stages).total;
-}
-size_t down_smem_bytes(const DecodeParams& p, int stages) {
-  return dn_smem(p.F, p.Fs, p.n_shared, p.T, p.dn_rows_max, stages).total;
-}
-
 namespace {
-constexpr size_t kSmemSoft = 112 * 1024;   // two CTAs of consecutive kernels share an SM
-constexpr size_t kSmemHard = 227 * 1024;
+constexpr size_t kSmemMax = 227 * 1024;
 
 template <typename K>
-cudaError_t launch(K kernel, int grid, size_t smem, bool pdl, cudaStream_t stream,
+cudaError_t launch(K kernel, int grid, int threads, size_t smem, bool pdl, cudaStream_t stream,
                    const DecodeParams& p) {
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kernel), smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -513,13 +623,47 @@ cudaError_t launch(K kernel, int grid, size_t smem, bool pdl, cudaStream_t strea
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
-int pick_stages(size_t fixed, size_t stage, int lo, int hi) {
+// Warps per CTA and where x lives for the gate/up kernel: 16 warps, with x in
+// shared memory if it fits beside their slots, else in the workspace; 8 or 4
+// warps when even that does not fit.
+bool gu_config(const DecodeParams& p, int num_sms, int* nw, bool* xs, size_t* smem,
+               int* nblk) {
+  const int g = row_granule_dev(p.H);
+  const int slots_max = p.T * p.k < p.E ? p.T * p.k : p.E;
+  *nblk = gu_blocks_max(p.n_shared ? p.Fs / 32 : 0, p.F / 32, slots_max, p.T * p.k, p.T, num_sms);
+  const int ws[3] = {16, 8, 4};
+  for (int i = 0; i < 3; ++i) {
+    for (int pass = 0; pass < 2; ++pass) {
+      const bool x_on_chip = pass == 0;
+      const size_t t = gu_smem(p.H, p.T, ws[i], x_on_chip, g, *nblk).total;
+      if (t <= kSmemMax) {
+        *nw = ws[i];
+        *xs = x_on_chip;
+        *smem = t;
+        return true;
+      }
+    }
+  }
+  return false;
+}
+
+int down_stages(const DnSmem& one, int lo, int hi) {
   int n = hi;
-  while (n > lo && fixed + (size_t)n * stage > kSmemSoft) --n;
-  while (n > 1 && fixed + (size_t)n * stage > kSmemHard) --n;
+  while (n > lo && one.ring + (size_t)n * one.stage > kSmemMax) --n;
   return n;
 }
 }  // namespace
+
+int decode_launches(const DecodeParams& p, int num_sms) {
+  size_t fsm = 0;
+  int rg = 0, rmax = 0;
+  if (fused_decode_supported(p, num_sms, &fsm, &rg, &rmax)) return 1;
+  int nw = 0, nblk = 0;
+  bool xs = true;
+  size_t sm = 0;
+  if (!gu_config(p, num_sms, &nw, &xs, &sm, &nblk)) return 2;
+  return xs ? 2 : 3;
+}
 
 cudaError_t launch_decode(const DecodeParams& p0, int num_sms, bool pdl, cudaStream_t stream) {
   DecodeParams p = p0;
@@ -534,10 +678,10 @@ cudaError_t launch_decode(const DecodeParams& p0, int num_sms, bool pdl, cudaStr
     }
   }
   // gate/up
-  const GuSmem g1 = gu_smem(p.H, p.T, 1);
-  p.gu_stages = pick_stages(g1.ring, g1.stage, 2, 6);
-  const size_t gsm = gu_smem(p.H, p.T, p.gu_stages).total;
-  if (gsm > kSmemHard) return cudaErrorInvalidConfiguration;
+  int nw = 0;
+  bool xs = true;
+  size_t gsm = 0;
+  if (!gu_config(p, num_sms, &nw, &xs, &gsm, &p.gu_nblk)) return cudaErrorInvalidConfiguration;
   // down
   int gd = row_granule_dev(p.F);
   if (p.n_shared && row_granule_dev(p.Fs) > gd) gd = row_granule_dev(p.Fs);
@@ -545,19 +689,25 @@ cudaError_t launch_decode(const DecodeParams& p0, int num_sms, bool pdl, cudaStr
   const int grid_dn = units < num_sms ? units : num_sms;
   p.dn_rows_max = (units + grid_dn - 1) / grid_dn * gd;
   const DnSmem d1 = dn_smem(p.F, p.Fs, p.n_shared, p.T, p.dn_rows_max, 1);
-  p.dn_stages = pick_stages(d1.ring, d1.stage, 2, 8);
+  p.dn_stages = down_stages(d1, 1, 8);
   const size_t dsm = dn_smem(p.F, p.Fs, p.n_shared, p.T, p.dn_rows_max, p.dn_stages).total;
-  if (dsm > kSmemHard) return cudaErrorInvalidConfiguration;
+  if (dsm > kSmemMax) return cudaErrorInvalidConfiguration;
 
   cudaError_t e;
-  const int T = p.T;
-  if (T <= 1) e = launch(gateup_kernel<1>, num_sms, gsm, pdl, stream, p);
-  else if (T <= 2) e = launch(gateup_kernel<2>, num_sms, gsm, pdl, stream, p);
-  else if (T <= 4) e = launch(gateup_kernel<4>, num_sms, gsm, pdl, stream, p);
-  else if (T <= 8) e = launch(gateup_kernel<8>, num_sms, gsm, pdl, stream, p);
-  else e = launch(gateup_kernel<16>, num_sms, gsm, pdl, stream, p);
+  const bool w8 = dlanes_per_row(p.H) == 8;
+  if (!xs) {
+    const int n = p.T * (p.H / 32) * 4;             // four threads per 32-value block
+    int grid = (n + 255) / 256;
+    if (grid > num_sms) grid = num_sms;
+    e = launch(quant_x_kernel, grid, 256, 0, pdl, stream, p);
+    if (e != cudaSuccess) return e;
+  }
+  if (w8) e = xs ? launch(gu_kernel<8, true>, num_sms, nw * 32, gsm, pdl, stream, p)
+                 : launch(gu_kernel<8, false>, num_sms, nw * 32, gsm, pdl, stream, p);
+  else e = xs ? launch(gu_kernel<0, true>, num_sms, nw * 32, gsm, pdl, stream, p)
+              : launch(gu_kernel<0, false>, num_sms, nw * 32, gsm, pdl, stream, p);
   if (e != cudaSuccess) return e;
-  return launch(down_kernel<kPairsPerStage>, grid_dn, dsm, pdl, stream, p);
+  return launch(down_kernel<kPairsPerStage>, grid_dn, kThreads, dsm, pdl, stream, p);
 }
 
 // Route + layer in one call: one fused launch when the shape allows, else the

@@ -9,7 +9,6 @@
 namespace moe {
 
 constexpr int kMaxPairs = MOE_MAX_DECODE_TOKENS * MOE_MAX_TOP_K;  // T*k
-constexpr int kChunkRows = 8;     // f-rows (gate + up) per gate/up stage
 constexpr int kPairsPerStage = 4; // h vectors per down stage
 
 inline int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
@@ -38,7 +37,7 @@ inline int64_t qvec_words(int64_t K) {
 }
 
 struct DecodeLayout {
-  int64_t h_r, h_s, rec_r, rec_s, cnt, sync, scores, total;  // byte offsets
+  int64_t h_r, h_s, rec_r, rec_s, sync, scores, xrec, total;  // byte offsets
 };
 
 inline DecodeLayout decode_layout(const moe_shape& s, int64_t T) {
@@ -54,10 +53,9 @@ inline DecodeLayout decode_layout(const moe_shape& s, int64_t T) {
   L.h_s = take(T * Fs * 4);
   L.rec_r = take(T * s.top_k * qvec_words(s.ffn) * 4);
   L.rec_s = take(Fs ? T * qvec_words(Fs) * 4 : 0);
-  const int64_t fmax = s.ffn > Fs ? s.ffn : Fs;
-  L.cnt = take((int64_t)(s.n_experts + 1) * (fmax / 32) * 4);
   L.sync = take(64);                       // grid-barrier counters of the fused kernel
   L.scores = take(T * s.n_experts * 4);    // router scores of the routed fused kernel
+  L.xrec = take(T * qvec_words(s.hidden) * 4);   // quantised x, when it does not fit on chip
   L.total = off;
   return L;
 }
@@ -78,9 +76,9 @@ struct DecodeParams {
   float* h_s;        // [T][Fs]
   uint32_t* rec_r;   // [T*k][qvec_words(F)]
   uint32_t* rec_s;   // [T][qvec_words(Fs)]
-  uint32_t* cnt;     // [(E+1)][max(F,Fs)/32]
   uint32_t* sync;    // [4]: h arrivals, departures, score arrivals (fused kernel)
   uint32_t* status;
+  uint32_t* xrec;    // [T][qvec_words(H)]: quantised x (gate/up kernel without room for it)
   // routing inside the fused kernel (route != 0)
   int route;
   const uint16_t* Wr;    // bf16 [E][H]
@@ -89,15 +87,15 @@ struct DecodeParams {
   float* w_out;          // [T][k]
   float* scores;         // workspace [T][E]
   // launch-derived
-  int gu_stages;     // gate/up ring depth
+  int gu_nblk;       // gate/up kernel: 32-row blocks a CTA may get
   int dn_stages;     // down ring depth
   int dn_rows_max;   // max output rows per down CTA
   int fz_rg;         // fused kernel: output rows per down unit
 };
 
-size_t gateup_smem_bytes(const DecodeParams& p, int stages);
-size_t down_smem_bytes(const DecodeParams& p, int stages);
 cudaError_t launch_decode(const DecodeParams& p, int num_sms, bool pdl, cudaStream_t stream);
+// Kernel launches of one launch_decode call (route = 0) for these sizes.
+int decode_launches(const DecodeParams& p, int num_sms);
 bool fused_decode_supported(const DecodeParams& p, int num_sms, size_t* smem, int* rg,
                             int* rows_max);
 cudaError_t launch_decode_routed(const DecodeParams& p, int num_sms, bool pdl,

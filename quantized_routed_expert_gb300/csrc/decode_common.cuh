@@ -1,6 +1,6 @@
 // Device helpers shared by the decode kernels: the route table built from
-// ids, the 16-bit block-quantised vector layout, row splitting and the
-// deferred F-block arrivals that quantise h.
+// ids, the 16-bit block-quantised vector layout, x quantisation, row
+// splitting and the gate/up unit.
 #pragma once
 
 #include "common.cuh"
@@ -41,15 +41,16 @@ __device__ __forceinline__ int slot_of_expert(const RouteTable& rt, int e) {
   return rt.word_off[e >> 5] + __popc(w & ((1u << (e & 31)) - 1u));
 }
 
-// Called by NT threads (named barrier BAR). P = T*k <= 256.
-template <int NT, int BAR>
+// Called by the nt threads 0..nt-1 (named barrier BAR; nt a multiple of 32).
+// P = T*k <= 256.
+template <int BAR>
 __device__ void build_route_table(RouteTable& rt, const int32_t* __restrict__ ids,
-                                  const float* __restrict__ wts, int P, int E) {
+                                  const float* __restrict__ wts, int P, int E, int nt) {
   const int tid = threadIdx.x;
   if (tid < MOE_MAX_EXPERTS / 32) rt.bitmap[tid] = 0u;
   if (tid == 0) rt.invalid = 0;
-  bar_sync<BAR, NT>();
-  for (int i = tid; i < P; i += NT) {
+  bar_sync_n(BAR, nt);
+  for (int i = tid; i < P; i += nt) {
     const int id = ids[i];
     const bool ok = id >= 0 && id < E;
     rt.sid[i] = ok ? id : -1;
@@ -57,7 +58,7 @@ __device__ void build_route_table(RouteTable& rt, const int32_t* __restrict__ id
     if (ok) atomicOr(&rt.bitmap[id >> 5], 1u << (id & 31));
     else atomicAdd(&rt.invalid, 1);
   }
-  bar_sync<BAR, NT>();
+  bar_sync_n(BAR, nt);
   if (tid < 32) {
     const int nw = (E + 31) >> 5;
     const int c = tid < nw ? __popc(rt.bitmap[tid]) : 0;
@@ -80,10 +81,10 @@ __device__ void build_route_table(RouteTable& rt, const int32_t* __restrict__ id
     }
     if (tid == 31) rt.n_slots = incl;
   }
-  bar_sync<BAR, NT>();
+  bar_sync_n(BAR, nt);
   // stable counting sort of the valid pairs by expert: rank = #smaller experts
   // + #earlier pairs of the same expert
-  for (int p = tid; p < P; p += NT) {
+  for (int p = tid; p < P; p += nt) {
     const int e = rt.sid[p];
     if (e < 0) continue;
     int rank = 0;
@@ -101,7 +102,7 @@ __device__ void build_route_table(RouteTable& rt, const int32_t* __restrict__ id
     rt.n_valid = P - rt.invalid;
     rt.slot_off[rt.n_slots] = rt.n_valid;
   }
-  bar_sync<BAR, NT>();
+  bar_sync_n(BAR, nt);
 }
 
 // The same table built by one warp, for P <= 64 pairs (T <= 4 tokens): two
@@ -341,100 +342,43 @@ __device__ __forceinline__ void quant_group8(const float (&v)[8], bool ok, int b
   if (ok && s == 0) reinterpret_cast<float*>(rec + dqvec_pair_words(K))[b] = quant_scale(e);
 }
 
-// Quantise T bf16 rows of K values (16-byte aligned) into records in shared
-// memory, four lanes per 32-value block (16 bytes each); all threads tid, tid +
-// nt, ... of the CTA (nt a multiple of 32).
+// Quantise T bf16 rows of K values (16-byte aligned) into records (shared or
+// global memory), four lanes per 32-value block (16 bytes each); all threads
+// tid, tid + nt, ... (nt a multiple of 32). Each thread has kXLoads loads in
+// flight before it quantises any of them.
 __device__ __forceinline__ void quant_x_lanes(const uint16_t* __restrict__ x, int T, int K,
                                               uint32_t* xq, int xq_words, int tid, int nt) {
+  constexpr int kXLoads = 4;
   const int nb = K / 32;
+  const int n = T * nb * 4;
 #pragma unroll 1
-  for (int i0 = tid & ~31; i0 < T * nb * 4; i0 += nt) {
-    const int i = i0 + (tid & 31);
-    const bool ok = i < T * nb * 4;
-    const int blk = ok ? i >> 2 : 0;
-    const int t = blk / nb, b = blk - t * nb;
-    uint4 raw = make_uint4(0, 0, 0, 0);
-    if (ok) raw = __ldcg(reinterpret_cast<const uint4*>(x + (size_t)t * K + b * 32) + (i & 3));
-    const uint32_t r[4] = {raw.x, raw.y, raw.z, raw.w};
-    float v[8];
+  for (int i0 = tid & ~31; i0 < n; i0 += kXLoads * nt) {
+    uint4 raw[kXLoads];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      v[2 * j] = __uint_as_float(r[j] << 16);
-      v[2 * j + 1] = __uint_as_float(r[j] & 0xFFFF0000u);
-    }
-    quant_group8(v, ok, b, K, xq + (size_t)t * xq_words);
-  }
-}
-
-// Quantise T bf16 rows of K values into records in shared memory. Each lane
-// loads 8 consecutive values (16 bytes); four lanes form one 32-value block, so
-// a warp covers 8 blocks per load; four such groups are loaded before any is
-// used, to keep loads in flight.
-__device__ __forceinline__ void quant_group(const uint4 raw, bool ok, int b, int K,
-                                            uint32_t* rec) {
-  const int lane = threadIdx.x & 31;
-  const int s = lane & 3;
-  const uint32_t r[4] = {raw.x, raw.y, raw.z, raw.w};
-  float v[8];
-  uint32_t e = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    v[2 * i] = __uint_as_float(r[i] << 16);
-    v[2 * i + 1] = __uint_as_float(r[i] & 0xFFFF0000u);
-  }
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint32_t ei = (__float_as_uint(v[i]) >> 23) & 0xFFu;
-    e = ei > e ? ei : e;
-  }
-  uint32_t o = __shfl_xor_sync(0xFFFFFFFFu, e, 1);
-  e = o > e ? o : e;
-  o = __shfl_xor_sync(0xFFFFFFFFu, e, 2);
-  e = o > e ? o : e;
-  int m[8], m2[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) m[i] = quant_one(v[i], e);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) m2[i] = __shfl_down_sync(0xFFFFFFFFu, m[i], 2);
-  const int lpr = dlanes_per_row(K);
-  if (ok && s < 2) {
-    uint32_t w[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = (uint32_t)(m[i] & 0xFFFF) | ((uint32_t)m2[i] << 16);
-    const int q = b >> 1;
-    const int c0 = 4 * (b & 1) + 2 * s;
-    uint4* r4 = reinterpret_cast<uint4*>(rec);
-    r4[qv_u4(q, c0, lpr)] = make_uint4(w[0], w[1], w[2], w[3]);
-    r4[qv_u4(q, c0 + 1, lpr)] = make_uint4(w[4], w[5], w[6], w[7]);
-  }
-  if (ok && s == 0) reinterpret_cast<float*>(rec + dqvec_pair_words(K))[b] = quant_scale(e);
-}
-
-__device__ __forceinline__ void quant_x_to_smem(const uint16_t* __restrict__ x, int T, int K,
-                                                uint32_t* xq, int xq_words, int warp,
-                                                int nwarps) {
-  const int lane = threadIdx.x & 31;
-  const int nb = K / 32;
-  const int gpr = (nb + 7) / 8;                 // 8-block groups per row
-  const int total = T * gpr;
-  for (int g0 = warp; g0 < total; g0 += 4 * nwarps) {
-    uint4 raw[4];
-    bool ok[4];
-    int bb[4], tt[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int g = g0 + u * nwarps;
-      tt[u] = g / gpr;
-      bb[u] = (g - tt[u] * gpr) * 8 + (lane >> 2);
-      ok[u] = g < total && bb[u] < nb;
-      raw[u] = ok[u] ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)tt[u] * K + bb[u] * 32 +
-                                                            (lane & 3) * 8))
-                     : make_uint4(0, 0, 0, 0);
+    for (int u = 0; u < kXLoads; ++u) {
+      const int i = i0 + u * nt + (tid & 31);
+      raw[u] = make_uint4(0, 0, 0, 0);
+      if (i < n) {
+        const int blk = i >> 2, t = blk / nb, b = blk - t * nb;
+        raw[u] = __ldcg(reinterpret_cast<const uint4*>(x + (size_t)t * K + b * 32) + (i & 3));
+      }
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      if (g0 + u * nwarps < total)       // warp-uniform
-        quant_group(raw[u], ok[u], bb[u], K, xq + (size_t)(tt[u] < T ? tt[u] : 0) * xq_words);
+    for (int u = 0; u < kXLoads; ++u) {
+      if (i0 + u * nt < n) {                 // warp-uniform: i0 + u * nt is a multiple of 32
+        const int i = i0 + u * nt + (tid & 31);
+        const bool ok = i < n;
+        const int blk = ok ? i >> 2 : 0;
+        const int t = blk / nb, b = blk - t * nb;
+        const uint32_t r[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[2 * j] = __uint_as_float(r[j] << 16);
+          v[2 * j + 1] = __uint_as_float(r[j] & 0xFFFF0000u);
+        }
+        quant_group8(v, ok, b, K, xq + (size_t)t * xq_words);
+      }
     }
   }
 }
@@ -442,12 +386,6 @@ __device__ __forceinline__ void quant_x_to_smem(const uint16_t* __restrict__ x, 
 // ---------------------------------------------------------------------------
 // Gate/up work: shared-expert rows are split evenly over the CTAs (known before
 // the routes are), routed rows (slots x F, slot-major) likewise after.
-struct Chunk {
-  int slot;   // -1 = shared expert, else routed slot index
-  int f0;
-  int rows;
-};
-
 struct RowRange {
   int a, b;   // [a, b) in flattened rows
 };
@@ -459,92 +397,125 @@ __device__ __forceinline__ RowRange split_rows(int total, int g, int cta, int nc
   return RowRange{(int)ua * g, (int)ub * g};
 }
 
-// The next chunk of [row, end) of a slot-major space with rows_per_slot rows.
-__device__ __forceinline__ Chunk next_chunk(int row, int end, int rows_per_slot, bool shared) {
-  Chunk c;
-  const int s = row / rows_per_slot;
-  c.slot = shared ? -1 : s;
-  c.f0 = row - s * rows_per_slot;
-  int n = rows_per_slot - c.f0;
-  if (end - row < n) n = end - row;
-  c.rows = n < kChunkRows ? n : kChunkRows;
-  return c;
-}
-
-// Arrivals on F-blocks, deferred: a warp records the rows it finished and
-// publishes them in batches behind one fence. The 32nd arrival on a block
-// quantises the block for every token of the slot and resets its counter.
-constexpr int kPendMax = 8;
-struct Pending {
-  int n;
-  int slot[kPendMax];
-  int f[kPendMax];
-};
-
-inline __device__ void flush_arrivals(const DecodeParams& p, const RouteTable& rt,
-                                            Pending& pd) {
+// One gate/up unit: the warp's f-row (gate row at `g`, up row at `u`) for every
+// token of the slot; writes h (fp32) for each (token, slot) pair. LPR is the
+// interleave width of the quantised x records (dlanes_per_row(H)); 0 = known
+// only at run time.
+template <int MAXT, int LPR>
+__device__ __forceinline__ void gateup_unit_t(const DecodeParams& p, const RouteTable& rt,
+                                           const uint8_t* g, const uint8_t* u, int slot, int f,
+                                           const uint32_t* xq, int xq_words) {
   const int lane = threadIdx.x & 31;
-  __threadfence();                       // this warp's h stores, before its arrivals
-  __syncwarp();
-  const int fmax = p.F > p.Fs ? p.F : p.Fs;
-  // lane i arrives for entry i (all arrivals in flight at once)
-  uint32_t old = 0;
-  if (lane < pd.n) {
-    const int slot = pd.slot[lane];
-    const int cid = slot < 0 ? p.E : rt.slot_expert[slot];
-    old = atomicAdd(p.cnt + (size_t)cid * (fmax / 32) + pd.f[lane] / 32, 1u);
-  }
-  const uint32_t last = __ballot_sync(0xFFFFFFFFu, lane < pd.n && old == 31u);
-  if (last) __threadfence();
-  // (entry, token) blocks to quantise, gathered in batches so that their loads
-  // are all in flight before the first block is reduced
-  constexpr int kBatch = 8;
-  int ent[kBatch], tokj[kBatch];
-  int nb = 0;
-  auto drain = [&]() {
-    const float* src[kBatch];
-    uint32_t* dst[kBatch];
-    int Fb[kBatch], blk[kBatch];
+  const int H = p.H;
+  const int npairs = H >> 6;
+  const int lpr = LPR ? LPR : dlanes_per_row(H);
+  const bool shared = slot < 0;
+  const int ntok = shared ? p.T : rt.slot_off[slot + 1] - rt.slot_off[slot];
+  const int lbase = shared ? 0 : rt.slot_off[slot];
+  const int xs_off = dqvec_pair_words(H);
+#pragma unroll 1
+  for (int g0 = 0; g0 < ntok; g0 += MAXT) {
+    const int ng = ntok - g0 < MAXT ? ntok - g0 : MAXT;
+    const uint32_t* rec[MAXT];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int i = ent[u < nb ? u : 0], j = tokj[u < nb ? u : 0];
-      const int slot = pd.slot[i];
-      const bool shared = slot < 0;
-      const int F = shared ? p.Fs : p.F;
-      const int words = dqvec_words(F);
-      const int pr = shared ? j : rt.list[rt.slot_off[slot] + j];
-      src[u] = shared ? p.h_s + (size_t)j * p.Fs : p.h_r + (size_t)pr * p.F;
-      dst[u] = shared ? p.rec_s + (size_t)j * words : p.rec_r + (size_t)pr * words;
-      Fb[u] = F;
-      blk[u] = pd.f[i] / 32;
+    for (int j = 0; j < MAXT; ++j) {
+      const int jj = g0 + (j < ng ? j : 0);
+      const int tok = shared ? jj : rt.list[lbase + jj] / p.k;
+      rec[j] = xq + (size_t)tok * xq_words;
     }
-    float v[kBatch];
+    float ag[MAXT], au[MAXT];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) v[u] = u < nb ? __ldcg(src[u] + blk[u] * 32 + lane) : 0.f;
+    for (int j = 0; j < MAXT; ++j) ag[j] = au[j] = 0.0f;
+    if (MAXT == 1 || ng == 1) {
+      // one token: the split-table dot products (fewer ALU-pipe operations;
+      // the same integers, so the same h as the general loop below)
+      for (int q = lane; q < npairs; q += 32) {
+        const int qbase = qv_base(q, lpr);
+        uint32_t wg[9], wu[9];
+        load_pair_smem(g + q * kPairB, wg);
+        load_pair_smem(u + q * kPairB, wu);
+        float dg0, dg1, du0, du1;
+        pair_scales(wg, dg0, dg1);
+        pair_scales(wu, du0, du1);
+        const uint4* r4 = reinterpret_cast<const uint4*>(rec[0]) + qbase;
+        uint32_t v[32];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u)
-      if (u < nb) quant_block_store(v[u], blk[u], Fb[u], dst[u]);
-    nb = 0;
-  };
-  for (int i = 0; i < pd.n; ++i) {
-    if (!((last >> i) & 1u)) continue;
-    const int slot = pd.slot[i];
-    const int ntok = slot < 0 ? p.T : rt.slot_off[slot + 1] - rt.slot_off[slot];
-    for (int j = 0; j < ntok; ++j) {
-      ent[nb] = i;
-      tokj[nb] = j;
-      if (++nb == kBatch) drain();
+        for (int c = 0; c < 8; ++c) {
+          const uint4 t4 = r4[c * lpr];
+          v[4 * c] = t4.x; v[4 * c + 1] = t4.y; v[4 * c + 2] = t4.z; v[4 * c + 3] = t4.w;
+        }
+        const float2 sc = reinterpret_cast<const float2*>(rec[0] + xs_off)[q];
+        int ig0, ig1, iu0, iu1;
+        iq4_pair_dot1(wg, v, ig0, ig1);
+        iq4_pair_dot1(wu, v, iu0, iu1);
+        ag[0] = fmaf((float)ig0, dg0 * sc.x, ag[0]);
+        ag[0] = fmaf((float)ig1, dg1 * sc.y, ag[0]);
+        au[0] = fmaf((float)iu0, du0 * sc.x, au[0]);
+        au[0] = fmaf((float)iu1, du1 * sc.y, au[0]);
+      }
+    } else {
+    for (int q = lane; q < npairs; q += 32) {
+      const int qbase = qv_base(q, lpr);
+      uint32_t w[9];
+      float dg0, dg1, du0, du1;
+      uint32_t a0[4], a1[4];
+      uint32_t tg0[8], tg1[8], tu0[8], tu1[8];
+      load_pair_smem(g + q * kPairB, w);
+      split_pair(w, dg0, dg1, a0, a1);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        iq4_lookup8(a0[i], tg0[2 * i], tg0[2 * i + 1]);
+        iq4_lookup8(a1[i], tg1[2 * i], tg1[2 * i + 1]);
+      }
+      load_pair_smem(u + q * kPairB, w);
+      split_pair(w, du0, du1, a0, a1);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        iq4_lookup8(a0[i], tu0[2 * i], tu0[2 * i + 1]);
+        iq4_lookup8(a1[i], tu1[2 * i], tu1[2 * i + 1]);
+      }
+#pragma unroll
+      for (int j = 0; j < MAXT; ++j) {
+        if (j < ng) {
+          const uint4* r4 = reinterpret_cast<const uint4*>(rec[j]) + qbase;
+          uint32_t v[32];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 t4 = r4[c * lpr];
+            v[4 * c] = t4.x; v[4 * c + 1] = t4.y; v[4 * c + 2] = t4.z; v[4 * c + 3] = t4.w;
+          }
+          const float2 sc = reinterpret_cast<const float2*>(rec[j] + xs_off)[q];
+          const int ig0 = iq4_dot_block(tg0, v);
+          const int ig1 = iq4_dot_block(tg1, v + 16);
+          const int iu0 = iq4_dot_block(tu0, v);
+          const int iu1 = iq4_dot_block(tu1, v + 16);
+          ag[j] = fmaf((float)ig0, dg0 * sc.x, ag[j]);
+          ag[j] = fmaf((float)ig1, dg1 * sc.y, ag[j]);
+          au[j] = fmaf((float)iu0, du0 * sc.x, au[j]);
+          au[j] = fmaf((float)iu1, du1 * sc.y, au[j]);
+        }
+      }
+    }
+    }
+#pragma unroll
+    for (int j = 0; j < MAXT; ++j) {
+      if (j < ng) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          ag[j] += __shfl_xor_sync(0xFFFFFFFFu, ag[j], o);
+          au[j] += __shfl_xor_sync(0xFFFFFFFFu, au[j], o);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < MAXT; ++j) {
+      if (j < ng && lane == j) {
+        const float hv = silu_mul(ag[j], au[j]);
+        if (shared) p.h_s[(size_t)(g0 + j) * p.Fs + f] = hv;
+        else p.h_r[(size_t)rt.list[lbase + g0 + j] * p.F + f] = hv;
+      }
     }
   }
-  if (nb) drain();
-  // reset the counters of the blocks this warp completed
-  if (lane < pd.n && old == 31u) {
-    const int slot = pd.slot[lane];
-    const int cid = slot < 0 ? p.E : rt.slot_expert[slot];
-    p.cnt[(size_t)cid * (fmax / 32) + pd.f[lane] / 32] = 0u;
-  }
-  __syncwarp();
-  pd.n = 0;
 }
 
 

@@ -87,124 +87,6 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
   return v;
 }
 
-// One gate/up unit: the warp's f-row (gate row at `g`, up row at `u`) for every
-// token of the slot; writes h (fp32) for each (token, slot) pair. LPR is the
-// interleave width of the quantised x records (dlanes_per_row(H)); 0 = known
-// only at run time.
-template <int MAXT, int LPR>
-__device__ __forceinline__ void gateup_unit_t(const DecodeParams& p, const RouteTable& rt,
-                                           const uint8_t* g, const uint8_t* u, int slot, int f,
-                                           const uint32_t* xq, int xq_words) {
-  const int lane = threadIdx.x & 31;
-  const int H = p.H;
-  const int npairs = H >> 6;
-  const int lpr = LPR ? LPR : dlanes_per_row(H);
-  const bool shared = slot < 0;
-  const int ntok = shared ? p.T : rt.slot_off[slot + 1] - rt.slot_off[slot];
-  const int lbase = shared ? 0 : rt.slot_off[slot];
-  const int xs_off = dqvec_pair_words(H);
-#pragma unroll 1
-  for (int g0 = 0; g0 < ntok; g0 += MAXT) {
-    const int ng = ntok - g0 < MAXT ? ntok - g0 : MAXT;
-    const uint32_t* rec[MAXT];
-#pragma unroll
-    for (int j = 0; j < MAXT; ++j) {
-      const int jj = g0 + (j < ng ? j : 0);
-      const int tok = shared ? jj : rt.list[lbase + jj] / p.k;
-      rec[j] = xq + (size_t)tok * xq_words;
-    }
-    float ag[MAXT], au[MAXT];
-#pragma unroll
-    for (int j = 0; j < MAXT; ++j) ag[j] = au[j] = 0.0f;
-    if constexpr (MAXT == 1) {
-      // one token: the split-table dot products (fewer ALU-pipe operations)
-      for (int q = lane; q < npairs; q += 32) {
-        const int qbase = qv_base(q, lpr);
-        uint32_t wg[9], wu[9];
-        load_pair_smem(g + q * kPairB, wg);
-        load_pair_smem(u + q * kPairB, wu);
-        float dg0, dg1, du0, du1;
-        pair_scales(wg, dg0, dg1);
-        pair_scales(wu, du0, du1);
-        const uint4* r4 = reinterpret_cast<const uint4*>(rec[0]) + qbase;
-        uint32_t v[32];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 t4 = r4[c * lpr];
-          v[4 * c] = t4.x; v[4 * c + 1] = t4.y; v[4 * c + 2] = t4.z; v[4 * c + 3] = t4.w;
-        }
-        const float2 sc = reinterpret_cast<const float2*>(rec[0] + xs_off)[q];
-        int ig0, ig1, iu0, iu1;
-        iq4_pair_dot1(wg, v, ig0, ig1);
-        iq4_pair_dot1(wu, v, iu0, iu1);
-        ag[0] = fmaf((float)ig0, dg0 * sc.x, ag[0]);
-        ag[0] = fmaf((float)ig1, dg1 * sc.y, ag[0]);
-        au[0] = fmaf((float)iu0, du0 * sc.x, au[0]);
-        au[0] = fmaf((float)iu1, du1 * sc.y, au[0]);
-      }
-    } else {
-    for (int q = lane; q < npairs; q += 32) {
-      const int qbase = qv_base(q, lpr);
-      uint32_t w[9];
-      float dg0, dg1, du0, du1;
-      uint32_t a0[4], a1[4];
-      uint32_t tg0[8], tg1[8], tu0[8], tu1[8];
-      load_pair_smem(g + q * kPairB, w);
-      split_pair(w, dg0, dg1, a0, a1);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        iq4_lookup8(a0[i], tg0[2 * i], tg0[2 * i + 1]);
-        iq4_lookup8(a1[i], tg1[2 * i], tg1[2 * i + 1]);
-      }
-      load_pair_smem(u + q * kPairB, w);
-      split_pair(w, du0, du1, a0, a1);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        iq4_lookup8(a0[i], tu0[2 * i], tu0[2 * i + 1]);
-        iq4_lookup8(a1[i], tu1[2 * i], tu1[2 * i + 1]);
-      }
-#pragma unroll
-      for (int j = 0; j < MAXT; ++j) {
-        if (j < ng) {
-          const uint4* r4 = reinterpret_cast<const uint4*>(rec[j]) + qbase;
-          uint32_t v[32];
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint4 t4 = r4[c * lpr];
-            v[4 * c] = t4.x; v[4 * c + 1] = t4.y; v[4 * c + 2] = t4.z; v[4 * c + 3] = t4.w;
-          }
-          const float2 sc = reinterpret_cast<const float2*>(rec[j] + xs_off)[q];
-          const int ig0 = iq4_dot_block(tg0, v);
-          const int ig1 = iq4_dot_block(tg1, v + 16);
-          const int iu0 = iq4_dot_block(tu0, v);
-          const int iu1 = iq4_dot_block(tu1, v + 16);
-          ag[j] = fmaf((float)ig0, dg0 * sc.x, ag[j]);
-          ag[j] = fmaf((float)ig1, dg1 * sc.y, ag[j]);
-          au[j] = fmaf((float)iu0, du0 * sc.x, au[j]);
-          au[j] = fmaf((float)iu1, du1 * sc.y, au[j]);
-        }
-      }
-    }
-    }
-#pragma unroll
-    for (int j = 0; j < MAXT; ++j) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        ag[j] += __shfl_xor_sync(0xFFFFFFFFu, ag[j], o);
-        au[j] += __shfl_xor_sync(0xFFFFFFFFu, au[j], o);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < MAXT; ++j) {
-      if (j < ng && lane == j) {
-        const float hv = silu_mul(ag[j], au[j]);
-        if (shared) p.h_s[(size_t)(g0 + j) * p.Fs + f] = hv;
-        else p.h_r[(size_t)rt.list[lbase + g0 + j] * p.F + f] = hv;
-      }
-    }
-  }
-}
-
 // One down unit: rows [r0, r0 + nrows) (CTA-local indices) of the slot's W_d at
 // `wrows`; for every pair of the slot, the row dot products into `part`.
 // NPS pairs share each decoded block; LPR as for gate/up (0 = run time).
@@ -251,8 +133,8 @@ __device__ __forceinline__ void down_unit_t(const DecodeParams& p, const RouteTa
       for (int j = 0; j < NPS; ++j) acc[j] = 0.0f;
       if (active) {
         const uint8_t* row = wrows + (size_t)rl * rbK;
-        if constexpr (NPS == 1) {
-          // one token: the split-table dot products
+        if (NPS == 1 || np == 1) {
+          // one token: the split-table dot products (same integers as below)
           for (int q = q0; q < npq; q += lpr) {
             const int qbase = qv_base(q, lpr);
             uint32_t w[9];

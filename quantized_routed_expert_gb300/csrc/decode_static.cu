@@ -81,14 +81,13 @@ extern "C" moe_status moe_iq4nl_decode_static(const moe_shape* shape,
   const moe_status st = scratch_address(&scratch);
   if (st != MOE_OK) return st;
   // The scratch keeps whatever the previous call left (a call that timed out
-  // may leave its counters non-zero). The decode kernels need their arrival
-  // and grid-barrier counters at zero when they start, so clear exactly those
-  // words on the stream first: a stream-ordered memset, not an allocation.
+  // may leave its counters non-zero). The fused decode kernel needs its
+  // grid-barrier counters at zero when it starts, so clear exactly those words
+  // on the stream first: a stream-ordered memset, not an allocation.
   // Everything else in the scratch is written before it is read within a call.
   const moe::DecodeLayout L = moe::decode_layout(*shape, T);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(reinterpret_cast<uint8_t*>(scratch) + L.cnt, 0,
-                      (size_t)(L.sync + 64 - L.cnt), s) != cudaSuccess) {
+  if (cudaMemsetAsync(reinterpret_cast<uint8_t*>(scratch) + L.sync, 0, 64, s) != cudaSuccess) {
     cudaGetLastError();
     return MOE_ERR_CUDA;
   }

@@ -105,8 +105,8 @@ moe::DecodeParams decode_params(const moe_shape* shape, const moe_expert_weights
   p.h_s = reinterpret_cast<float*>(base + L.h_s);
   p.rec_r = reinterpret_cast<uint32_t*>(base + L.rec_r);
   p.rec_s = reinterpret_cast<uint32_t*>(base + L.rec_s);
-  p.cnt = reinterpret_cast<uint32_t*>(base + L.cnt);
   p.sync = reinterpret_cast<uint32_t*>(base + L.sync);
+  p.xrec = reinterpret_cast<uint32_t*>(base + L.xrec);
   p.status = status;
   return p;
 }
@@ -256,7 +256,8 @@ int32_t moe_launches_per_call(const moe_shape* shape, int32_t T, int32_t call) {
     size_t sm = 0;
     int rg = 0, rmax = 0;
     if (moe::fused_decode_supported(p, sms, &sm, &rg, &rmax)) return 1;
-    return call == 2 ? 3 : 2;
+    const int n = moe::decode_launches(p, sms);
+    return call == 2 ? n + 1 : n;
   }
   if (call == 3) return moe::prefill_launches(*shape, T);
   return MOE_ERR_INVALID_ARG;

@@ -206,10 +206,16 @@ cudaError_t launch_route(const RouteParams& p, bool pdl, cudaStream_t stream) {
     while (t < p.T) t <<= 1;
     TT = t;
   }
+  // Decode batches: 16-CTA clusters (a non-portable size where allowed, else
+  // 8) split the experts, and the tokens go in tiles small enough to give
+  // about 128 CTAs (each cluster reads the router rows from L2 once).
+  const bool decode = p.T <= MOE_MAX_DECODE_TOKENS;
+  if (decode)
+    while (TT > 1 && (p.T + TT - 1) / TT * 16 < 128) TT >>= 1;
   const int ntiles = (p.T + TT - 1) / TT;
-  // Split the experts of a tile over a cluster when there are few tiles: 16
-  // CTAs (a non-portable cluster size) where allowed, else 8.
-  int C = ntiles >= 32 ? 1 : (ntiles >= 8 ? 4 : 16);
+  // Longer chunks: split the experts of a tile over a cluster only when there
+  // are few tiles.
+  int C = decode ? 16 : (ntiles >= 32 ? 1 : (ntiles >= 8 ? 4 : 16));
   while (C > 1 && C > p.E) C >>= 1;
   const size_t sm = route_smem(p.H, p.E, C, TT);
   if (sm > 200 * 1024) return cudaErrorInvalidConfiguration;
