@@ -13,9 +13,6 @@ namespace moe {
 constexpr int kBlockW = 32;       // weights per IQ4_NL block
 constexpr int kBlockB = 18;       // bytes per IQ4_NL block
 constexpr int kPairB = 36;        // bytes per pair of consecutive blocks
-constexpr int kThreads = 288;     // 8 consumer warps + 1 producer warp
-constexpr int kConsumers = 256;
-constexpr int kProducerWarp = 8;
 
 // ---------------------------------------------------------------------------
 // The IQ4_NL table as packed int8 (bytes T[0..3], T[4..7], T[8..11], T[12..15]).
@@ -275,14 +272,6 @@ __device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// Named barrier among the 256 consumer threads (id 1); id 2 adds the producer warp.
-__device__ __forceinline__ void consumers_sync() {
-  asm volatile("bar.sync 1, 256;" ::: "memory");
-}
-__device__ __forceinline__ void all_sync_named() {
-  asm volatile("bar.sync 2, 288;" ::: "memory");
 }
 
 // Host: raise a kernel's dynamic shared memory limit once per (kernel, device),

@@ -132,7 +132,7 @@ __host__ __device__ inline GuSmem gu_smem(int H, int T, int nw, bool xs, int g, 
 __global__ void __launch_bounds__(256) quant_x_kernel(const __grid_constant__ DecodeParams p) {
   pdl_wait();
   pdl_trigger();
-  quant_x_lanes(p.x, p.T, p.H, p.xrec, dqvec_words(p.H), blockIdx.x * blockDim.x + threadIdx.x,
+  quant_x_lanes<4>(p.x, p.T, p.H, p.xrec, dqvec_words(p.H), blockIdx.x * blockDim.x + threadIdx.x,
                 gridDim.x * blockDim.x);
 }
 
@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(512, 1) gu_kernel(const __grid_constant__ Deco
   pdl_wait();
   pdl_trigger();
   uint32_t* xq = XS ? reinterpret_cast<uint32_t*>(smem + L.xq) : p.xrec;
-  if (XS) quant_x_lanes(p.x, p.T, H, xq, xq_words, threadIdx.x, blockDim.x);
+  if (XS) quant_x_lanes<4>(p.x, p.T, H, xq, xq_words, threadIdx.x, blockDim.x);
   if (p.T * p.k <= 64) {
     if (warp == 0) build_route_table_warp(rt, p.ids, p.weights, p.T * p.k, p.E);
     __syncthreads();
@@ -334,269 +334,233 @@ __global__ void __launch_bounds__(512, 1) gu_kernel(const __grid_constant__ Deco
   }
 }
 
+// ---------------------------------------------------------------------------
+// Down projection of the two-kernel path, then the combine. Work is split as
+// in the gate/up kernel: 32-row blocks of every expert's W_d (H output rows),
+// the shared expert's blocks on the last CTAs and the routed blocks by cost.
+// Every warp streams units of RU rows (two slots) and computes them with the
+// fused kernel's per-row code, reading the quantised h records from global
+// memory (a CTA's blocks belong to one or two experts, so their records stay
+// in L1). Each (pair, row) dot product goes to a partial buffer, which the
+// combine kernel sums per token in the fixed order: shared expert first, then
+// the routed experts ascending (the fused kernel's order).
+
+// Rows per down unit for K inputs: a power of two, at least the rows that make
+// a copy a multiple of 16 bytes, at most 32, and otherwise the most rows that
+// fit in 4608 bytes (a gate/up unit at H = 4096).
+__host__ __device__ inline int dn_rows_per_unit(int K) {
+  const int rbK = K / 32 * kBlockB;
+  int ru = 32;
+  while (ru > 1 && ru * rbK > 4608) ru >>= 1;
+  const int gd = row_granule_dev(K);
+  return ru < gd ? gd : ru;
+}
+
 struct DnSmem {
-  size_t yacc, bar, ring, stage, total;
+  size_t slots, bars, total, slot_bytes;
 };
-__host__ __device__ inline DnSmem dn_smem(int F, int Fs, int n_shared, int T, int rows_max,
-                                          int nst) {
+__host__ __device__ inline DnSmem dn_smem(int F, int Fs, int n_shared, int nw) {
   DnSmem m;
-  m.yacc = align_up_dev(sizeof(RouteTable), 16);
-  m.bar = align_up_dev(m.yacc + (size_t)rows_max * T * 4, 16);
-  m.ring = align_up_dev(m.bar + (size_t)16 * nst, 128);
-  size_t rb = (size_t)(F / 32) * kBlockB;
-  size_t rec = (size_t)dqvec_words(F) * 4;
+  size_t ub = (size_t)dn_rows_per_unit(F) * (F / 32) * kBlockB;
   if (n_shared) {
-    const size_t rbs = (size_t)(Fs / 32) * kBlockB;
-    const size_t recs = (size_t)dqvec_words(Fs) * 4;
-    rb = rb > rbs ? rb : rbs;
-    rec = rec > recs ? rec : recs;
+    const size_t us = (size_t)dn_rows_per_unit(Fs) * (Fs / 32) * kBlockB;
+    ub = us > ub ? us : ub;
   }
-  m.stage = align_up_dev(align_up_dev((size_t)rows_max * rb, 16) + kPairsPerStage * rec, 128);
-  m.total = m.ring + (size_t)nst * m.stage;
+  m.slot_bytes = align_up_dev(ub, 128);
+  m.slots = align_up_dev(sizeof(RouteTable), 128);
+  m.bars = m.slots + (size_t)nw * kGuSlots * m.slot_bytes;
+  m.total = m.bars + (size_t)nw * kGuSlots * 8;
   return m;
 }
 
-// ---------------------------------------------------------------------------
-// Down + combine. Each CTA owns output rows [n0, n1) and walks the stages:
-// the shared expert (if any) first, then the routed experts in ascending id;
-// each stage holds those rows of one expert's W_d and the quantised h of up
-// to kPairsPerStage of its (token, slot) pairs.
-struct StageIt {
-  int slot;  // -1 = shared expert
-  int g0;
-};
-
-__device__ __forceinline__ int stage_ntok(const DecodeParams& p, const RouteTable& rt, int slot) {
-  return slot < 0 ? p.T : rt.slot_off[slot + 1] - rt.slot_off[slot];
-}
-__device__ __forceinline__ StageIt stage_first(const DecodeParams& p, const RouteTable& rt) {
-  if (p.n_shared && p.T > 0) return StageIt{-1, 0};
-  return StageIt{0, 0};
-}
-__device__ __forceinline__ bool stage_done(const RouteTable& rt, const StageIt& s) {
-  return s.slot >= rt.n_slots;
-}
-__device__ __forceinline__ void stage_next(const DecodeParams& p, const RouteTable& rt,
-                                           StageIt& s) {
-  s.g0 += kPairsPerStage;
-  if (s.g0 >= stage_ntok(p, rt, s.slot)) {
-    s.slot += 1;
-    s.g0 = 0;
-  }
-}
-
-template <int NPS>
-__global__ void __launch_bounds__(kThreads, 2) down_kernel(const DecodeParams p) {
+template <int LPR>
+__global__ void __launch_bounds__(512, 1) dn_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int H = p.H;
-  const int NST = p.dn_stages;
-  const DnSmem L = dn_smem(p.F, p.Fs, p.n_shared, p.T, p.dn_rows_max, NST);
+  const int nw = blockDim.x >> 5;
+  const DnSmem L = dn_smem(p.F, p.Fs, p.n_shared, nw);
   RouteTable& rt = *reinterpret_cast<RouteTable*>(smem);
-  float* yacc = reinterpret_cast<float*>(smem + L.yacc);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar);
-  uint64_t* empty = full + NST;
-  uint8_t* ring = smem + L.ring;
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  int gd = row_granule_dev(p.F);
-  if (p.n_shared && row_granule_dev(p.Fs) > gd) gd = row_granule_dev(p.Fs);
-  const RowRange rows = split_rows(H, gd, blockIdx.x, gridDim.x);
-  const int n0 = rows.a;
-  const int nrows = rows.b - rows.a;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint8_t* myslots = smem + L.slots + (size_t)warp * kGuSlots * L.slot_bytes;
+  uint64_t* mybar = bars + warp * kGuSlots;
+  const int P = p.T * p.k;
+  const int ru = dn_rows_per_unit(p.F), rus = p.n_shared ? dn_rows_per_unit(p.Fs) : 32;
+  const uint32_t rbK = (uint32_t)(p.F / 32 * kBlockB), rbKs = (uint32_t)(p.Fs / 32 * kBlockB);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NST; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumers / 32);
-    }
+#pragma unroll 1
+    for (int i = 0; i < nw * kGuSlots; ++i) mbar_init(&bars[i], 1);
     mbar_fence_init();
   }
   __syncthreads();
 
-  if (warp == kProducerWarp) {
-    all_sync_named();  // route table ready (ids come from the router, already complete)
-    if (lane == 0) {
-      auto desc = [&](const StageIt& si, const uint8_t*& wsrc, uint32_t& wbytes, int& np,
-                      uint32_t& rbytes) {
-        const bool sh = si.slot < 0;
-        const int K = sh ? p.Fs : p.F;
-        const int rbK = K / 32 * kBlockB;
-        const int64_t erow = sh ? 0 : (int64_t)rt.slot_expert[si.slot] * H;
-        wsrc = (sh ? p.sh_down : p.down) + (erow + n0) * rbK;
-        wbytes = (uint32_t)(nrows * rbK);
-        const int nt = stage_ntok(p, rt, si.slot) - si.g0;
-        np = nt < NPS ? nt : NPS;
-        rbytes = (uint32_t)dqvec_words(K) * 4;
-      };
-      auto issue_recs = [&](const StageIt& si, int s) {
-        const uint8_t* wsrc;
-        uint32_t wbytes, rbytes;
-        int np;
-        desc(si, wsrc, wbytes, np, rbytes);
-        uint8_t* dst = ring + (size_t)s * L.stage + wbytes;
-        for (int j = 0; j < np; ++j) {
-          const uint32_t* src;
-          if (si.slot < 0) src = p.rec_s + (size_t)(si.g0 + j) * (rbytes / 4);
-          else src = p.rec_r + (size_t)rt.list[rt.slot_off[si.slot] + si.g0 + j] * (rbytes / 4);
-          bulk_g2s(dst + (size_t)j * rbytes, src, rbytes, &full[s]);
-        }
-      };
-      const uint64_t pol = l2_evict_first_policy();   // weights: read once per call
-      int it = 0;
-      bool waited = false;
-      StageIt si = stage_first(p, rt);
-      while (!stage_done(rt, si)) {
-        const int s = it % NST;
-        const uint32_t par = ((it / NST) & 1) ^ 1;
-        if (!mbar_wait(&empty[s], par, p.status)) break;
-        const uint8_t* wsrc;
-        uint32_t wbytes, rbytes;
-        int np;
-        desc(si, wsrc, wbytes, np, rbytes);
-        mbar_arrive_expect_tx(&full[s], wbytes + np * rbytes);
-        if (wbytes) bulk_g2s_hint(ring + (size_t)s * L.stage, wsrc, wbytes, &full[s], pol);
-        if (waited) issue_recs(si, s);
-        ++it;
-        stage_next(p, rt, si);
-        if (!waited && (it == NST || stage_done(rt, si))) {
-          // the quantised h comes from the gate/up kernel: wait for it
-          pdl_wait();
-          waited = true;
-          StageIt sj = stage_first(p, rt);
-          for (int j = 0; j < it; ++j) {
-            issue_recs(sj, j);
-            stage_next(p, rt, sj);
-          }
-        }
+  const int G = gridDim.x, c = blockIdx.x;
+  const int S = p.n_shared ? H / 32 : 0;
+  const int sb0 = gu_shared_cum(S, c, G), sb1 = gu_shared_cum(S, c + 1, G);
+  const int n_sh_u = (sb1 - sb0) * (32 / rus);
+  int rb0 = 0, n_u = n_sh_u;
+  auto count = [&](int nu) { return warp < nu ? (nu - warp + nw - 1) / nw : 0; };
+  const int n_sh = count(n_sh_u);
+  int n_tot = n_sh;
+  int issued = 0, consumed = 0;
+  bool ok = true;
+  const uint64_t pol = l2_evict_first_policy();   // weights: read once per call
+  // a warp's units in order (u = warp, warp + nw, ...): slot (-1 shared) and
+  // first output row, kept up to date without divisions
+  struct Cursor {
+    int u, sl, row;
+  };
+  auto cur_get = [&](Cursor& k, int& sl, int& row) {
+    if (k.u < n_sh_u) {
+      sl = -1;
+      row = sb0 * 32 + k.u * rus;
+      return;
+    }
+    if (k.sl < 0) {
+      const int r = rb0 * 32 + (k.u - n_sh_u) * ru;
+      k.sl = r / H;
+      k.row = r - k.sl * H;
+    }
+    sl = k.sl;
+    row = k.row;
+  };
+  auto cur_next = [&](Cursor& k) {
+    if (k.sl >= 0) {
+      k.row += nw * ru;
+      while (k.row >= H) {
+        k.row -= H;
+        ++k.sl;
       }
     }
-    __syncwarp();
-    pdl_wait();
-    pdl_trigger();
-    return;
-  }
+    k.u += nw;
+  };
+  Cursor ci{warp, -1, 0}, cc{warp, -1, 0};
+  auto issue_upto = [&](int limit) {
+    while (issued < limit && issued - consumed < kGuSlots) {
+      int sl, row;
+      cur_get(ci, sl, row);
+      if (lane == 0) {
+        const int s = issued % kGuSlots;
+        const uint8_t* src = sl < 0 ? p.sh_down + (size_t)row * rbKs
+                                    : p.down + ((size_t)rt.slot_expert[sl] * H + row) * rbK;
+        const uint32_t bytes = sl < 0 ? rus * rbKs : ru * rbK;    // multiples of 16
+        mbar_arrive_expect_tx(&mybar[s], bytes);
+        bulk_g2s_hint(myslots + (size_t)s * L.slot_bytes, src, bytes, &mybar[s], pol);
+      }
+      cur_next(ci);
+      ++issued;
+    }
+  };
 
-  // Consumers.
-  build_route_table<1>(rt, p.ids, p.weights, p.T * p.k, p.E, kConsumers);
-  for (int i = threadIdx.x; i < nrows * p.T; i += kConsumers) yacc[i] = 0.0f;
-  consumers_sync();
-  all_sync_named();
-  pdl_wait();
+  issue_upto(n_sh);
+  // ids and weights come from a kernel that finished before the gate/up kernel
+  // passed its own dependency wait: they may be read before this one's
+  if (P <= 64) {
+    if (warp == 0) build_route_table_warp(rt, p.ids, p.weights, P, p.E);
+    __syncthreads();
+  } else {
+    build_route_table<0>(rt, p.ids, p.weights, P, p.E, blockDim.x);
+  }
+  {
+    const int bps = H / 32;
+    rb0 = gu_routed_cum(rt, bps, S, p.T, c, G);
+    const int rb1 = gu_routed_cum(rt, bps, S, p.T, c + 1, G);
+    n_u = n_sh_u + (rb1 - rb0) * (32 / ru);
+  }
+  n_tot = count(n_u);
+  issue_upto(n_tot);
+  pdl_wait();                  // the records come from the gate/up kernel
   pdl_trigger();
 
-  int it = 0;
-  for (StageIt si = stage_first(p, rt); !stage_done(rt, si); stage_next(p, rt, si), ++it) {
-    const int s = it % NST;
-    if (!mbar_wait(&full[s], (it / NST) & 1, p.status)) break;
-    const bool sh = si.slot < 0;
-    const int K = sh ? p.Fs : p.F;
-    const int rbK = K / 32 * kBlockB;
-    const int lpr = dlanes_per_row(K);
-    const int rpw = 32 / lpr;
-    const int npq = K / 64;
-    const int words = dqvec_words(K);
-    const int pw = dqvec_pair_words(K);
-    const int nt = stage_ntok(p, rt, si.slot) - si.g0;
-    const int np = nt < NPS ? nt : NPS;
-    const uint8_t* wst = ring + (size_t)s * L.stage;
-    const uint32_t* recs = reinterpret_cast<const uint32_t*>(wst + (size_t)nrows * rbK);
-    int tok[NPS];
-    float wgt[NPS];
-#pragma unroll
-    for (int j = 0; j < NPS; ++j) {
-      const int jj = si.g0 + (j < np ? j : 0);
-      if (sh) {
-        tok[j] = jj;
-        wgt[j] = 1.0f;
-      } else {
-        const int pr = rt.list[rt.slot_off[si.slot] + jj];
-        tok[j] = pr / p.k;
-        wgt[j] = rt.wt[pr];
-      }
-    }
-    const int q0 = lane % lpr;
-    for (int rbase = warp * rpw; rbase < nrows; rbase += (kConsumers / 32) * rpw) {
-      const int r = rbase + lane / lpr;
-      const bool active = r < nrows;
-      float acc[NPS];
-#pragma unroll
-      for (int j = 0; j < NPS; ++j) acc[j] = 0.0f;
-      if (active && np == 1) {
-        // one token: the split-table dot products (same integers as below)
-        const uint8_t* row = wst + (size_t)r * rbK;
-        const float* sc = reinterpret_cast<const float*>(recs + pw);
+  const int words = dqvec_words(p.F), words_s = dqvec_words(p.Fs);
 #pragma unroll 1
-        for (int q = q0; q < npq; q += lpr) {
-          const int qbase = qv_base(q, lpr);
-          uint32_t w[9];
-          load_pair_smem(row + q * kPairB, w);
-          float d0, d1;
-          pair_scales(w, d0, d1);
-          const uint4* r4 = reinterpret_cast<const uint4*>(recs) + qbase;
-          uint32_t v[32];
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint4 u = r4[c * lpr];
-            v[4 * c] = u.x; v[4 * c + 1] = u.y; v[4 * c + 2] = u.z; v[4 * c + 3] = u.w;
-          }
-          int i0, i1;
-          iq4_pair_dot1(w, v, i0, i1);
-          acc[0] = fmaf((float)i0, d0 * sc[2 * q], acc[0]);
-          acc[0] = fmaf((float)i1, d1 * sc[2 * q + 1], acc[0]);
-        }
-      } else if (active) {
-        const uint8_t* row = wst + (size_t)r * rbK;
-#pragma unroll 1
-        for (int q = q0; q < npq; q += lpr) {
-          const int qbase = qv_base(q, lpr);
-          uint32_t w[9];
-          float d0, d1;
-          uint32_t a0[4], a1[4];
-          uint32_t t0[8], t1[8];
-          load_pair_smem(row + q * kPairB, w);
-          split_pair(w, d0, d1, a0, a1);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            iq4_lookup8(a0[i], t0[2 * i], t0[2 * i + 1]);
-            iq4_lookup8(a1[i], t1[2 * i], t1[2 * i + 1]);
-          }
-#pragma unroll
-          for (int j = 0; j < NPS; ++j) {
-            if (j < np) {
-              const uint32_t* rec = recs + (size_t)j * words;
-              const uint4* r4 = reinterpret_cast<const uint4*>(rec) + qbase;
-              uint32_t v[32];
-#pragma unroll
-              for (int c = 0; c < 8; ++c) {
-                const uint4 u = r4[c * lpr];
-                v[4 * c] = u.x; v[4 * c + 1] = u.y; v[4 * c + 2] = u.z; v[4 * c + 3] = u.w;
-              }
-              const float* sc = reinterpret_cast<const float*>(rec + pw);
-              const int i0 = iq4_dot_block(t0, v);
-              const int i1 = iq4_dot_block(t1, v + 16);
-              acc[j] = fmaf((float)i0, d0 * sc[2 * q], acc[j]);
-              acc[j] = fmaf((float)i1, d1 * sc[2 * q + 1], acc[j]);
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < NPS; ++j)
-        if (j < np)
-          for (int o = lpr >> 1; o > 0; o >>= 1) acc[j] += __shfl_xor_sync(0xFFFFFFFFu, acc[j], o);
-      if (active && q0 == 0) {
-#pragma unroll
-        for (int j = 0; j < NPS; ++j)
-          if (j < np) yacc[r * p.T + tok[j]] += wgt[j] * acc[j];
-      }
-    }
+  for (int j = 0; ok && j < n_tot; ++j) {
+    ok = mbar_wait(&mybar[j % kGuSlots], (uint32_t)((j / kGuSlots) & 1), p.status);
+    if (!ok) break;
+    const uint8_t* d = myslots + (size_t)(j % kGuSlots) * L.slot_bytes;
+    int sl, row;
+    cur_get(cc, sl, row);
+    cur_next(cc);
+    const bool shared = sl < 0;
+    const int ntok = shared ? p.T : rt.slot_off[sl + 1] - rt.slot_off[sl];
+    const int lbase = shared ? 0 : rt.slot_off[sl];
+    auto pidx = [&](int jj) { return shared ? P + jj : rt.list[lbase + jj]; };
+    auto rec_of = [&](int jj) -> const uint32_t* {
+      return shared ? p.rec_s + (size_t)jj * words_s : p.rec_r + (size_t)pidx(jj) * words;
+    };
+    auto store = [&](int jj, int rl, float v) { p.part[(size_t)pidx(jj) * H + row + rl] = v; };
+    if (ntok == 1)
+      down_rows<1, LPR>(d, shared ? p.Fs : p.F, shared ? rus : ru, 1, rec_of, store);
+    else
+      down_rows<kGuMaxT, LPR>(d, shared ? p.Fs : p.F, shared ? rus : ru, ntok, rec_of, store);
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
+    ++consumed;
+    issue_upto(n_tot);
   }
-  consumers_sync();
-  for (int i = threadIdx.x; i < nrows * p.T; i += kConsumers) {
-    const int t = i / nrows, r = i - t * nrows;
-    p.y[(size_t)t * H + n0 + r] = yacc[r * p.T + t];
+  // after a timeout: no bulk copy of this warp stays in flight
+  while (consumed < issued) {
+    mbar_wait(&mybar[consumed % kGuSlots], (uint32_t)((consumed / kGuSlots) & 1), p.status);
+    ++consumed;
+  }
+}
+
+// y[t][n] = shared expert's partial + the routed partials of token t, in the
+// route table's order (experts ascending, then pair index), each times its
+// weight: the fused kernel's combine. One warp per token first sorts the
+// token's valid pairs into that order (ranks by ballots), which needs only the
+// ids and weights; then every thread sums its outputs.
+__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ DecodeParams p) {
+  __shared__ int tp[MOE_MAX_DECODE_TOKENS][MOE_MAX_TOP_K];   // pair indices in order
+  __shared__ float tw[MOE_MAX_DECODE_TOKENS][MOE_MAX_TOP_K];
+  __shared__ int tc[MOE_MAX_DECODE_TOKENS];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int k = p.k;
+  // ids and weights come from a kernel that finished before the gate/up
+  // kernel passed its own dependency wait: they may be read before this one's
+#pragma unroll 1
+  for (int t = warp; t < p.T; t += blockDim.x >> 5) {
+    const int pr = t * k + lane;
+    int e = -1;
+    float w = 0.0f;
+    if (lane < k) {
+      const int id = p.ids[pr];
+      if (id >= 0 && id < p.E) {
+        e = id;
+        w = p.weights[pr];
+      }
+    }
+    int rank = 0;
+#pragma unroll 1
+    for (int j = 0; j < k; ++j) {
+      const int ej = __shfl_sync(0xFFFFFFFFu, e, j);
+      rank += ej >= 0 && (ej < e || (ej == e && j < lane));
+    }
+    const unsigned valid = __ballot_sync(0xFFFFFFFFu, e >= 0);
+    if (e >= 0) {
+      tp[t][rank] = pr;
+      tw[t][rank] = w;
+    }
+    if (lane == 0) tc[t] = __popc(valid);
+  }
+  __syncthreads();
+  pdl_wait();
+  pdl_trigger();
+  const int H = p.H, P = p.T * k;
+#pragma unroll 1
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < p.T * H; i += gridDim.x * blockDim.x) {
+    const int t = i / H, n = i - t * H;
+    const int cnt = tc[t];
+    float v[MOE_MAX_TOP_K];
+#pragma unroll
+    for (int r = 0; r < MOE_MAX_TOP_K; ++r)
+      v[r] = r < cnt ? p.part[(size_t)tp[t][r] * H + n] : 0.0f;
+    float acc = 0.0f;
+    if (p.n_shared) acc = p.part[(size_t)(P + t) * H + n];
+#pragma unroll
+    for (int r = 0; r < MOE_MAX_TOP_K; ++r)
+      if (r < cnt) acc += tw[t][r] * v[r];
+    p.y[i] = acc;
   }
 }
 
@@ -647,11 +611,6 @@ bool gu_config(const DecodeParams& p, int num_sms, int* nw, bool* xs, size_t* sm
   return false;
 }
 
-int down_stages(const DnSmem& one, int lo, int hi) {
-  int n = hi;
-  while (n > lo && one.ring + (size_t)n * one.stage > kSmemMax) --n;
-  return n;
-}
 }  // namespace
 
 int decode_launches(const DecodeParams& p, int num_sms) {
@@ -661,8 +620,8 @@ int decode_launches(const DecodeParams& p, int num_sms) {
   int nw = 0, nblk = 0;
   bool xs = true;
   size_t sm = 0;
-  if (!gu_config(p, num_sms, &nw, &xs, &sm, &nblk)) return 2;
-  return xs ? 2 : 3;
+  if (!gu_config(p, num_sms, &nw, &xs, &sm, &nblk)) return 3;
+  return xs ? 3 : 4;
 }
 
 cudaError_t launch_decode(const DecodeParams& p0, int num_sms, bool pdl, cudaStream_t stream) {
@@ -683,14 +642,9 @@ cudaError_t launch_decode(const DecodeParams& p0, int num_sms, bool pdl, cudaStr
   size_t gsm = 0;
   if (!gu_config(p, num_sms, &nw, &xs, &gsm, &p.gu_nblk)) return cudaErrorInvalidConfiguration;
   // down
-  int gd = row_granule_dev(p.F);
-  if (p.n_shared && row_granule_dev(p.Fs) > gd) gd = row_granule_dev(p.Fs);
-  const int units = p.H / gd;
-  const int grid_dn = units < num_sms ? units : num_sms;
-  p.dn_rows_max = (units + grid_dn - 1) / grid_dn * gd;
-  const DnSmem d1 = dn_smem(p.F, p.Fs, p.n_shared, p.T, p.dn_rows_max, 1);
-  p.dn_stages = down_stages(d1, 1, 8);
-  const size_t dsm = dn_smem(p.F, p.Fs, p.n_shared, p.T, p.dn_rows_max, p.dn_stages).total;
+  int dnw = 16;
+  while (dnw > 4 && dn_smem(p.F, p.Fs, p.n_shared, dnw).total > kSmemMax) dnw >>= 1;
+  const size_t dsm = dn_smem(p.F, p.Fs, p.n_shared, dnw).total;
   if (dsm > kSmemMax) return cudaErrorInvalidConfiguration;
 
   cudaError_t e;
@@ -707,7 +661,13 @@ cudaError_t launch_decode(const DecodeParams& p0, int num_sms, bool pdl, cudaStr
   else e = xs ? launch(gu_kernel<0, true>, num_sms, nw * 32, gsm, pdl, stream, p)
               : launch(gu_kernel<0, false>, num_sms, nw * 32, gsm, pdl, stream, p);
   if (e != cudaSuccess) return e;
-  return launch(down_kernel<kPairsPerStage>, grid_dn, kThreads, dsm, pdl, stream, p);
+  const bool d8 = lanes_per_row(p.F) == 8 && (!p.n_shared || lanes_per_row(p.Fs) == 8);
+  e = d8 ? launch(dn_kernel<8>, num_sms, dnw * 32, dsm, pdl, stream, p)
+         : launch(dn_kernel<0>, num_sms, dnw * 32, dsm, pdl, stream, p);
+  if (e != cudaSuccess) return e;
+  int cgrid = (p.T * p.H + 255) / 256;
+  if (cgrid > num_sms) cgrid = num_sms;
+  return launch(combine_kernel, cgrid, 256, 0, pdl, stream, p);
 }
 
 // Route + layer in one call: one fused launch when the shape allows, else the

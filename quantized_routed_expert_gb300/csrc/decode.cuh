@@ -9,7 +9,6 @@
 namespace moe {
 
 constexpr int kMaxPairs = MOE_MAX_DECODE_TOKENS * MOE_MAX_TOP_K;  // T*k
-constexpr int kPairsPerStage = 4; // h vectors per down stage
 
 inline int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 
@@ -37,7 +36,7 @@ inline int64_t qvec_words(int64_t K) {
 }
 
 struct DecodeLayout {
-  int64_t h_r, h_s, rec_r, rec_s, sync, scores, xrec, total;  // byte offsets
+  int64_t h_r, h_s, rec_r, rec_s, sync, scores, xrec, part, total;  // byte offsets
 };
 
 inline DecodeLayout decode_layout(const moe_shape& s, int64_t T) {
@@ -56,6 +55,7 @@ inline DecodeLayout decode_layout(const moe_shape& s, int64_t T) {
   L.sync = take(64);                       // grid-barrier counters of the fused kernel
   L.scores = take(T * s.n_experts * 4);    // router scores of the routed fused kernel
   L.xrec = take(T * qvec_words(s.hidden) * 4);   // quantised x, when it does not fit on chip
+  L.part = take((T * s.top_k + (Fs ? T : 0)) * s.hidden * 4);   // down partials per pair
   L.total = off;
   return L;
 }
@@ -79,6 +79,7 @@ struct DecodeParams {
   uint32_t* sync;    // [4]: h arrivals, departures, score arrivals (fused kernel)
   uint32_t* status;
   uint32_t* xrec;    // [T][qvec_words(H)]: quantised x (gate/up kernel without room for it)
+  float* part;       // [T*k (+T)][H]: down partials per pair (two-kernel path)
   // routing inside the fused kernel (route != 0)
   int route;
   const uint16_t* Wr;    // bf16 [E][H]
@@ -88,7 +89,6 @@ struct DecodeParams {
   float* scores;         // workspace [T][E]
   // launch-derived
   int gu_nblk;       // gate/up kernel: 32-row blocks a CTA may get
-  int dn_stages;     // down ring depth
   int dn_rows_max;   // max output rows per down CTA
   int fz_rg;         // fused kernel: output rows per down unit
 };

@@ -346,9 +346,9 @@ __device__ __forceinline__ void quant_group8(const float (&v)[8], bool ok, int b
 // global memory), four lanes per 32-value block (16 bytes each); all threads
 // tid, tid + nt, ... (nt a multiple of 32). Each thread has kXLoads loads in
 // flight before it quantises any of them.
+template <int kXLoads>
 __device__ __forceinline__ void quant_x_lanes(const uint16_t* __restrict__ x, int T, int K,
                                               uint32_t* xq, int xq_words, int tid, int nt) {
-  constexpr int kXLoads = 4;
   const int nb = K / 32;
   const int n = T * nb * 4;
 #pragma unroll 1
@@ -382,6 +382,108 @@ __device__ __forceinline__ void quant_x_lanes(const uint16_t* __restrict__ x, in
     }
   }
 }
+
+// The down rows of one expert, [0, nrows) of `wrows` (K inputs each), for its
+// ntok tokens: rec_of(j) is token j's quantised h record, store(j, row, v) takes
+// the row's dot product. Lanes split a row lpr ways (pairs q = q0, q0 + lpr,
+// ..., accumulated in that order, then an xor butterfly); NPS tokens share each
+// decoded block; LPR = lpr when known at compile time, else 0.
+template <int NPS, int LPR, typename RecOf, typename Store>
+__device__ __forceinline__ void down_rows(const uint8_t* wrows, int K, int nrows, int ntok,
+                                          RecOf rec_of, Store store) {
+  const int lane = threadIdx.x & 31;
+  const int rbK = (K >> 5) * kBlockB;
+  const int lpr = LPR ? LPR : dlanes_per_row(K);
+  const int rpw = 32 / lpr;
+  const int npq = K >> 6;
+  const int pw = dqvec_pair_words(K);
+  const int q0 = lane & (lpr - 1);
+#pragma unroll 1
+  for (int g0 = 0; g0 < ntok; g0 += NPS) {
+    const int np = ntok - g0 < NPS ? ntok - g0 : NPS;
+    const uint32_t* rp[NPS];
+#pragma unroll
+    for (int j = 0; j < NPS; ++j) rp[j] = rec_of(g0 + (j < np ? j : 0));
+#pragma unroll 1
+    for (int rb = 0; rb < nrows; rb += rpw) {
+      const int rl = rb + lane / lpr;
+      const bool active = rl < nrows;
+      float acc[NPS];
+#pragma unroll
+      for (int j = 0; j < NPS; ++j) acc[j] = 0.0f;
+      if (active) {
+        const uint8_t* row = wrows + (size_t)rl * rbK;
+        if (NPS == 1 || np == 1) {
+          // one token: the split-table dot products (same integers as below)
+          for (int q = q0; q < npq; q += lpr) {
+            const int qbase = qv_base(q, lpr);
+            uint32_t w[9];
+            load_pair_smem(row + q * kPairB, w);
+            float d0, d1;
+            pair_scales(w, d0, d1);
+            const uint4* r4 = reinterpret_cast<const uint4*>(rp[0]) + qbase;
+            uint32_t v[32];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint4 t4 = r4[c * lpr];
+              v[4 * c] = t4.x; v[4 * c + 1] = t4.y; v[4 * c + 2] = t4.z; v[4 * c + 3] = t4.w;
+            }
+            const float2 sc = reinterpret_cast<const float2*>(rp[0] + pw)[q];
+            int i0, i1;
+            iq4_pair_dot1(w, v, i0, i1);
+            acc[0] = fmaf((float)i0, d0 * sc.x, acc[0]);
+            acc[0] = fmaf((float)i1, d1 * sc.y, acc[0]);
+          }
+        } else {
+        for (int q = q0; q < npq; q += lpr) {
+          const int qbase = qv_base(q, lpr);
+          uint32_t w[9];
+          float d0, d1;
+          uint32_t a0[4], a1[4];
+          uint32_t t0[8], t1[8];
+          load_pair_smem(row + q * kPairB, w);
+          split_pair(w, d0, d1, a0, a1);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            iq4_lookup8(a0[i], t0[2 * i], t0[2 * i + 1]);
+            iq4_lookup8(a1[i], t1[2 * i], t1[2 * i + 1]);
+          }
+#pragma unroll
+          for (int j = 0; j < NPS; ++j) {
+            if (j < np) {
+              const uint4* r4 = reinterpret_cast<const uint4*>(rp[j]) + qbase;
+              uint32_t v[32];
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                const uint4 t4 = r4[c * lpr];
+                v[4 * c] = t4.x; v[4 * c + 1] = t4.y; v[4 * c + 2] = t4.z; v[4 * c + 3] = t4.w;
+              }
+              const float2 sc = reinterpret_cast<const float2*>(rp[j] + pw)[q];
+              const int i0 = iq4_dot_block(t0, v);
+              const int i1 = iq4_dot_block(t1, v + 16);
+              acc[j] = fmaf((float)i0, d0 * sc.x, acc[j]);
+              acc[j] = fmaf((float)i1, d1 * sc.y, acc[j]);
+            }
+          }
+        }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < NPS; ++j)
+        if (j < np) {
+#pragma unroll
+          for (int o = (LPR ? LPR : 8) >> 1; o > 0; o >>= 1)
+            if (LPR || o < lpr) acc[j] += __shfl_xor_sync(0xFFFFFFFFu, acc[j], o);
+        }
+      if (active && q0 == 0) {
+#pragma unroll
+        for (int j = 0; j < NPS; ++j)
+          if (j < np) store(g0 + j, rl, acc[j]);
+      }
+    }
+  }
+}
+
 
 // ---------------------------------------------------------------------------
 // Gate/up work: shared-expert rows are split evenly over the CTAs (known before

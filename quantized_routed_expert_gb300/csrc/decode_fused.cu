@@ -94,114 +94,18 @@ template <int NPS, int LPR>
 __device__ __forceinline__ void down_unit_t(const DecodeParams& p, const RouteTable& rt,
                                          const uint8_t* wrows, int slot, int r0, int nrows,
                                          const uint32_t* recs, float* part, int rows_max) {
-  const int lane = threadIdx.x & 31;
   const bool shared = slot < 0;
   const int K = shared ? p.Fs : p.F;
-  const int rbK = (K >> 5) * kBlockB;
-  const int lpr = LPR ? LPR : dlanes_per_row(K);
-  const int rpw = 32 / lpr;
-  const int npq = K >> 6;
   const int words = dqvec_words(K);
-  const int pw = dqvec_pair_words(K);
   const int P = p.T * p.k;
   const int ntok = shared ? p.T : rt.slot_off[slot + 1] - rt.slot_off[slot];
   const int lbase = shared ? 0 : rt.slot_off[slot];
   const uint32_t* rec_sh = recs + (size_t)P * dqvec_words(p.F);
-  const int q0 = lane & (lpr - 1);
-#pragma unroll 1
-  for (int g0 = 0; g0 < ntok; g0 += NPS) {
-    const int np = ntok - g0 < NPS ? ntok - g0 : NPS;
-    int pidx[NPS];
-    const uint32_t* rp[NPS];
-#pragma unroll
-    for (int j = 0; j < NPS; ++j) {
-      const int jj = g0 + (j < np ? j : 0);
-      if (shared) {
-        pidx[j] = P + jj;
-        rp[j] = rec_sh + (size_t)jj * words;
-      } else {
-        pidx[j] = rt.list[lbase + jj];
-        rp[j] = recs + (size_t)pidx[j] * words;
-      }
-    }
-#pragma unroll 1
-    for (int rb = 0; rb < nrows; rb += rpw) {
-      const int rl = rb + lane / lpr;
-      const bool active = rl < nrows;
-      float acc[NPS];
-#pragma unroll
-      for (int j = 0; j < NPS; ++j) acc[j] = 0.0f;
-      if (active) {
-        const uint8_t* row = wrows + (size_t)rl * rbK;
-        if (NPS == 1 || np == 1) {
-          // one token: the split-table dot products (same integers as below)
-          for (int q = q0; q < npq; q += lpr) {
-            const int qbase = qv_base(q, lpr);
-            uint32_t w[9];
-            load_pair_smem(row + q * kPairB, w);
-            float d0, d1;
-            pair_scales(w, d0, d1);
-            const uint4* r4 = reinterpret_cast<const uint4*>(rp[0]) + qbase;
-            uint32_t v[32];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const uint4 t4 = r4[c * lpr];
-              v[4 * c] = t4.x; v[4 * c + 1] = t4.y; v[4 * c + 2] = t4.z; v[4 * c + 3] = t4.w;
-            }
-            const float2 sc = reinterpret_cast<const float2*>(rp[0] + pw)[q];
-            int i0, i1;
-            iq4_pair_dot1(w, v, i0, i1);
-            acc[0] = fmaf((float)i0, d0 * sc.x, acc[0]);
-            acc[0] = fmaf((float)i1, d1 * sc.y, acc[0]);
-          }
-        } else {
-        for (int q = q0; q < npq; q += lpr) {
-          const int qbase = qv_base(q, lpr);
-          uint32_t w[9];
-          float d0, d1;
-          uint32_t a0[4], a1[4];
-          uint32_t t0[8], t1[8];
-          load_pair_smem(row + q * kPairB, w);
-          split_pair(w, d0, d1, a0, a1);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            iq4_lookup8(a0[i], t0[2 * i], t0[2 * i + 1]);
-            iq4_lookup8(a1[i], t1[2 * i], t1[2 * i + 1]);
-          }
-#pragma unroll
-          for (int j = 0; j < NPS; ++j) {
-            if (j < np) {
-              const uint4* r4 = reinterpret_cast<const uint4*>(rp[j]) + qbase;
-              uint32_t v[32];
-#pragma unroll
-              for (int c = 0; c < 8; ++c) {
-                const uint4 t4 = r4[c * lpr];
-                v[4 * c] = t4.x; v[4 * c + 1] = t4.y; v[4 * c + 2] = t4.z; v[4 * c + 3] = t4.w;
-              }
-              const float2 sc = reinterpret_cast<const float2*>(rp[j] + pw)[q];
-              const int i0 = iq4_dot_block(t0, v);
-              const int i1 = iq4_dot_block(t1, v + 16);
-              acc[j] = fmaf((float)i0, d0 * sc.x, acc[j]);
-              acc[j] = fmaf((float)i1, d1 * sc.y, acc[j]);
-            }
-          }
-        }
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < NPS; ++j)
-        if (j < np) {
-#pragma unroll
-          for (int o = (LPR ? LPR : 8) >> 1; o > 0; o >>= 1)
-            if (LPR || o < lpr) acc[j] += __shfl_xor_sync(0xFFFFFFFFu, acc[j], o);
-        }
-      if (active && q0 == 0) {
-#pragma unroll
-        for (int j = 0; j < NPS; ++j)
-          if (j < np) part[(size_t)pidx[j] * rows_max + r0 + rl] = acc[j];
-      }
-    }
-  }
+  auto pidx = [&](int jj) { return shared ? P + jj : rt.list[lbase + jj]; };
+  down_rows<NPS, LPR>(
+      wrows, K, nrows, ntok,
+      [&](int jj) { return shared ? rec_sh + (size_t)jj * words : recs + (size_t)pidx(jj) * words; },
+      [&](int jj, int rl, float v) { part[(size_t)pidx(jj) * rows_max + r0 + rl] = v; });
 }
 
 // What one warp needs to issue the bulk copies of its units: the warp's unit
@@ -341,7 +245,7 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
     mbar_arrive_expect_tx(rx_bar, bytes);
     bulk_g2s(smem + L.r_x, p.x, bytes, rx_bar);
   }
-  quant_x_lanes(p.x, p.T, H, xq, xq_words, threadIdx.x, kFT);
+  quant_x_lanes<1>(p.x, p.T, H, xq, xq_words, threadIdx.x, kFT);
 
   if (ROUTE) {
     // Scores of this CTA's experts: 16 chunks of H per expert, one warp per

@@ -107,6 +107,7 @@ moe::DecodeParams decode_params(const moe_shape* shape, const moe_expert_weights
   p.rec_s = reinterpret_cast<uint32_t*>(base + L.rec_s);
   p.sync = reinterpret_cast<uint32_t*>(base + L.sync);
   p.xrec = reinterpret_cast<uint32_t*>(base + L.xrec);
+  p.part = reinterpret_cast<float*>(base + L.part);
   p.status = status;
   return p;
 }
