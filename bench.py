@@ -52,6 +52,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=None,
                     help="run only the first N layers (small profiling cases)")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="keep only N routed experts per layer, same sizes otherwise (small "
+                         "profiling cases)")
     return ap.parse_args()
 
 
@@ -64,7 +67,7 @@ def peaks():
         return FALLBACK_HBM_GBS, 1900.0, "fallback"
 
 
-def workload(cfg: int, tokens, layers=None):
+def workload(cfg: int, tokens, layers=None, experts=None):
     import copy
     import synth
     s = synth.SHAPES[cfg]
@@ -72,6 +75,10 @@ def workload(cfg: int, tokens, layers=None):
         s = copy.copy(s)
         s.L = int(layers)
         s.name = f"{s.name} (first {s.L} layers)"
+    if experts is not None and s.k <= experts < s.E:
+        s = copy.copy(s)
+        s.name = f"{s.name} ({int(experts)} of its {s.E} experts)"
+        s.E = int(experts)
     T = s.T if tokens is None else int(tokens)
     if cfg != 4 and T > 16:
         T = 16
@@ -202,9 +209,9 @@ class OracleRun:
     so that generation stays outside the timed calls and repeated passes."""
 
     def __init__(self, cfg: int, T: int, layers=None, max_tokens: int = 16, threads=None,
-                 cache_bytes: float = 3e9):
+                 cache_bytes: float = 3e9, experts=None):
         import synth
-        self.s, _ = workload(cfg, None, layers)
+        self.s, _ = workload(cfg, None, layers, experts)
         self.seed = synth.seed_of(cfg)
         self.T_full = T
         self.T = min(T, max_tokens)              # a bounded sample of a prefill chunk
@@ -260,10 +267,10 @@ class OracleRun:
 
 
 def oracle_baseline(cfg: int, T: int, layers=None, budget_s: float = 10.0,
-                    wall_s: float = 120.0):
+                    wall_s: float = 120.0, experts=None):
     """cpu_baseline: passes over the input sets until about budget_s seconds of
     oracle time (or wall_s of wall time, weight generation included)."""
-    run = OracleRun(cfg, T, layers)
+    run = OracleRun(cfg, T, layers, experts=experts)
     t_wall = time.perf_counter()
     toks, spent, passes, calls = 0.0, 0.0, 0, 0
     while spent < budget_s and time.perf_counter() - t_wall < wall_s:
@@ -282,8 +289,8 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    s, T = workload(args.config, args.tokens, args.layers)
-    run = OracleRun(args.config, T, args.layers)
+    s, T = workload(args.config, args.tokens, args.layers, args.experts)
+    run = OracleRun(args.config, T, args.layers, experts=args.experts)
     per = []
     for i in range(args.warmup + args.steps):
         tps, dt, done = run.one_pass(i % N_SETS, budget_s=3.0)
@@ -327,7 +334,7 @@ def run_libmoe(args):
     import synth
     from synth.layers import Layer, x_sets
 
-    s, T = workload(args.config, args.tokens, args.layers)
+    s, T = workload(args.config, args.tokens, args.layers, args.experts)
     seed = synth.seed_of(args.config)
     prefill = args.config == 4
     shape = moe.make_shape(s.H, s.F, s.E, s.k, s.Fs, s.n_shared)
@@ -487,7 +494,7 @@ def run_libmoe(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tps, cores, desc = oracle_baseline(args.config, T, args.layers)
+        tps, cores, desc = oracle_baseline(args.config, T, args.layers, experts=args.experts)
         cpu = {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
 
     # the dominant kernel: for the fused decode every launch of the step is the

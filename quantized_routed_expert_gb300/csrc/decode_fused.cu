@@ -393,7 +393,11 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
       sl = r / p.F;
       f = r - sl * p.F;
     }
-    gateup_unit_t<MAXT, LPR>(p, rt, d, d + rbH, sl, f, xq, xq_words);
+    // one-token experts (most of them) take the code built for one token
+    if (MAXT == 1 || (sl < 0 ? p.T : rt.slot_off[sl + 1] - rt.slot_off[sl]) == 1)
+      gateup_unit_t<1, LPR>(p, rt, d, d + rbH, sl, f, xq, xq_words);
+    else
+      gateup_unit_t<MAXT, LPR>(p, rt, d, d + rbH, sl, f, xq, xq_words);
     __syncwarp();
     ++consumed;
     issue_upto(n_tot);
@@ -450,7 +454,11 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
     const bool sh = p.n_shared && su == 0;
     const int r0 = gi * RG;
     const int nr = nrows_cta - r0 < RG ? nrows_cta - r0 : RG;
-    down_unit_t<MAXT, LPR>(p, rt, d, sh ? -1 : su - p.n_shared, r0, nr, recs, part, rows_max);
+    const int dsl = sh ? -1 : su - p.n_shared;
+    if (MAXT == 1 || (sh ? p.T : rt.slot_off[dsl + 1] - rt.slot_off[dsl]) == 1)
+      down_unit_t<1, LPR>(p, rt, d, dsl, r0, nr, recs, part, rows_max);
+    else
+      down_unit_t<MAXT, LPR>(p, rt, d, dsl, r0, nr, recs, part, rows_max);
     __syncwarp();
     ++consumed;
     issue_upto(n_tot);
@@ -495,12 +503,24 @@ bool fused_decode_supported(const DecodeParams& p, int num_sms, size_t* smem, in
   if (p.H % 256 || p.F % 256 || (p.n_shared && p.Fs % 256)) return false;
   const int grid = num_sms;
   const int rmax = (p.H + grid - 1) / grid;
-  // down rows per unit: the rows one pass of a warp covers (finer units
-  // balance the down phase over the warps)
+  // down rows per unit: one pass of a warp (32 / lanes per row rows; finer
+  // units balance the down phase over the warps), unless the CTA then has
+  // more than two units per warp: those beyond a warp's two slots could not be
+  // fetched before the h barrier. Then whole passes are added while a unit
+  // fits in max(a gate/up unit, 4608 bytes), or all of the CTA's rows.
   int K = p.F;
   if (p.n_shared && p.Fs > K) K = p.Fs;
-  int r = 32 / lanes_per_row(K);
-  if (r > rmax) r = rmax;
+  const int rpw = 32 / lanes_per_row(K);
+  const int64_t rbK = row_bytes(K);
+  int64_t budget = 2 * row_bytes(p.H);
+  if (budget < 4608) budget = 4608;
+  const int slots = (p.T * p.k < p.E ? p.T * p.k : p.E) + p.n_shared;
+  auto units = [&](int rows) { return slots * ((rmax + rows - 1) / rows); };
+  int r = rpw < rmax ? rpw : rmax;
+  if (units(r) > 2 * kFW) {
+    while (r + rpw <= rmax && (r + rpw) * rbK <= budget) r += rpw;
+    if (rmax * rbK <= budget) r = rmax;
+  }
   const FusedSmem m = fused_smem(p.H, p.F, p.Fs, p.n_shared, p.T, p.k, rmax, r, p.route, p.E,
                                  grid);
   if (m.total > 227 * 1024) return false;

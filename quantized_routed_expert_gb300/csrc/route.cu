@@ -212,6 +212,11 @@ cudaError_t launch_route(const RouteParams& p, bool pdl, cudaStream_t stream) {
   const bool decode = p.T <= MOE_MAX_DECODE_TOKENS;
   if (decode)
     while (TT > 1 && (p.T + TT - 1) / TT * 16 < 128) TT >>= 1;
+  // Longer chunks: tiles small enough for several CTAs per SM (about three
+  // waves of CTAs on 152 SMs), so that the SIMT contraction has warps to
+  // hide its latencies; every tile reads the router rows from L2.
+  if (!decode)
+    while (TT > 1 && (p.T + TT - 1) / TT < 448) TT >>= 1;
   const int ntiles = (p.T + TT - 1) / TT;
   // Longer chunks: split the experts of a tile over a cluster only when there
   // are few tiles.
