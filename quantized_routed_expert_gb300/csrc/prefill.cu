@@ -63,31 +63,72 @@ struct BucketParams {
 };
 
 constexpr int kBucketThreads = 1024;
+constexpr int kBucketWarps = kBucketThreads / 32;
 
+// Counting sort of the (token, expert) pairs by expert, stable in the pair
+// index, in one CTA with three passes: every warp counts its contiguous share
+// of the pairs per expert (match_any groups one round of 32 pairs; no atomics
+// decide any order); the per-expert totals are scanned into bucket starts and
+// the per-warp counts into each warp's offsets within every bucket; every warp
+// then walks its share again and places each pair at its bucket start + its
+// warp's offset + the pairs of that expert before it in the warp. Dynamic
+// shared memory: kBucketWarps x E counters.
 __global__ void __launch_bounds__(kBucketThreads) pf_bucket_kernel(BucketParams p) {
-  __shared__ int cnt[MOE_MAX_EXPERTS + 2];
-  __shared__ int run[MOE_MAX_EXPERTS];
+  extern __shared__ int wc[];                   // [kBucketWarps][E]
+  __shared__ int start[MOE_MAX_EXPERTS + 2];
   __shared__ int wsum[32];
   __shared__ int invalid;
-  __shared__ uint8_t wcnt[32][MOE_MAX_EXPERTS];
-  pdl_wait();
-  pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int P = p.T * p.k, E = p.E;
-  for (int i = tid; i < E; i += kBucketThreads) { cnt[i] = 0; run[i] = 0; }
+#pragma unroll 1
+  for (int i = tid; i < kBucketWarps * E; i += kBucketThreads) wc[i] = 0;
   if (tid == 0) invalid = 0;
   __syncthreads();
+  pdl_wait();
+  pdl_trigger();
+  const int per = (P + kBucketWarps - 1) / kBucketWarps;
+  const int p0 = warp * per, p1 = p0 + per < P ? p0 + per : P;
+  int* mine = wc + warp * E;
+  // the ids of 8 rounds of 32 pairs, all loads in flight at once
+  constexpr int kR = 8;
+  auto load_ids = [&](int r0, int (&e)[kR]) {
+#pragma unroll
+    for (int u = 0; u < kR; ++u) {
+      const int pi = r0 + 32 * u + lane;
+      const int id = pi < p1 ? p.ids[pi] : -1;
+      e[u] = pi < p1 && id >= 0 && id < E ? id : (pi < p1 ? -2 : -1);   // -2: invalid pair
+    }
+  };
+  // pass 1: per-warp counts
   int bad = 0;
-  for (int i = tid; i < P; i += kBucketThreads) {
-    const int e = p.ids[i];
-    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
-    else ++bad;
+#pragma unroll 1
+  for (int r0 = p0; r0 < p1; r0 += 32 * kR) {
+    int e[kR];
+    load_ids(r0, e);
+#pragma unroll
+    for (int u = 0; u < kR; ++u) {
+      bad += e[u] == -2;
+      const uint32_t m = __match_any_sync(0xFFFFFFFFu, e[u]);
+      if (e[u] >= 0 && (m & ((1u << lane) - 1u)) == 0) mine[e[u]] += __popc(m);
+      __syncwarp();
+    }
   }
-  if (bad) atomicAdd(&invalid, bad);
+  bad = __reduce_add_sync(0xFFFFFFFFu, (unsigned)bad);
+  if (lane == 0 && bad) atomicAdd(&invalid, bad);
   __syncthreads();
-  // exclusive scan of cnt[0..E) (E <= 1024: one element per thread)
+  // pass 2: per-expert totals -> bucket starts; per-warp offsets within them
   {
-    const int c = tid < E ? cnt[tid] : 0;
+    int c = 0;
+    if (tid < E) {
+      int run = 0;
+#pragma unroll 1
+      for (int w = 0; w < kBucketWarps; ++w) {
+        const int v = wc[w * E + tid];
+        wc[w * E + tid] = run;
+        run += v;
+      }
+      c = run;
+    }
     int incl = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -98,95 +139,77 @@ __global__ void __launch_bounds__(kBucketThreads) pf_bucket_kernel(BucketParams 
     __syncthreads();
     if (warp == 0) {
       const int v = wsum[lane];
-      int s = v;
+      int s2 = v;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const int u = __shfl_up_sync(0xFFFFFFFFu, s, o);
-        if (lane >= o) s += u;
+        const int u = __shfl_up_sync(0xFFFFFFFFu, s2, o);
+        if (lane >= o) s2 += u;
       }
-      wsum[lane] = s - v;
+      wsum[lane] = s2 - v;
     }
     __syncthreads();
-    const int excl = incl - c + wsum[warp];
-    __syncthreads();
-    if (tid < E) cnt[tid] = excl;               // cnt now holds bucket starts
+    if (tid < E) start[tid] = incl - c + wsum[warp];
   }
-  __syncthreads();
   const int n_valid = P - invalid;
   if (tid == 0) {
-    cnt[E] = n_valid;
-    cnt[E + 1] = n_valid + (p.n_shared ? p.T : 0);
+    start[E] = n_valid;
+    start[E + 1] = n_valid + (p.n_shared ? p.T : 0);
   }
   __syncthreads();
-  for (int i = tid; i < E + 2; i += kBucketThreads) p.bucket_off[i] = cnt[i];
-  // stable ranks, 1024 pairs at a time
-  for (int c0 = 0; c0 < P; c0 += kBucketThreads) {
-    const int pi = c0 + tid;
-    int e = -1;
-    if (pi < P) {
-      const int id = p.ids[pi];
-      e = (id >= 0 && id < E) ? id : -1;
+  for (int i = tid; i < E + 2; i += kBucketThreads) p.bucket_off[i] = start[i];
+  // pass 3: places
+#pragma unroll 1
+  for (int r0 = p0; r0 < p1; r0 += 32 * kR) {
+    int e[kR];
+    load_ids(r0, e);
+#pragma unroll
+    for (int u = 0; u < kR; ++u) {
+      const int pi = r0 + 32 * u + lane;
+      const uint32_t m = __match_any_sync(0xFFFFFFFFu, e[u]);
+      const int before = __popc(m & ((1u << lane) - 1u));
+      if (e[u] >= 0) {
+        const int row = start[e[u]] + mine[e[u]] + before;
+        p.row_of[pi] = row;
+        p.row_tok[row] = pi / p.k;
+      } else if (e[u] == -2) {
+        p.row_of[pi] = -1;
+      }
+      __syncwarp();
+      if (e[u] >= 0 && before == 0) mine[e[u]] += __popc(m);
+      __syncwarp();
     }
-    for (int i = tid; i < 32 * E; i += kBucketThreads) wcnt[i / E][i % E] = 0;
-    __syncthreads();
-    const uint32_t m = __match_any_sync(0xFFFFFFFFu, e);
-    const int rw = __popc(m & ((1u << lane) - 1u));
-    if (e >= 0 && rw == 0) wcnt[warp][e] = (uint8_t)__popc(m);
-    __syncthreads();
-    if (e >= 0) {
-      int before = 0;
-      for (int w = 0; w < warp; ++w) before += wcnt[w][e];
-      const int row = cnt[e] + run[e] + before + rw;
-      const bool in_range = row >= cnt[e] && row < cnt[e + 1];
-      p.row_of[pi] = in_range ? row : -1;
-      if (in_range) p.row_tok[row] = pi / p.k;
-    } else if (pi < P) {
-      p.row_of[pi] = -1;
-    }
-    __syncthreads();
-    for (int i = tid; i < E; i += kBucketThreads) {
-      int s = 0;
-      for (int w = 0; w < 32; ++w) s += wcnt[w][i];
-      run[i] += s;
-    }
-    __syncthreads();
   }
   if (p.n_shared)
     for (int t = tid; t < p.T; t += kBucketThreads) p.row_tok[n_valid + t] = t;
-  // per token: the rows to combine, shared expert first, then experts ascending
+  __syncthreads();     // row_of complete (this CTA's global writes)
+  // per token: the rows to combine, shared expert first, then experts
+  // ascending (rows are grouped by expert: ascending rows); each routed entry
+  // goes to its rank among the token's rows
   const int kk = p.k + 1;
+#pragma unroll 1
   for (int t = tid; t < p.T; t += kBucketThreads) {
-    int n = 0;
     int32_t* cr = p.comb_row + (size_t)t * kk;
     float* cw = p.comb_w + (size_t)t * kk;
+    const int first = p.n_shared ? 1 : 0;
     if (p.n_shared) {
-      cr[n] = n_valid + t;
-      cw[n] = 1.0f;
-      ++n;
+      cr[0] = n_valid + t;
+      cw[0] = 1.0f;
     }
-    const int first = n;
-    for (int j = 0; j < p.k; ++j) {
-      const int pi = t * p.k + j;
-      const int id = p.ids[pi];
-      if (id < 0 || id >= E || p.row_of[pi] < 0) continue;
-      cr[n] = p.row_of[pi];
-      cw[n] = p.w[pi];
-      ++n;
+    int rows[MOE_MAX_TOP_K];
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_TOP_K; ++j) rows[j] = j < p.k ? p.row_of[t * p.k + j] : -1;
+    int nv = 0;
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_TOP_K; ++j) {
+      if (rows[j] < 0) continue;
+      int rank = 0;
+#pragma unroll
+      for (int i = 0; i < MOE_MAX_TOP_K; ++i) rank += rows[i] >= 0 && rows[i] < rows[j];
+      cr[first + rank] = rows[j];
+      cw[first + rank] = p.w[t * p.k + j];
+      ++nv;
     }
-    // sort the routed part by expert id (rows are grouped by expert, so by row)
-    for (int a = first + 1; a < n; ++a) {
-      const int r = cr[a];
-      const float wv = cw[a];
-      int b = a - 1;
-      while (b >= first && cr[b] > r) {
-        cr[b + 1] = cr[b];
-        cw[b + 1] = cw[b];
-        --b;
-      }
-      cr[b + 1] = r;
-      cw[b + 1] = wv;
-    }
-    for (int j = n; j < kk; ++j) {
+    for (int j = first + nv; j < kk; ++j) {
       cr[j] = -1;
       cw[j] = 0.0f;
     }
@@ -653,15 +676,27 @@ __global__ void pf_combine_kernel(const float* __restrict__ o, const int32_t* __
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     const int32_t* cr = comb_row + (size_t)t * kk;
     const float* cw = comb_w + (size_t)t * kk;
-    for (int j = 0; j < kk; ++j) {
-      const int r = cr[j];
-      if (r < 0) break;
-      const float wv = cw[j];
-      const float4 v = reinterpret_cast<const float4*>(o + (size_t)r * H)[c];
-      acc.x = fmaf(wv, v.x, acc.x);
-      acc.y = fmaf(wv, v.y, acc.y);
-      acc.z = fmaf(wv, v.z, acc.z);
-      acc.w = fmaf(wv, v.w, acc.w);
+    // rows in groups of four: the group's loads are all in flight before the
+    // first of its terms is added (terms in the fixed order)
+    for (int j0 = 0; j0 < kk; j0 += 4) {
+      int r[4];
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) r[u] = j0 + u < kk ? cr[j0 + u] : -1;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        v[u] = r[u] >= 0 ? reinterpret_cast<const float4*>(o + (size_t)r[u] * H)[c]
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (r[u] < 0) break;
+        const float wv = cw[j0 + u];
+        acc.x = fmaf(wv, v[u].x, acc.x);
+        acc.y = fmaf(wv, v[u].y, acc.y);
+        acc.z = fmaf(wv, v[u].z, acc.z);
+        acc.w = fmaf(wv, v[u].w, acc.w);
+      }
+      if (r[3] < 0) break;
     }
     reinterpret_cast<float4*>(y + (size_t)t * H)[c] = acc;
   }
@@ -778,7 +813,10 @@ cudaError_t launch_prefill(const moe_shape& s, const moe_expert_weights& w, cons
 
   BucketParams bp{ids, weights, T, k, E, s.n_shared, boff, row_of, row_tok, comb_row, comb_w,
                   status};
-  cudaError_t e = launch_ex(pf_bucket_kernel, dim3(1), dim3(kBucketThreads), 0, pdl, stream, bp);
+  const size_t bsm = (size_t)kBucketWarps * E * 4;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(pf_bucket_kernel), bsm);
+  if (e != cudaSuccess) return e;
+  e = launch_ex(pf_bucket_kernel, dim3(1), dim3(kBucketThreads), bsm, pdl, stream, bp);
   if (e != cudaSuccess) return e;
   e = launch_ex(pf_gather_kernel, dim3(num_sms * 4), dim3(256), 0, pdl, stream, x,
                 (const int32_t*)boff, (const int32_t*)row_tok, E, H, x16);
