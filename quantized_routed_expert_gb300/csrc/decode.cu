@@ -1,12 +1,14 @@
-// Decode kernels of libmoe (sm_103a): gate/up + SwiGLU, then down + combine.
+// Decode kernels of libmoe (sm_103a) for the batches and shapes the fused
+// kernel does not take: gate/up + SwiGLU, then down, then the combine.
 //
 // Each distinct expert's IQ4_NL rows are streamed from HBM once per call by
-// 1D bulk copies (TMA) into a shared-memory ring; each block is decoded once
-// (a byte_perm table lookup to int8) and its exact integer dot product with
-// every token routed to that expert is taken with dp2a against 16-bit block-
-// quantised activations. This is the paired-token decode of the Red Lite page
-// ("What we learned", section 4: decode each weight block once for both
-// tokens, and merge the tokens' experts into one dispatch), for 1..16 tokens.
+// 1D bulk copies (TMA) into per-warp shared-memory slots; each block is
+// decoded once (prmt table lookups to int8) and its exact integer dot product
+// with every token routed to that expert is taken with dp2a against 16-bit
+// block-quantised activations. This is the paired-token decode of the Red
+// Lite page ("What we learned", section 4: decode each weight block once for
+// both tokens, and merge the tokens' experts into one dispatch), for 1..16
+// tokens.
 #include <cstdio>
 
 #include "common.cuh"
