@@ -14,7 +14,6 @@
 
 #include "common.cuh"
 #include "prefill.cuh"
-#include "route.cuh"
 #include "tc.cuh"
 
 namespace moe {
@@ -705,152 +704,6 @@ __global__ void pf_combine_kernel(const float* __restrict__ o, const int32_t* __
 
 // ---------------------------------------------------------------------------
 // Host side.
-// ---------------------------------------------------------------------------
-// 5. Router for chunks: scores on tcgen05 (kind::f16 with bf16 operands), then
-// sigmoid, bias and top-k in the epilogue. A CTA takes 128 tokens (M) and all
-// E experts (N = E rounded up to 16, at most 256): D[t][e] = sum_h x[t][h]
-// Wr[e][h], fp32 in TMEM, bf16 products exact. Warp 0 copies x and Wr K-steps
-// by TMA into a four-deep ring, warp 1 issues the MMAs, then every thread
-// takes one token's row of D: key = sigmoid(s) + bias, kept in a sorted list
-// of 16 by a compare-and-swap pass per expert in ascending order (strict >,
-// so among equal keys the lower index stays first; a NaN key never enters),
-// and the first k are the choice; the weights are the chosen sigmoids over
-// their sum in choice order.
-constexpr int kRtStagesMax = 4;
-constexpr int kRtM = 128;
-__host__ __device__ inline int rt_stages(int N) {
-  const int stage_b = kRtM * kTK * 2 + N * kTK * 2;
-  int n = kRtStagesMax;
-  while (n > 2 && (size_t)n * stage_b > (size_t)200 * 1024) --n;
-  return n;
-}
-
-__global__ void __launch_bounds__(128, 1)
-route_mma_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mw,
-                 const RouteParams p, int N) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int stage_b = kRtM * kTK * 2 + N * kTK * 2;     // x tile, then Wr tile
-  const int NS = rt_stages(N);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * stage_b);
-  uint64_t* empty = full + kRtStagesMax;
-  uint64_t* acc = empty + kRtStagesMax;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc + 1);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint32_t ncols = 32;
-  while ((int)ncols < N) ncols <<= 1;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    mbar_init(acc, 1);
-    mbar_fence_init();
-  }
-  if (warp == 1) tmem_alloc(tmem_slot, ncols);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const int t0 = blockIdx.x * kRtM;
-  const int nks = p.H / kTK;
-  bool ok = true;
-  pdl_wait();
-  pdl_trigger();
-  if (warp == 0 && lane == 0) {
-    for (int ks = 0; ks < nks; ++ks) {
-      const int s = ks % NS;
-      if (!mbar_wait(&empty[s], ((ks / NS) & 1) ^ 1, nullptr)) break;
-      uint8_t* st = smem + (size_t)s * stage_b;
-      mbar_arrive_expect_tx(&full[s], (uint32_t)stage_b);
-      tma_load_2d(st, &mx, ks * kTK, t0, &full[s]);
-      tma_load_2d(st + kRtM * kTK * 2, &mw, ks * kTK, 0, &full[s]);
-    }
-  } else if (warp == 1 && lane == 0) {
-    // kind::f16 with bf16 A and B (bits 7 and 10), fp32 D
-    const uint32_t idesc = idesc_f16_f32(kRtM, N) | (1u << 7) | (1u << 10);
-    for (int ks = 0; ks < nks; ++ks) {
-      const int s = ks % NS;
-      if (!mbar_wait(&full[s], (ks / NS) & 1, nullptr)) { ok = false; break; }
-      tc_fence_after();
-      uint8_t* st = smem + (size_t)s * stage_b;
-      const uint64_t ad = sw128_kmajor_desc(smem_u32(st));
-      const uint64_t bd = sw128_kmajor_desc(smem_u32(st + kRtM * kTK * 2));
-#pragma unroll
-      for (int kk = 0; kk < kTK / 16; ++kk)
-        tc_mma_f16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
-      tc_commit(&empty[s]);
-    }
-    if (ok) tc_commit(acc);
-  }
-  __syncwarp();
-  // epilogue: thread = token t0 + 32 warp + lane
-  const bool done = mbar_wait(acc, 0, nullptr);
-  tc_fence_after();
-  const int t = t0 + warp * 32 + lane;
-  float bk[16], bp[16];
-  int bi[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    bk[j] = -INFINITY;
-    bp[j] = 0.0f;
-    bi[j] = -1;
-  }
-  float s0 = 0.0f;
-  for (int c = 0; c < N; c += 32) {
-    uint32_t v[32];
-    tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c, v);
-    tmem_ld_wait();
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int e = c + j;
-      if (e >= p.E) break;
-      const float sc = __uint_as_float(v[j]);
-      if (e == 0) s0 = sc;
-      float ck = 1.0f / (1.0f + expf(-sc));
-      float cp = ck;
-      ck += p.bias ? p.bias[e] : 0.0f;
-      int ci = e;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        if (ck > bk[i]) {
-          const float tk = bk[i], tp = bp[i];
-          const int ti = bi[i];
-          bk[i] = ck; bp[i] = cp; bi[i] = ci;
-          ck = tk; cp = tp; ci = ti;
-        }
-      }
-    }
-  }
-  if (done && t < p.T) {
-    float psum = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      if (j < p.k) {
-        if (bi[j] < 0) {                 // only with NaN keys: expert 0
-          bi[j] = 0;
-          bp[j] = 1.0f / (1.0f + expf(-s0));
-        }
-        psum += bp[j];
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      if (j < p.k) {
-        p.ids[(size_t)t * p.k + j] = bi[j];
-        p.w[(size_t)t * p.k + j] = bp[j] / psum;
-      }
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, ncols);
-  }
-}
-
 namespace {
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1026,23 +879,6 @@ cudaError_t launch_prefill(const moe_shape& s, const moe_expert_weights& w, cons
   return launch_ex(pf_combine_kernel, dim3((unsigned)grid), dim3(256), 0, pdl, stream,
                    (const float*)o, (const int32_t*)comb_row, (const float*)comb_w, T, k + 1, H,
                    y);
-}
-
-
-bool route_mma_supported(const RouteParams& p) {
-  return p.T >= 2 * kRtM && p.E <= 256 && p.H % kTK == 0;
-}
-
-cudaError_t launch_route_mma(const RouteParams& p, bool pdl, cudaStream_t stream) {
-  const int N = (p.E + 15) & ~15;
-  CUtensorMap mx, mw;
-  if (!make_tmap(&mx, p.x, p.T, p.H, kRtM) || !make_tmap(&mw, p.Wr, p.E, p.H, N))
-    return cudaErrorInvalidValue;
-  const size_t sm = 1024 + (size_t)rt_stages(N) * (kRtM * kTK * 2 + N * kTK * 2) + 256;
-  const cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(route_mma_kernel), sm);
-  if (e != cudaSuccess) return e;
-  return launch_ex(route_mma_kernel, dim3((unsigned)((p.T + kRtM - 1) / kRtM)), dim3(128), sm, pdl,
-                   stream, mx, mw, p, N);
 }
 
 }  // namespace moe

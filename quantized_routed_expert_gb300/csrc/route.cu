@@ -198,7 +198,6 @@ void wide_cluster_store(int tt, size_t sm, int ok) {
 }  // namespace
 
 cudaError_t launch_route(const RouteParams& p, bool pdl, cudaStream_t stream) {
-  if (route_mma_supported(p)) return launch_route_mma(p, pdl, stream);
   // token tile: x tile <= 128 KB; cluster: split experts for small T
   int TT = 16;
   while (TT > 1 && (size_t)TT * p.H * 2 > 128 * 1024) TT >>= 1;

@@ -16,9 +16,5 @@ struct RouteParams {
 };
 
 cudaError_t launch_route(const RouteParams& p, bool pdl, cudaStream_t stream);
-// Chunks of at least 256 tokens with at most 256 experts: scores on tensor
-// cores (prefill.cu).
-bool route_mma_supported(const RouteParams& p);
-cudaError_t launch_route_mma(const RouteParams& p, bool pdl, cudaStream_t stream);
 
 }  // namespace moe
