@@ -141,6 +141,72 @@ __device__ __forceinline__ void load_pair_smem(const uint8_t* p, uint32_t (&w)[9
 }
 
 // ---------------------------------------------------------------------------
+// Top-k of one token by one warp (router, sigmoid + bias selection). keys[e],
+// e < E, are sigmoid(score) + bias. The choice: the largest key first, ties to
+// the lower index; NaN and -inf keys are never chosen, and once no key is left
+// every further choice is expert 0.
+// A key becomes an order-preserving integer (larger key, larger integer; -0
+// and +0 equal; 0 for a key never chosen). Lane l holds keys l, l + 32, ... in
+// NPL registers. Each round takes the warp's largest integer by one reduction
+// and the lowest index holding it by a second, and the owning lane clears that
+// register: no shared memory, no divergent branch.
+__device__ __forceinline__ uint32_t ordered_key_bits(float k) {
+  const uint32_t u = __float_as_uint(k + 0.0f);       // -0 -> +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+template <int NPL>
+__device__ __forceinline__ int warp_topk_ids_t(const float* keys, int E, int k) {
+  const int lane = threadIdx.x & 31;
+  uint32_t v[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * i;
+    const float kv = e < E ? keys[e] : -INFINITY;
+    v[i] = kv > -INFINITY ? ordered_key_bits(kv) : 0u;    // NaN and -inf: 0
+  }
+  int id = 0;
+#pragma unroll 1
+  for (int j = 0; j < k; ++j) {
+    uint32_t m[NPL];
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) m[i] = v[i];
+#pragma unroll
+    for (int st = 1; st < NPL; st *= 2)
+#pragma unroll
+      for (int i = 0; i + st < NPL; i += 2 * st) m[i] = m[i] > m[i + st] ? m[i] : m[i + st];
+    const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, m[0]);
+    // with mx == 0 (no key left) every lane offers its first slot: expert 0
+    uint32_t hit = 0;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) hit |= (v[i] == mx ? 1u : 0u) << i;
+    const uint32_t cand = hit ? (uint32_t)(lane + 32 * (__ffs(hit) - 1)) : 0xFFFFFFFFu;
+    const uint32_t bi = __reduce_min_sync(0xFFFFFFFFu, cand);
+    if (lane == j) id = (int)bi;
+    const bool mine = (int)(bi & 31u) == lane;
+    const int ri = (int)(bi >> 5);
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) v[i] = (mine && i == ri) ? 0u : v[i];
+  }
+  return id;
+}
+// Lane j < k returns the j-th chosen expert id (E <= 1024).
+__device__ __forceinline__ int warp_topk_ids(const float* keys, int E, int k) {
+  const int n = (E + 31) >> 5;
+  if (n <= 2) return warp_topk_ids_t<2>(keys, E, k);
+  if (n <= 4) return warp_topk_ids_t<4>(keys, E, k);
+  if (n <= 8) return warp_topk_ids_t<8>(keys, E, k);
+  if (n <= 16) return warp_topk_ids_t<16>(keys, E, k);
+  return warp_topk_ids_t<32>(keys, E, k);
+}
+// Renormalised weights: lane j < k holds the j-th choice's sigmoid p and gets
+// p over the sum of the k chosen sigmoids, added in choice order.
+__device__ __forceinline__ float warp_renorm(float p, int k) {
+  float sum = 0.0f;
+  for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, p, j);
+  return p / sum;
+}
+
+// ---------------------------------------------------------------------------
 // 16-bit block quantisation of an activation vector (x or h).
 // For 32 values with largest biased fp32 exponent e: M_i = rint(v_i 2^(141-e))
 // clamped to 32767 (so |M_i| <= 2^15 - 1), scale = 2^(e-141). Blocks whose

@@ -177,73 +177,6 @@ __device__ __forceinline__ void build_route_table_warp(RouteTable& rt,
   __syncwarp();
 }
 
-// Top-k of one token by one warp. keys[E] (shared memory) are p + b and are
-// consumed: each chosen entry is set to -inf. probs[E] are the sigmoids.
-// The choice: the largest key, ties to the lower index; a NaN key is never
-// chosen (if no key is left, expert 0). Lane j < k returns the j-th id and
-// its renormalised weight; the sum of the chosen p runs in choice order.
-__device__ __forceinline__ uint32_t ordered_key_bits(float k) {
-  const uint32_t u = __float_as_uint(k + 0.0f);       // -0 -> +0
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-// Best and second-best key of one lane over e = lane, lane + 32, ... below
-// E32 (keys padded with -inf up to a multiple of 32). Strict >: among equal
-// keys the lower index ranks first; NaN never ranks. e = E means none.
-__device__ __forceinline__ void lane_best2(const float* keys, int E32, int E, float& b1, int& e1,
-                                           float& b2, int& e2) {
-  b1 = -INFINITY;
-  b2 = -INFINITY;
-  e1 = E;
-  e2 = E;
-#pragma unroll 4
-  for (int e = (int)(threadIdx.x & 31); e < E32; e += 32) {
-    const float kv = keys[e];
-    if (kv > b1) {
-      b2 = b1; e2 = e1; b1 = kv; e1 = e;
-    } else if (kv > b2) {
-      b2 = kv; e2 = e;
-    }
-  }
-}
-// Top-k of one token by one warp. keys (E values, padded with -inf to a
-// multiple of 32, in shared memory) are p + b and are consumed: each chosen
-// entry is set to -inf. probs[E] are the sigmoids. The choice: the largest
-// key, ties to the lower index; a NaN key is never chosen (if no key is left,
-// expert 0). Each round takes the warp's best by two reductions; the winning
-// lane moves up its cached second best and rescans only when it has none.
-// Lane j < k returns the j-th id and its renormalised weight; the sum of the
-// chosen p runs in choice order.
-__device__ __forceinline__ int2 warp_topk(float* keys, const float* probs, int E, int k) {
-  const int lane = threadIdx.x & 31;
-  const int E32 = (E + 31) & ~31;
-  float b1, b2;
-  int e1, e2;
-  lane_best2(keys, E32, E, b1, e1, b2, e2);
-  bool have2 = true;
-  float psum = 0.0f, psel = 0.0f;
-  int isel = 0;
-  for (int j = 0; j < k; ++j) {
-    const uint32_t ok = e1 < E ? ordered_key_bits(b1) : 0u;
-    const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, ok);
-    const uint32_t cand = (mx != 0u && ok == mx) ? (uint32_t)e1 : 0xFFFFFFFFu;
-    uint32_t bi = __reduce_min_sync(0xFFFFFFFFu, cand);
-    if (bi >= (uint32_t)E) bi = 0;
-    const float pr = probs[bi];
-    psum += pr;
-    if (lane == j) { psel = pr; isel = (int)bi; }
-    if ((int)(bi & 31u) == lane) {
-      keys[bi] = -INFINITY;
-      if (have2) {
-        b1 = b2; e1 = e2; have2 = false;
-      } else {
-        lane_best2(keys, E32, E, b1, e1, b2, e2);
-        have2 = true;
-      }
-    }
-  }
-  return make_int2(isel, __float_as_int(psel / psum));
-}
-
 __host__ __device__ __forceinline__ size_t align_up_dev(size_t v, size_t a) {
   return (v + a - 1) / a * a;
 }

@@ -343,9 +343,8 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
       const int t = warp;
       float* keys = keys_all + (size_t)t * E32;
       float* probs = keys + (size_t)p.T * E32;
-      const int2 r = warp_topk(keys, probs, p.E, p.k);
-      const int id = r.x;
-      const float wv = __int_as_float(r.y);
+      const int id = warp_topk_ids(keys, p.E, p.k);
+      const float wv = warp_renorm(lane < p.k ? probs[id] : 0.0f, p.k);
       if (lane < p.k) {
         ids_s[t * p.k + lane] = id;
         w_s[t * p.k + lane] = wv;

@@ -106,6 +106,84 @@ def test_route_token_tiles_ragged():
     check_route(ids.cpu().numpy(), w.cpu().numpy(), L, x_host)
 
 
+@pytest.mark.parametrize("cfg,T", [(4, 300), (1, 256), (0, 263)])
+def test_route_chunk_tensor_cores(cfg, T):
+    # chunks of 256+ tokens take the tensor-core router (16-token tiles; 300 =
+    # 18 full tiles and a ragged one). The chosen sets must match the oracle
+    # exactly. The MMA's fp32 accumulation (its own order and rounding over
+    # H/16 steps) moves a score by about 1e-5, and a weight by up to (1 - p)
+    # times that, relative: the weights are held to 1e-4 relative, and as a
+    # whole to the float bar of the layer outputs.
+    moe = lib()
+    from synth.layers import bf16_tensor
+    L = layer_of(cfg)
+    s = L.shape
+    x_host = gapped_rows(L, T)
+    ids, w = moe.route_topk(moe_shape(s), L.router_w, L.bias, bf16_tensor(x_host, DEV))
+    torch.cuda.synchronize()
+    ids, w = ids.cpu().numpy(), w.cpu().numpy()
+    ids_ref, w_ref, _, scores = oracle.route(L.router_w_host, L.bias_host, x_host, s.k)
+    assert np.array_equal(np.sort(ids, 1), np.sort(ids_ref, 1))
+    key = 1.0 / (1.0 + np.exp(-scores)) + L.bias_host.astype(np.float64)[None, :]
+    assert np.all(np.diff(np.take_along_axis(key, ids.astype(np.int64), 1), axis=1) <= 1e-5)
+    got = np.empty_like(w_ref)
+    for t in range(T):
+        ref = dict(zip(ids_ref[t].tolist(), w_ref[t].tolist()))
+        got[t] = [ref[int(e)] for e in ids[t]]
+    assert np.allclose(w, got, rtol=1e-4, atol=0)
+    check_close(w, got, f"chunk router weights cfg{cfg}")
+
+
+def _tied_router(E: int, H: int, seed: int):
+    """Zero router rows and biases on a 1/64 grid with many repeats: every
+    score is 0, every sigmoid exactly 1/2, every key exactly 1/2 + bias in
+    fp32 and fp64 alike, so the k-th choice falls inside a group of equal keys."""
+    rng = np.random.default_rng(seed)
+    bias = (rng.integers(0, 6, E) / 64.0).astype(np.float32)
+    wr_host = np.zeros((E, H), np.uint16)
+    return wr_host, bias
+
+
+@pytest.mark.parametrize("E,k,T", [(64, 4, 1), (64, 4, 40), (64, 4, 2048), (512, 10, 2),
+                                   (384, 6, 16), (100, 16, 3)])
+def test_route_exact_ties_go_to_lower_index(E, k, T):
+    # moe_route_topk on decode batches (cluster tiles) and chunks (token tiles)
+    moe = lib()
+    from synth.layers import bf16_tensor
+    H = 256
+    wr_host, bias = _tied_router(E, H, 11 * E + T)
+    x_host = synth.x_rows(5, 0, H, T)
+    ids_ref, w_ref, gap, _ = oracle.route(wr_host, bias, x_host, k)
+    assert gap[0] == 0.0                                         # the cut is inside a tie
+    shape = moe.make_shape(H, 256, E, k, 256, 1)
+    ids, w = moe.route_topk(shape, bf16_tensor(wr_host, DEV), torch.from_numpy(bias).to(DEV),
+                            bf16_tensor(x_host, DEV))
+    torch.cuda.synchronize()
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)           # order included
+    assert np.allclose(w.cpu().numpy(), w_ref, rtol=2e-6, atol=0)
+
+
+@pytest.mark.parametrize("E,k,T", [(64, 4, 1), (512, 10, 2), (384, 6, 4), (64, 4, 9)])
+def test_decode_routed_exact_ties(E, k, T):
+    # the fused kernel's in-kernel routing (1..4 tokens) and the router launched
+    # before the two-kernel path (5..16 tokens), on keys with exact ties
+    moe = lib()
+    from synth.layers import bf16_tensor
+    s = synth.Shape(f"ties E{E}", 256, 256, E, k, T, 1)
+    L = layer_of(s, 0, seed=13)
+    wr_host, bias = _tied_router(E, s.H, 3 * E + T)
+    x_host = synth.x_rows(9, 0, s.H, T)
+    ids_ref, w_ref, _, _ = oracle.route(wr_host, bias, x_host, k)
+    ws = moe.workspace(moe_shape(s), T, moe.DECODE, DEV)
+    ids, w, y = moe.iq4nl_decode_routed(moe_shape(s), bf16_tensor(wr_host, DEV),
+                                        torch.from_numpy(bias).to(DEV), weights_of(L),
+                                        bf16_tensor(x_host, DEV), ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)
+    assert np.allclose(w.cpu().numpy(), w_ref, rtol=2e-6, atol=0)
+    check_close(y.cpu().numpy(), oracle_layer(L, x_host, ids_ref, w_ref), f"ties E{E} T{T}")
+
+
 # ---------------------------------------------------------------- decode
 
 @pytest.mark.parametrize("cfg,T,layer", [(0, 4, 0), (0, 1, 0), (1, 1, 0), (1, 1, 37), (2, 2, 0),
