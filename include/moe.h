@@ -144,8 +144,9 @@ moe_status moe_iq4nl_decode(const moe_shape* shape, const moe_expert_weights* w,
 
 /* Route + decode in one call: what moe_route_topk followed by moe_iq4nl_decode
  * computes, for 1..16 tokens, with the same outputs (ids, weights, y) and the
- * same arithmetic. For 1..4 tokens and hidden, ffn, ffn_shared multiples of 256
- * it is a single persistent launch: the router runs inside the layer kernel
+ * same arithmetic. For 1..4 tokens, at most 512 experts and hidden, ffn,
+ * ffn_shared multiples of 256 it is a single persistent launch: the router runs
+ * inside the layer kernel
  * (each CTA scores a slice of the experts, a grid-wide barrier, then every CTA
  * takes the top-k itself), which removes one kernel boundary per layer from the
  * critical path. The ids written here are always valid.

@@ -189,6 +189,11 @@ __device__ __forceinline__ int warp_topk_ids_t(const float* keys, int E, int k) 
   }
   return id;
 }
+// Lane j < k returns the j-th chosen expert id. Two widths only (E <= 64 and
+// E <= 512), for kernels whose code size matters.
+__device__ __forceinline__ int warp_topk_ids_512(const float* keys, int E, int k) {
+  return E <= 64 ? warp_topk_ids_t<2>(keys, E, k) : warp_topk_ids_t<16>(keys, E, k);
+}
 // Lane j < k returns the j-th chosen expert id (E <= 1024).
 __device__ __forceinline__ int warp_topk_ids(const float* keys, int E, int k) {
   const int n = (E + 31) >> 5;

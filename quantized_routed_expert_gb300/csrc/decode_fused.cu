@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
       const int t = warp;
       float* keys = keys_all + (size_t)t * E32;
       float* probs = keys + (size_t)p.T * E32;
-      const int id = warp_topk_ids(keys, p.E, p.k);
+      const int id = warp_topk_ids_512(keys, p.E, p.k);
       const float wv = warp_renorm(lane < p.k ? probs[id] : 0.0f, p.k);
       if (lane < p.k) {
         ids_s[t * p.k + lane] = id;
@@ -500,6 +500,7 @@ bool fused_decode_supported(const DecodeParams& p, int num_sms, size_t* smem, in
                             int* rows_max) {
   if (p.T < 1 || p.T > 4) return false;
   if (p.H % 256 || p.F % 256 || (p.n_shared && p.Fs % 256)) return false;
+  if (p.route && p.E > 512) return false;         // in-kernel top-k holds 16 keys a lane
   const int grid = num_sms;
   const int rmax = (p.H + grid - 1) / grid;
   // down rows per unit: one pass of a warp (32 / lanes per row rows; finer

@@ -257,6 +257,7 @@ int32_t moe_launches_per_call(const moe_shape* shape, int32_t T, int32_t call) {
     size_t sm = 0;
     int rg = 0, rmax = 0;
     if (moe::fused_decode_supported(p, sms, &sm, &rg, &rmax)) return 1;
+    p.route = 0;                     // otherwise the router runs first, then the layer
     const int n = moe::decode_launches(p, sms);
     return call == 2 ? n + 1 : n;
   }

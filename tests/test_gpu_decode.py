@@ -163,10 +163,12 @@ def test_route_exact_ties_go_to_lower_index(E, k, T):
     assert np.allclose(w.cpu().numpy(), w_ref, rtol=2e-6, atol=0)
 
 
-@pytest.mark.parametrize("E,k,T", [(64, 4, 1), (512, 10, 2), (384, 6, 4), (64, 4, 9)])
+@pytest.mark.parametrize("E,k,T", [(64, 4, 1), (512, 10, 2), (384, 6, 4), (64, 4, 9),
+                                   (1024, 16, 2)])
 def test_decode_routed_exact_ties(E, k, T):
-    # the fused kernel's in-kernel routing (1..4 tokens) and the router launched
-    # before the two-kernel path (5..16 tokens), on keys with exact ties
+    # the fused kernel's in-kernel routing (1..4 tokens, up to 512 experts) and
+    # the router launched before the layer (5..16 tokens, or more experts), on
+    # keys with exact ties
     moe = lib()
     from synth.layers import bf16_tensor
     s = synth.Shape(f"ties E{E}", 256, 256, E, k, T, 1)
