@@ -134,6 +134,20 @@ def test_route_chunk_tensor_cores(cfg, T):
     check_close(w, got, f"chunk router weights cfg{cfg}")
 
 
+@pytest.mark.parametrize("T", [4096, 7200])
+def test_route_long_chunk_many_experts(T):
+    # more than 256 experts keep long chunks on the SIMT router, with 8-token
+    # (T = 4096) and 16-token (T = 7200) tiles
+    moe = lib()
+    from synth.layers import Layer, bf16_tensor
+    s = synth.Shape("long chunk E384", 256, 256, 384, 6, T, 1)
+    L = Layer(s, 21, 0, device=DEV)
+    x_host = gapped_rows(L, T)
+    ids, w = moe.route_topk(moe_shape(s), L.router_w, L.bias, bf16_tensor(x_host, DEV))
+    torch.cuda.synchronize()
+    check_route(ids.cpu().numpy(), w.cpu().numpy(), L, x_host)
+
+
 def _tied_router(E: int, H: int, seed: int):
     """Zero router rows and biases on a 1/64 grid with many repeats: every
     score is 0, every sigmoid exactly 1/2, every key exactly 1/2 + bias in
