@@ -47,6 +47,9 @@ def parse():
                     help="workload: 1 Xing decode (default), 2 Qwen3-Next paired decode, "
                          "3 DeepSeek-like wide decode, 4 Xing prefill chunk")
     ap.add_argument("--tokens", type=int, default=None, help="decode batch (config 3: 1/4/16)")
+    ap.add_argument("--same-tokens", action="store_true",
+                    help="every token of a batch is token 0 (decode: the forced-overlap "
+                         "variant, each expert of the union read once for all of them)")
     ap.add_argument("--impl", default="libmoe", choices=["libmoe", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -342,6 +345,8 @@ def run_libmoe(args):
     wts = [moe.ExpertWeights(L.gate, L.up, L.down, L.sh_gate, L.sh_up, L.sh_down)
            for L in layers]
     xs = x_sets(s, seed, N_SETS, T, device=dev)                   # [S, L, T, H] bf16
+    if args.same_tokens:
+        xs[:, :, 1:, :] = xs[:, :, :1, :]
     ids = torch.zeros((s.L, T, s.k), dtype=torch.int32, device=dev)
     w = torch.zeros((s.L, T, s.k), dtype=torch.float32, device=dev)
     y = torch.zeros((s.L, T, s.H), dtype=torch.float32, device=dev)
@@ -415,19 +420,24 @@ def run_libmoe(args):
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
+    # one event between consecutive steps: the first and last bracket the
+    # timed region, the others give the per-step spread
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     cur = torch.cuda.current_stream()
     torch.cuda.nvtx.range_push("timed")          # lets a profiler keep to this region
-    e0.record(cur)
+    evs[0].record(cur)
     for i in range(args.steps):
         graphs[i % N_SETS].replay()
-    e1.record(cur)
+        evs[i + 1].record(cur)
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev)
+    ms = max_over_ranks(evs[0].elapsed_time(evs[-1]) / args.steps, dist, dev)
+    per_step = np.array([evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)])
+    step_stats = {"median": float(np.median(per_step)),
+                  "p10": float(np.percentile(per_step, 10)),
+                  "p90": float(np.percentile(per_step, 90)), "of_rank": rank}
     st = int(status.item())
 
     # ---- per-call durations: one graph per kind of call over all layers (the
@@ -520,6 +530,7 @@ def run_libmoe(args):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "step_ms": step_stats,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": ("iq4_nl weights x int16 activations, exact int dot, f32 accumulate"
                       if not prefill else "fp16 x fp16 -> f32 (tcgen05 kind::f16)"),
@@ -529,7 +540,8 @@ def run_libmoe(args):
                        "kernels",
                        "l2": f"inputs larger than L2: {bytes_per_step / 1e9:.3f} GB of distinct "
                              "expert bytes per step vs 129 MB L2",
-                       "parallelism": f"replicas x{world}"},
+                       "parallelism": f"replicas x{world}",
+                       **({"same_tokens": True} if args.same_tokens else {})},
             "hbm_gbs": step_gbs, "hbm_frac_of_measured": step_gbs / hbm,
             "bytes_per_step": bytes_per_step,
             "roofline": ({"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
