@@ -112,16 +112,33 @@ def whole_job_rate(units_per_rank: int, world: int, seconds: float) -> float:
 PROFILE_DECODE_FUSED = "decode_fused_xing_decode.md"
 
 
-def sources_digest() -> str:
-    """Digest of the kernel sources; a profile's counters apply only to the
-    sources they were taken on."""
-    import glob
+# What the fused decode kernel is built and launched from: its translation
+# unit (the .cu and every header it includes), the host code that chooses and
+# launches it, and the compiler flags. Changing any of these voids its counters;
+# the prefill, router and utility kernels are other translation units.
+FUSED_DECODE_SOURCES = (
+    "quantized_routed_expert_gb300/csrc/decode_fused.cu",
+    "quantized_routed_expert_gb300/csrc/decode_common.cuh",
+    "quantized_routed_expert_gb300/csrc/decode.cuh",
+    "quantized_routed_expert_gb300/csrc/common.cuh",
+    "quantized_routed_expert_gb300/csrc/decode.cu",
+    "quantized_routed_expert_gb300/csrc/moe_api.cu",
+    "quantized_routed_expert_gb300/csrc/route.cuh",
+    "quantized_routed_expert_gb300/csrc/prefill.cuh",
+    "quantized_routed_expert_gb300/csrc/util_kernels.cuh",
+    "include/moe.h",
+    "quantized_routed_expert_gb300/build.py",
+)
+
+
+def sources_digest(files=FUSED_DECODE_SOURCES) -> str:
+    """Digest of the sources a kernel is built and launched from; a profile's
+    counters apply only to the sources they were taken on."""
     import hashlib
     h = hashlib.sha256()
-    src = os.path.join(ROOT, "quantized_routed_expert_gb300", "csrc")
-    for p in sorted(glob.glob(os.path.join(src, "*.cu")) + glob.glob(os.path.join(src, "*.cuh"))):
-        h.update(os.path.basename(p).encode())
-        with open(p, "rb") as f:
+    for rel in files:
+        h.update(rel.encode())
+        with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
