@@ -102,6 +102,24 @@ def test_prefill_full_chunk_sampled_tokens():
     assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
 
 
+def test_prefill_largest_chunk_sampled_tokens():
+    # the largest chunk the call takes (16384 tokens), Xing shape: the bucket
+    # sort, the tile schedule and the tensor-core router at their maximum
+    moe = lib()
+    s = synth.SHAPES[4]
+    L = layer_of(4, 2)
+    T = 16384
+    assert moe.workspace_bytes(moe_shape(s), T, moe.PREFILL) > 0
+    assert moe.workspace_bytes(moe_shape(s), T + 1, moe.PREFILL) == 0
+    x_host = synth.x_rows(L.seed, 2, s.H, T)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ids, w, y = run_prefill(L, x_host, status=status)
+    assert int(status.item()) == 0
+    rows = np.random.default_rng(1).choice(T, 10, replace=False)
+    rows = np.sort(np.concatenate([rows, [0, T - 1]]))
+    check_close(y[rows], oracle_rows(L, x_host, ids, w, rows), "prefill T=16384 sampled")
+
+
 @pytest.mark.parametrize("H,F,E,k,T,ns", [
     (128, 128, 1, 1, 3, 0),        # one expert, no shared expert: a dense SwiGLU
     (256, 384, 16, 4, 300, 1),     # three 128-row weight tiles, ragged token tiles
