@@ -190,24 +190,42 @@ moe_status moe_iq4nl_decode_static(const moe_shape* shape, const moe_expert_weig
                                    const float* weights, float* y, uint32_t* status,
                                    void* stream);
 
-/* Prefill: the whole layer for a chunk of 1..max_tokens tokens. Tokens are
+/* Prefill: the whole layer for a chunk of 1..max_tokens tokens (at most 16384).
+ * The Xolotl engine blog ("DeepSeek-V4.1-Flash at 27 Tokens/s on One RTX 4090",
+ * section "Prompts: fast, and exact") runs a long prompt in chunks, streaming
+ * each layer's experts once per chunk and running them as one batched multiply
+ * on the tensor cores; this call is that step for one layer. Tokens are
  * bucketed by expert with a counting sort (no atomics decide any order), each
  * expert's tokens run as one grouped tensor-core contraction (tcgen05,
  * fp16 operands, fp32 accumulation) on weights dequantised on the fly, and a
  * gather-combine forms y in the fixed order above. Dequantised weights are
  * round-to-nearest-even fp16 of d*T[q]; x and h also enter as fp16.
+ * Shape rule beyond moe_shape's: hidden, ffn and ffn_shared are multiples of
+ * 128 (the contraction's 128-row weight tiles); other shapes are refused with
+ * MOE_ERR_UNSUPPORTED and nothing is launched.
  * Arguments as for moe_iq4nl_decode; ws from moe_workspace_bytes(shape, >= T, 1). */
 moe_status moe_iq4nl_prefill_grouped(const moe_shape* shape, const moe_expert_weights* w,
                                      const uint16_t* x, int32_t T, const int32_t* ids,
                                      const float* weights, float* y, void* ws,
                                      size_t ws_bytes, uint32_t* status, void* stream);
 
-/* Dequantise n_blocks consecutive IQ4_NL blocks (the block layout above).
- *   blocks : device, 2-byte aligned
- *   out    : out_fp16 == 0: fp32 [n_blocks*32], the exact product d*T[q]
- *            out_fp16 == 1: fp16 [n_blocks*32], round-to-nearest-even of d*T[q]
- *            4-byte aligned */
-moe_status moe_iq4nl_dequantize(const void* blocks, int64_t n_blocks, int32_t out_fp16,
+/* Dequantise n_blocks consecutive IQ4_NL blocks (the block layout above),
+ * through one of the block decoders the layer kernels use, so that each can be
+ * checked bit for bit against the format's definition:
+ *   MOE_DEQUANT_FP32           fp32 [n_blocks*32], the exact product d*T[q], through
+ *                              the table lookup of the decode dot products for an
+ *                              expert with several tokens;
+ *   MOE_DEQUANT_FP16           fp16 [n_blocks*32], round-to-nearest-even of d*T[q],
+ *                              through the decoder of the prefill contraction;
+ *   MOE_DEQUANT_FP32_ONE_TOKEN fp32 [n_blocks*32], the exact product d*T[q], through
+ *                              the split-table dot product of the decode path for
+ *                              an expert with one token.
+ *   blocks : device, 2-byte aligned        out : device, 4-byte aligned
+ * Any other mode is refused with MOE_ERR_INVALID_ARG. */
+#define MOE_DEQUANT_FP32 0
+#define MOE_DEQUANT_FP16 1
+#define MOE_DEQUANT_FP32_ONE_TOKEN 2
+moe_status moe_iq4nl_dequantize(const void* blocks, int64_t n_blocks, int32_t mode,
                                 void* out, void* stream);
 
 /* The invalid-route rule on its own (wpnews vLLM article, route sanitising):
@@ -227,6 +245,22 @@ int32_t moe_launches_per_call(const moe_shape* shape, int32_t T, int32_t call);
 /* 1 (default) launches kernels with programmatic dependent launch; 0 does not.
  * Host-side, process-wide. Returns the previous setting. */
 int32_t moe_set_pdl(int32_t enable);
+
+/* Limit, in nanoseconds, of a CTA's waits on the other CTAs of its grid: the
+ * grid-wide barriers of the single-launch decode kernels (a CTA waits there
+ * until every CTA has published its router scores, or its rows of h). Those
+ * kernels launch one CTA per SM and check before launching that a CTA fits on
+ * an SM (an occupancy query; otherwise the multi-kernel path runs), but a
+ * device shared with other work (MPS, partitioned SMs) can still keep some
+ * CTAs from starting; the limit bounds that wait instead of hanging the GPU.
+ * A wait that reaches it gives up and sets MOE_STATUS_TIMEOUT in *status; the
+ * call's outputs are then undefined, the kernel still waits for its own copies
+ * in flight (on the fixed 2 s limit of waits on copies, not on this one) and
+ * leaves the workspace ready for the next call. 0 makes a CTA give up the
+ * first time it finds a barrier incomplete (a way for tests to take the
+ * timeout path without a fault). Host-side, process-wide, read at each call;
+ * the default is 2e9 (2 s). Returns the previous limit. */
+uint64_t moe_set_barrier_wait_ns(uint64_t ns);
 
 /* A static description of a status code (host). */
 const char* moe_status_string(int32_t status);

@@ -39,6 +39,7 @@ STATUS_TIMEOUT = 0x80000000
 MAX_DECODE_TOKENS = 16
 STATIC_SCRATCH_BYTES = 8 << 20
 DECODE, PREFILL = 0, 1
+DEQUANT_FP32, DEQUANT_FP16, DEQUANT_FP32_ONE_TOKEN = 0, 1, 2
 
 
 class Shape(ctypes.Structure):
@@ -77,13 +78,16 @@ _lib.moe_launches_per_call.argtypes = [ctypes.POINTER(Shape), ctypes.c_int32, ct
 _lib.moe_launches_per_call.restype = ctypes.c_int32
 _lib.moe_set_pdl.argtypes = [ctypes.c_int32]
 _lib.moe_set_pdl.restype = ctypes.c_int32
+_lib.moe_set_barrier_wait_ns.argtypes = [ctypes.c_uint64]
+_lib.moe_set_barrier_wait_ns.restype = ctypes.c_uint64
 _lib.moe_status_string.argtypes = [ctypes.c_int32]
 _lib.moe_status_string.restype = ctypes.c_char_p
 _lib.moe_version.restype = ctypes.c_char_p
 
 EXPORTS = ("moe_route_topk", "moe_workspace_bytes", "moe_iq4nl_decode", "moe_iq4nl_decode_routed",
            "moe_iq4nl_decode_static", "moe_iq4nl_prefill_grouped", "moe_iq4nl_dequantize", "moe_sanitize_routes",
-           "moe_launches_per_call", "moe_set_pdl", "moe_status_string", "moe_version")
+           "moe_launches_per_call", "moe_set_pdl", "moe_set_barrier_wait_ns", "moe_status_string",
+           "moe_version")
 
 
 class MoeError(RuntimeError):
@@ -120,6 +124,12 @@ def set_pdl(enable: bool) -> bool:
     return bool(_lib.moe_set_pdl(1 if enable else 0))
 
 
+def set_barrier_wait_ns(ns: int) -> int:
+    """Limit of a CTA's waits on the other CTAs of its grid (grid barriers of
+    the single-launch decode kernels), in ns; returns the previous limit."""
+    return int(_lib.moe_set_barrier_wait_ns(int(ns)))
+
+
 def make_shape(hidden, ffn, n_experts, top_k, ffn_shared=None, n_shared=1) -> Shape:
     return Shape(int(hidden), int(ffn), int(ffn if ffn_shared is None else ffn_shared),
                  int(n_experts), int(top_k), int(n_shared))
@@ -141,24 +151,93 @@ def _stream(stream):
     return stream.cuda_stream
 
 
-def _dev(t, dtype, name):
+def _meta(t, dtype, name, shape=None):
+    """Type, dtype and shape (when given) of one tensor argument."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch tensor")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be on a CUDA device")
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def _on_cuda(t, name):
+    """A contiguous CUDA tensor."""
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     return t
 
 
+def _dev(t, dtype, name, shape=None):
+    """Check one tensor argument: type, dtype, shape (when given), then that it
+    is a contiguous CUDA tensor."""
+    return _on_cuda(_meta(t, dtype, name, shape), name)
+
+
+def _same_device(*tensors):
+    """All tensor arguments on one CUDA device, and that device current (the
+    library launches on the current device)."""
+    devs = {t.device for t in tensors if isinstance(t, torch.Tensor)}
+    if len(devs) > 1:
+        raise ValueError(f"arguments are on different devices: {sorted(map(str, devs))}")
+    if devs:
+        d = devs.pop()
+        if d.type == "cuda" and d.index is not None and d.index != torch.cuda.current_device():
+            raise ValueError(f"arguments are on {d}, but the current device is "
+                             f"cuda:{torch.cuda.current_device()}")
+
+
+def _status_arg(status):
+    if status is None:
+        return
+    if not isinstance(status, torch.Tensor) or status.dtype not in (torch.int32, torch.uint32) \
+            or status.numel() < 1:
+        raise TypeError("status must be an int32 or uint32 tensor with at least one element")
+    if not status.is_cuda:
+        raise ValueError("status must be on a CUDA device")
+
+
+def _block_bytes(rows: int, K: int) -> int:
+    return rows * (K // 32) * 18
+
+
 class ExpertWeights:
-    """Device tensors (uint8, IQ4_NL blocks) of one layer; keeps them alive."""
+    """Device tensors (uint8, IQ4_NL blocks) of one layer; keeps them alive.
+    Entries may also be raw device addresses (int), which are not checked."""
 
     def __init__(self, gate, up, down, sh_gate=None, sh_up=None, sh_down=None):
         self.tensors = (gate, up, down, sh_gate, sh_up, sh_down)
         self.c = _Weights(*[_ptr(t) for t in self.tensors])
+
+    def check(self, shape: "Shape"):
+        """Each weight tensor holds at least the bytes the shape reads."""
+        H, F, E = shape.hidden, shape.ffn, shape.n_experts
+        need = [E * _block_bytes(F, H), E * _block_bytes(F, H), E * _block_bytes(H, F)]
+        if shape.n_shared:
+            Fs = shape.ffn_shared
+            need += [_block_bytes(Fs, H), _block_bytes(Fs, H), _block_bytes(H, Fs)]
+        names = ("gate", "up", "down", "sh_gate", "sh_up", "sh_down")
+        for name, t, n in zip(names, self.tensors, need):
+            if t is None:
+                raise ValueError(f"expert weights: {name} is missing")
+            if isinstance(t, torch.Tensor):
+                nb = t.numel() * t.element_size()
+                if nb < n:
+                    raise ValueError(f"expert weights: {name} holds {nb} bytes, the shape "
+                                     f"reads {n}")
+        return [t for t in self.tensors if isinstance(t, torch.Tensor)]
+
+    def check_device(self):
+        names = ("gate", "up", "down", "sh_gate", "sh_up", "sh_down")
+        for name, t in zip(names, self.tensors):
+            if isinstance(t, torch.Tensor):
+                if not t.is_cuda:
+                    raise ValueError(f"expert weights: {name} must be on a CUDA device")
+                if not t.is_contiguous():
+                    raise ValueError(f"expert weights: {name} must be contiguous")
 
 
 def workspace_bytes(shape: Shape, max_tokens: int, mode: int = DECODE) -> int:
@@ -176,29 +255,74 @@ def workspace(shape: Shape, max_tokens: int, mode: int = DECODE, device="cuda"):
 def route_topk(shape: Shape, router_w, router_bias, x, ids=None, weights=None, stream=None):
     """router_w: bf16 [E,H]; router_bias: fp32 [E] or None; x: bf16 [T,H].
     Returns (ids int32 [T,k], weights fp32 [T,k])."""
-    _dev(router_w, torch.bfloat16, "router_w")
-    _dev(x, torch.bfloat16, "x")
-    if router_bias is not None:
-        _dev(router_bias, torch.float32, "router_bias")
+    ok = _shape_ok(shape)
+    E, H, k = shape.n_experts, shape.hidden, shape.top_k
+    if not isinstance(x, torch.Tensor) or x.dim() != 2:
+        raise ValueError("x must be a [T, hidden] tensor")
     T = x.shape[0]
+    _meta(router_w, torch.bfloat16, "router_w", (E, H) if ok else None)
+    _meta(x, torch.bfloat16, "x", (T, H) if ok else None)
+    if router_bias is not None:
+        _meta(router_bias, torch.float32, "router_bias", (E,) if ok else None)
+    for t, name, dt in ((ids, "ids", torch.int32), (weights, "weights", torch.float32)):
+        if t is not None:
+            _meta(t, dt, name, (T, k) if ok else None)
+    _on_cuda(router_w, "router_w")
+    _on_cuda(x, "x")
+    if router_bias is not None:
+        _on_cuda(router_bias, "router_bias")
     if ids is None:
-        ids = torch.empty((T, shape.top_k), dtype=torch.int32, device=x.device)
+        ids = torch.empty((T, k), dtype=torch.int32, device=x.device)
     if weights is None:
-        weights = torch.empty((T, shape.top_k), dtype=torch.float32, device=x.device)
+        weights = torch.empty((T, k), dtype=torch.float32, device=x.device)
+    _on_cuda(ids, "ids")
+    _on_cuda(weights, "weights")
+    _same_device(router_w, router_bias, x, ids, weights)
     _check(_lib.moe_route_topk(ctypes.byref(shape), _ptr(router_w), _ptr(router_bias), _ptr(x),
                                int(T), _ptr(ids), _ptr(weights), _stream(stream)),
            "moe_route_topk")
     return ids, weights
 
 
-def _layer(fn, name, shape, w: ExpertWeights, x, ids, weights, y, ws, status, stream):
-    _dev(x, torch.bfloat16, "x")
-    _dev(ids, torch.int32, "ids")
-    _dev(weights, torch.float32, "weights")
+def _shape_ok(shape: Shape) -> bool:
+    """The library's own shape rule (an invalid shape is left to the C call,
+    which refuses it with its status code)."""
+    return int(_lib.moe_workspace_bytes(ctypes.byref(shape), 1, DECODE)) > 0
+
+
+def _layer_args(shape, w: ExpertWeights, x, ids, weights, y, status):
+    """Shapes, dtypes and devices of a layer call's tensors; returns (T, y)."""
+    if not isinstance(x, torch.Tensor) or x.dim() != 2:
+        raise ValueError("x must be a [T, hidden] tensor")
     T = x.shape[0]
+    ok = _shape_ok(shape)
+    H, k = shape.hidden, shape.top_k
+    wts = w.check(shape) if ok else []
+    _meta(x, torch.bfloat16, "x", (T, H) if ok else None)
+    _meta(ids, torch.int32, "ids", (T, k) if ok else None)
+    _meta(weights, torch.float32, "weights", (T, k) if ok else None)
+    if y is not None:
+        _meta(y, torch.float32, "y", (T, H) if ok else None)
+    if status is not None and (not isinstance(status, torch.Tensor) or status.dtype not in (
+            torch.int32, torch.uint32) or status.numel() < 1):
+        raise TypeError("status must be an int32 or uint32 tensor with at least one element")
+    for t, name in ((x, "x"), (ids, "ids"), (weights, "weights")):
+        _on_cuda(t, name)
     if y is None:
-        y = torch.empty((T, shape.hidden), dtype=torch.float32, device=x.device)
-    _dev(y, torch.float32, "y")
+        y = torch.empty((T, H), dtype=torch.float32, device=x.device)
+    _on_cuda(y, "y")
+    _status_arg(status)
+    if ok:
+        w.check_device()
+    _same_device(x, ids, weights, y, status, *wts)
+    return T, y
+
+
+def _layer(fn, name, shape, w: ExpertWeights, x, ids, weights, y, ws, status, stream):
+    T, y = _layer_args(shape, w, x, ids, weights, y, status)
+    if ws is not None:
+        _dev(ws, torch.uint8, "ws")
+        _same_device(x, ws)
     _check(fn(ctypes.byref(shape), ctypes.byref(w.c), _ptr(x), int(T), _ptr(ids),
               _ptr(weights), _ptr(y), _ptr(ws), int(ws.numel() if ws is not None else 0),
               _ptr(status), _stream(stream)), name)
@@ -220,13 +344,7 @@ def iq4nl_decode_static(shape: Shape, w: ExpertWeights, x, ids, weights, y=None,
     may overlap on the GPU race, so keep them on one stream. The first call on
     a device sets the scratch up and should come before any stream capture.
     Pass ``y`` to keep this wrapper from allocating the output itself."""
-    _dev(x, torch.bfloat16, "x")
-    _dev(ids, torch.int32, "ids")
-    _dev(weights, torch.float32, "weights")
-    T = x.shape[0]
-    if y is None:
-        y = torch.empty((T, shape.hidden), dtype=torch.float32, device=x.device)
-    _dev(y, torch.float32, "y")
+    T, y = _layer_args(shape, w, x, ids, weights, y, status)
     _check(_lib.moe_iq4nl_decode_static(ctypes.byref(shape), ctypes.byref(w.c), _ptr(x), int(T),
                                         _ptr(ids), _ptr(weights), _ptr(y), _ptr(status),
                                         _stream(stream)), "moe_iq4nl_decode_static")
@@ -236,20 +354,29 @@ def iq4nl_decode_static(shape: Shape, w: ExpertWeights, x, ids, weights, y=None,
 def iq4nl_decode_routed(shape: Shape, router_w, router_bias, w: ExpertWeights, x, ws, ids=None,
                         weights=None, y=None, status=None, stream=None):
     """Route and decode 1..16 tokens in one call. Returns (ids, weights, y)."""
-    _dev(router_w, torch.bfloat16, "router_w")
+    ok = _shape_ok(shape)
+    E, H, k = shape.n_experts, shape.hidden, shape.top_k
+    _meta(router_w, torch.bfloat16, "router_w", (E, H) if ok else None)
     if router_bias is not None:
-        _dev(router_bias, torch.float32, "router_bias")
-    _dev(x, torch.bfloat16, "x")
+        _meta(router_bias, torch.float32, "router_bias", (E,) if ok else None)
+    if not isinstance(x, torch.Tensor) or x.dim() != 2:
+        raise ValueError("x must be a [T, hidden] tensor")
     T = x.shape[0]
+    for t, name, dt in ((ids, "ids", torch.int32), (weights, "weights", torch.float32)):
+        if t is not None:
+            _meta(t, dt, name, (T, k) if ok else None)
+    _on_cuda(router_w, "router_w")
+    if router_bias is not None:
+        _on_cuda(router_bias, "router_bias")
+    _on_cuda(x, "x")
     if ids is None:
-        ids = torch.empty((T, shape.top_k), dtype=torch.int32, device=x.device)
+        ids = torch.empty((T, k), dtype=torch.int32, device=x.device)
     if weights is None:
-        weights = torch.empty((T, shape.top_k), dtype=torch.float32, device=x.device)
-    if y is None:
-        y = torch.empty((T, shape.hidden), dtype=torch.float32, device=x.device)
-    _dev(ids, torch.int32, "ids")
-    _dev(weights, torch.float32, "weights")
-    _dev(y, torch.float32, "y")
+        weights = torch.empty((T, k), dtype=torch.float32, device=x.device)
+    T, y = _layer_args(shape, w, x, ids, weights, y, status)
+    if ws is not None:
+        _dev(ws, torch.uint8, "ws")
+    _same_device(router_w, router_bias, x, ws)
     _check(_lib.moe_iq4nl_decode_routed(ctypes.byref(shape), _ptr(router_w), _ptr(router_bias),
                                         ctypes.byref(w.c), _ptr(x), int(T), _ptr(ids),
                                         _ptr(weights), _ptr(y), _ptr(ws),
@@ -265,16 +392,25 @@ def iq4nl_prefill_grouped(shape: Shape, w: ExpertWeights, x, ids, weights, ws, y
                   weights, y, ws, status, stream)
 
 
-def iq4nl_dequantize(blocks, fp16: bool = False, out=None, stream=None):
-    """blocks: uint8 device tensor of 18-byte blocks -> fp32 (exact) or fp16 [n*32]."""
+def iq4nl_dequantize(blocks, fp16: bool = False, out=None, stream=None, mode=None):
+    """blocks: uint8 device tensor of 18-byte blocks -> fp32 (exact) or fp16 [n*32].
+    ``mode`` picks the decoder: DEQUANT_FP32 (the decode lookup for experts
+    with several tokens; the default), DEQUANT_FP16 (the prefill decoder;
+    also ``fp16=True``) or DEQUANT_FP32_ONE_TOKEN (the decode split table)."""
+    if mode is None:
+        mode = DEQUANT_FP16 if fp16 else DEQUANT_FP32
+    if mode not in (DEQUANT_FP32, DEQUANT_FP16, DEQUANT_FP32_ONE_TOKEN):
+        raise ValueError(f"unknown dequantisation mode {mode}")
+    if not isinstance(blocks, torch.Tensor) or blocks.numel() % 18:
+        raise ValueError("blocks must be a tensor of a whole number of 18-byte blocks")
     _dev(blocks, torch.uint8, "blocks")
-    if blocks.numel() % 18:
-        raise ValueError("blocks must hold a whole number of 18-byte blocks")
     n = blocks.numel() // 18
+    dt = torch.float16 if mode == DEQUANT_FP16 else torch.float32
     if out is None:
-        out = torch.empty(n * 32, dtype=torch.float16 if fp16 else torch.float32,
-                          device=blocks.device)
-    _check(_lib.moe_iq4nl_dequantize(_ptr(blocks), n, 1 if fp16 else 0, _ptr(out),
+        out = torch.empty(n * 32, dtype=dt, device=blocks.device)
+    _dev(out, dt, "out", (n * 32,))
+    _same_device(blocks, out)
+    _check(_lib.moe_iq4nl_dequantize(_ptr(blocks), n, int(mode), _ptr(out),
                                      _stream(stream)), "moe_iq4nl_dequantize")
     return out
 
@@ -282,9 +418,13 @@ def iq4nl_dequantize(blocks, fp16: bool = False, out=None, stream=None):
 def sanitize_routes(ids, weights, n_experts: int, ids_out=None, weights_out=None, status=None,
                     stream=None):
     _dev(ids, torch.int32, "ids")
-    _dev(weights, torch.float32, "weights")
+    _dev(weights, torch.float32, "weights", tuple(ids.shape))
     ids_out = torch.empty_like(ids) if ids_out is None else ids_out
     weights_out = torch.empty_like(weights) if weights_out is None else weights_out
+    _dev(ids_out, torch.int32, "ids_out", tuple(ids.shape))
+    _dev(weights_out, torch.float32, "weights_out", tuple(ids.shape))
+    _status_arg(status)
+    _same_device(ids, weights, ids_out, weights_out, status)
     _check(_lib.moe_sanitize_routes(_ptr(ids), _ptr(weights), ids.numel(), int(n_experts),
                                     _ptr(ids_out), _ptr(weights_out), _ptr(status),
                                     _stream(stream)), "moe_sanitize_routes")

@@ -91,6 +91,7 @@ struct DecodeParams {
   int gu_nblk;       // gate/up kernel: 32-row blocks a CTA may get
   int dn_rows_max;   // max output rows per down CTA
   int fz_rg;         // fused kernel: output rows per down unit
+  uint64_t wait_ns;  // limit of a CTA's waits on other CTAs (grid barriers)
 };
 
 cudaError_t launch_decode(const DecodeParams& p, int num_sms, bool pdl, cudaStream_t stream);
@@ -98,6 +99,7 @@ cudaError_t launch_decode(const DecodeParams& p, int num_sms, bool pdl, cudaStre
 int decode_launches(const DecodeParams& p, int num_sms);
 bool fused_decode_supported(const DecodeParams& p, int num_sms, size_t* smem, int* rg,
                             int* rows_max);
+bool fused_resident(const DecodeParams& p, size_t smem);
 cudaError_t launch_decode_routed(const DecodeParams& p, int num_sms, bool pdl,
                                  cudaStream_t stream);
 cudaError_t launch_decode_fused(const DecodeParams& p, int num_sms, size_t smem, bool pdl,

@@ -17,6 +17,8 @@
 #include "decode.cuh"
 #include "decode_common.cuh"
 
+#include <mutex>
+
 namespace moe {
 
 constexpr int kFW = 16;            // warps per CTA
@@ -315,11 +317,11 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
     if (threadIdx.x == 0) {
       const uint64_t t0 = global_timer_ns();
       while (ld_acquire_u32(&p.sync[2]) < gridDim.x) {
-        __nanosleep(32);
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
+        if (global_timer_ns() - t0 >= p.wait_ns) {
           if (p.status) atomicOr(p.status, MOE_STATUS_TIMEOUT);
           break;
         }
+        __nanosleep(32);
       }
       __threadfence();
     }
@@ -409,11 +411,11 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
     atomicAdd(&p.sync[0], 1u);
     const uint64_t t0 = global_timer_ns();
     while (ld_acquire_u32(&p.sync[0]) < gridDim.x) {
-      __nanosleep(64);
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 >= p.wait_ns) {
         if (p.status) atomicOr(p.status, MOE_STATUS_TIMEOUT);
         break;
       }
+      __nanosleep(64);
     }
     __threadfence();
   }
@@ -496,6 +498,52 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
 }
 
 // ---------------------------------------------------------------------------
+namespace {
+// The instantiation a launch with these parameters uses.
+const void* fused_kernel_for(const DecodeParams& p) {
+  const bool w8 = lanes_per_row(p.H) == 8 && lanes_per_row(p.F) == 8 &&
+                  (!p.n_shared || lanes_per_row(p.Fs) == 8);
+#define MOE_FK(T_, R_, L_) reinterpret_cast<const void*>(decode_fused_kernel<T_, R_, L_>)
+  const int t = p.T == 1 ? 1 : (p.T == 2 ? 2 : 4);
+  if (p.route) {
+    if (w8) return t == 1 ? MOE_FK(1, true, 8) : t == 2 ? MOE_FK(2, true, 8) : MOE_FK(4, true, 8);
+    return t == 1 ? MOE_FK(1, true, 0) : t == 2 ? MOE_FK(2, true, 0) : MOE_FK(4, true, 0);
+  }
+  if (w8) return t == 1 ? MOE_FK(1, false, 8) : t == 2 ? MOE_FK(2, false, 8) : MOE_FK(4, false, 8);
+  return t == 1 ? MOE_FK(1, false, 0) : t == 2 ? MOE_FK(2, false, 0) : MOE_FK(4, false, 0);
+#undef MOE_FK
+}
+}  // namespace
+
+// Whether one CTA of the fused kernel with `smem` bytes of shared memory fits
+// on an SM of the current device (cached per kernel, device and size). The
+// grid is one CTA per SM and its barriers need every CTA resident; where the
+// occupancy query says no, the two-kernel path runs instead.
+bool fused_resident(const DecodeParams& p, size_t smem) {
+  static std::mutex mu;
+  struct Entry { const void* k; int dev; size_t smem; bool ok; };
+  static Entry cache[64];
+  static int n = 0;
+  const void* k = fused_kernel_for(p);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return false; }
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n; ++i)
+      if (cache[i].k == k && cache[i].dev == dev && cache[i].smem == smem) return cache[i].ok;
+  }
+  bool ok = false;
+  if (ensure_smem_attr(k, smem) == cudaSuccess) {
+    int blocks = 0;
+    ok = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k, kFT, smem) == cudaSuccess &&
+         blocks >= 1;
+  }
+  cudaGetLastError();
+  std::lock_guard<std::mutex> lock(mu);
+  if (n < 64) cache[n++] = Entry{k, dev, smem, ok};
+  return ok;
+}
+
 bool fused_decode_supported(const DecodeParams& p, int num_sms, size_t* smem, int* rg,
                             int* rows_max) {
   if (p.T < 1 || p.T > 4) return false;
@@ -524,6 +572,8 @@ bool fused_decode_supported(const DecodeParams& p, int num_sms, size_t* smem, in
   const FusedSmem m = fused_smem(p.H, p.F, p.Fs, p.n_shared, p.T, p.k, rmax, r, p.route, p.E,
                                  grid);
   if (m.total > 227 * 1024) return false;
+  // one CTA per SM, all resident at once (the grid barriers wait for every CTA)
+  if (!fused_resident(p, m.total)) return false;
   *smem = m.total;
   *rg = r;
   *rows_max = rmax;

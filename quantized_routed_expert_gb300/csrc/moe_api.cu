@@ -18,6 +18,8 @@
 namespace {
 
 std::atomic<int> g_pdl{1};
+constexpr uint64_t kDefaultBarrierWaitNs = 2000000000ull;   // 2 s
+std::atomic<uint64_t> g_barrier_wait_ns{kDefaultBarrierWaitNs};
 
 int num_sms() {
   static std::atomic<int> cache[64];
@@ -109,6 +111,7 @@ moe::DecodeParams decode_params(const moe_shape* shape, const moe_expert_weights
   p.xrec = reinterpret_cast<uint32_t*>(base + L.xrec);
   p.part = reinterpret_cast<float*>(base + L.part);
   p.status = status;
+  p.wait_ns = g_barrier_wait_ns.load();
   return p;
 }
 
@@ -206,15 +209,17 @@ moe_status moe_iq4nl_prefill_grouped(const moe_shape* shape, const moe_expert_we
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-moe_status moe_iq4nl_dequantize(const void* blocks, int64_t n_blocks, int32_t out_fp16,
+moe_status moe_iq4nl_dequantize(const void* blocks, int64_t n_blocks, int32_t mode,
                                 void* out, void* stream) {
-  if (n_blocks < 0 || (out_fp16 != 0 && out_fp16 != 1)) return MOE_ERR_INVALID_ARG;
+  if (n_blocks < 0 || (mode != MOE_DEQUANT_FP32 && mode != MOE_DEQUANT_FP16 &&
+                       mode != MOE_DEQUANT_FP32_ONE_TOKEN))
+    return MOE_ERR_INVALID_ARG;
   if (n_blocks == 0) return MOE_OK;
   if (!blocks || !out) return MOE_ERR_INVALID_ARG;
   if (!aligned(blocks, 2) || !aligned(out, 4)) return MOE_ERR_MISALIGNED;
   const int sms = num_sms();
   if (sms <= 0) return MOE_ERR_CUDA;
-  const cudaError_t e = moe::launch_dequant(blocks, n_blocks, out_fp16, out, sms,
+  const cudaError_t e = moe::launch_dequant(blocks, n_blocks, mode, out, sms,
                                             reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -266,6 +271,8 @@ int32_t moe_launches_per_call(const moe_shape* shape, int32_t T, int32_t call) {
 }
 
 int32_t moe_set_pdl(int32_t enable) { return g_pdl.exchange(enable ? 1 : 0); }
+
+uint64_t moe_set_barrier_wait_ns(uint64_t ns) { return g_barrier_wait_ns.exchange(ns); }
 
 const char* moe_status_string(int32_t status) {
   switch (status) {

@@ -307,16 +307,8 @@ __device__ __forceinline__ void sw128_store_chunk(uint8_t* tile, int r, int c, u
 // 16-byte chunks (8 fp16 each, K order) of row r, chunks c0..c0+3.
 __device__ __forceinline__ void dequant_block_to_tile(const uint32_t (&q)[4], uint16_t dbits,
                                                       uint8_t* tile, int r, int c0) {
-  const __half dh = __ushort_as_half(dbits);
-  const __half2 d2 = __halves2half2(dh, dh);
-  uint32_t lo[4], hi[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) iq4_lookup8_split(q[i], lo[i], hi[i]);
   uint32_t w[16];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) offsets_to_half4(lo[i], d2, w[2 * i], w[2 * i + 1]);     // 0..15
-#pragma unroll
-  for (int i = 0; i < 4; ++i) offsets_to_half4(hi[i], d2, w[8 + 2 * i], w[8 + 2 * i + 1]);  // 16..31
+  dequant_block_half(q, dbits, w);
 #pragma unroll
   for (int c = 0; c < 4; ++c)
     sw128_store_chunk(tile, r, c0 + c, make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]));

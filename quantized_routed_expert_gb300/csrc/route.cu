@@ -13,6 +13,8 @@
 #include "common.cuh"
 #include "route.cuh"
 
+#include <mutex>
+
 namespace cg = cooperative_groups;
 
 namespace moe {
@@ -343,37 +345,57 @@ __global__ void __launch_bounds__(kRmWarps * 32, 1) route_mma_kernel(RouteParams
 }
 
 namespace {
-// Permits clusters of more than 8 CTAs for a kernel, once; an error means the
-// device does not offer them and the caller falls back to 8.
+// Both caches below are process-wide, keyed by device, and guarded by one
+// mutex (host threads may launch concurrently, on several devices).
+std::mutex g_cluster_mu;
+
+// Permits clusters of more than 8 CTAs for a kernel on the current device,
+// once; an error means the device does not offer them and the caller falls
+// back to 8.
 cudaError_t allow_wide_clusters(const void* kernel) {
-  static const void* done[8];
+  static const void* done_k[32];
+  static int done_dev[32];
   static int n = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_cluster_mu);
   for (int i = 0; i < n; ++i)
-    if (done[i] == kernel) return cudaSuccess;
-  const cudaError_t e =
-      cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (done_k[i] == kernel && done_dev[i] == dev) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return e;
   }
-  if (n < 8) done[n++] = kernel;
+  if (n < 32) {
+    done_k[n] = kernel;
+    done_dev[n] = dev;
+    ++n;
+  }
   return cudaSuccess;
 }
-// Whether 16-CTA clusters can run for (token tile, shared memory size); -1 = not asked yet.
+// Whether 16-CTA clusters can run for (device, token tile, shared memory
+// size); -1 = not asked yet.
 struct WideEntry {
-  int tt;
+  int dev, tt;
   size_t sm;
   int ok;
 };
-WideEntry g_wide[32];
+WideEntry g_wide[64];
 int g_nwide = 0;
 int wide_cluster_cache(int tt, size_t sm) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return 0; }
+  std::lock_guard<std::mutex> lock(g_cluster_mu);
   for (int i = 0; i < g_nwide; ++i)
-    if (g_wide[i].tt == tt && g_wide[i].sm == sm) return g_wide[i].ok;
+    if (g_wide[i].dev == dev && g_wide[i].tt == tt && g_wide[i].sm == sm) return g_wide[i].ok;
   return -1;
 }
 void wide_cluster_store(int tt, size_t sm, int ok) {
-  if (g_nwide < 32) g_wide[g_nwide++] = WideEntry{tt, sm, ok};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return; }
+  std::lock_guard<std::mutex> lock(g_cluster_mu);
+  if (g_nwide < 64) g_wide[g_nwide++] = WideEntry{dev, tt, sm, ok};
 }
 }  // namespace
 

@@ -136,4 +136,21 @@ __device__ __forceinline__ void offsets_to_half4(uint32_t u, __half2 d2, uint32_
   o23 = *reinterpret_cast<uint32_t*>(&w23);
 }
 
+// One 32-weight block (its 4 index words, fp16 scale bits) to 32 fp16 weights
+// d*T[q] in K order, two to a word: words 0..7 hold weights 0..15 (low
+// nibbles), words 8..15 weights 16..31 (high nibbles). The prefill producers
+// call this for every block they put into an A tile.
+__device__ __forceinline__ void dequant_block_half(const uint32_t (&q)[4], uint16_t dbits,
+                                                   uint32_t (&w)[16]) {
+  const __half dh = __ushort_as_half(dbits);
+  const __half2 d2 = __halves2half2(dh, dh);
+  uint32_t lo[4], hi[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) iq4_lookup8_split(q[i], lo[i], hi[i]);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) offsets_to_half4(lo[i], d2, w[2 * i], w[2 * i + 1]);     // 0..15
+#pragma unroll
+  for (int i = 0; i < 4; ++i) offsets_to_half4(hi[i], d2, w[8 + 2 * i], w[8 + 2 * i + 1]);  // 16..31
+}
+
 }  // namespace moe

@@ -1,5 +1,6 @@
 // Small kernels of libmoe: the IQ4_NL dequantiser and the route sanitiser.
 #include "common.cuh"
+#include "tc.cuh"
 #include "util_kernels.cuh"
 
 #include <mutex>
@@ -26,36 +27,92 @@ cudaError_t ensure_smem_attr(const void* kernel, size_t bytes) {
   return cudaSuccess;
 }
 
-// One thread per output pair of weights (j, j+16) of a block: the block's
-// index byte j holds both codes. Exact fp32 product d*T[q], or the fp16
-// round-to-nearest-even of it (an fp16 multiply of two fp16 values whose exact
-// product is rounded once).
-__global__ void dequant_kernel(const uint8_t* __restrict__ blocks, int64_t n_blocks, int fp16,
+// The block decoder on its own, run through the very device functions the
+// layer kernels use, one mode per decoder, so that a bit-exact comparison of
+// its output covers the code that runs:
+//   MOE_DEQUANT_FP32: split_pair + iq4_lookup8 + iq4_dot_block (decode, an
+//     expert with several tokens);
+//   MOE_DEQUANT_FP16: dequant_block_half (the prefill producers);
+//   MOE_DEQUANT_FP32_ONE_TOKEN: pair_scales + iq4_pair_dot1 (decode, an expert
+//     with one token: the split table, no merge).
+// The dot-product decoders give a table value as the dot product of the block
+// with a one-hot activation vector in the pair layout (word j holds the 16-bit
+// values of positions j and j + 16), scaled by d exactly as the kernels scale
+// a block's integer sum (fmaf of the integer, as float, by d times a unit
+// activation scale, onto -0). One thread takes one pair of consecutive blocks (36
+// bytes, the unit every layer kernel reads); a last odd block is paired with
+// a zero block.
+__device__ __forceinline__ void load_pair_bytes(const uint8_t* b, bool two, uint32_t (&w)[9]) {
+#pragma unroll
+  for (int i = 0; i < 9; ++i) {
+    uint32_t v = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int o = 4 * i + j;
+      const uint32_t byte = (o < kBlockB || two) ? b[o] : 0u;
+      v |= byte << (8 * j);
+    }
+    w[i] = v;
+  }
+}
+
+__global__ void dequant_kernel(const uint8_t* __restrict__ blocks, int64_t n_blocks, int mode,
                                void* __restrict__ out) {
-  const int64_t n = n_blocks * 16;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t b = i >> 4;
-    const int j = (int)(i & 15);
-    const uint8_t* blk = blocks + b * kBlockB;
-    const uint16_t dbits = (uint16_t)blk[0] | ((uint16_t)blk[1] << 8);
-    const uint8_t qb = blk[2 + j];
-    // table value via the same byte_perm lookup the kernels use
-    uint32_t r0, r1;
-    iq4_lookup8((uint32_t)qb, r0, r1);
-    const int t_lo = (int)(int8_t)(r0 & 0xFF);
-    const int t_hi = (int)(int8_t)((r0 >> 8) & 0xFF);
-    const int64_t o = b * 32;
-    if (fp16) {
-      const __half d = __ushort_as_half(dbits);
-      __half* oh = reinterpret_cast<__half*>(out);
-      oh[o + j] = __hmul(d, __int2half_rn(t_lo));
-      oh[o + j + 16] = __hmul(d, __int2half_rn(t_hi));
+  const int64_t n_pairs = (n_blocks + 1) / 2;
+  for (int64_t pi = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; pi < n_pairs;
+       pi += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t b0 = 2 * pi;
+    const bool two = b0 + 1 < n_blocks;
+    uint32_t w[9];
+    load_pair_bytes(blocks + b0 * kBlockB, two, w);
+    const int nb = two ? 2 : 1;
+    if (mode == MOE_DEQUANT_FP16) {
+      uint32_t q0[4], q1[4], h[2][16];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) q0[i] = prmt(w[i], w[i + 1], 0x5432u);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) q1[i] = w[5 + i];
+      dequant_block_half(q0, (uint16_t)(w[0] & 0xFFFFu), h[0]);
+      dequant_block_half(q1, (uint16_t)(w[4] >> 16), h[1]);
+      uint32_t* o = reinterpret_cast<uint32_t*>(out) + b0 * 16;
+      for (int b = 0; b < nb; ++b)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o[16 * b + i] = h[b][i];
+      continue;
+    }
+    float* o = reinterpret_cast<float*>(out) + b0 * 32;
+    float d0, d1;
+    uint32_t t0[8], t1[8];
+    if (mode == MOE_DEQUANT_FP32) {
+      uint32_t a0[4], a1[4];
+      split_pair(w, d0, d1, a0, a1);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        iq4_lookup8(a0[i], t0[2 * i], t0[2 * i + 1]);
+        iq4_lookup8(a1[i], t1[2 * i], t1[2 * i + 1]);
+      }
     } else {
-      const float d = __half2float(__ushort_as_half(dbits));
-      float* of = reinterpret_cast<float*>(out);
-      of[o + j] = d * (float)t_lo;
-      of[o + j + 16] = d * (float)t_hi;
+      pair_scales(w, d0, d1);
+    }
+#pragma unroll 1
+    for (int pos = 0; pos < 32; ++pos) {
+      // one-hot at position pos of both blocks: word pos % 16, half pos / 16
+      uint32_t v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = 0u;
+      const uint32_t one = pos < 16 ? 1u : 0x10000u;
+      v[pos & 15] = one;
+      v[16 + (pos & 15)] = one;
+      int i0, i1;
+      if (mode == MOE_DEQUANT_FP32) {
+        i0 = iq4_dot_block(t0, v);
+        i1 = iq4_dot_block(t1, v + 16);
+      } else {
+        iq4_pair_dot1(w, v, i0, i1);
+      }
+      // (an addend of -0 keeps the sign of a zero product, as d*T has it)
+      o[pos] = fmaf((float)i0, d0 * 1.0f, -0.0f);
+      if (two) o[32 + pos] = fmaf((float)i1, d1 * 1.0f, -0.0f);
     }
   }
 }
@@ -79,14 +136,14 @@ __global__ void sanitize_kernel(const int32_t* __restrict__ ids, const float* __
   }
 }
 
-cudaError_t launch_dequant(const void* blocks, int64_t n_blocks, int fp16, void* out,
+cudaError_t launch_dequant(const void* blocks, int64_t n_blocks, int mode, void* out,
                            int num_sms, cudaStream_t stream) {
-  const int64_t n = n_blocks * 16;
-  int64_t grid = (n + 255) / 256;
+  const int64_t n = (n_blocks + 1) / 2;
+  int64_t grid = (n + 127) / 128;
   if (grid > (int64_t)num_sms * 16) grid = (int64_t)num_sms * 16;
   if (grid < 1) grid = 1;
-  dequant_kernel<<<(int)grid, 256, 0, stream>>>(reinterpret_cast<const uint8_t*>(blocks),
-                                                 n_blocks, fp16, out);
+  dequant_kernel<<<(int)grid, 128, 0, stream>>>(reinterpret_cast<const uint8_t*>(blocks),
+                                                 n_blocks, mode, out);
   return cudaGetLastError();
 }
 

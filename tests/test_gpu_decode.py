@@ -53,21 +53,62 @@ def _edge_blocks():
     return np.concatenate([blocks, extra])
 
 
-def test_dequant_fp32_bit_exact():
+@pytest.mark.parametrize("mode", ["multi", "one_token", "fp16"])
+@pytest.mark.parametrize("odd", [False, True])
+def test_dequant_hot_path_decoders_bit_exact(mode, odd):
+    # Each mode runs one of the block decoders the layer kernels call, on the
+    # 36-byte block pairs they read: the decode lookup for experts with several
+    # tokens (split_pair + iq4_lookup8 + iq4_dot_block), the decode split table
+    # for experts with one token (iq4_pair_dot1) and the prefill producers'
+    # fp16 decoder (dequant_block_half). The dot-product decoders give each
+    # table value through a one-hot activation vector. Every value must equal
+    # the oracle's dequantisation bit for bit: exact d*T in fp32, or its
+    # round-to-nearest-even fp16 (a last odd block checks the pair tail).
     moe = lib()
     b = _edge_blocks()
-    out = moe.iq4nl_dequantize(torch.from_numpy(b.reshape(-1)).to(DEV)).cpu().numpy()
-    ref = oracle.dequant(b, oracle.EXACT).astype(np.float32)      # exact in fp32
-    assert np.array_equal(out.view(np.uint32), ref.view(np.uint32))
+    if odd:
+        b = b[:-1]
+    assert (len(b) % 2 == 1) == odd
+    m = {"multi": moe.DEQUANT_FP32, "one_token": moe.DEQUANT_FP32_ONE_TOKEN,
+         "fp16": moe.DEQUANT_FP16}[mode]
+    out = moe.iq4nl_dequantize(torch.from_numpy(b.reshape(-1)).to(DEV), mode=m).cpu().numpy()
+    if mode == "fp16":
+        ref = oracle.dequant(b, oracle.MMA16).astype(np.float16)   # already fp16 values
+        assert np.array_equal(out.view(np.uint16), ref.reshape(-1).view(np.uint16))
+    else:
+        ref = oracle.dequant(b, oracle.EXACT).astype(np.float32)   # exact in fp32
+        got, want = out.view(np.uint32), ref.reshape(-1).view(np.uint32)
+        bad = np.flatnonzero(got != want)
+        assert bad.size == 0, (mode, bad[:8], out[bad[:8]], ref.reshape(-1)[bad[:8]])
 
 
-def test_dequant_fp16_bit_exact():
+def test_dequant_every_code_in_every_position():
+    # 16 blocks whose 32 positions cycle through all 16 codes with a shift per
+    # block, so each code sits in each position (low and high nibble) of some
+    # block, for each decoder.
     moe = lib()
-    b = _edge_blocks()
-    out = moe.iq4nl_dequantize(torch.from_numpy(b.reshape(-1)).to(DEV), fp16=True)
-    out = out.cpu().numpy()
-    ref = oracle.dequant(b, oracle.MMA16).astype(np.float16)      # already fp16 values
-    assert np.array_equal(out.view(np.uint16), ref.view(np.uint16))
+    blocks = np.zeros((32, 18), np.uint8)
+    for i in range(32):
+        blocks[i, 0:2] = np.frombuffer(np.float16(0.5 + i / 64).tobytes(), np.uint8)
+        for j in range(16):
+            lo, hi = (j + i) % 16, (j + 16 + i) % 16
+            blocks[i, 2 + j] = lo | (hi << 4)
+    flat = torch.from_numpy(blocks.reshape(-1)).to(DEV)
+    ref32 = oracle.dequant(blocks, oracle.EXACT).astype(np.float32).reshape(-1)
+    ref16 = oracle.dequant(blocks, oracle.MMA16).astype(np.float16).reshape(-1)
+    for m in (moe.DEQUANT_FP32, moe.DEQUANT_FP32_ONE_TOKEN):
+        out = moe.iq4nl_dequantize(flat, mode=m).cpu().numpy()
+        assert np.array_equal(out.view(np.uint32), ref32.view(np.uint32)), m
+    out = moe.iq4nl_dequantize(flat, mode=moe.DEQUANT_FP16).cpu().numpy()
+    assert np.array_equal(out.view(np.uint16), ref16.view(np.uint16))
+
+
+def test_dequant_refuses_unknown_mode():
+    moe = lib()
+    b = torch.zeros(36, dtype=torch.uint8, device=DEV)
+    out = torch.zeros(64, dtype=torch.float32, device=DEV)
+    st = moe._lib.moe_iq4nl_dequantize(b.data_ptr(), 2, 3, out.data_ptr(), None)
+    assert st == moe.MOE_ERR_INVALID_ARG
 
 
 def test_sanitize_worked_example():
@@ -249,6 +290,87 @@ def test_decode_invalid_and_duplicate_routes():
     assert int(status.item()) & 0xFFFF == 2
     ref = oracle_layer(L, x_host, bad, w)
     check_close(y, ref, "invalid/duplicate routes")
+
+
+def _wide_range_x(x_host: np.ndarray) -> np.ndarray:
+    """Per token: block 3 holds one value 2^12 times its neighbours' scale,
+    block 7 only values near 2^-100, block 11 alternates 2^-20 and 2^10 scales
+    (a range of 2^30 inside one 32-value block)."""
+    x = synth.bf16_bits_to_f32(x_host).astype(np.float64)
+    for t in range(x.shape[0]):
+        x[t, 100] = 4096.0 * (1.0 if t % 2 == 0 else -1.0)
+        x[t, 224:256] *= 2.0 ** -100
+        x[t, 352:384:2] *= 2.0 ** -20
+        x[t, 353:384:2] *= 2.0 ** 10
+    return synth.to_bf16_bits(x)
+
+
+@pytest.mark.parametrize("cfg,T", [(1, 1), (2, 2), (3, 4), (3, 16)])
+def test_decode_wide_range_blocks(cfg, T):
+    # The decode path quantises x and h to 16-bit integers with one power-of-
+    # two scale per 32 values; this is where that rounding bites. x gets
+    # blocks that span up to 2^30, and the shared expert's gate row 5 gets
+    # block scales 2^10 above its neighbours', so the first 32-value block of
+    # the shared expert's h spans more than 2^10 as well. Routes are passed in
+    # (taken from the oracle on the same x), so both sides use the same ids.
+    from synth.layers import Layer
+    s = synth.SHAPES[cfg]
+    L = Layer(s, synth.seed_of(cfg), 0, device=DEV)
+    sh = [m.copy() for m in L.shared_bytes_host()]
+    nbh = s.H // 32
+    big = np.frombuffer(np.float16(0.25).tobytes(), np.uint8)
+    sh[0][5 * nbh:6 * nbh, 0:2] = big                     # row 5 of the shared gate
+    L.sh_gate.copy_(torch.from_numpy(sh[0].reshape(-1)).to(DEV))
+    L.shared_bytes_host = lambda: sh
+    x_host = _wide_range_x(gapped_rows(L, T))
+    ids, w, _, _ = oracle.route(L.router_w_host, L.bias_host, x_host, s.k)
+    _, _, y = run_decode(L, x_host, ids, w.astype(np.float32))
+    ref = oracle_layer(L, x_host, ids, w.astype(np.float32).astype(np.float64))
+    check_close(y, ref, f"wide-range blocks cfg{cfg} T{T}")
+    del L
+    torch.cuda.empty_cache()
+
+
+def test_barrier_timeout_is_reported_and_recovers():
+    # The single-launch decode kernel waits at grid barriers for every CTA.
+    # With the barrier limit set to 0, a CTA gives up the first time it finds
+    # a barrier incomplete: the call must still return, with MOE_STATUS_TIMEOUT
+    # in the status word, and the next call on the same workspace with the
+    # default limit must be correct again (the kernel drained its own copies
+    # and left the barrier counters at zero).
+    moe = lib()
+    from synth.layers import bf16_tensor
+    L = layer_of(1, 4)
+    s = L.shape
+    shape = moe_shape(s)
+    assert moe.launches_per_call(shape, 1, moe.CALL_DECODE_ROUTED) == 1   # fused path
+    x_host = gapped_rows(L, 1)
+    x = bf16_tensor(x_host, DEV)
+    ws = moe.workspace(shape, 1, moe.DECODE, DEV)
+    ids0, w0, y0 = moe.iq4nl_decode_routed(shape, L.router_w, L.bias, weights_of(L), x, ws)
+    torch.cuda.synchronize()
+    y0 = y0.cpu().numpy()
+    check_close(y0, oracle_layer(L, x_host, ids0.cpu().numpy(), w0.cpu().numpy()),
+                "before the timeout")
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    old = moe.set_barrier_wait_ns(0)
+    try:
+        moe.iq4nl_decode_routed(shape, L.router_w, L.bias, weights_of(L), x, ws, status=status)
+        torch.cuda.synchronize()
+    finally:
+        assert moe.set_barrier_wait_ns(old) == 0
+    assert old == 2_000_000_000
+    st = int(status.item()) & 0xFFFFFFFF
+    assert st & moe.STATUS_TIMEOUT, hex(st)
+    assert st & moe.STATUS_INVALID_ROUTE_MASK == 0
+    status.zero_()
+    for _ in range(2):
+        ids1, w1, y1 = moe.iq4nl_decode_routed(shape, L.router_w, L.bias, weights_of(L), x, ws,
+                                               status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert np.array_equal(ids1.cpu().numpy(), ids0.cpu().numpy())
+        assert np.array_equal(y1.cpu().numpy().view(np.uint32), y0.view(np.uint32))
 
 
 def test_workspace_reused_across_layers():

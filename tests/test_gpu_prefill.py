@@ -97,6 +97,11 @@ def test_prefill_full_chunk_sampled_tokens():
     rows = np.random.default_rng(0).choice(T, 12, replace=False)
     rows = np.sort(np.concatenate([rows, [0, T - 1]]))
     check_close(y[rows], oracle_rows(L, x_host, ids, w, rows), "prefill T=2048 sampled")
+    # Distance to the exact definition (fp64, unrounded operands) on the same
+    # rows, held to the layer's float bar: fp16 operands keep the chunk inside it.
+    md, l2 = check_close(y[rows], oracle_rows(L, x_host, ids, w, rows, oracle.EXACT),
+                         "prefill T=2048 sampled vs exact")
+    print(f"prefill T=2048 vs exact: max|diff|/max|ref| = {md:.3e}, rel-L2 = {l2:.3e}")
     # deterministic: a second run gives the same bits
     _, _, y2 = run_prefill(L, x_host, ids, w)
     assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))

@@ -80,6 +80,41 @@ def test_static_after_a_different_token_count():
     assert int(status.item()) == 0
 
 
+def test_static_call_allocates_no_device_memory():
+    # The raw C call, with every buffer made beforehand: the device's free
+    # memory (cudaMemGetInfo, which sees every allocation in the process, the
+    # caching allocator's included) and torch's own counters are the same
+    # before and after a call. The first call on the device is made before
+    # measuring, since loading the library's kernels may map their code and
+    # the fixed scratch itself.
+    import ctypes
+    moe = lib()
+    L = layer_of(1)
+    shape, x, ids, w = inputs(L, 4)
+    y = torch.empty((4, shape.hidden), dtype=torch.float32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    wts = weights_of(L)
+    stream = torch.cuda.current_stream().cuda_stream
+
+    def call():
+        st = moe._lib.moe_iq4nl_decode_static(ctypes.byref(shape), ctypes.byref(wts.c),
+                                              x.data_ptr(), 4, ids.data_ptr(), w.data_ptr(),
+                                              y.data_ptr(), status.data_ptr(), stream)
+        assert st == moe.MOE_OK
+        torch.cuda.synchronize()
+
+    call()
+    free0, _ = torch.cuda.mem_get_info()
+    alloc0, reserved0 = torch.cuda.memory_allocated(), torch.cuda.memory_reserved()
+    for _ in range(3):
+        call()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, (free0, free1)
+    assert torch.cuda.memory_allocated() == alloc0
+    assert torch.cuda.memory_reserved() == reserved0
+    assert int(status.item()) == 0
+
+
 def test_static_refuses_a_layout_beyond_the_scratch():
     moe = lib()
     L = layer_of(1)
