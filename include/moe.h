@@ -72,6 +72,7 @@ typedef enum {
 #define MOE_MAX_DECODE_TOKENS 16
 #define MOE_MAX_HIDDEN 8192
 #define MOE_MAX_FFN 8192
+#define MOE_MAX_LAYERS 128
 
 /* Sizes of one MoE layer. hidden, ffn and ffn_shared are multiples of 64
  * (IQ4_NL needs 32; the kernels pair blocks) and at most 8192.
@@ -158,6 +159,48 @@ moe_status moe_iq4nl_decode_routed(const moe_shape* shape, const uint16_t* route
                                    float* y, void* ws, size_t ws_bytes, uint32_t* status,
                                    void* stream);
 
+/* One layer's weights for moe_iq4nl_decode_layers: its experts and its router. */
+typedef struct {
+  moe_expert_weights experts;
+  const uint16_t* router_w;     /* bf16 [E][H], 16-byte aligned */
+  const float* router_bias;     /* fp32 [E] or NULL */
+} moe_layer_weights;
+
+/* Route + decode of n_layers consecutive MoE layers of one shape in one call:
+ * for each layer l in order, what moe_iq4nl_decode_routed computes, with the
+ * same arithmetic and the same outputs. The PocketLLM "Xing4.0-29B-A4B" page
+ * (Performance) measures its decode step bound by kernel launches (11,536 a
+ * step, 178 ms of host submission against 46.5 ms of device work); for 1..4
+ * tokens, at most 512 experts and hidden, ffn, ffn_shared multiples of 256,
+ * this call is ONE persistent launch over all the layers, with bounded
+ * grid-wide waits between the phases of a layer and between layers (limit:
+ * moe_set_barrier_wait_ns). Weights that do not depend on the routes (the
+ * next layer's router rows and shared expert) are fetched a layer ahead.
+ * Other sizes run layer by layer (router, then the layer), with the same
+ * results.
+ *   n_layers : 1..MOE_MAX_LAYERS
+ *   layers   : HOST array [n_layers]; read during the call only (its pointers
+ *              are copied into the launch); the device pointers it holds
+ *              follow the rules of moe_expert_weights and moe_route_topk
+ *   x        : bf16, 16-byte aligned: chained == 0: [n_layers][T][H], each
+ *              layer's own input; chained == 1: [T][H], the first layer's
+ *              input, layer l + 1's input then being bf16(y_l) (round to
+ *              nearest even)
+ *   ids, weights : out [n_layers][T][k], per layer as moe_route_topk writes them
+ *   y        : out fp32 [n_layers][T][H], 16-byte aligned: every layer's output
+ *   ws       : workspace of moe_workspace_bytes(shape, >= T, 0) bytes. Besides
+ *              its counters, which return to zero, it keeps a call counter that
+ *              tags the router scores of each call; zero-filling the whole
+ *              workspace again is always allowed.
+ *   status   : as for moe_iq4nl_decode
+ * Layers run one after another in both modes (layer l + 1 starts once every
+ * row of y_l is written). */
+moe_status moe_iq4nl_decode_layers(const moe_shape* shape, int32_t n_layers,
+                                   const moe_layer_weights* layers, const uint16_t* x,
+                                   int32_t T, int32_t chained, int32_t* ids, float* weights,
+                                   float* y, void* ws, size_t ws_bytes, uint32_t* status,
+                                   void* stream);
+
 /* Decode without a caller-provided workspace. This call has no counterpart on
  * the pages; it is a convenience of this library. It exists for callers that
  * cannot allocate device memory at the point where they run the layer: code
@@ -238,8 +281,9 @@ moe_status moe_sanitize_routes(const int32_t* ids, const float* weights, int64_t
 
 /* Kernel launches one call makes for this shape and token count (host, no
  * device work): call 0 = moe_route_topk, 1 = moe_iq4nl_decode,
- * 2 = moe_iq4nl_decode_routed, 3 = moe_iq4nl_prefill_grouped. Returns a
- * negative moe_status for bad arguments. */
+ * 2 = moe_iq4nl_decode_routed, 3 = moe_iq4nl_prefill_grouped, and
+ * 4 + 2*n_layers + chained = moe_iq4nl_decode_layers of n_layers layers
+ * (chained 0 or 1). Returns a negative moe_status for bad arguments. */
 int32_t moe_launches_per_call(const moe_shape* shape, int32_t T, int32_t call);
 
 /* 1 (default) launches kernels with programmatic dependent launch; 0 does not.

@@ -54,6 +54,11 @@ class _Weights(ctypes.Structure):
                 ("gate", "up", "down", "sh_gate", "sh_up", "sh_down")]
 
 
+class _LayerWeights(ctypes.Structure):
+    _fields_ = [("experts", _Weights), ("router_w", ctypes.c_void_p),
+                ("router_bias", ctypes.c_void_p)]
+
+
 _P = ctypes.c_void_p
 _lib.moe_route_topk.argtypes = [ctypes.POINTER(Shape), _P, _P, _P, ctypes.c_int32, _P, _P, _P]
 _lib.moe_route_topk.restype = ctypes.c_int
@@ -67,6 +72,10 @@ _lib.moe_iq4nl_decode_routed.argtypes = [ctypes.POINTER(Shape), _P, _P, ctypes.P
                                          _P, ctypes.c_int32, _P, _P, _P, _P, ctypes.c_size_t, _P,
                                          _P]
 _lib.moe_iq4nl_decode_routed.restype = ctypes.c_int
+_lib.moe_iq4nl_decode_layers.argtypes = [ctypes.POINTER(Shape), ctypes.c_int32,
+                                         ctypes.POINTER(_LayerWeights), _P, ctypes.c_int32,
+                                         ctypes.c_int32, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
+_lib.moe_iq4nl_decode_layers.restype = ctypes.c_int
 _lib.moe_iq4nl_decode_static.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(_Weights), _P,
                                          ctypes.c_int32, _P, _P, _P, _P, _P]
 _lib.moe_iq4nl_decode_static.restype = ctypes.c_int
@@ -85,6 +94,7 @@ _lib.moe_status_string.restype = ctypes.c_char_p
 _lib.moe_version.restype = ctypes.c_char_p
 
 EXPORTS = ("moe_route_topk", "moe_workspace_bytes", "moe_iq4nl_decode", "moe_iq4nl_decode_routed",
+           "moe_iq4nl_decode_layers",
            "moe_iq4nl_decode_static", "moe_iq4nl_prefill_grouped", "moe_iq4nl_dequantize", "moe_sanitize_routes",
            "moe_launches_per_call", "moe_set_pdl", "moe_set_barrier_wait_ns", "moe_status_string",
            "moe_version")
@@ -110,6 +120,12 @@ def status_string(status: int) -> str:
 
 
 CALL_ROUTE, CALL_DECODE, CALL_DECODE_ROUTED, CALL_PREFILL = 0, 1, 2, 3
+MAX_LAYERS = 128
+
+
+def call_decode_layers(n_layers: int, chained: bool) -> int:
+    """The `call` code of moe_iq4nl_decode_layers for launches_per_call."""
+    return 4 + 2 * int(n_layers) + (1 if chained else 0)
 
 
 def launches_per_call(shape: Shape, T: int, call: int) -> int:
@@ -382,6 +398,72 @@ def iq4nl_decode_routed(shape: Shape, router_w, router_bias, w: ExpertWeights, x
                                         _ptr(weights), _ptr(y), _ptr(ws),
                                         int(ws.numel() if ws is not None else 0), _ptr(status),
                                         _stream(stream)), "moe_iq4nl_decode_routed")
+    return ids, weights, y
+
+
+def iq4nl_decode_layers(shape: Shape, layers, x, ws, chained: bool = False, ids=None,
+                        weights=None, y=None, status=None, stream=None):
+    """Route and decode several layers of one shape in one call.
+    layers: a sequence of (ExpertWeights, router_w bf16 [E,H], router_bias fp32 [E] or None).
+    x: bf16 [L,T,H] (each layer's input) or, with chained=True, [T,H] (the first
+    layer's; layer l+1 then takes bf16(y_l)). Returns (ids [L,T,k], weights [L,T,k],
+    y fp32 [L,T,H])."""
+    L = len(layers)
+    if L < 1 or L > MAX_LAYERS:
+        raise ValueError(f"1..{MAX_LAYERS} layers, got {L}")
+    ok = _shape_ok(shape)
+    E, H, k = shape.n_experts, shape.hidden, shape.top_k
+    if not isinstance(x, torch.Tensor):
+        raise TypeError("x must be a torch tensor")
+    if chained:
+        if x.dim() != 2:
+            raise ValueError("x must be [T, hidden] for a chained call")
+        T = x.shape[0]
+        _meta(x, torch.bfloat16, "x", (T, H) if ok else None)
+    else:
+        if x.dim() != 3 or x.shape[0] != L:
+            raise ValueError(f"x must be [{L}, T, hidden] (one input per layer)")
+        T = x.shape[1]
+        _meta(x, torch.bfloat16, "x", (L, T, H) if ok else None)
+    keep, arr = [], (_LayerWeights * L)()
+    for i, (w, wr, b) in enumerate(layers):
+        if ok:
+            keep += w.check(shape)
+        _meta(wr, torch.bfloat16, f"layers[{i}] router_w", (E, H) if ok else None)
+        if b is not None:
+            _meta(b, torch.float32, f"layers[{i}] router_bias", (E,) if ok else None)
+        arr[i].experts = w.c
+        arr[i].router_w = _ptr(wr)
+        arr[i].router_bias = _ptr(b)
+        keep += [wr] + ([b] if b is not None else [])
+    for t, name, dt, shp in ((ids, "ids", torch.int32, (L, T, k)),
+                             (weights, "weights", torch.float32, (L, T, k)),
+                             (y, "y", torch.float32, (L, T, H))):
+        if t is not None:
+            _meta(t, dt, name, shp if ok else None)
+    _on_cuda(x, "x")
+    for w, _, _ in layers:
+        if ok:
+            w.check_device()
+    for t in keep:
+        _on_cuda(t, "layer weights")
+    if ids is None:
+        ids = torch.empty((L, T, k), dtype=torch.int32, device=x.device)
+    if weights is None:
+        weights = torch.empty((L, T, k), dtype=torch.float32, device=x.device)
+    if y is None:
+        y = torch.empty((L, T, H), dtype=torch.float32, device=x.device)
+    for t, name in ((ids, "ids"), (weights, "weights"), (y, "y")):
+        _on_cuda(t, name)
+    _status_arg(status)
+    if ws is not None:
+        _dev(ws, torch.uint8, "ws")
+    _same_device(x, ids, weights, y, status, ws, *keep)
+    _check(_lib.moe_iq4nl_decode_layers(ctypes.byref(shape), L, arr, _ptr(x), int(T),
+                                        1 if chained else 0, _ptr(ids), _ptr(weights), _ptr(y),
+                                        _ptr(ws), int(ws.numel() if ws is not None else 0),
+                                        _ptr(status), _stream(stream)),
+           "moe_iq4nl_decode_layers")
     return ids, weights, y
 
 

@@ -154,16 +154,11 @@ __device__ __forceinline__ uint32_t ordered_key_bits(float k) {
   const uint32_t u = __float_as_uint(k + 0.0f);       // -0 -> +0
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+// The selection itself, on the order-preserving integers v[i] of keys
+// lane + 32 i (0 for a key never chosen); v is consumed.
 template <int NPL>
-__device__ __forceinline__ int warp_topk_ids_t(const float* keys, int E, int k) {
+__device__ __forceinline__ int warp_topk_bits(uint32_t (&v)[NPL], int k) {
   const int lane = threadIdx.x & 31;
-  uint32_t v[NPL];
-#pragma unroll
-  for (int i = 0; i < NPL; ++i) {
-    const int e = lane + 32 * i;
-    const float kv = e < E ? keys[e] : -INFINITY;
-    v[i] = kv > -INFINITY ? ordered_key_bits(kv) : 0u;    // NaN and -inf: 0
-  }
   int id = 0;
 #pragma unroll 1
   for (int j = 0; j < k; ++j) {
@@ -188,6 +183,25 @@ __device__ __forceinline__ int warp_topk_ids_t(const float* keys, int E, int k) 
     for (int i = 0; i < NPL; ++i) v[i] = (mine && i == ri) ? 0u : v[i];
   }
   return id;
+}
+// Keys in registers: lane l holds keys l, l + 32, ... (-inf beyond E).
+template <int NPL>
+__device__ __forceinline__ int warp_topk_regs(const float (&kv)[NPL], int k) {
+  uint32_t v[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) v[i] = kv[i] > -INFINITY ? ordered_key_bits(kv[i]) : 0u;
+  return warp_topk_bits<NPL>(v, k);
+}
+template <int NPL>
+__device__ __forceinline__ int warp_topk_ids_t(const float* keys, int E, int k) {
+  const int lane = threadIdx.x & 31;
+  float kv[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * i;
+    kv[i] = e < E ? keys[e] : -INFINITY;                  // NaN and -inf: never chosen
+  }
+  return warp_topk_regs<NPL>(kv, k);
 }
 // Lane j < k returns the j-th chosen expert id. Two widths only (E <= 64 and
 // E <= 512), for kernels whose code size matters.

@@ -36,7 +36,7 @@ inline int64_t qvec_words(int64_t K) {
 }
 
 struct DecodeLayout {
-  int64_t h_r, h_s, rec_r, rec_s, sync, scores, xrec, part, total;  // byte offsets
+  int64_t h_r, h_s, rec_r, rec_s, sync, scores, xrec, part, tscores, xc, total;  // byte offsets
 };
 
 inline DecodeLayout decode_layout(const moe_shape& s, int64_t T) {
@@ -56,6 +56,8 @@ inline DecodeLayout decode_layout(const moe_shape& s, int64_t T) {
   L.scores = take(T * s.n_experts * 4);    // router scores of the routed fused kernel
   L.xrec = take(T * qvec_words(s.hidden) * 4);   // quantised x, when it does not fit on chip
   L.part = take((T * s.top_k + (Fs ? T : 0)) * s.hidden * 4);   // down partials per pair
+  L.tscores = take(2 * T * s.n_experts * 8);   // tagged router scores (multi-layer kernel)
+  L.xc = take(T * s.hidden * 2);               // chained bf16 input (multi-layer, launch per layer)
   L.total = off;
   return L;
 }
@@ -76,7 +78,8 @@ struct DecodeParams {
   float* h_s;        // [T][Fs]
   uint32_t* rec_r;   // [T*k][qvec_words(F)]
   uint32_t* rec_s;   // [T][qvec_words(Fs)]
-  uint32_t* sync;    // [4]: h arrivals, departures, score arrivals (fused kernel)
+  uint32_t* sync;    // [0..3]: h arrivals, departures, score arrivals (fused kernel);
+                     // [4..7]: h arrivals, y arrivals, departures, epoch (multi-layer kernel)
   uint32_t* status;
   uint32_t* xrec;    // [T][qvec_words(H)]: quantised x (gate/up kernel without room for it)
   float* part;       // [T*k (+T)][H]: down partials per pair (two-kernel path)
@@ -92,6 +95,26 @@ struct DecodeParams {
   int dn_rows_max;   // max output rows per down CTA
   int fz_rg;         // fused kernel: output rows per down unit
   uint64_t wait_ns;  // limit of a CTA's waits on other CTAs (grid barriers)
+  // several layers in one call (moe_iq4nl_decode_layers)
+  int L;             // layers
+  int chained;       // 1: layer l + 1's input is bf16(y_l)
+  uint64_t* tscores; // workspace [2][T][E]: score | tag << 32
+  uint16_t* xc;      // workspace [T][H]: chained input, launch-per-layer path
+};
+
+// Per-layer pointers of a multi-layer call (kernel parameter space).
+struct LayerPtrs {
+  const uint8_t* gate;
+  const uint8_t* up;
+  const uint8_t* down;
+  const uint8_t* sh_gate;
+  const uint8_t* sh_up;
+  const uint8_t* sh_down;
+  const uint16_t* Wr;
+  const float* bias;
+};
+struct LayerTable {
+  LayerPtrs layer[MOE_MAX_LAYERS];
 };
 
 cudaError_t launch_decode(const DecodeParams& p, int num_sms, bool pdl, cudaStream_t stream);
@@ -104,5 +127,9 @@ cudaError_t launch_decode_routed(const DecodeParams& p, int num_sms, bool pdl,
                                  cudaStream_t stream);
 cudaError_t launch_decode_fused(const DecodeParams& p, int num_sms, size_t smem, bool pdl,
                                 cudaStream_t stream);
+bool layers_supported(const DecodeParams& p, int num_sms, size_t* smem, int* rg, int* rows_max);
+int layers_launches(const DecodeParams& p, int num_sms);
+cudaError_t launch_decode_layers(const DecodeParams& p, const LayerTable& lt, int num_sms,
+                                 bool pdl, cudaStream_t stream);
 
 }  // namespace moe

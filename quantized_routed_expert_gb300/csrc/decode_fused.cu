@@ -83,33 +83,6 @@ __host__ __device__ inline FusedSmem fused_smem(int H, int F, int Fs, int ns, in
   return m;
 }
 
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// One down unit: rows [r0, r0 + nrows) (CTA-local indices) of the slot's W_d at
-// `wrows`; for every pair of the slot, the row dot products into `part`.
-// NPS pairs share each decoded block; LPR as for gate/up (0 = run time).
-template <int NPS, int LPR>
-__device__ __forceinline__ void down_unit_t(const DecodeParams& p, const RouteTable& rt,
-                                         const uint8_t* wrows, int slot, int r0, int nrows,
-                                         const uint32_t* recs, float* part, int rows_max) {
-  const bool shared = slot < 0;
-  const int K = shared ? p.Fs : p.F;
-  const int words = dqvec_words(K);
-  const int P = p.T * p.k;
-  const int ntok = shared ? p.T : rt.slot_off[slot + 1] - rt.slot_off[slot];
-  const int lbase = shared ? 0 : rt.slot_off[slot];
-  const uint32_t* rec_sh = recs + (size_t)P * dqvec_words(p.F);
-  auto pidx = [&](int jj) { return shared ? P + jj : rt.list[lbase + jj]; };
-  down_rows<NPS, LPR>(
-      wrows, K, nrows, ntok,
-      [&](int jj) { return shared ? rec_sh + (size_t)jj * words : recs + (size_t)pidx(jj) * words; },
-      [&](int jj, int rl, float v) { part[(size_t)pidx(jj) * rows_max + r0 + rl] = v; });
-}
-
 // What one warp needs to issue the bulk copies of its units: the warp's unit
 // sequence is its shared-expert gate/up rows, then its routed gate/up rows,
 // then its down-row groups (shared expert first, then the routed slots).

@@ -191,6 +191,60 @@ moe_status moe_iq4nl_decode_routed(const moe_shape* shape, const uint16_t* route
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+moe_status moe_iq4nl_decode_layers(const moe_shape* shape, int32_t n_layers,
+                                   const moe_layer_weights* layers, const uint16_t* x,
+                                   int32_t T, int32_t chained, int32_t* ids, float* weights,
+                                   float* y, void* ws, size_t ws_bytes, uint32_t* status,
+                                   void* stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (n_layers < 1 || n_layers > MOE_MAX_LAYERS || !layers) return MOE_ERR_INVALID_ARG;
+  if (chained != 0 && chained != 1) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || T > MOE_MAX_DECODE_TOKENS) return MOE_ERR_INVALID_ARG;
+  for (int l = 0; l < n_layers; ++l) {
+    st = check_weights(shape, &layers[l].experts);
+    if (st != MOE_OK) return st;
+    if (!layers[l].router_w) return MOE_ERR_INVALID_ARG;
+    if (!aligned(layers[l].router_w, 16) ||
+        (layers[l].router_bias && !aligned(layers[l].router_bias, 4)))
+      return MOE_ERR_MISALIGNED;
+  }
+  if (T == 0) return MOE_OK;
+  if (!x || !ids || !weights || !y) return MOE_ERR_INVALID_ARG;
+  if (!ws) return MOE_ERR_WORKSPACE;
+  if (!aligned(x, 16) || !aligned(y, 16) || !aligned(ids, 4) || !aligned(weights, 4) ||
+      !aligned(ws, 256) || (status && !aligned(status, 4)))
+    return MOE_ERR_MISALIGNED;
+  const moe::DecodeLayout L = moe::decode_layout(*shape, T);
+  if (ws_bytes < (size_t)L.total) return MOE_ERR_WORKSPACE;
+  const int sms = num_sms();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  moe::DecodeParams p =
+      decode_params(shape, &layers[0].experts, x, T, ids, weights, y, ws, L, status);
+  p.route = 1;
+  p.ids_out = ids;
+  p.w_out = weights;
+  p.L = n_layers;
+  p.chained = chained;
+  p.tscores = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(ws) + L.tscores);
+  p.xc = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(ws) + L.xc);
+  p.scores = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + L.scores);
+  static_assert(sizeof(moe::LayerTable) <= 16 * 1024, "layer table fits the launch parameters");
+  moe::LayerTable lt;
+  std::memset(&lt, 0, sizeof(lt));
+  for (int l = 0; l < n_layers; ++l) {
+    const moe_expert_weights& e = layers[l].experts;
+    lt.layer[l] = moe::LayerPtrs{
+        reinterpret_cast<const uint8_t*>(e.gate),    reinterpret_cast<const uint8_t*>(e.up),
+        reinterpret_cast<const uint8_t*>(e.down),    reinterpret_cast<const uint8_t*>(e.sh_gate),
+        reinterpret_cast<const uint8_t*>(e.sh_up),   reinterpret_cast<const uint8_t*>(e.sh_down),
+        layers[l].router_w, layers[l].router_bias};
+  }
+  const cudaError_t e = moe::launch_decode_layers(p, lt, sms, g_pdl.load() != 0,
+                                                  reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 moe_status moe_iq4nl_prefill_grouped(const moe_shape* shape, const moe_expert_weights* w,
                                      const uint16_t* x, int32_t T, const int32_t* ids,
                                      const float* weights, float* y, void* ws,
@@ -267,6 +321,23 @@ int32_t moe_launches_per_call(const moe_shape* shape, int32_t T, int32_t call) {
     return call == 2 ? n + 1 : n;
   }
   if (call == 3) return moe::prefill_launches(*shape, T);
+  if (call >= 6) {                           // 4 + 2 * n_layers + chained
+    const int n_layers = (call - 4) / 2, chained = (call - 4) % 2;
+    if (n_layers < 1 || n_layers > MOE_MAX_LAYERS || T > MOE_MAX_DECODE_TOKENS)
+      return MOE_ERR_INVALID_ARG;
+    moe::DecodeParams p{};
+    p.H = shape->hidden;
+    p.F = shape->ffn;
+    p.Fs = shape->n_shared ? shape->ffn_shared : 0;
+    p.E = shape->n_experts;
+    p.k = shape->top_k;
+    p.n_shared = shape->n_shared;
+    p.T = T;
+    p.route = 1;
+    p.L = n_layers;
+    p.chained = chained;
+    return moe::layers_launches(p, sms);
+  }
   return MOE_ERR_INVALID_ARG;
 }
 

@@ -116,6 +116,10 @@ def test_static_call_allocates_no_device_memory():
 
 
 def test_static_refuses_a_layout_beyond_the_scratch():
+    # The C entry point itself refuses a shape whose decode workspace exceeds
+    # the fixed scratch, before it launches anything (called directly: the
+    # Python wrapper would already refuse these tensors as too small).
+    import ctypes
     moe = lib()
     L = layer_of(1)
     big = moe.make_shape(8192, 8192, 64, 16)
@@ -123,6 +127,11 @@ def test_static_refuses_a_layout_beyond_the_scratch():
     x = torch.zeros((16, 8192), dtype=torch.bfloat16, device=DEV)
     ids = torch.zeros((16, 16), dtype=torch.int32, device=DEV)
     w = torch.zeros((16, 16), dtype=torch.float32, device=DEV)
-    with pytest.raises(moe.MoeError) as e:
-        moe.iq4nl_decode_static(big, weights_of(L), x, ids, w)
-    assert e.value.status == moe.MOE_ERR_UNSUPPORTED
+    y = torch.zeros((16, 8192), dtype=torch.float32, device=DEV)
+    st = moe._lib.moe_iq4nl_decode_static(ctypes.byref(big), ctypes.byref(weights_of(L).c),
+                                          x.data_ptr(), 16, ids.data_ptr(), w.data_ptr(),
+                                          y.data_ptr(), None,
+                                          torch.cuda.current_stream().cuda_stream)
+    assert st == moe.MOE_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert bool(torch.all(y == 0))                    # nothing ran
