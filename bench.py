@@ -50,6 +50,10 @@ def parse():
     ap.add_argument("--same-tokens", action="store_true",
                     help="every token of a batch is token 0 (decode: the forced-overlap "
                          "variant, each expert of the union read once for all of them)")
+    ap.add_argument("--step", default="routed", choices=["routed", "layers", "chained"],
+                    help="decode step: routed = one moe_iq4nl_decode_routed call per layer; "
+                         "layers = one moe_iq4nl_decode_layers call for all layers (each its "
+                         "own input); chained = the same with layer l+1's input bf16(y_l)")
     ap.add_argument("--impl", default="libmoe", choices=["libmoe", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -372,7 +376,15 @@ def run_libmoe(args):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     layer_fn = moe.iq4nl_prefill_grouped if prefill else moe.iq4nl_decode
 
+    multi = (not prefill) and args.step in ("layers", "chained")
+    chained = args.step == "chained"
+    spec = [(wts[l], layers[l].router_w, layers[l].bias) for l in range(s.L)]
+
     def step(xin):
+        if multi:
+            moe.iq4nl_decode_layers(shape, spec, xin[0] if chained else xin, ws,
+                                    chained=chained, ids=ids, weights=w, y=y, status=status)
+            return
         for l in range(s.L):
             if prefill:
                 moe.route_topk(shape, layers[l].router_w, layers[l].bias, xin[l], ids[l], w[l])
@@ -384,6 +396,9 @@ def run_libmoe(args):
     if prefill:
         launches_per_layer = (moe.launches_per_call(shape, T, moe.CALL_ROUTE) +
                               moe.launches_per_call(shape, T, moe.CALL_PREFILL))
+    elif multi:
+        launches_per_layer = moe.launches_per_call(
+            shape, T, moe.call_decode_layers(s.L, chained)) / s.L
     else:
         launches_per_layer = moe.launches_per_call(shape, T, moe.CALL_DECODE_ROUTED)
 
@@ -497,26 +512,28 @@ def run_libmoe(args):
     e2e = None
     if not args.no_e2e:
         xin = torch.empty_like(xs[0])
+        xuse = xin[:1] if (multi and chained) else xin     # what a step reads
         g2 = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g2, stream=stream):
             step(xin)
-        host_x = [xs[i].cpu().pin_memory() for i in range(N_SETS)]
+        host_x = [(xs[i][:1] if (multi and chained) else xs[i]).cpu().pin_memory()
+                  for i in range(N_SETS)]
         host_y = torch.empty(y.shape, dtype=y.dtype).pin_memory()
         for i in range(args.warmup):
-            xin.copy_(host_x[i % N_SETS], non_blocking=True)
+            xuse.copy_(host_x[i % N_SETS], non_blocking=True)
             g2.replay()
             host_y.copy_(y, non_blocking=True)
         torch.cuda.synchronize()
         barrier()
         t0 = time.perf_counter()
         for i in range(args.steps):
-            xin.copy_(host_x[i % N_SETS], non_blocking=True)
+            xuse.copy_(host_x[i % N_SETS], non_blocking=True)
             g2.replay()
             host_y.copy_(y, non_blocking=True)
         torch.cuda.synchronize()
         dt = max_over_ranks((time.perf_counter() - t0) / args.steps, dist, dev)
         e2e = {"value": whole_job_rate(T, world, dt), "unit": UNIT,
-               "h2d_bytes_per_step": int(xin.numel() * xin.element_size()),
+               "h2d_bytes_per_step": int(xuse.numel() * xuse.element_size()),
                "d2h_bytes_per_step": int(y.numel() * y.element_size())}
 
     cpu = None
@@ -529,7 +546,14 @@ def run_libmoe(args):
     # launch duration is the timed step over its L launches; otherwise the
     # layer call timed on its own
     fused = (not prefill) and launches_per_layer == 1
-    if fused:
+    if multi and launches_per_layer * s.L == 1:
+        kernel = ("decode_layers_kernel (route + experts + combine of all "
+                  f"{s.L} layers, one launch per step{', chained' if chained else ''})")
+        launch_ms = ms
+        unit_bytes = bytes_per_step
+        achieved = unit_bytes / (launch_ms * 1e-3) / 1e9
+        prof = None
+    elif fused:
         kernel = "decode_fused_kernel (route + experts + combine, one launch per layer)"
         launch_ms = ms / s.L
         unit_bytes = bytes_per_step / s.L
@@ -575,10 +599,12 @@ def run_libmoe(args):
                           "avg_call_ms": layer_ms, "algorithmic_flops_per_call": flops_layer}),
             "layer_call_ms": layer_call_ms, "route_call_ms": route_ms,
             "step_call": "moe_iq4nl_prefill_grouped after moe_route_topk" if prefill else
-                         "moe_iq4nl_decode_routed (route + layer in one call)",
+                         (f"moe_iq4nl_decode_layers ({'chained' if chained else 'own inputs'},"
+                          " all layers in one call)" if multi else
+                          "moe_iq4nl_decode_routed (route + layer in one call)"),
             "launches_per_layer": launches_per_layer,
             "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
-            "gpu_launches": args.steps * s.L * launches_per_layer,
+            "gpu_launches": int(round(args.steps * s.L * launches_per_layer)),
             "status_word": st,
         }
         print(json.dumps(line), flush=True)
