@@ -18,7 +18,9 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_build", "libmoe.so")
+# MOE_LIBRARY may name another build of libmoe (the phase-stamp profiling
+# build, _build_profile/libmoe.so); there is no other implementation.
+LIB_PATH = os.environ.get("MOE_LIBRARY") or os.path.join(_HERE, "_build", "libmoe.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(

@@ -43,15 +43,22 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), profile: bool = False) -> str:
+    """Compile every csrc/*.cu and link _build/libmoe.so. profile=True builds the
+    phase-stamp variant (-DMOE_PROFILE, exporting moe_profile_stamps) into
+    _build_profile/libmoe.so instead; the product library never has it."""
+    build_dir = os.path.join(HERE, "_build_profile") if profile else BUILD
+    lib = os.path.join(build_dir, "libmoe.so")
+    if profile:
+        extra_flags = tuple(extra_flags) + ("-DMOE_PROFILE",)
+    os.makedirs(build_dir, exist_ok=True)
     deps = _deps()
-    if not force and not _stale(LIB, deps):
-        return LIB
+    if not force and not _stale(lib, deps):
+        return lib
     objs = []
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc(), *FLAGS, *extra_flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -63,16 +70,17 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     srcs = _sources()
     with concurrent.futures.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     import sys
     print(build(force="--force" in sys.argv, verbose=True,
-                extra_flags=["-Xptxas", "-v"] if "--ptxas" in sys.argv else []))
+                extra_flags=["-Xptxas", "-v"] if "--ptxas" in sys.argv else [],
+                profile="--profile" in sys.argv))

@@ -34,6 +34,23 @@
 
 namespace moe {
 
+// Phase stamps (builds with MOE_PROFILE only): thread 0 of each CTA records
+// %globaltimer at each phase boundary of the first kProfLayers layers, read
+// back with moe_profile_stamps. The product build has none of this.
+#ifdef MOE_PROFILE
+constexpr int kProfCtas = 256, kProfLayers = 64, kProfPhases = 12;
+__device__ uint64_t g_prof[kProfCtas * kProfLayers * kProfPhases];
+#define MOE_STAMP(l, ph)                                                                     \
+  do {                                                                                       \
+    if (threadIdx.x == 0 && (l) < kProfLayers && blockIdx.x < kProfCtas)                      \
+      g_prof[((size_t)blockIdx.x * kProfLayers + (l)) * kProfPhases + (ph)] = global_timer_ns(); \
+  } while (0)
+#else
+#define MOE_STAMP(l, ph) \
+  do {                   \
+  } while (0)
+#endif
+
 constexpr int kLW = 16;            // warps per CTA
 constexpr int kLT = kLW * 32;      // threads per CTA
 constexpr int kLSlots = 2;         // bulk-copy slots per warp
@@ -392,6 +409,7 @@ __global__ void __launch_bounds__(kLT, 1)
   for (int l = 0; l < Lyr; ++l) {
     const LayerPtrs& W = lt.layer[l];
     float* yl = p.y + (size_t)l * T * H;
+    MOE_STAMP(l, 0);
     // the next layer's router rows and shared down rows of this CTA into L2,
     // while this layer waits on its exchanges
     if (threadIdx.x == 0 && l + 1 < Lyr) {
@@ -409,12 +427,14 @@ __global__ void __launch_bounds__(kLT, 1)
       __syncthreads();
       if (*gave_up) wait_ns = 0;
     }
+    MOE_STAMP(l, 1);
     if (p.chained && l > 0)
       load_x_layer<true>(nullptr, p.y + (size_t)(l - 1) * T * H, T, H, rx, xq, xq_words);
     else
       load_x_layer<false>(p.x + (p.chained ? (size_t)0 : (size_t)l * T * H), nullptr, T, H, rx,
                           xq, xq_words);
     __syncthreads();
+    MOE_STAMP(l, 2);
 
     // ---- scores of this CTA's experts: 16 chunks of H per expert, one warp
     // per (expert, chunk), chunk partials summed in a fixed order
@@ -470,6 +490,7 @@ __global__ void __launch_bounds__(kLT, 1)
       }
     }
     __syncthreads();
+    MOE_STAMP(l, 3);
 
     // ---- top-k: warp t takes token t, in every CTA
     if (warp < T) {
@@ -494,6 +515,7 @@ __global__ void __launch_bounds__(kLT, 1)
       if (warp == 0) build_route_table_warp(rt, rids, rw, T * k, E);
     }
     __syncthreads();
+    MOE_STAMP(l, 4);
     if (*gave_up) wait_ns = 0;
 #pragma unroll 1
     for (int i = threadIdx.x; i < (T * k + (p.n_shared ? T : 0)) * rows_max; i += kLT)
@@ -538,11 +560,13 @@ __global__ void __launch_bounds__(kLT, 1)
 
     // ---- h of this layer: every CTA's rows written
     __syncthreads();
+    MOE_STAMP(l, 5);
     if (threadIdx.x == 0) {
       grid_arrive(&p.sync[kSyncH]);
       grid_wait(&p.sync[kSyncH], (uint32_t)(G * (l + 1)), wait_ns, p.status, gave_up);
     }
     __syncthreads();
+    MOE_STAMP(l, 6);
     if (*gave_up) wait_ns = 0;
     if (S.stage_bytes) {
       float* stage = reinterpret_cast<float*>(smem + S.stage);
@@ -567,6 +591,7 @@ __global__ void __launch_bounds__(kLT, 1)
       quant_h<false>(p, rt, nullptr, recs, threadIdx.x, kLT);
     }
     __syncthreads();
+    MOE_STAMP(l, 7);
 
     // ---- down
 #pragma unroll 1
@@ -589,6 +614,7 @@ __global__ void __launch_bounds__(kLT, 1)
       issue_upto(limit);
     }
     __syncthreads();
+    MOE_STAMP(l, 8);
 
     // ---- combine in the fixed order: shared expert, then routed experts ascending
 #pragma unroll 1
@@ -604,6 +630,7 @@ __global__ void __launch_bounds__(kLT, 1)
       yl[(size_t)t * H + dn.a + r] = acc;
     }
     __syncthreads();
+    MOE_STAMP(l, 9);
     if (threadIdx.x == 0) grid_arrive(&p.sync[kSyncY]);
     // the records and partials are read: the next layer's router rows may
     // land over them (from L2, prefetched above)
@@ -796,3 +823,12 @@ cudaError_t launch_decode_layers(const DecodeParams& p0, const LayerTable& lt, i
 }
 
 }  // namespace moe
+
+#ifdef MOE_PROFILE
+// Copies the phase stamps (uint64 [256 CTAs][64 layers][12 phases], ns of
+// %globaltimer) to host memory. Profiling builds only.
+extern "C" int moe_profile_stamps(void* host, size_t bytes) {
+  const size_t n = sizeof(moe::g_prof) < bytes ? sizeof(moe::g_prof) : bytes;
+  return cudaMemcpyFromSymbol(host, moe::g_prof, n) == cudaSuccess ? 0 : -1;
+}
+#endif
