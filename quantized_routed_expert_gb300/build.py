@@ -47,7 +47,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=(), profile: b
     """Compile every csrc/*.cu and link _build/libmoe.so. profile=True builds the
     phase-stamp variant (-DMOE_PROFILE, exporting moe_profile_stamps) into
     _build_profile/libmoe.so instead; the product library never has it."""
-    build_dir = os.path.join(HERE, "_build_profile") if profile else BUILD
+    build_dir = os.path.join(HERE, "_build_profile" + os.environ.get("MOE_PROFILE_TAG", "")) \
+        if profile else BUILD
     lib = os.path.join(build_dir, "libmoe.so")
     if profile:
         extra_flags = tuple(extra_flags) + ("-DMOE_PROFILE",)

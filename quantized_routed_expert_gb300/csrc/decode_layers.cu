@@ -40,6 +40,16 @@ namespace moe {
 #ifdef MOE_PROFILE
 constexpr int kProfCtas = 256, kProfLayers = 64, kProfPhases = 12;
 __device__ uint64_t g_prof[kProfCtas * kProfLayers * kProfPhases];
+// per warp: [0] routed gate/up first unit landed, [1] routed gate/up done,
+// [2] down unit landed, [3] down done, [4] top-k saw every score (warp 0)
+constexpr int kProfW = 8;
+__device__ uint64_t g_profw[kProfCtas * kProfLayers * 16 * kProfW];
+#define MOE_WSTAMP(l, k)                                                                      \
+  do {                                                                                        \
+    if ((threadIdx.x & 31) == 0 && (l) < kProfLayers && blockIdx.x < kProfCtas)              \
+      g_profw[(((size_t)blockIdx.x * kProfLayers + (l)) * 16 + (threadIdx.x >> 5)) * kProfW + \
+              (k)] = global_timer_ns();                                                       \
+  } while (0)
 #define MOE_STAMP(l, ph)                                                                     \
   do {                                                                                       \
     if (threadIdx.x == 0 && (l) < kProfLayers && blockIdx.x < kProfCtas)                      \
@@ -47,6 +57,9 @@ __device__ uint64_t g_prof[kProfCtas * kProfLayers * kProfPhases];
   } while (0)
 #else
 #define MOE_STAMP(l, ph) \
+  do {                   \
+  } while (0)
+#define MOE_WSTAMP(l, k) \
   do {                   \
   } while (0)
 #endif
@@ -140,7 +153,7 @@ struct LUnitPlan {
   size_t slot_bytes;
   uint64_t* mybar;
   uint64_t pol;
-  int warp, layer, ub, n_sh, n_rt, rr_a, n_dn, sh_a, ngroups, nrows_cta, dn_a, rg;
+  int warp, layer, ub, n_sh, n_rt, rr_a, n_dn, sh_a, sh_w, sh_nw, ngroups, nrows_cta, dn_a, rg;
 };
 
 // Issue unit j of a warp's sequence into slot j % kLSlots (one lane calls).
@@ -160,7 +173,7 @@ __device__ __noinline__ void issue_unit_layers(const DecodeParams& p, const Laye
   if (lj < u.n_sh + u.n_rt) {
     const uint8_t *g, *up;
     if (lj < u.n_sh) {
-      const size_t f = (size_t)(u.sh_a + u.warp + kLW * lj);
+      const size_t f = (size_t)(u.sh_a + u.sh_w + u.sh_nw * lj);
       g = W.sh_gate + f * rbH;
       up = W.sh_up + f * rbH;
     } else {
@@ -189,10 +202,11 @@ __device__ __noinline__ void issue_unit_layers(const DecodeParams& p, const Laye
   }
 }
 
-// Raise a grid counter (thread 0, after the CTA's writes).
+// Raise a grid counter (thread 0, after a CTA barrier that follows the CTA's
+// writes): a release fence at GPU scope, then a relaxed add.
 __device__ __forceinline__ void grid_arrive(uint32_t* ctr) {
-  __threadfence();
-  atomicAdd(ctr, 1u);
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
 }
 // Wait (thread 0) until a grid counter reaches target, for at most wait_ns;
 // a timeout is recorded in *status and in the CTA's flag *gave_up.
@@ -205,9 +219,8 @@ __device__ __forceinline__ void grid_wait(const uint32_t* ctr, uint32_t target, 
       *gave_up = 1u;
       break;
     }
-    __nanosleep(64);
+    __nanosleep(32);
   }
-  __threadfence();
 }
 
 // A token's activations (bf16 from the caller, or fp32 y of the previous
@@ -289,6 +302,8 @@ __device__ __forceinline__ void layer_topk(const uint64_t* sc, uint32_t want, in
       }
       break;
     }
+    // every CTA polls the same few lines: back off between rounds
+    __nanosleep(100);
   }
   float kv[NPL];
 #pragma unroll
@@ -351,7 +366,11 @@ __global__ void __launch_bounds__(kLT, 1)
   const int nrows_cta = dn.b - dn.a;
   const int ngroups = (nrows_cta + RG - 1) / RG;
   auto count = [&](int a, int b) { return a + warp < b ? (b - a - warp + kLW - 1) / kLW : 0; };
-  const int n_sh = count(shr.a, shr.b);
+  // The shared expert's rows go to the warps that do not take a token's
+  // top-k (warps T..15): they compute them while the scores are exchanged.
+  const int sh_w = warp - T, sh_nw = kLW - T;
+  const int n_sh = (sh_w >= 0 && shr.a + sh_w < shr.b) ? (shr.b - shr.a - sh_w + sh_nw - 1) / sh_nw
+                                                      : 0;
   const int re0 = lr_e0(E, cta, G), re1 = lr_e0(E, cta + 1, G);
   const int ne = re1 - re0;
   const uint64_t pol = l2_evict_first_policy();
@@ -367,6 +386,8 @@ __global__ void __launch_bounds__(kLT, 1)
   up.n_sh = n_sh;
   up.n_rt = up.rr_a = up.n_dn = 0;
   up.sh_a = shr.a;
+  up.sh_w = sh_w;
+  up.sh_nw = sh_nw;
   up.ngroups = ngroups;
   up.nrows_cta = nrows_cta;
   up.dn_a = dn.a;
@@ -492,7 +513,21 @@ __global__ void __launch_bounds__(kLT, 1)
     __syncthreads();
     MOE_STAMP(l, 3);
 
-    // ---- top-k: warp t takes token t, in every CTA
+    // ---- top-k: warp t takes token t, in every CTA; meanwhile the other
+    // warps compute the shared expert's rows (known before the routes)
+    if (warp >= T) {
+#pragma unroll 1
+      for (int j = up.ub; ok && j < up.ub + n_sh; ++j) {
+        ok = wait_unit(j);
+        if (!ok) break;
+        const uint8_t* d = up.myslots + (size_t)(j % kLSlots) * S.slot_bytes;
+        const int f = shr.a + sh_w + sh_nw * (j - up.ub);
+        gateup_unit_t<1, LPR>(p, rt, d, d + rbH, -1, f, xq, xq_words);
+        __syncwarp();
+        ++consumed;
+        issue_upto(up.ub + n_sh);
+      }
+    }
     if (warp < T) {
       int id;
       float wv;
@@ -503,6 +538,7 @@ __global__ void __launch_bounds__(kLT, 1)
         layer_topk<2>(sc, want, E, k, W.bias, prob, id, wv, wait_ns, p.status, gave_up);
       else
         layer_topk<16>(sc, want, E, k, W.bias, prob, id, wv, wait_ns, p.status, gave_up);
+      MOE_WSTAMP(l, 4);
       if (lane < k) {
         rids[warp * k + lane] = id;
         rw[warp * k + lane] = wv;
@@ -532,24 +568,18 @@ __global__ void __launch_bounds__(kLT, 1)
     const int limit = ub + n_tot + (l + 1 < Lyr ? n_sh : 0);
     issue_upto(limit);
 
-    // ---- gate/up: the shared expert's rows (landed long ago), then the
-    // routed rows as they arrive
+    // ---- gate/up: the routed rows as they arrive (the shared expert's were
+    // computed above)
 #pragma unroll 1
-    for (int j = ub; ok && j < ub + n_sh + n_rt; ++j) {
+    for (int j = ub + n_sh; ok && j < ub + n_sh + n_rt; ++j) {
       ok = wait_unit(j);
       if (!ok) break;
+      if (j == ub + n_sh) MOE_WSTAMP(l, 0);
       const uint8_t* d = up.myslots + (size_t)(j % kLSlots) * S.slot_bytes;
       const int lj = j - ub;
-      int sl, f;
-      if (lj < n_sh) {
-        sl = -1;
-        f = shr.a + warp + kLW * lj;
-      } else {
-        const int r = rr_a + warp + kLW * (lj - n_sh);
-        sl = r / p.F;
-        f = r - sl * p.F;
-      }
-      if (MAXT == 1 || (sl < 0 ? T : rt.slot_off[sl + 1] - rt.slot_off[sl]) == 1)
+      const int r = rr_a + warp + kLW * (lj - n_sh);
+      const int sl = r / p.F, f = r - sl * p.F;
+      if (MAXT == 1 || rt.slot_off[sl + 1] - rt.slot_off[sl] == 1)
         gateup_unit_t<1, LPR>(p, rt, d, d + rbH, sl, f, xq, xq_words);
       else
         gateup_unit_t<MAXT, LPR>(p, rt, d, d + rbH, sl, f, xq, xq_words);
@@ -558,6 +588,7 @@ __global__ void __launch_bounds__(kLT, 1)
       issue_upto(limit);
     }
 
+    MOE_WSTAMP(l, 1);
     // ---- h of this layer: every CTA's rows written
     __syncthreads();
     MOE_STAMP(l, 5);
@@ -598,6 +629,7 @@ __global__ void __launch_bounds__(kLT, 1)
     for (int j = ub + n_sh + n_rt; ok && j < ub + n_tot; ++j) {
       ok = wait_unit(j);
       if (!ok) break;
+      if (j == ub + n_sh + n_rt) MOE_WSTAMP(l, 2);
       const uint8_t* d = up.myslots + (size_t)(j % kLSlots) * S.slot_bytes;
       const int u = warp + kLW * (j - ub - n_sh - n_rt);
       const int su = u / ngroups, gi = u - su * ngroups;
@@ -613,6 +645,7 @@ __global__ void __launch_bounds__(kLT, 1)
       ++consumed;
       issue_upto(limit);
     }
+    MOE_WSTAMP(l, 3);
     __syncthreads();
     MOE_STAMP(l, 8);
 
@@ -738,10 +771,14 @@ bool layers_supported(const DecodeParams& p, int num_sms, size_t* smem, int* rg,
   if (budget < 4608) budget = 4608;
   const int slots = (p.T * p.k < p.E ? p.T * p.k : p.E) + p.n_shared;
   auto units = [&](int rows) { return slots * ((rmax + rows - 1) / rows); };
+  // down rows per unit: one pass of a warp, grown (in whole passes, while a
+  // unit fits in max(a gate/up unit, 4608 bytes)) until each warp has at most
+  // one down unit: a warp fetches its down rows while it finishes gate/up, so
+  // a second unit would be fetched only after the h barrier
   int r = rpw < rmax ? rpw : rmax;
-  if (units(r) > 2 * kLW) {
-    while (r + rpw <= rmax && (r + rpw) * rbK <= budget) r += rpw;
-    if (rmax * rbK <= budget) r = rmax;
+  if (units(r) > kLW) {
+    while (r + rpw <= rmax && (r + rpw) * rbK <= budget && units(r) > kLW) r += rpw;
+    if (units(r) > kLW && rmax * rbK <= budget) r = rmax;
   }
   const LayersSmem m = layers_smem(p.H, p.F, p.Fs, p.n_shared, p.T, p.k, rmax, r, p.E, grid);
   if (m.total > 227 * 1024) return false;
@@ -830,5 +867,10 @@ cudaError_t launch_decode_layers(const DecodeParams& p0, const LayerTable& lt, i
 extern "C" int moe_profile_stamps(void* host, size_t bytes) {
   const size_t n = sizeof(moe::g_prof) < bytes ? sizeof(moe::g_prof) : bytes;
   return cudaMemcpyFromSymbol(host, moe::g_prof, n) == cudaSuccess ? 0 : -1;
+}
+// Per-warp stamps (uint64 [256][64][16 warps][8]).
+extern "C" int moe_profile_warp_stamps(void* host, size_t bytes) {
+  const size_t n = sizeof(moe::g_profw) < bytes ? sizeof(moe::g_profw) : bytes;
+  return cudaMemcpyFromSymbol(host, moe::g_profw, n) == cudaSuccess ? 0 : -1;
 }
 #endif
