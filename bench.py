@@ -43,14 +43,17 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=1,
+    ap.add_argument("--config", type=int, default=None,
                     help="workload: 1 Xing decode (default), 2 Qwen3-Next paired decode, "
                          "3 DeepSeek-like wide decode, 4 Xing prefill chunk")
     ap.add_argument("--tokens", type=int, default=None, help="decode batch (config 3: 1/4/16)")
     ap.add_argument("--same-tokens", action="store_true",
                     help="every token of a batch is token 0 (decode: the forced-overlap "
                          "variant, each expert of the union read once for all of them)")
-    ap.add_argument("--step", default="routed", choices=["routed", "layers", "chained"],
+    ap.add_argument("--no-workloads", dest="workloads", action="store_false",
+                    help="skip the other configurations' block (measured after the headline "
+                         "when no --config is given)")
+    ap.add_argument("--step", default="layers", choices=["routed", "layers", "chained"],
                     help="decode step: routed = one moe_iq4nl_decode_routed call per layer; "
                          "layers = one moe_iq4nl_decode_layers call for all layers (each its "
                          "own input); chained = the same with layer l+1's input bf16(y_l)")
@@ -62,7 +65,13 @@ def parse():
     ap.add_argument("--experts", type=int, default=None,
                     help="keep only N routed experts per layer, same sizes otherwise (small "
                          "profiling cases)")
-    return ap.parse_args()
+    a = ap.parse_args()
+    # the other configurations are measured only on a default (headline) run
+    a.workloads = a.workloads and a.config is None and a.layers is None and a.experts is None \
+        and a.tokens is None and not a.same_tokens
+    if a.config is None:
+        a.config = 1
+    return a
 
 
 def peaks():
@@ -113,15 +122,13 @@ def whole_job_rate(units_per_rank: int, world: int, seconds: float) -> float:
 
 # ---------------------------------------------------------------- ncu traffic
 
-PROFILE_DECODE_FUSED = "decode_fused_xing_decode.md"
+# ncu figures of a kernel, kept machine-readable next to their summaries:
+# profiles/<name>.json with "sources_digest", "tokens", "layers" and
+# "dram_bytes_per_launch" (read + write DRAM bytes of one launch).
+PROFILE_DECODE_FUSED = "decode_fused_xing_decode.json"
+PROFILE_DECODE_LAYERS = "decode_layers_xing_decode.json"
 
-
-# What the fused decode kernel is built and launched from: its translation
-# unit (the .cu and every header it includes), the host code that chooses and
-# launches it, and the compiler flags. Changing any of these voids its counters;
-# the prefill, router and utility kernels are other translation units.
-FUSED_DECODE_SOURCES = (
-    "quantized_routed_expert_gb300/csrc/decode_fused.cu",
+_DECODE_COMMON = (
     "quantized_routed_expert_gb300/csrc/decode_common.cuh",
     "quantized_routed_expert_gb300/csrc/decode.cuh",
     "quantized_routed_expert_gb300/csrc/common.cuh",
@@ -133,6 +140,11 @@ FUSED_DECODE_SOURCES = (
     "include/moe.h",
     "quantized_routed_expert_gb300/build.py",
 )
+# What each decode kernel is built and launched from: its translation unit (the
+# .cu and every header it includes), the host code that chooses and launches it,
+# and the compiler flags. Changing any of these voids its counters.
+FUSED_DECODE_SOURCES = ("quantized_routed_expert_gb300/csrc/decode_fused.cu",) + _DECODE_COMMON
+LAYERS_DECODE_SOURCES = ("quantized_routed_expert_gb300/csrc/decode_layers.cu",) + _DECODE_COMMON
 
 
 def sources_digest(files=FUSED_DECODE_SOURCES) -> str:
@@ -147,26 +159,20 @@ def sources_digest(files=FUSED_DECODE_SOURCES) -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(name: str, T: int):
-    """DRAM bytes per launch recorded in profiles/<name> ("key: value" lines),
-    if they were taken on these kernel sources and this token count."""
-    import re
+def profiled_traffic(name: str, T: int, files=FUSED_DECODE_SOURCES, layers=None):
+    """DRAM bytes per launch recorded in profiles/<name>, if they were taken on
+    these kernel sources, this token count (and layer count, when given)."""
     path = os.path.join(ROOT, "profiles", name)
-    d = {}
     try:
         with open(path) as f:
-            for ln in f:
-                m = re.match(r"^([a-z_]+): (\S+)\s*$", ln)
-                if m and m.group(1) not in d:
-                    d[m.group(1)] = m.group(2)
-    except OSError:
-        return None
-    try:
-        if d.get("sources_digest") != sources_digest() or int(d.get("tokens", -1)) != T:
+            d = json.load(f)
+        if d.get("sources_digest") != sources_digest(files) or int(d.get("tokens", -1)) != T:
+            return None
+        if layers is not None and int(d.get("layers", -1)) != layers:
             return None
         return {"dram_bytes_per_launch": float(d["dram_bytes_per_launch"]),
                 "source": f"profiles/{name}"}
-    except (KeyError, ValueError):
+    except (OSError, KeyError, ValueError, TypeError):
         return None
 
 
@@ -353,6 +359,58 @@ def run_libmoe(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    ctx = (world, rank, local, dist, dev)
+    line = measure(args, ctx)
+    if line is not None and world == 1 and args.workloads:
+        line["workloads"] = other_workloads(args, ctx)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+# The other configurations, measured in the same process after the headline,
+# with the same timing code (no e2e and no CPU baseline for these).
+OTHER_WORKLOADS = (
+    {"config": 2, "tokens": None, "step": "layers", "steps": 10, "warmup": 3},
+    {"config": 2, "tokens": None, "step": "chained", "steps": 10, "warmup": 3},
+    {"config": 3, "tokens": 1, "step": "layers", "steps": 10, "warmup": 3},
+    {"config": 3, "tokens": 4, "step": "routed", "steps": 10, "warmup": 3},
+    {"config": 3, "tokens": 16, "step": "routed", "steps": 10, "warmup": 3},
+    {"config": 4, "tokens": None, "step": "routed", "steps": 10, "warmup": 3},
+)
+
+
+def other_workloads(args, ctx):
+    import copy
+    import torch
+    out = []
+    for w in OTHER_WORKLOADS:
+        a = copy.copy(args)
+        a.config, a.tokens, a.step = w["config"], w["tokens"], w["step"]
+        a.steps, a.warmup = w["steps"], w["warmup"]
+        a.no_e2e, a.no_cpu_baseline, a.same_tokens = True, True, False
+        a.layers, a.experts = None, None
+        r = measure(a, ctx)
+        torch.cuda.empty_cache()
+        rf = r["roofline"]
+        out.append({"workload": r["config"]["workload"], "tokens_per_step": r["config"]["tokens_per_step"],
+                    "layers": r["config"]["layers"], "step_call": r["step_call"],
+                    "steps": a.steps, "warmup": a.warmup,
+                    "ms_per_step": r["ms_per_step"], "step_ms": r["step_ms"],
+                    "value": r["value"], "unit": UNIT,
+                    "roofline": {k: rf[k] for k in ("bound", "achieved", "peak", "unit", "frac",
+                                                    "kernel")},
+                    "clocks": r["clocks"], "gpu_launches": r["gpu_launches"],
+                    "status_word": r["status_word"]})
+    return out
+
+
+def measure(args, ctx):
+    """One workload: build it, time it, return the bench line (rank 0) or None."""
+    import torch
+    world, rank, local, dist, dev = ctx
 
     import quantized_routed_expert_gb300 as moe
     import synth
@@ -451,7 +509,15 @@ def run_libmoe(args):
     barrier()
     torch.cuda.synchronize()
     clocks.start()
-    time.sleep(0.3)
+    # keep the GPU under the same load for about half a second before the timed
+    # region (untimed replays), so the clock samples show the clocks under load
+    t_load = time.perf_counter()
+    i_load = 0
+    while time.perf_counter() - t_load < 0.5:
+        for _ in range(8):
+            graphs[i_load % N_SETS].replay()
+            i_load += 1
+        torch.cuda.synchronize()
     # one event between consecutive steps: the first and last bracket the
     # timed region, the others give the per-step spread
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
@@ -552,7 +618,8 @@ def run_libmoe(args):
         launch_ms = ms
         unit_bytes = bytes_per_step
         achieved = unit_bytes / (launch_ms * 1e-3) / 1e9
-        prof = None
+        prof = (profiled_traffic(PROFILE_DECODE_LAYERS, T, LAYERS_DECODE_SOURCES, s.L)
+                if not chained else None)
     elif fused:
         kernel = "decode_fused_kernel (route + experts + combine, one launch per layer)"
         launch_ms = ms / s.L
@@ -607,10 +674,8 @@ def run_libmoe(args):
             "gpu_launches": int(round(args.steps * s.L * launches_per_layer)),
             "status_word": st,
         }
-        print(json.dumps(line), flush=True)
-    if dist is not None:
-        dist.destroy_process_group()
-    return 0
+        return line
+    return None
 
 
 def main():

@@ -1,23 +1,27 @@
 """Host-side bookkeeping of bench.py that needs no GPU: which committed ncu
 counters the bench line may quote, and how it reads them."""
+import json
 import os
+import re
 import shutil
+
+import pytest
 
 import bench
 
+KERNELS = [(bench.FUSED_DECODE_SOURCES, ["decode_fused.cu", "decode.cu", "moe_api.cu"]),
+           (bench.LAYERS_DECODE_SOURCES, ["decode_layers.cu", "decode.cu", "moe_api.cu"])]
 
-def test_fused_kernel_sources_exist():
-    for rel in bench.FUSED_DECODE_SOURCES:
+
+@pytest.mark.parametrize("files,roots", KERNELS)
+def test_kernel_sources_exist_and_cover_their_includes(files, roots):
+    # every project header the kernel's translation unit pulls in, and every
+    # header of the host files that launch it, is part of the digest
+    for rel in files:
         assert os.path.isfile(os.path.join(bench.ROOT, rel)), rel
-
-
-def test_fused_kernel_sources_cover_its_includes():
-    # every project header the fused kernel's translation unit pulls in, and
-    # every header of the host file that launches it, is part of the digest
-    import re
     csrc = os.path.join(bench.ROOT, "quantized_routed_expert_gb300", "csrc")
-    listed = {os.path.basename(p) for p in bench.FUSED_DECODE_SOURCES}
-    todo, seen = ["decode_fused.cu", "decode.cu", "moe_api.cu"], set()
+    listed = {os.path.basename(p) for p in files}
+    todo, seen = list(roots), set()
     while todo:
         f = todo.pop()
         if f in seen:
@@ -32,24 +36,35 @@ def test_fused_kernel_sources_cover_its_includes():
     assert seen <= listed, seen - listed
 
 
+def test_committed_profiles_are_machine_readable():
+    for name in (bench.PROFILE_DECODE_FUSED, bench.PROFILE_DECODE_LAYERS):
+        path = os.path.join(bench.ROOT, "profiles", name)
+        if not os.path.exists(path):
+            continue
+        with open(path) as f:
+            d = json.load(f)
+        for key in ("kernel", "tokens", "sources_digest", "dram_bytes_per_launch"):
+            assert key in d, (name, key)
+
+
 def test_traffic_is_quoted_only_for_the_profiled_sources(tmp_path, monkeypatch):
-    prof = os.path.join(bench.ROOT, "profiles", bench.PROFILE_DECODE_FUSED)
-    got = bench.profiled_traffic(bench.PROFILE_DECODE_FUSED, 1)
-    with open(prof) as f:
-        head = dict(ln.split(": ", 1) for ln in f.read().splitlines()[:4] if ": " in ln)
-    if head.get("sources_digest") == bench.sources_digest():
-        assert got is not None and got["dram_bytes_per_launch"] == float(head["dram_bytes_per_launch"])
-    else:
-        assert got is None
-    # another token count, or sources edited since the capture: no figure
-    assert bench.profiled_traffic(bench.PROFILE_DECODE_FUSED, 2) is None
     root = tmp_path / "repo"
-    for rel in bench.FUSED_DECODE_SOURCES + ("profiles/" + bench.PROFILE_DECODE_FUSED,):
+    files = bench.LAYERS_DECODE_SOURCES
+    for rel in files:
         dst = root / rel
         dst.parent.mkdir(parents=True, exist_ok=True)
         shutil.copy(os.path.join(bench.ROOT, rel), dst)
     monkeypatch.setattr(bench, "ROOT", str(root))
-    assert bench.sources_digest() == head.get("sources_digest") or got is None
-    with open(root / bench.FUSED_DECODE_SOURCES[0], "a") as f:
+    (root / "profiles").mkdir()
+    rec = {"kernel": "k", "tokens": 1, "layers": 38, "sources_digest": bench.sources_digest(files),
+           "dram_bytes_per_launch": 123.0}
+    (root / "profiles" / "p.json").write_text(json.dumps(rec))
+    got = bench.profiled_traffic("p.json", 1, files, 38)
+    assert got == {"dram_bytes_per_launch": 123.0, "source": "profiles/p.json"}
+    # another token count, another layer count, or sources edited since the capture
+    assert bench.profiled_traffic("p.json", 2, files, 38) is None
+    assert bench.profiled_traffic("p.json", 1, files, 4) is None
+    assert bench.profiled_traffic("missing.json", 1, files) is None
+    with open(root / files[0], "a") as f:
         f.write("\n// edited\n")
-    assert bench.profiled_traffic(bench.PROFILE_DECODE_FUSED, 1) is None
+    assert bench.profiled_traffic("p.json", 1, files, 38) is None

@@ -90,7 +90,9 @@ def _check_chained(Ls, x0, ids, w, y, what):
         x_l = synth.to_bf16_bits(y[l])          # round to nearest even, as the kernel
 
 
-@pytest.mark.parametrize("cfg,T,n", [(1, 1, 4), (2, 2, 3), (0, 4, 3)])
+# Xing, 1 and 2 tokens: T * E <= 128, so the layers exchange partial router
+# scores; Qwen3-Next (512 experts): the y barrier and the score exchange.
+@pytest.mark.parametrize("cfg,T,n", [(1, 1, 4), (1, 2, 3), (2, 2, 3), (0, 4, 3)])
 def test_layers_chained_layer_by_layer(cfg, T, n):
     from synth.layers import bf16_tensor
     moe = lib()
@@ -140,26 +142,30 @@ def test_layers_launch_per_layer_path(chained):
             check_close(y[l], oracle_layer(L, xs[l], ids[l], w[l]), f"per-layer {l}")
 
 
-def test_layers_barrier_timeout_is_reported_and_recovers():
+@pytest.mark.parametrize("chained", [False, True])
+def test_layers_barrier_timeout_is_reported_and_recovers(chained):
+    # every grid-wide wait of the kernel (score tags, h counter, y counter,
+    # partial-score flags) gives up at once with the limit at 0
     from synth.layers import bf16_tensor
     moe = lib()
     Ls = layers_of(1, 3)
     shape = moe_shape(Ls[0].shape)
     xs = bf16_tensor(np.stack([gapped_rows(L, 1) for L in Ls]), DEV)
+    xin = xs[0] if chained else xs
     ws = moe.workspace(shape, 1, moe.DECODE, DEV)
-    _, _, y0 = moe.iq4nl_decode_layers(shape, spec(Ls), xs, ws)
+    _, _, y0 = moe.iq4nl_decode_layers(shape, spec(Ls), xin, ws, chained=chained)
     torch.cuda.synchronize()
     y0 = y0.cpu().numpy()
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     old = moe.set_barrier_wait_ns(0)
     try:
-        moe.iq4nl_decode_layers(shape, spec(Ls), xs, ws, status=status)
+        moe.iq4nl_decode_layers(shape, spec(Ls), xin, ws, chained=chained, status=status)
         torch.cuda.synchronize()
     finally:
         moe.set_barrier_wait_ns(old)
     assert int(status.item()) & 0xFFFFFFFF & moe.STATUS_TIMEOUT
     status.zero_()
-    _, _, y1 = moe.iq4nl_decode_layers(shape, spec(Ls), xs, ws, status=status)
+    _, _, y1 = moe.iq4nl_decode_layers(shape, spec(Ls), xin, ws, chained=chained, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     assert np.array_equal(y1.cpu().numpy().view(np.uint32), y0.view(np.uint32))
