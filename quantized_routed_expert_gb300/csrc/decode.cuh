@@ -35,13 +35,8 @@ inline int64_t qvec_words(int64_t K) {
   return groups * lpr * 32 + align_up(K / 32, 4);
 }
 
-// Chained multi-layer calls with T * E up to this exchange partial router
-// scores (each CTA's rows of y against every expert) instead of a y barrier
-// and a score exchange.
-constexpr int kPartialScoreMax = 64;
-
-struct DecodeLayout {  // byte offsets
-  int64_t h_r, h_s, rec_r, rec_s, sync, scores, xrec, part, tscores, xc, psc, pflag, total;
+struct DecodeLayout {
+  int64_t h_r, h_s, rec_r, rec_s, sync, scores, xrec, part, tscores, xc, total;  // byte offsets
 };
 
 inline DecodeLayout decode_layout(const moe_shape& s, int64_t T) {
@@ -63,10 +58,6 @@ inline DecodeLayout decode_layout(const moe_shape& s, int64_t T) {
   L.part = take((T * s.top_k + (Fs ? T : 0)) * s.hidden * 4);   // down partials per pair
   L.tscores = take(2 * T * s.n_experts * 8);   // tagged router scores (multi-layer kernel)
   L.xc = take(T * s.hidden * 2);               // chained bf16 input (multi-layer, launch per layer)
-  // chained multi-layer kernel, small T * E: per-CTA partial router scores
-  // [256][T][E] and their per-CTA flags [256]
-  L.psc = take(T * s.n_experts <= kPartialScoreMax ? 256 * T * s.n_experts * 4 : 0);
-  L.pflag = take(256 * 8);
   L.total = off;
   return L;
 }
@@ -109,9 +100,6 @@ struct DecodeParams {
   int chained;       // 1: layer l + 1's input is bf16(y_l)
   uint64_t* tscores; // workspace [2][T][E]: score | tag << 32
   uint16_t* xc;      // workspace [T][H]: chained input, launch-per-layer path
-  int pscore;        // 1: chained layers exchange partial scores (T * E <= kPartialScoreMax)
-  float* gpart;      // workspace [grid][T][E]: partial router scores of the next layer
-  uint64_t* pflag;   // workspace [grid]: epoch tag, set once a CTA's partials and y are out
 };
 
 // Per-layer pointers of a multi-layer call (kernel parameter space).

@@ -65,7 +65,6 @@ __device__ uint64_t g_profw[kProfCtas * kProfLayers * 16 * kProfW];
 #endif
 
 constexpr int kLW = 16;            // warps per CTA
-constexpr int kPartialLoads = 32;  // partials one thread loads (8 threads, up to 256 CTAs)
 constexpr int kLT = kLW * 32;      // threads per CTA
 constexpr int kLSlots = 2;         // bulk-copy slots per warp
 
@@ -74,8 +73,8 @@ constexpr int kLSlots = 2;         // bulk-copy slots per warp
 constexpr int kSyncH = 4, kSyncY = 5, kSyncOut = 6, kSyncEpoch = 7;
 
 struct LayersSmem {
-  size_t xq, slots, bars, recs, part, rwr, rx, rpart, rprob, rids, rw, rsc, rred, xown, stage,
-      stage_bytes, total, slot_bytes;
+  size_t xq, slots, bars, recs, part, rwr, rx, rpart, rprob, rids, rw, stage, stage_bytes,
+      total, slot_bytes;
 };
 
 // Experts whose scores CTA c takes: a balanced split of E over the grid.
@@ -111,14 +110,8 @@ __host__ __device__ inline LayersSmem layers_smem(int H, int F, int Fs, int ns, 
   m.rprob = align_up_dev(m.rpart + (size_t)epc * 16 * T * 4, 16);
   m.rids = align_up_dev(m.rprob + (size_t)T * E32 * 4, 16);
   m.rw = align_up_dev(m.rids + (size_t)T * k * 4, 16);
-  m.rsc = align_up_dev(m.rw + (size_t)T * k * 4, 16);   // scores summed from partials
-  m.rred = align_up_dev(m.rsc + (size_t)T * E32 * 4, 16);  // [8][64] group sums
-  const size_t rend = m.rred + (size_t)8 * 64 * 4;
+  const size_t rend = m.rw + (size_t)T * k * 4;
   end = end > rend ? end : rend;
-  // bf16 of this CTA's rows of y (the next layer's input rows), kept past the
-  // combine for the partial scores
-  m.xown = align_up_dev(end, 16);
-  end = m.xown + (size_t)T * rows_max * 2;
   // stage every h row of a layer in shared memory when it fits
   const size_t hb = ((size_t)T * k * F + (ns ? (size_t)T * Fs : 0)) * 4;
   const size_t st = align_up_dev(end, 128);
@@ -328,27 +321,6 @@ __device__ __forceinline__ void layer_topk(const uint64_t* sc, uint32_t want, in
   wv = warp_renorm(lane < k ? prob[id] : 0.0f, k);
 }
 
-// One token's top-k by one warp from its E scores in shared memory.
-template <int NPL>
-__device__ __forceinline__ void layer_topk_smem(const float* sc, int E, int k, const float* bias,
-                                                float* prob, int& id, float& wv) {
-  const int lane = threadIdx.x & 31;
-  float kv[NPL];
-#pragma unroll
-  for (int i = 0; i < NPL; ++i) {
-    const int e = lane + 32 * i;
-    kv[i] = -INFINITY;
-    if (e < E) {
-      const float pr = 1.0f / (1.0f + expf(-sc[e]));
-      prob[e] = pr;
-      kv[i] = pr + (bias ? bias[e] : 0.0f);
-    }
-  }
-  id = warp_topk_regs<NPL>(kv, k);
-  __syncwarp();
-  wv = warp_renorm(lane < k ? prob[id] : 0.0f, k);
-}
-
 template <int MAXT, int LPR>
 __global__ void __launch_bounds__(kLT, 1)
     decode_layers_kernel(const __grid_constant__ DecodeParams p,
@@ -373,7 +345,6 @@ __global__ void __launch_bounds__(kLT, 1)
   float* rpart = reinterpret_cast<float*>(smem + S.rpart);
   float* rprob = reinterpret_cast<float*>(smem + S.rprob);
   int32_t* rids = reinterpret_cast<int32_t*>(smem + S.rids);
-  __nv_bfloat16* xown = reinterpret_cast<__nv_bfloat16*>(smem + S.xown);
   float* rw = reinterpret_cast<float*>(smem + S.rw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int xq_words = dqvec_words(H);
@@ -470,74 +441,6 @@ __global__ void __launch_bounds__(kLT, 1)
         prefetch_l2(Wn.sh_down + (size_t)dn.a * rbS, (uint32_t)(nrows_cta * rbS));
       }
     }
-    // A chained layer after the first with partial scores: its router scores
-    // are the sums of every CTA's partials over its rows of y_{l-1}, published
-    // with a per-CTA flag that also releases those rows of y. That exchange
-    // stands for both the y barrier and the score exchange.
-    const bool ps = p.pscore && l > 0;
-    float* rsc = reinterpret_cast<float*>(smem + S.rsc);
-    uint64_t* tsc = p.tscores + (size_t)(l & 1) * T * E;
-    if (ps) {
-      if (warp == 0) {
-        const uint64_t want = (uint64_t)epoch + (uint64_t)l + 1u;
-        bool got[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) got[i] = lane + 32 * i >= G;
-        const uint64_t t0 = global_timer_ns();
-        for (;;) {
-          bool all = true;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            if (!got[i]) got[i] = ld_relaxed_u64(p.pflag + lane + 32 * i) == want;
-            all = all && got[i];
-          }
-          if (__all_sync(0xFFFFFFFFu, all)) break;
-          if (__shfl_sync(0xFFFFFFFFu, global_timer_ns() - t0 >= wait_ns ? 1 : 0, 0)) {
-            if (lane == 0) {
-              if (p.status) atomicOr(p.status, MOE_STATUS_TIMEOUT);
-              *gave_up = 1u;
-            }
-            break;
-          }
-          __nanosleep(64);
-        }
-        asm volatile("fence.acq_rel.gpu;" ::: "memory");   // acquire: the rows of y, the partials
-      }
-      __syncthreads();
-      MOE_STAMP(l, 1);
-      if (*gave_up) wait_ns = 0;
-      // scores (T * E <= 64): thread group g (64 threads, one per (token,
-      // expert)) loads CTAs g, g + 8, ... at once (each warp load one
-      // 128-byte line: the partials of one CTA are contiguous) and sums them
-      // in CTA order; the eight group sums are added in group order
-      {
-        const int te = threadIdx.x & 63, g = threadIdx.x >> 6;
-        const int nte = T * E;
-        float v[kPartialLoads];
-#pragma unroll
-        for (int i = 0; i < kPartialLoads; ++i) {
-          const int c = g + 8 * i;
-          v[i] = (te < nte && c < G) ? __ldcg(p.gpart + (size_t)c * nte + te) : 0.0f;
-        }
-        float acc = 0.0f;
-#pragma unroll
-        for (int i = 0; i < kPartialLoads; ++i) acc += v[i];
-        float* red = reinterpret_cast<float*>(smem + S.rred);
-        red[g * 64 + te] = acc;
-        __syncthreads();
-        if (threadIdx.x < nte) {
-          float sc = 0.0f;
-#pragma unroll
-          for (int gg = 0; gg < 8; ++gg) sc += red[gg * 64 + threadIdx.x];
-          const int t = threadIdx.x / E, e = threadIdx.x - t * E;
-          rsc[t * E32 + e] = sc;
-        }
-      }
-      load_x_layer<true>(nullptr, p.y + (size_t)(l - 1) * T * H, T, H, rx, xq, xq_words);
-      __syncthreads();
-      MOE_STAMP(l, 2);
-      MOE_STAMP(l, 3);
-    } else {
     // ---- this layer's input, after every CTA finished the previous layer
     if (l > 0) {
       if (threadIdx.x == 0)
@@ -556,6 +459,7 @@ __global__ void __launch_bounds__(kLT, 1)
 
     // ---- scores of this CTA's experts: 16 chunks of H per expert, one warp
     // per (expert, chunk), chunk partials summed in a fixed order
+    uint64_t* tsc = p.tscores + (size_t)(l & 1) * T * E;
     if (ne > 0) {
       const bool landed = __syncthreads_and(mbar_wait(rwr_bar, (uint32_t)(l & 1), p.status));
       rwr_landed = l;
@@ -608,7 +512,6 @@ __global__ void __launch_bounds__(kLT, 1)
     }
     __syncthreads();
     MOE_STAMP(l, 3);
-    }   // scores
 
     // ---- top-k: warp t takes token t, in every CTA; meanwhile the other
     // warps compute the shared expert's rows (known before the routes)
@@ -631,16 +534,10 @@ __global__ void __launch_bounds__(kLT, 1)
       const uint64_t* sc = tsc + (size_t)warp * E;
       const uint32_t want = epoch + (uint32_t)l + 1u;
       float* prob = rprob + (size_t)warp * E32;
-      if (ps) {
-        if (E <= 64)
-          layer_topk_smem<2>(rsc + (size_t)warp * E32, E, k, W.bias, prob, id, wv);
-        else
-          layer_topk_smem<16>(rsc + (size_t)warp * E32, E, k, W.bias, prob, id, wv);
-      } else if (E <= 64) {
+      if (E <= 64)
         layer_topk<2>(sc, want, E, k, W.bias, prob, id, wv, wait_ns, p.status, gave_up);
-      } else {
+      else
         layer_topk<16>(sc, want, E, k, W.bias, prob, id, wv, wait_ns, p.status, gave_up);
-      }
       MOE_WSTAMP(l, 4);
       if (lane < k) {
         rids[warp * k + lane] = id;
@@ -764,56 +661,13 @@ __global__ void __launch_bounds__(kLT, 1)
         if (pr / k == t) acc += rt.wt[pr] * part[(size_t)pr * rows_max + r];
       }
       yl[(size_t)t * H + dn.a + r] = acc;
-      xown[t * rows_max + r] = __float2bfloat16_rn(acc);   // the next layer's input
     }
     __syncthreads();
     MOE_STAMP(l, 9);
     if (threadIdx.x == 0) grid_arrive(&p.sync[kSyncY]);
-    if (p.pscore && l + 1 < Lyr) {
-      // partial router scores of the next layer over this CTA's rows of its
-      // input: one warp per expert (lane r takes row r), a fixed butterfly
-      // (E <= 64: four experts per warp, their router values loaded at once)
-      const uint16_t* wr = lt.layer[l + 1].Wr + dn.a;
-#pragma unroll 1
-      for (int r0 = 0; r0 < nrows_cta; r0 += 32) {
-        const int r = r0 + lane;
-        float wv[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int e = warp + kLW * i;
-          wv[i] = (e < E && r < nrows_cta)
-                      ? __uint_as_float((uint32_t)__ldg(wr + (size_t)e * H + r) << 16) : 0.0f;
-        }
-        float xv[2];
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-          xv[t] = (t < T && r < nrows_cta) ? __bfloat162float(xown[t * rows_max + r]) : 0.0f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            float a = wv[i] * xv[t];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
-            const int e = warp + kLW * i;
-            if (lane == 0 && e < E && t < T) {
-              float* dst = p.gpart + ((size_t)cta * T + t) * E + e;
-              *dst = r0 == 0 ? a : *dst + a;
-            }
-          }
-      }
-      __syncthreads();
-      // release this CTA's rows of y and its partials: one flag, tagged with
-      // the next layer
-      if (threadIdx.x == 0) {
-        asm volatile("fence.acq_rel.gpu;" ::: "memory");
-        asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p.pflag + cta),
-                     "l"((uint64_t)epoch + (uint64_t)l + 2u)
-                     : "memory");
-      }
-    } else if (ok && l + 1 < Lyr) {
-      // the records and partials are read: the next layer's router rows may
-      // land over them (from L2, prefetched above)
+    // the records and partials are read: the next layer's router rows may
+    // land over them (from L2, prefetched above)
+    if (ok && l + 1 < Lyr) {
       if (threadIdx.x == 0) {
         fence_proxy_async_shared();
         issue_router_rows(l + 1);

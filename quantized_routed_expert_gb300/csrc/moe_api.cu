@@ -228,10 +228,6 @@ moe_status moe_iq4nl_decode_layers(const moe_shape* shape, int32_t n_layers,
   p.chained = chained;
   p.tscores = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(ws) + L.tscores);
   p.xc = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(ws) + L.xc);
-  p.pscore = (chained && T <= 2 && shape->n_experts <= 64 &&
-              T * shape->n_experts <= moe::kPartialScoreMax && sms <= 256) ? 1 : 0;
-  p.gpart = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + L.psc);
-  p.pflag = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(ws) + L.pflag);
   p.scores = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + L.scores);
   static_assert(sizeof(moe::LayerTable) <= 16 * 1024, "layer table fits the launch parameters");
   moe::LayerTable lt;

@@ -90,8 +90,6 @@ def _check_chained(Ls, x0, ids, w, y, what):
         x_l = synth.to_bf16_bits(y[l])          # round to nearest even, as the kernel
 
 
-# Xing, 1 and 2 tokens: T * E <= 128, so the layers exchange partial router
-# scores; Qwen3-Next (512 experts): the y barrier and the score exchange.
 @pytest.mark.parametrize("cfg,T,n", [(1, 1, 4), (1, 2, 3), (2, 2, 3), (0, 4, 3)])
 def test_layers_chained_layer_by_layer(cfg, T, n):
     from synth.layers import bf16_tensor
@@ -144,8 +142,8 @@ def test_layers_launch_per_layer_path(chained):
 
 @pytest.mark.parametrize("chained", [False, True])
 def test_layers_barrier_timeout_is_reported_and_recovers(chained):
-    # every grid-wide wait of the kernel (score tags, h counter, y counter,
-    # partial-score flags) gives up at once with the limit at 0
+    # every grid-wide wait of the kernel (score tags, h counter, y counter)
+    # gives up at once with the limit at 0
     from synth.layers import bf16_tensor
     moe = lib()
     Ls = layers_of(1, 3)
