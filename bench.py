@@ -372,9 +372,14 @@ def run_libmoe(args):
 
 # The other configurations, measured in the same process after the headline,
 # with the same timing code (no e2e and no CPU baseline for these).
+# The Qwen3-Next-shaped layer at one token and at two identical tokens is the
+# Red Lite page's reuse check (section 4: a second token on the same experts
+# costs about 1.06x one token when each block is decoded once for both).
 OTHER_WORKLOADS = (
     {"config": 2, "tokens": None, "step": "layers", "steps": 10, "warmup": 3},
     {"config": 2, "tokens": None, "step": "chained", "steps": 10, "warmup": 3},
+    {"config": 2, "tokens": 1, "step": "layers", "steps": 10, "warmup": 3},
+    {"config": 2, "tokens": 2, "step": "layers", "steps": 10, "warmup": 3, "same_tokens": True},
     {"config": 3, "tokens": 1, "step": "layers", "steps": 10, "warmup": 3},
     {"config": 3, "tokens": 4, "step": "routed", "steps": 10, "warmup": 3},
     {"config": 3, "tokens": 16, "step": "routed", "steps": 10, "warmup": 3},
@@ -390,12 +395,14 @@ def other_workloads(args, ctx):
         a = copy.copy(args)
         a.config, a.tokens, a.step = w["config"], w["tokens"], w["step"]
         a.steps, a.warmup = w["steps"], w["warmup"]
-        a.no_e2e, a.no_cpu_baseline, a.same_tokens = True, True, False
+        a.no_e2e, a.no_cpu_baseline = True, True
+        a.same_tokens = bool(w.get("same_tokens", False))
         a.layers, a.experts = None, None
         r = measure(a, ctx)
         torch.cuda.empty_cache()
         rf = r["roofline"]
         out.append({"workload": r["config"]["workload"], "tokens_per_step": r["config"]["tokens_per_step"],
+                    "same_tokens": a.same_tokens,
                     "layers": r["config"]["layers"], "step_call": r["step_call"],
                     "steps": a.steps, "warmup": a.warmup,
                     "ms_per_step": r["ms_per_step"], "step_ms": r["step_ms"],
@@ -404,6 +411,13 @@ def other_workloads(args, ctx):
                                                     "kernel")},
                     "clocks": r["clocks"], "gpu_launches": r["gpu_launches"],
                     "status_word": r["status_word"]})
+    # the reuse check: a step of two identical tokens against a step of one
+    one = [o for o in out if "qwen3" in o["workload"] and o["tokens_per_step"] == 1]
+    two = [o for o in out if "qwen3" in o["workload"] and o["same_tokens"]]
+    if one and two:
+        out.append({"reuse_check": "Qwen3-Next-shaped layer, 48 layers: ms per step of two "
+                                   "identical tokens / ms per step of one token",
+                    "ratio": two[0]["ms_per_step"] / one[0]["ms_per_step"]})
     return out
 
 
