@@ -41,7 +41,9 @@ namespace moe {
 constexpr int kProfCtas = 256, kProfLayers = 64, kProfPhases = 12;
 __device__ uint64_t g_prof[kProfCtas * kProfLayers * kProfPhases];
 // per warp: [0] routed gate/up first unit landed, [1] routed gate/up done,
-// [2] down unit landed, [3] down done, [4] top-k saw every score (warp 0)
+// [2] down unit landed, [3] down done, [4] top-k and weights done (token
+// warps) or the shared expert's rows done (the other warps),
+// [5] every score seen, [6] selection done, [7] route table built (warp 0)
 constexpr int kProfW = 8;
 __device__ uint64_t g_profw[kProfCtas * kProfLayers * 16 * kProfW];
 #define MOE_WSTAMP(l, k)                                                                      \
@@ -270,7 +272,7 @@ template <int NPL>
 __device__ __forceinline__ void layer_topk(const uint64_t* sc, uint32_t want, int E, int k,
                                            const float* bias, float* prob, int& id, float& wv,
                                            uint64_t wait_ns, uint32_t* status,
-                                           volatile uint32_t* gave_up) {
+                                           volatile uint32_t* gave_up, int l) {
   const int lane = threadIdx.x & 31;
   float s[NPL];
   bool got[NPL];
@@ -305,6 +307,7 @@ __device__ __forceinline__ void layer_topk(const uint64_t* sc, uint32_t want, in
     // every CTA polls the same few lines: back off between rounds
     __nanosleep(100);
   }
+  MOE_WSTAMP(l, 5);
   float kv[NPL];
 #pragma unroll
   for (int i = 0; i < NPL; ++i) {
@@ -317,6 +320,7 @@ __device__ __forceinline__ void layer_topk(const uint64_t* sc, uint32_t want, in
     }
   }
   id = warp_topk_regs<NPL>(kv, k);
+  MOE_WSTAMP(l, 6);
   __syncwarp();
   wv = warp_renorm(lane < k ? prob[id] : 0.0f, k);
 }
@@ -527,6 +531,7 @@ __global__ void __launch_bounds__(kLT, 1)
         ++consumed;
         issue_upto(up.ub + n_sh);
       }
+      MOE_WSTAMP(l, 4);
     }
     if (warp < T) {
       int id;
@@ -535,9 +540,9 @@ __global__ void __launch_bounds__(kLT, 1)
       const uint32_t want = epoch + (uint32_t)l + 1u;
       float* prob = rprob + (size_t)warp * E32;
       if (E <= 64)
-        layer_topk<2>(sc, want, E, k, W.bias, prob, id, wv, wait_ns, p.status, gave_up);
+        layer_topk<2>(sc, want, E, k, W.bias, prob, id, wv, wait_ns, p.status, gave_up, l);
       else
-        layer_topk<16>(sc, want, E, k, W.bias, prob, id, wv, wait_ns, p.status, gave_up);
+        layer_topk<16>(sc, want, E, k, W.bias, prob, id, wv, wait_ns, p.status, gave_up, l);
       MOE_WSTAMP(l, 4);
       if (lane < k) {
         rids[warp * k + lane] = id;
@@ -548,7 +553,10 @@ __global__ void __launch_bounds__(kLT, 1)
         }
       }
       if (T > 1) bar_sync_n(1, T * 32);     // the token warps only
-      if (warp == 0) build_route_table_warp(rt, rids, rw, T * k, E);
+      if (warp == 0) {
+        build_route_table_warp(rt, rids, rw, T * k, E);
+        MOE_WSTAMP(l, 7);
+      }
     }
     __syncthreads();
     MOE_STAMP(l, 4);

@@ -22,6 +22,32 @@ namespace {
 int64_t up256(int64_t v) { return (v + 255) / 256 * 256; }
 }  // namespace
 
+// Per-tile stamps of the GEMM kernels (builds with MOE_PROFILE only), read back
+// with moe_profile_prefill: [gate/up, down][CTA < 256][tile < 15, 15 = kernel]
+// [8]: 0 MMA tile start, 1 MMA last commit, 2 dequant start, 3 dequant done,
+// 4 accumulator seen by the epilogue, 5 epilogue done, 6 tokens, 7 bucket.
+#ifdef MOE_PROFILE
+__device__ uint64_t g_pfprof[2 * 256 * 16 * 8];
+#define PF_STAMP(tile, k, v)                                                            \
+  do {                                                                                  \
+    if (blockIdx.x < 256 && (tile) < 15)                                                \
+      g_pfprof[(((size_t)(GATEUP ? 0 : 1) * 256 + blockIdx.x) * 16 + (tile)) * 8 + (k)] = \
+          (v);                                                                          \
+  } while (0)
+#define PF_STAMP_K(k, v)                                                                \
+  do {                                                                                  \
+    if (blockIdx.x < 256)                                                               \
+      g_pfprof[(((size_t)(GATEUP ? 0 : 1) * 256 + blockIdx.x) * 16 + 15) * 8 + (k)] = (v); \
+  } while (0)
+#else
+#define PF_STAMP(tile, k, v) \
+  do {                       \
+  } while (0)
+#define PF_STAMP_K(k, v) \
+  do {                   \
+  } while (0)
+#endif
+
 PrefillLayout prefill_layout(const moe_shape& s, int64_t T) {
   PrefillLayout L{};
   int64_t off = 0;
@@ -369,6 +395,7 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
   if (warp == 1) tmem_alloc(tmem_slot, 512);
   pdl_wait();
   pdl_trigger();
+  if (threadIdx.x == 0) PF_STAMP_K(0, global_timer_ns());
   // bucket offsets and the tile prefix (tiles of a bucket: weight tiles x token tiles)
   const int nb = p.E + p.n_shared;
   for (int i = threadIdx.x; i < p.E + 2; i += S::kThreads) boff[i] = p.bucket_off[i];
@@ -438,6 +465,9 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
         const uint32_t idesc = idesc_f16_f32(kTM, (ti.nvalid + 15) & ~15);
         if (!mbar_wait(acc_empty, (tc & 1) ^ 1, p.status)) break;
         tc_fence_after();
+        PF_STAMP(tc, 0, global_timer_ns());
+        PF_STAMP(tc, 6, (uint64_t)ti.nvalid);
+        PF_STAMP(tc, 7, (uint64_t)ti.bucket);
         for (int ks = 0; ks < K / kTK; ++ks, ++it) {
           const int s = it % S::kStages;
           const uint32_t par = (it / S::kStages) & 1;
@@ -459,6 +489,7 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
           tc_commit(&empty[s]);
         }
         if (tc < 0) break;
+        PF_STAMP(tc, 1, global_timer_ns());
         tc_commit(acc_full);
       }
     }
@@ -504,6 +535,7 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
       const bool sh = ti.bucket >= p.E;
       const int K = sh ? p.Ks : p.K;
       const int nks = K / kTK;
+      if (warp == S::kCtl && lane == 0) PF_STAMP(tc, 2, global_timer_ns());
       // publish one dequantised K-step of this thread
       auto publish = [&](int s) {
         fence_proxy_async_smem();
@@ -609,9 +641,11 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
         }
       }
       if (!ok) break;
+      if (warp == S::kCtl && lane == 0) PF_STAMP(tc, 3, global_timer_ns());
       // epilogue: TMEM lanes of this warp's quarter, a share of the token columns
       if (!mbar_wait(acc_full, tc & 1, p.status)) { ok = false; break; }
       tc_fence_after();
+      if (warp == S::kCtl && lane == 0) PF_STAMP(tc, 4, global_timer_ns());
       const int q = warp & 3;
       constexpr int kCols = kTN / (S::kDq / 4);
       const int ch = dw >> 2;                   // column share
@@ -642,11 +676,13 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
       }
       tc_fence_before();
       __syncwarp();
+      if (warp == S::kCtl && lane == 0) PF_STAMP(tc, 5, global_timer_ns());
       if (lane == 0) mbar_arrive(acc_empty);
     }
   }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) PF_STAMP_K(1, global_timer_ns());
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -874,3 +910,12 @@ cudaError_t launch_prefill(const moe_shape& s, const moe_expert_weights& w, cons
 }
 
 }  // namespace moe
+
+#ifdef MOE_PROFILE
+// Copies the GEMM tile stamps (uint64 [2][256][16][8], ns of %globaltimer).
+// Profiling builds only.
+extern "C" int moe_profile_prefill(void* host, size_t bytes) {
+  const size_t n = sizeof(moe::g_pfprof) < bytes ? sizeof(moe::g_pfprof) : bytes;
+  return cudaMemcpyFromSymbol(host, moe::g_pfprof, n) == cudaSuccess ? 0 : -1;
+}
+#endif
