@@ -268,33 +268,31 @@ __device__ __forceinline__ void load_x_layer(const uint16_t* __restrict__ xb,
 }
 
 // One token's top-k by one warp, from the tagged scores of all E experts.
+// The bias is read before the wait, so that its latency overlaps it. Each
+// polling round issues every lane's loads before it checks any tag.
 template <int NPL>
 __device__ __forceinline__ void layer_topk(const uint64_t* sc, uint32_t want, int E, int k,
                                            const float* bias, float* prob, int& id, float& wv,
                                            uint64_t wait_ns, uint32_t* status,
                                            volatile uint32_t* gave_up, int l) {
   const int lane = threadIdx.x & 31;
-  float s[NPL];
-  bool got[NPL];
+  float bv[NPL];
 #pragma unroll
   for (int i = 0; i < NPL; ++i) {
-    s[i] = 0.0f;
-    got[i] = lane + 32 * i >= E;
+    const int e = lane + 32 * i;
+    bv[i] = (bias && e < E) ? __ldg(bias + e) : 0.0f;
   }
+  uint64_t v[NPL];
   const uint64_t t0 = global_timer_ns();
   for (;;) {
-    bool all = true;
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
-      if (!got[i]) {
-        const uint64_t v = ld_relaxed_u64(sc + lane + 32 * i);
-        if ((uint32_t)(v >> 32) == want) {
-          s[i] = __uint_as_float((uint32_t)v);
-          got[i] = true;
-        }
-      }
-      all = all && got[i];
+      const int e = lane + 32 * i;
+      v[i] = ld_relaxed_u64(sc + (e < E ? e : E - 1));
     }
+    bool all = true;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) all = all && (uint32_t)(v[i] >> 32) == want;
     if (__all_sync(0xFFFFFFFFu, all)) break;
     // the give-up decision is the warp's (lane 0's clock), so every lane leaves together
     if (__shfl_sync(0xFFFFFFFFu, global_timer_ns() - t0 >= wait_ns ? 1 : 0, 0)) {
@@ -314,9 +312,9 @@ __device__ __forceinline__ void layer_topk(const uint64_t* sc, uint32_t want, in
     const int e = lane + 32 * i;
     kv[i] = -INFINITY;
     if (e < E) {
-      const float pr = 1.0f / (1.0f + expf(-s[i]));
+      const float pr = 1.0f / (1.0f + expf(-__uint_as_float((uint32_t)v[i])));
       prob[e] = pr;
-      kv[i] = pr + (bias ? bias[e] : 0.0f);
+      kv[i] = pr + bv[i];
     }
   }
   id = warp_topk_regs<NPL>(kv, k);
@@ -467,6 +465,7 @@ __global__ void __launch_bounds__(kLT, 1)
     if (ne > 0) {
       const bool landed = __syncthreads_and(mbar_wait(rwr_bar, (uint32_t)(l & 1), p.status));
       rwr_landed = l;
+      MOE_STAMP(l, 10);
       ok = ok && landed;
       const uint16_t* wr_s = reinterpret_cast<const uint16_t*>(smem + S.rwr);
       const int hc = H / 16;
