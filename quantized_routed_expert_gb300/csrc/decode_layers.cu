@@ -75,8 +75,8 @@ constexpr int kLSlots = 2;         // bulk-copy slots per warp
 constexpr int kSyncH = 4, kSyncY = 5, kSyncOut = 6, kSyncEpoch = 7;
 
 struct LayersSmem {
-  size_t xq, slots, bars, recs, part, rwr, rx, rpart, rprob, rids, rw, stage, stage_bytes,
-      total, slot_bytes;
+  size_t xq, slots, bars, recs, part, rwr, rx, rpart, rprob, rids, rw, rcand, stage,
+      stage_bytes, total, slot_bytes;
 };
 
 // Experts whose scores CTA c takes: a balanced split of E over the grid.
@@ -112,7 +112,8 @@ __host__ __device__ inline LayersSmem layers_smem(int H, int F, int Fs, int ns, 
   m.rprob = align_up_dev(m.rpart + (size_t)epc * 16 * T * 4, 16);
   m.rids = align_up_dev(m.rprob + (size_t)T * E32 * 4, 16);
   m.rw = align_up_dev(m.rids + (size_t)T * k * 4, 16);
-  const size_t rend = m.rw + (size_t)T * k * 4;
+  m.rcand = align_up_dev(m.rw + (size_t)T * k * 4, 16);
+  const size_t rend = m.rcand + (size_t)kLW * k * 8;
   end = end > rend ? end : rend;
   // stage every h row of a layer in shared memory when it fits
   const size_t hb = ((size_t)T * k * F + (ns ? (size_t)T * Fs : 0)) * 4;
@@ -267,22 +268,14 @@ __device__ __forceinline__ void load_x_layer(const uint16_t* __restrict__ xb,
   }
 }
 
-// One token's top-k by one warp, from the tagged scores of all E experts.
-// The bias is read before the wait, so that its latency overlaps it. Each
-// polling round issues every lane's loads before it checks any tag.
+// A token's tagged scores of all E experts, polled by one warp until every
+// tag is the current one (or the wait gives up). Each polling round issues
+// every lane's loads before it checks any tag. Lane l gets experts l + 32 i.
 template <int NPL>
-__device__ __forceinline__ void layer_topk(const uint64_t* sc, uint32_t want, int E, int k,
-                                           const float* bias, float* prob, int& id, float& wv,
-                                           uint64_t wait_ns, uint32_t* status,
-                                           volatile uint32_t* gave_up, int l) {
+__device__ __forceinline__ void poll_scores(const uint64_t* sc, uint32_t want, int E,
+                                            uint64_t (&v)[NPL], uint64_t wait_ns,
+                                            uint32_t* status, volatile uint32_t* gave_up) {
   const int lane = threadIdx.x & 31;
-  float bv[NPL];
-#pragma unroll
-  for (int i = 0; i < NPL; ++i) {
-    const int e = lane + 32 * i;
-    bv[i] = (bias && e < E) ? __ldg(bias + e) : 0.0f;
-  }
-  uint64_t v[NPL];
   const uint64_t t0 = global_timer_ns();
   for (;;) {
 #pragma unroll
@@ -305,6 +298,24 @@ __device__ __forceinline__ void layer_topk(const uint64_t* sc, uint32_t want, in
     // every CTA polls the same few lines: back off between rounds
     __nanosleep(100);
   }
+}
+
+// One token's top-k by one warp, from the tagged scores of all E experts.
+// The bias is read before the wait, so that its latency overlaps it.
+template <int NPL>
+__device__ __forceinline__ void layer_topk(const uint64_t* sc, uint32_t want, int E, int k,
+                                           const float* bias, float* prob, int& id, float& wv,
+                                           uint64_t wait_ns, uint32_t* status,
+                                           volatile uint32_t* gave_up, int l) {
+  const int lane = threadIdx.x & 31;
+  float bv[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * i;
+    bv[i] = (bias && e < E) ? __ldg(bias + e) : 0.0f;
+  }
+  uint64_t v[NPL];
+  poll_scores<NPL>(sc, want, E, v, wait_ns, status, gave_up);
   MOE_WSTAMP(l, 5);
   float kv[NPL];
 #pragma unroll
@@ -321,6 +332,67 @@ __device__ __forceinline__ void layer_topk(const uint64_t* sc, uint32_t want, in
   MOE_WSTAMP(l, 6);
   __syncwarp();
   wv = warp_renorm(lane < k ? prob[id] : 0.0f, k);
+}
+
+// The selection spread over the warps of a CTA (more than 64 experts): each
+// warp takes a range of one token's experts, turns their scores into sigmoids
+// and keys, and picks its own k best in the order of the one-warp selection
+// (largest key first, ties to the lower expert). Lane 0 records each pick as
+// (key bits << 32) | expert; a pick made after the range ran out of keys has
+// key bits 0. sc_prob holds the token's scores and gets its sigmoids.
+template <int NPL>
+__device__ __forceinline__ void topk_part(float* sc_prob, const float (&bsel)[4], int base, int E,
+                                          int k, uint64_t* cand) {
+  const int lane = threadIdx.x & 31;
+  uint32_t v[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = base + lane + 32 * i;
+    v[i] = 0u;
+    if (e < E) {
+      const float pr = 1.0f / (1.0f + expf(-sc_prob[e]));
+      sc_prob[e] = pr;
+      const float kv = pr + bsel[i];
+      v[i] = kv > -INFINITY ? ordered_key_bits(kv) : 0u;
+    }
+  }
+#pragma unroll 1
+  for (int j = 0; j < k; ++j) {
+    uint32_t m[NPL];
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) m[i] = v[i];
+#pragma unroll
+    for (int st = 1; st < NPL; st *= 2)
+#pragma unroll
+      for (int i = 0; i + st < NPL; i += 2 * st) m[i] = m[i] > m[i + st] ? m[i] : m[i + st];
+    const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, m[0]);
+    uint32_t hit = 0;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) hit |= (v[i] == mx ? 1u : 0u) << i;
+    const uint32_t c = hit ? (uint32_t)(lane + 32 * (__ffs(hit) - 1)) : 0xFFFFFFFFu;
+    const uint32_t bi = __reduce_min_sync(0xFFFFFFFFu, c);
+    if (lane == 0) cand[j] = ((uint64_t)mx << 32) | (uint32_t)(base + (int)bi);
+    const bool mine = (int)(bi & 31u) == lane;
+    const int ri = (int)(bi >> 5);
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) v[i] = (mine && i == ri) ? 0u : v[i];
+  }
+}
+// The token's k experts from the n candidates of its warps (stored by
+// ascending expert range, so a lower position among equal keys is a lower
+// expert): lane j < k gets the j-th. A choice made once no key is left is
+// expert 0, as in the one-warp selection.
+__device__ __forceinline__ int topk_merge(const uint64_t* cand, int n, int k) {
+  const int lane = threadIdx.x & 31;
+  uint32_t v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int q = lane + 32 * i;
+    v[i] = q < n ? (uint32_t)(cand[q] >> 32) : 0u;
+  }
+  const int pos = warp_topk_bits<8>(v, k);
+  const uint64_t c = cand[lane < k ? pos : 0];
+  return (uint32_t)(c >> 32) == 0u ? 0 : (int)(uint32_t)c;
 }
 
 template <int MAXT, int LPR>
@@ -348,6 +420,7 @@ __global__ void __launch_bounds__(kLT, 1)
   float* rprob = reinterpret_cast<float*>(smem + S.rprob);
   int32_t* rids = reinterpret_cast<int32_t*>(smem + S.rids);
   float* rw = reinterpret_cast<float*>(smem + S.rw);
+  uint64_t* rcand = reinterpret_cast<uint64_t*>(smem + S.rcand);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int xq_words = dqvec_words(H);
   const int rbH = H / 32 * kBlockB;
@@ -495,8 +568,9 @@ __global__ void __launch_bounds__(kLT, 1)
         }
 #pragma unroll
         for (int t = 0; t < 4; ++t)
+          if (t < T)
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xFFFFFFFFu, acc[t], o);
+            for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xFFFFFFFFu, acc[t], o);
         if (lane == 0) {
 #pragma unroll
           for (int t = 0; t < 4; ++t)
@@ -517,7 +591,19 @@ __global__ void __launch_bounds__(kLT, 1)
     MOE_STAMP(l, 3);
 
     // ---- top-k: warp t takes token t, in every CTA; meanwhile the other
-    // warps compute the shared expert's rows (known before the routes)
+    // warps compute the shared expert's rows (known before the routes). With
+    // more than 64 experts warp t only gathers the scores, and the selection
+    // is spread over all warps: kLW / T warps per token.
+    const bool split_sel = E > 64;
+    const int Wt = kLW / T, tt = warp / Wt;
+    const int nsel = E <= Wt * 32 ? 1 : (E <= Wt * 64 ? 2 : 4);   // E <= 512, Wt >= 4
+    const int sbase = (warp - tt * Wt) * 32 * nsel;
+    float bsel[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = sbase + lane + 32 * i;
+      bsel[i] = (split_sel && W.bias && tt < T && i < nsel && e < E) ? __ldg(W.bias + e) : 0.0f;
+    }
     if (warp >= T) {
 #pragma unroll 1
       for (int j = up.ub; ok && j < up.ub + n_sh; ++j) {
@@ -532,17 +618,7 @@ __global__ void __launch_bounds__(kLT, 1)
       }
       MOE_WSTAMP(l, 4);
     }
-    if (warp < T) {
-      int id;
-      float wv;
-      const uint64_t* sc = tsc + (size_t)warp * E;
-      const uint32_t want = epoch + (uint32_t)l + 1u;
-      float* prob = rprob + (size_t)warp * E32;
-      if (E <= 64)
-        layer_topk<2>(sc, want, E, k, W.bias, prob, id, wv, wait_ns, p.status, gave_up, l);
-      else
-        layer_topk<16>(sc, want, E, k, W.bias, prob, id, wv, wait_ns, p.status, gave_up, l);
-      MOE_WSTAMP(l, 4);
+    auto finish_routes = [&](int id, float wv) {     // the token warps
       if (lane < k) {
         rids[warp * k + lane] = id;
         rw[warp * k + lane] = wv;
@@ -555,6 +631,48 @@ __global__ void __launch_bounds__(kLT, 1)
       if (warp == 0) {
         build_route_table_warp(rt, rids, rw, T * k, E);
         MOE_WSTAMP(l, 7);
+      }
+    };
+    const uint32_t want = epoch + (uint32_t)l + 1u;
+    if (!split_sel) {
+      if (warp < T) {
+        int id;
+        float wv;
+        layer_topk<2>(tsc + (size_t)warp * E, want, E, k, W.bias, rprob + (size_t)warp * E32, id,
+                      wv, wait_ns, p.status, gave_up, l);
+        MOE_WSTAMP(l, 4);
+        finish_routes(id, wv);
+      }
+    } else {
+      if (warp < T) {
+        uint64_t v[16];
+        poll_scores<16>(tsc + (size_t)warp * E, want, E, v, wait_ns, p.status, gave_up);
+        MOE_WSTAMP(l, 5);
+        float* sc_s = rprob + (size_t)warp * E32;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int e = lane + 32 * i;
+          if (e < E) sc_s[e] = __uint_as_float((uint32_t)v[i]);
+        }
+      }
+      __syncthreads();
+      if (tt < T) {
+        float* sc_s = rprob + (size_t)tt * E32;
+        if (nsel == 1)
+          topk_part<1>(sc_s, bsel, sbase, E, k, rcand + (size_t)warp * k);
+        else if (nsel == 2)
+          topk_part<2>(sc_s, bsel, sbase, E, k, rcand + (size_t)warp * k);
+        else
+          topk_part<4>(sc_s, bsel, sbase, E, k, rcand + (size_t)warp * k);
+      }
+      __syncthreads();
+      if (warp < T) {
+        const int id = topk_merge(rcand + (size_t)warp * Wt * k, Wt * k, k);
+        MOE_WSTAMP(l, 6);
+        const float* prob = rprob + (size_t)warp * E32;
+        const float wv = warp_renorm(lane < k ? prob[id] : 0.0f, k);
+        MOE_WSTAMP(l, 4);
+        finish_routes(id, wv);
       }
     }
     __syncthreads();

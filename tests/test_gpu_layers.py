@@ -185,3 +185,38 @@ def test_layers_argument_errors():
     with pytest.raises(moe.MoeError) as e:                # more than 16 tokens
         moe.iq4nl_decode_layers(shape, spec(Ls), big, ws)
     assert e.value.status == moe.MOE_ERR_INVALID_ARG
+
+
+# (experts, k, tokens): the one-warp selection (64 experts) and the selection
+# spread over the warps (1, 2, 3 and 4 tokens; a warp range with no expert)
+@pytest.mark.parametrize("E,k,T", [(64, 4, 1), (512, 10, 1), (512, 10, 2), (384, 6, 3),
+                                   (100, 16, 4), (512, 16, 4)])
+def test_layers_exact_ties(E, k, T):
+    # keys with exact ties (zero router rows, biases on a 1/64 grid): every
+    # layer's ordered ids equal the oracle's, ties to the lower index
+    from synth.layers import bf16_tensor
+    moe = lib()
+    s = synth.Shape(f"layer ties E{E}", 256, 256, E, k, T, 2)
+    Ls = layers_of(s, 2, seed=17)
+    shape = moe_shape(s)
+    assert moe.launches_per_call(shape, T, moe.call_decode_layers(2, False)) == 1
+    rng = np.random.default_rng(E * 7 + T)
+    spec_t, routers = [], []
+    for L in Ls:
+        wr_host = np.zeros((E, s.H), np.uint16)
+        bias = (rng.integers(0, 6, E) / 64.0).astype(np.float32)
+        routers.append((wr_host, bias))
+        spec_t.append((weights_of(L), bf16_tensor(wr_host, DEV), torch.from_numpy(bias).to(DEV)))
+    xs = np.stack([synth.x_rows(9, l, s.H, T) for l in range(2)])
+    ws = moe.workspace(shape, T, moe.DECODE, DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ids, w, y = moe.iq4nl_decode_layers(shape, spec_t, bf16_tensor(xs, DEV), ws, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ids, w, y = ids.cpu().numpy(), w.cpu().numpy(), y.cpu().numpy()
+    for l, (L, (wr_host, bias)) in enumerate(zip(Ls, routers)):
+        ids_ref, w_ref, gap, _ = oracle.route(wr_host, bias, xs[l], k)
+        assert gap[0] == 0.0                                   # the cut is inside a tie
+        assert np.array_equal(ids[l], ids_ref), l              # order included
+        assert np.allclose(w[l], w_ref, rtol=2e-6, atol=0)
+        check_close(y[l], oracle_layer(L, xs[l], ids_ref, w_ref), f"layer ties E{E} T{T} {l}")
