@@ -226,7 +226,12 @@ moe_status moe_iq4nl_decode_layers(const moe_shape* shape, int32_t n_layers,
  *    Calls whose work may overlap on the GPU (other streams, other threads
  *    without ordering between their streams) race on it and give wrong
  *    results. Order them on one stream, or use moe_iq4nl_decode with a
- *    workspace each. */
+ *    workspace each.
+ *  - The kept address belongs to the device's current context. Do not call
+ *    this function after cudaDeviceReset (or anything else that destroys that
+ *    context) in the same process: the kept address is not looked up again
+ *    and no longer names the scratch. Use moe_iq4nl_decode with a workspace
+ *    in a process that resets its devices. */
 #define MOE_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
 moe_status moe_iq4nl_decode_static(const moe_shape* shape, const moe_expert_weights* w,
                                    const uint16_t* x, int32_t T, const int32_t* ids,

@@ -30,6 +30,9 @@ std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices];
 
 // Set-up, once per device, with that device current: the scratch's address.
+// It is kept for the life of the process and never looked up again, so it goes
+// stale if the device's context is destroyed (cudaDeviceReset); moe.h rules
+// out calls after a reset.
 moe_status scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
