@@ -310,7 +310,13 @@ template <bool GATEUP, bool RAW>
 struct GemmCfg {
   static constexpr int kCtl = RAW ? 3 : 2;                        // control warps
   static constexpr int kDq = (RAW && GATEUP) ? 16 : 8;            // dequantising warps
-  static constexpr int kThreads = (kCtl + kDq) * 32;
+  // Down: four epilogue warps of their own and two accumulators (N <= 256
+  // columns each), so that a tile's epilogue overlaps the next tile's MMAs.
+  // Gate/up needs all 512 TMEM columns for one tile: its dequantising warps
+  // run the epilogue.
+  static constexpr int kEpi = GATEUP ? 0 : 4;
+  static constexpr int kAcc = GATEUP ? 1 : 2;
+  static constexpr int kThreads = (kCtl + kDq + kEpi) * 32;
   static constexpr int kA = kTM * kTK * 2;                        // 16 KB
   static constexpr int kB = kTN * kTK * 2;                        // 32 KB
   static constexpr int kStage = (GATEUP ? 2 : 1) * kA + kB;
@@ -320,7 +326,7 @@ struct GemmCfg {
   static constexpr int kRawStage = (GATEUP ? 2 : 1) * kRawMat;
   static constexpr int kRawRing = 2;                              // raw ring depth
   static constexpr int kRawStages = RAW ? kRawRing : 0;           // raw stages allocated
-  static constexpr int kBars = 3 * kStages + 2 + 2 * kRawStages;
+  static constexpr int kBars = 3 * kStages + 2 * kAcc + 2 * kRawStages;
   static constexpr size_t kTotal =
       1024 /*align slack*/ + (size_t)kStages * kStage + (size_t)kRawStages * kRawStage + 4096;
 };
@@ -369,9 +375,9 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
   uint64_t* full_a = bars;
   uint64_t* full_b = bars + S::kStages;
   uint64_t* empty = bars + 2 * S::kStages;
-  uint64_t* acc_full = bars + 3 * S::kStages;
-  uint64_t* acc_empty = acc_full + 1;
-  uint64_t* full_raw = acc_empty + 1;
+  uint64_t* acc_full = bars + 3 * S::kStages;       // [kAcc]
+  uint64_t* acc_empty = acc_full + S::kAcc;         // [kAcc]
+  uint64_t* full_raw = acc_empty + S::kAcc;
   uint64_t* empty_raw = full_raw + S::kRawStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + S::kBars);
   int* boff = reinterpret_cast<int*>(tmem_slot + 4);           // [E+2] bucket offsets
@@ -384,8 +390,10 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
       mbar_init(&full_b[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(acc_full, 1);
-    mbar_init(acc_empty, S::kDq);
+    for (int b = 0; b < S::kAcc; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], S::kEpi ? S::kEpi : S::kDq);
+    }
     for (int s = 0; s < S::kRawStages; ++s) {
       mbar_init(&full_raw[s], 1);
       mbar_init(&empty_raw[s], S::kDq);
@@ -463,7 +471,9 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
         const TileInfo ti = tile_info(t);
         const int K = ti.bucket < p.E ? p.K : p.Ks;
         const uint32_t idesc = idesc_f16_f32(kTM, (ti.nvalid + 15) & ~15);
-        if (!mbar_wait(acc_empty, (tc & 1) ^ 1, p.status)) break;
+        const int ab = tc % S::kAcc;
+        const uint32_t acc = tmem + (uint32_t)(ab * kTN);
+        if (!mbar_wait(&acc_empty[ab], ((tc / S::kAcc) & 1) ^ 1, p.status)) break;
         tc_fence_after();
         PF_STAMP(tc, 0, global_timer_ns());
         PF_STAMP(tc, 6, (uint64_t)ti.nvalid);
@@ -483,14 +493,14 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
 #pragma unroll
           for (int kk = 0; kk < kTK / 16; ++kk) {
             const uint32_t accum = (ks > 0 || kk > 0) ? 1u : 0u;
-            tc_mma_f16(tmem, ad0 + 2 * kk, bd + 2 * kk, idesc, accum);
-            if (GATEUP) tc_mma_f16(tmem + kTN, ad1 + 2 * kk, bd + 2 * kk, idesc, accum);
+            tc_mma_f16(acc, ad0 + 2 * kk, bd + 2 * kk, idesc, accum);
+            if (GATEUP) tc_mma_f16(acc + kTN, ad1 + 2 * kk, bd + 2 * kk, idesc, accum);
           }
           tc_commit(&empty[s]);
         }
         if (tc < 0) break;
         PF_STAMP(tc, 1, global_timer_ns());
-        tc_commit(acc_full);
+        tc_commit(&acc_full[ab]);
       }
     }
   } else if (RAW && warp == 2) {
@@ -519,8 +529,8 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
         if (!ok) break;
       }
     }
-  } else {
-    // ---- dequantise weight tiles, then the epilogue of each tile
+  } else if (warp < S::kCtl + S::kDq) {
+    // ---- dequantise weight tiles (and, for gate/up, the epilogue of each tile)
     const int d = threadIdx.x - S::kCtl * 32;
     const int dw = warp - S::kCtl;
     const int r = d & (kTM - 1);
@@ -642,6 +652,7 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
       }
       if (!ok) break;
       if (warp == S::kCtl && lane == 0) PF_STAMP(tc, 3, global_timer_ns());
+      if constexpr (S::kEpi == 0) {
       // epilogue: TMEM lanes of this warp's quarter, a share of the token columns
       if (!mbar_wait(acc_full, tc & 1, p.status)) { ok = false; break; }
       tc_fence_after();
@@ -653,31 +664,54 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
       for (int c = 0; c < kCols; c += 32) {
         const int col = ch * kCols + c;
         if (col >= ti.nvalid) break;            // warp-uniform
-        uint32_t g[32];
+        uint32_t g[32], u[32];
         tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + col, g);
-        if (GATEUP) {
-          uint32_t u[32];
-          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + kTN + col, u);
-          tmem_ld_wait();
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + kTN + col, u);
+        tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (col + j < ti.nvalid) {
-              const float hv = silu_mul(__uint_as_float(g[j]), __uint_as_float(u[j]));
-              p.h[(size_t)(ti.row0 + ti.n0 + col + j) * p.ldh + mrow] = __float2half_rn(hv);
-            }
+        for (int j = 0; j < 32; ++j) {
+          if (col + j < ti.nvalid) {
+            const float hv = silu_mul(__uint_as_float(g[j]), __uint_as_float(u[j]));
+            p.h[(size_t)(ti.row0 + ti.n0 + col + j) * p.ldh + mrow] = __float2half_rn(hv);
           }
-        } else {
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (col + j < ti.nvalid)
-              p.o[(size_t)(ti.row0 + ti.n0 + col + j) * p.ldo + mrow] = __uint_as_float(g[j]);
         }
       }
       tc_fence_before();
       __syncwarp();
       if (warp == S::kCtl && lane == 0) PF_STAMP(tc, 5, global_timer_ns());
       if (lane == 0) mbar_arrive(acc_empty);
+      }
+    }
+  }
+  if constexpr (S::kEpi > 0) {
+    if (warp >= S::kCtl + S::kDq) {
+      // ---- epilogue warps: each takes its TMEM lane quarter (32 weight rows)
+      // and every token column of the tile, from the tile's accumulator
+      const int q = warp & 3;
+      int tc = 0;
+      for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tc) {
+        const TileInfo ti = tile_info(t);
+        const int ab = tc % S::kAcc;
+        if (!mbar_wait(&acc_full[ab], (tc / S::kAcc) & 1, p.status)) break;
+        tc_fence_after();
+        if (warp == S::kCtl + S::kDq && lane == 0) PF_STAMP(tc, 4, global_timer_ns());
+        const int mrow = ti.m0 + q * 32 + lane;
+        const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * kTN);
+        for (int col = 0; col < kTN; col += 32) {
+          if (col >= ti.nvalid) break;            // warp-uniform
+          uint32_t g[32];
+          tmem_ld32(base + col, g);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (col + j < ti.nvalid)
+              p.o[(size_t)(ti.row0 + ti.n0 + col + j) * p.ldo + mrow] = __uint_as_float(g[j]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (warp == S::kCtl + S::kDq && lane == 0) PF_STAMP(tc, 5, global_timer_ns());
+        if (lane == 0) mbar_arrive(&acc_empty[ab]);
+      }
     }
   }
   tc_fence_before();
