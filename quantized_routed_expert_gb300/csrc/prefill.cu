@@ -78,13 +78,10 @@ PrefillLayout prefill_layout(const moe_shape& s, int64_t T) {
 // [0, n_valid); the shared expert's bucket (every token, in order) follows.
 struct BucketParams {
   const int32_t* ids;
-  const float* w;
   int T, k, E, n_shared;
   int32_t* bucket_off;   // [E+2]
   int32_t* row_of;       // [T*k]
   int32_t* row_tok;      // [rows]
-  int32_t* comb_row;     // [T][k+1]: combine order (shared first, then experts ascending)
-  float* comb_w;         // [T][k+1]
   uint32_t* status;
 };
 
@@ -207,49 +204,59 @@ __global__ void __launch_bounds__(kBucketThreads) pf_bucket_kernel(BucketParams 
   }
   if (p.n_shared)
     for (int t = tid; t < p.T; t += kBucketThreads) p.row_tok[n_valid + t] = t;
-  __syncthreads();     // row_of complete (this CTA's global writes)
-  // per token: the rows to combine, shared expert first, then experts
-  // ascending (rows are grouped by expert: ascending rows); each routed entry
-  // goes to its rank among the token's rows
-  const int kk = p.k + 1;
-#pragma unroll 1
-  for (int t = tid; t < p.T; t += kBucketThreads) {
-    int32_t* cr = p.comb_row + (size_t)t * kk;
-    float* cw = p.comb_w + (size_t)t * kk;
-    const int first = p.n_shared ? 1 : 0;
-    if (p.n_shared) {
-      cr[0] = n_valid + t;
-      cw[0] = 1.0f;
-    }
-    int rows[MOE_MAX_TOP_K];
-#pragma unroll
-    for (int j = 0; j < MOE_MAX_TOP_K; ++j) rows[j] = j < p.k ? p.row_of[t * p.k + j] : -1;
-    int nv = 0;
-#pragma unroll
-    for (int j = 0; j < MOE_MAX_TOP_K; ++j) {
-      if (rows[j] < 0) continue;
-      int rank = 0;
-#pragma unroll
-      for (int i = 0; i < MOE_MAX_TOP_K; ++i) rank += rows[i] >= 0 && rows[i] < rows[j];
-      cr[first + rank] = rows[j];
-      cw[first + rank] = p.w[t * p.k + j];
-      ++nv;
-    }
-    for (int j = first + nv; j < kk; ++j) {
-      cr[j] = -1;
-      cw[j] = 0.0f;
-    }
-  }
   if (tid == 0 && p.status && invalid)
     atomicAdd(p.status, (uint32_t)(invalid < 0xFFFF ? invalid : 0xFFFF));
 }
 
 // ---------------------------------------------------------------------------
-// 2. Activations in bucket order, fp16 (round to nearest even from bf16).
+// 2. Activations in bucket order, fp16 (round to nearest even from bf16), and
+// each token's combine list: its rows in the fixed order of the sum (shared
+// expert first, then experts ascending: rows are grouped by expert, so
+// ascending rows) with their weights.
+struct CombineListParams {
+  const int32_t* row_of;   // [T*k], -1 for an invalid pair
+  const float* w;          // [T*k]
+  int T, k, n_shared;
+  int32_t* comb_row;       // [T][k+1]
+  float* comb_w;           // [T][k+1]
+};
 __global__ void pf_gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ bucket_off,
-                                 const int32_t* __restrict__ row_tok, int E, int H, __half* xs) {
+                                 const int32_t* __restrict__ row_tok, int E, int H, __half* xs,
+                                 const CombineListParams cl) {
   pdl_wait();
   pdl_trigger();
+  {
+    const int n_valid = bucket_off[E];
+    const int kk = cl.k + 1;
+    const int first = cl.n_shared ? 1 : 0;
+#pragma unroll 1
+    for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < cl.T; t += gridDim.x * blockDim.x) {
+      int32_t* cr = cl.comb_row + (size_t)t * kk;
+      float* cw = cl.comb_w + (size_t)t * kk;
+      if (cl.n_shared) {
+        cr[0] = n_valid + t;
+        cw[0] = 1.0f;
+      }
+      int rows[MOE_MAX_TOP_K];
+#pragma unroll
+      for (int j = 0; j < MOE_MAX_TOP_K; ++j) rows[j] = j < cl.k ? cl.row_of[t * cl.k + j] : -1;
+      int nv = 0;
+#pragma unroll
+      for (int j = 0; j < MOE_MAX_TOP_K; ++j) {
+        if (rows[j] < 0) continue;
+        int rank = 0;
+#pragma unroll
+        for (int i = 0; i < MOE_MAX_TOP_K; ++i) rank += rows[i] >= 0 && rows[i] < rows[j];
+        cr[first + rank] = rows[j];
+        cw[first + rank] = cl.w[t * cl.k + j];
+        ++nv;
+      }
+      for (int j = first + nv; j < kk; ++j) {
+        cr[j] = -1;
+        cw[j] = 0.0f;
+      }
+    }
+  }
   const int rows = bucket_off[E + 1];
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -873,15 +880,15 @@ cudaError_t launch_prefill(const moe_shape& s, const moe_expert_weights& w, cons
   __half* h16 = reinterpret_cast<__half*>(ws + L.h16);
   float* o = reinterpret_cast<float*>(ws + L.o);
 
-  BucketParams bp{ids, weights, T, k, E, s.n_shared, boff, row_of, row_tok, comb_row, comb_w,
-                  status};
+  BucketParams bp{ids, T, k, E, s.n_shared, boff, row_of, row_tok, status};
   const size_t bsm = (size_t)kBucketWarps * E * 4;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(pf_bucket_kernel), bsm);
   if (e != cudaSuccess) return e;
   e = launch_ex(pf_bucket_kernel, dim3(1), dim3(kBucketThreads), bsm, pdl, stream, bp);
   if (e != cudaSuccess) return e;
+  const CombineListParams cl{(const int32_t*)row_of, weights, T, k, s.n_shared, comb_row, comb_w};
   e = launch_ex(pf_gather_kernel, dim3(num_sms * 4), dim3(256), 0, pdl, stream, x,
-                (const int32_t*)boff, (const int32_t*)row_tok, E, H, x16);
+                (const int32_t*)boff, (const int32_t*)row_tok, E, H, x16, cl);
   if (e != cudaSuccess) return e;
 
   TmapSet tm_x, tm_h;
