@@ -22,6 +22,14 @@
 // next layer's shared-expert rows as soon as a warp's slots free up in the
 // down phase.
 //
+// Fifteen warps compute; the sixteenth only issues the weight copies. A bulk
+// copy is taken in by the copy engine no faster than memory delivers, so the
+// thread that issues it stalls meanwhile: with every computing warp issuing
+// its own rows, the issuing took as many cycles as the dot products. The
+// copy warp's lane w keeps computing warp w's two slots filled in the warp's
+// unit order, each slot once the warp has released its previous unit (an
+// mbarrier arrival) and its rows are known (the layer's route table built).
+//
 // Every wait is bounded: waits on other CTAs by the host-set barrier limit,
 // waits on this CTA's own copies by the fixed 2 s limit (after a timeout each
 // warp still drains its copies before the kernel ends).
@@ -43,14 +51,23 @@ __device__ uint64_t g_prof[kProfCtas * kProfLayers * kProfPhases];
 // per warp: [0] routed gate/up first unit landed, [1] routed gate/up done,
 // [2] down unit landed, [3] down done, [4] top-k and weights done (token
 // warps) or the shared expert's rows done (the other warps),
-// [5] every score seen, [6] selection done, [7] route table built (warp 0)
-constexpr int kProfW = 8;
+// [5] every score seen, [6] selection done, [7] route table built (warp 0),
+// [8..11] clock64 cycles of the routed gate/up loop: waiting, computing,
+// issuing copies, the whole loop; [12] its units; [13..15] the down loop's
+// waiting, computing, issuing cycles
+constexpr int kProfW = 16;
 __device__ uint64_t g_profw[kProfCtas * kProfLayers * 16 * kProfW];
 #define MOE_WSTAMP(l, k)                                                                      \
   do {                                                                                        \
     if ((threadIdx.x & 31) == 0 && (l) < kProfLayers && blockIdx.x < kProfCtas)              \
       g_profw[(((size_t)blockIdx.x * kProfLayers + (l)) * 16 + (threadIdx.x >> 5)) * kProfW + \
               (k)] = global_timer_ns();                                                       \
+  } while (0)
+#define MOE_WPUT(l, k, v)                                                                     \
+  do {                                                                                        \
+    if ((threadIdx.x & 31) == 0 && (l) < kProfLayers && blockIdx.x < kProfCtas)              \
+      g_profw[(((size_t)blockIdx.x * kProfLayers + (l)) * 16 + (threadIdx.x >> 5)) * kProfW + \
+              (k)] = (v);                                                                     \
   } while (0)
 #define MOE_STAMP(l, ph)                                                                     \
   do {                                                                                       \
@@ -64,18 +81,23 @@ __device__ uint64_t g_profw[kProfCtas * kProfLayers * 16 * kProfW];
 #define MOE_WSTAMP(l, k) \
   do {                   \
   } while (0)
+#define MOE_WPUT(l, k, v) \
+  do {                    \
+  } while (0)
 #endif
 
-constexpr int kLW = 16;            // warps per CTA
-constexpr int kLT = kLW * 32;      // threads per CTA
-constexpr int kLSlots = 2;         // bulk-copy slots per warp
+constexpr int kLW = 15;            // computing warps per CTA (warp 15 issues the copies)
+constexpr int kLT = kLW * 32;      // computing threads per CTA
+constexpr int kLTP = kLT + 32;     // threads per CTA: the computing warps and the copy warp
+constexpr int kLSlots = 2;         // bulk-copy slots per computing warp
+constexpr int kLBar = 2;           // named barrier of the computing warps
 
 // Sync words of this kernel in the decode workspace (after the fused
 // kernel's four): h arrivals, y arrivals, departures, epoch base.
 constexpr int kSyncH = 4, kSyncY = 5, kSyncOut = 6, kSyncEpoch = 7;
 
 struct LayersSmem {
-  size_t xq, slots, bars, recs, part, rwr, rx, rpart, rprob, rids, rw, rcand, stage,
+  size_t xq, slots, bars, ebars, recs, part, rwr, rx, rpart, rprob, rids, rw, rcand, stage,
       stage_bytes, total, slot_bytes;
 };
 
@@ -96,7 +118,10 @@ __host__ __device__ inline LayersSmem layers_smem(int H, int F, int Fs, int ns, 
   m.xq = align_up_dev(sizeof(RouteTable), 128);
   m.slots = align_up_dev(m.xq + (size_t)T * dqvec_words(H) * 4, 128);
   m.bars = m.slots + (size_t)kLW * kLSlots * m.slot_bytes;
-  m.recs = align_up_dev(m.bars + (size_t)(kLW * kLSlots + 4) * 8, 128);
+  // the slots' "free" barriers, then the copy warp's words: the layer whose
+  // routes are known, the stop flag, the units issued per computing warp
+  m.ebars = align_up_dev(m.bars + (size_t)(kLW * kLSlots + 4) * 8, 16);
+  m.recs = align_up_dev(m.ebars + (size_t)kLW * kLSlots * 8 + 8 + (size_t)kLW * 4, 128);
   const size_t recs =
       (size_t)T * k * dqvec_words(F) * 4 + (ns ? (size_t)T * dqvec_words(Fs) * 4 : 0);
   m.part = align_up_dev(m.recs + recs, 16);
@@ -146,6 +171,30 @@ __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
 
 __device__ __forceinline__ void fence_proxy_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// CTA barriers of the computing warps only (the copy warp never joins them).
+__device__ __forceinline__ void csync() { asm volatile("bar.sync %0, %1;" ::"n"(kLBar), "n"(kLT) : "memory"); }
+__device__ __forceinline__ bool csync_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
+      " bar.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u), "n"(kLBar), "n"(kLT)
+      : "memory");
+  return r != 0;
+}
+// Whether the phase of parity `parity` of an mbarrier has completed (no wait).
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
 }
 
 // What a warp needs to issue the copies of its units. Its sequence: per layer
@@ -341,7 +390,7 @@ __device__ __forceinline__ void layer_topk(const uint64_t* sc, uint32_t want, in
 // (key bits << 32) | expert; a pick made after the range ran out of keys has
 // key bits 0. sc_prob holds the token's scores and gets its sigmoids.
 template <int NPL>
-__device__ __forceinline__ void topk_part(float* sc_prob, const float (&bsel)[4], int base, int E,
+__device__ __forceinline__ void topk_part(float* sc_prob, const float (&bsel)[8], int base, int E,
                                           int k, uint64_t* cand) {
   const int lane = threadIdx.x & 31;
   uint32_t v[NPL];
@@ -396,7 +445,7 @@ __device__ __forceinline__ int topk_merge(const uint64_t* cand, int n, int k) {
 }
 
 template <int MAXT, int LPR>
-__global__ void __launch_bounds__(kLT, 1)
+__global__ void __launch_bounds__(kLTP, 1)
     decode_layers_kernel(const __grid_constant__ DecodeParams p,
                          const __grid_constant__ LayerTable lt) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -413,6 +462,10 @@ __global__ void __launch_bounds__(kLT, 1)
   uint64_t* rwr_bar = recs_bar + 1;               // router rows of a layer
   uint32_t* epoch_s = reinterpret_cast<uint32_t*>(rwr_bar + 1);
   volatile uint32_t* gave_up = epoch_s + 1;       // this CTA saw a wait time out
+  uint64_t* ebars = reinterpret_cast<uint64_t*>(smem + S.ebars);     // slot freed
+  volatile uint32_t* routes_known = reinterpret_cast<uint32_t*>(ebars + kLW * kLSlots);
+  volatile uint32_t* stop = routes_known + 1;
+  volatile uint32_t* final_iss = stop + 1;       // units the copy warp issued, per warp
   uint32_t* recs = reinterpret_cast<uint32_t*>(smem + S.recs);
   float* part = reinterpret_cast<float*>(smem + S.part);
   uint16_t* rx = reinterpret_cast<uint16_t*>(smem + S.rx);
@@ -430,8 +483,12 @@ __global__ void __launch_bounds__(kLT, 1)
   if (threadIdx.x == 0) {
 #pragma unroll 1
     for (int i = 0; i < kLW * kLSlots + 2; ++i) mbar_init(&bars[i], 1);
+#pragma unroll 1
+    for (int i = 0; i < kLW * kLSlots; ++i) mbar_init(&ebars[i], 1);
     mbar_fence_init();
     *gave_up = 0u;
+    *routes_known = 0u;
+    *stop = 0u;
   }
   __syncthreads();
 
@@ -440,47 +497,132 @@ __global__ void __launch_bounds__(kLT, 1)
   const RowRange dn = split_rows(H, 1, cta, G);
   const int nrows_cta = dn.b - dn.a;
   const int ngroups = (nrows_cta + RG - 1) / RG;
-  auto count = [&](int a, int b) { return a + warp < b ? (b - a - warp + kLW - 1) / kLW : 0; };
+  // units of computing warp w among the rows [a, b) of a layer, dealt round-robin
+  auto count_w = [&](int w, int a, int b) { return a + w < b ? (b - a - w + kLW - 1) / kLW : 0; };
+  auto count = [&](int a, int b) { return count_w(warp, a, b); };
   // The shared expert's rows go to the warps that do not take a token's
   // top-k (warps T..15): they compute them while the scores are exchanged.
-  const int sh_w = warp - T, sh_nw = kLW - T;
-  const int n_sh = (sh_w >= 0 && shr.a + sh_w < shr.b) ? (shr.b - shr.a - sh_w + sh_nw - 1) / sh_nw
-                                                      : 0;
+  const int sh_nw = kLW - T;
+  auto n_sh_of = [&](int w) {
+    const int sw = w - T;
+    return (sw >= 0 && shr.a + sw < shr.b) ? (shr.b - shr.a - sw + sh_nw - 1) / sh_nw : 0;
+  };
+  const int sh_w = warp - T;
+  const int n_sh = n_sh_of(warp);
   const int re0 = lr_e0(E, cta, G), re1 = lr_e0(E, cta + 1, G);
   const int ne = re1 - re0;
   const uint64_t pol = l2_evict_first_policy();
 
-  LUnitPlan up;
-  up.myslots = slots + (size_t)warp * kLSlots * S.slot_bytes;
-  up.slot_bytes = S.slot_bytes;
-  up.mybar = bars + warp * kLSlots;
-  up.pol = pol;
-  up.warp = warp;
-  up.layer = 0;
-  up.ub = 0;
-  up.n_sh = n_sh;
-  up.n_rt = up.rr_a = up.n_dn = 0;
-  up.sh_a = shr.a;
-  up.sh_w = sh_w;
-  up.sh_nw = sh_nw;
-  up.ngroups = ngroups;
-  up.nrows_cta = nrows_cta;
-  up.dn_a = dn.a;
-  up.rg = RG;
-  int issued = 0, consumed = 0;
+  // The unit sequence of computing warp w (per layer: its shared gate/up
+  // rows, routed gate/up rows, down groups), before the layer's routes.
+  auto plan_of = [&](int w) {
+    LUnitPlan u;
+    u.myslots = slots + (size_t)w * kLSlots * S.slot_bytes;
+    u.slot_bytes = S.slot_bytes;
+    u.mybar = bars + w * kLSlots;
+    u.pol = pol;
+    u.warp = w;
+    u.layer = 0;
+    u.ub = 0;
+    u.n_sh = n_sh_of(w);
+    u.n_rt = u.rr_a = u.n_dn = 0;
+    u.sh_a = shr.a;
+    u.sh_w = w - T;
+    u.sh_nw = sh_nw;
+    u.ngroups = ngroups;
+    u.nrows_cta = nrows_cta;
+    u.dn_a = dn.a;
+    u.rg = RG;
+    return u;
+  };
+  // ... and its routed and down units once the route table is built
+  auto plan_routes = [&](LUnitPlan& u) {
+    const RowRange rr = split_rows(rt.n_slots * p.F, 1, cta, G);
+    u.n_rt = count_w(u.warp, rr.a, rr.b);
+    u.rr_a = rr.a;
+    const int n_dn_units = (rt.n_slots + p.n_shared) * ngroups;
+    u.n_dn = u.warp < n_dn_units ? (n_dn_units - u.warp + kLW - 1) / kLW : 0;
+  };
+
+  if (warp == kLW) {
+    // ---- the copy warp: lane w < kLW issues computing warp w's units in
+    // order, each once its slot is free (the warp's release of the unit two
+    // back) and its rows are known (shared rows always, routed and down rows
+    // once the layer's route table is built). The computing warps never
+    // issue a weight copy, so they never stall while the copy engine takes
+    // one in.
+    const int w = lane;
+    const bool mine = w < kLW;
+    LUnitPlan u = plan_of(mine ? w : 0);
+    int iss = 0, lim = mine ? u.n_sh : 0, lp = 0;
+    bool known = false;
+    const uint64_t idle_ns = 2 * kWaitLimitNs + p.wait_ns;
+    uint64_t t_act = global_timer_ns();
+#pragma unroll 1
+    while (lp < Lyr) {
+      bool any = false;
+#pragma unroll 1
+      for (;;) {
+        bool can = mine && iss < lim;
+        if (can && iss >= kLSlots)
+          can = mbar_test(&ebars[w * kLSlots + iss % kLSlots],
+                          (uint32_t)(((iss / kLSlots) + 1) & 1));
+        if (!__any_sync(0xFFFFFFFFu, can)) break;
+        if (can) {
+          issue_unit_layers(p, lt, rt, u, iss);
+          ++iss;
+        }
+        any = true;
+      }
+      if (!known) {
+        if (*routes_known >= (uint32_t)(lp + 1)) {     // layer lp's route table is built
+          __threadfence_block();
+          if (mine) {
+            plan_routes(u);
+            lim = u.ub + u.n_sh + u.n_rt + u.n_dn + (lp + 1 < Lyr ? u.n_sh : 0);
+          }
+          known = true;
+          any = true;
+        }
+      } else if (__all_sync(0xFFFFFFFFu, !mine || iss == lim)) {
+        // every unit of layer lp issued (and the next layer's shared rows)
+        u.ub += u.n_sh + u.n_rt + u.n_dn;
+        u.layer = lp + 1;
+        u.n_rt = u.rr_a = u.n_dn = 0;
+        ++lp;
+        known = false;
+        any = true;
+      }
+      if (*stop) break;
+      const uint64_t now = global_timer_ns();
+      if (any) {
+        t_act = now;
+      } else {
+        if (now - t_act > idle_ns) {
+          if (lane == 0 && p.status) atomicOr(p.status, MOE_STATUS_TIMEOUT);
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    if (mine) final_iss[w] = (uint32_t)iss;
+    __syncthreads();     // the computing warps' final barrier
+    return;
+  }
+
+  LUnitPlan up = plan_of(warp);
+  int consumed = 0;
   bool ok = true;
   int rwr_issued = -1, rwr_landed = -1;     // layers whose router rows were fetched / waited
   uint64_t wait_ns = p.wait_ns;             // 0 once this CTA saw a timeout
 
-  auto issue_upto = [&](int limit) {
-    while (issued < limit && issued - consumed < kLSlots) {
-      if (lane == 0) issue_unit_layers(p, lt, rt, up, issued);
-      ++issued;
-    }
-  };
   auto wait_unit = [&](int j) {     // the whole warp; the result is the warp's
     return __all_sync(0xFFFFFFFFu,
                       mbar_wait(&up.mybar[j % kLSlots], (uint32_t)((j / kLSlots) & 1), p.status));
+  };
+  auto release_unit = [&](int j) {  // the warp is done with unit j's slot
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ebars[warp * kLSlots + j % kLSlots]);
   };
   auto issue_router_rows = [&](int l) {     // thread 0
     if (ne > 0) {
@@ -494,11 +636,10 @@ __global__ void __launch_bounds__(kLT, 1)
   // the stream finishes.
   if (threadIdx.x == 0) issue_router_rows(0);
   rwr_issued = 0;
-  issue_upto(n_sh);
   pdl_wait();
   pdl_trigger();
   if (threadIdx.x == 0) *epoch_s = ld_acquire_u32(&p.sync[kSyncEpoch]);
-  __syncthreads();
+  csync();
   const uint32_t epoch = *epoch_s;
 
 #pragma unroll 1
@@ -520,7 +661,7 @@ __global__ void __launch_bounds__(kLT, 1)
     if (l > 0) {
       if (threadIdx.x == 0)
         grid_wait(&p.sync[kSyncY], (uint32_t)(G * l), wait_ns, p.status, gave_up);
-      __syncthreads();
+      csync();
       if (*gave_up) wait_ns = 0;
     }
     MOE_STAMP(l, 1);
@@ -529,14 +670,14 @@ __global__ void __launch_bounds__(kLT, 1)
     else
       load_x_layer<false>(p.x + (p.chained ? (size_t)0 : (size_t)l * T * H), nullptr, T, H, rx,
                           xq, xq_words);
-    __syncthreads();
+    csync();
     MOE_STAMP(l, 2);
 
     // ---- scores of this CTA's experts: 16 chunks of H per expert, one warp
     // per (expert, chunk), chunk partials summed in a fixed order
     uint64_t* tsc = p.tscores + (size_t)(l & 1) * T * E;
     if (ne > 0) {
-      const bool landed = __syncthreads_and(mbar_wait(rwr_bar, (uint32_t)(l & 1), p.status));
+      const bool landed = csync_and(mbar_wait(rwr_bar, (uint32_t)(l & 1), p.status));
       rwr_landed = l;
       MOE_STAMP(l, 10);
       ok = ok && landed;
@@ -577,7 +718,7 @@ __global__ void __launch_bounds__(kLT, 1)
             if (t < T) rpart[(el * 16 + c) * T + t] = acc[t];
         }
       }
-      __syncthreads();
+      csync();
 #pragma unroll 1
       for (int i = threadIdx.x; i < ne * T; i += kLT) {
         const int el = i / T, t = i - el * T;
@@ -587,7 +728,7 @@ __global__ void __launch_bounds__(kLT, 1)
                        ((uint64_t)(epoch + (uint32_t)l + 1u) << 32) | __float_as_uint(sc));
       }
     }
-    __syncthreads();
+    csync();
     MOE_STAMP(l, 3);
 
     // ---- top-k: warp t takes token t, in every CTA; meanwhile the other
@@ -596,11 +737,12 @@ __global__ void __launch_bounds__(kLT, 1)
     // is spread over all warps: kLW / T warps per token.
     const bool split_sel = E > 64;
     const int Wt = kLW / T, tt = warp / Wt;
-    const int nsel = E <= Wt * 32 ? 1 : (E <= Wt * 64 ? 2 : 4);   // E <= 512, Wt >= 4
+    // experts per lane of a selecting warp: E <= 512 <= 256 Wt (Wt >= 3)
+    const int nsel = E <= Wt * 32 ? 1 : (E <= Wt * 64 ? 2 : (E <= Wt * 128 ? 4 : 8));
     const int sbase = (warp - tt * Wt) * 32 * nsel;
-    float bsel[4];
+    float bsel[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 8; ++i) {
       const int e = sbase + lane + 32 * i;
       bsel[i] = (split_sel && W.bias && tt < T && i < nsel && e < E) ? __ldg(W.bias + e) : 0.0f;
     }
@@ -612,9 +754,8 @@ __global__ void __launch_bounds__(kLT, 1)
         const uint8_t* d = up.myslots + (size_t)(j % kLSlots) * S.slot_bytes;
         const int f = shr.a + sh_w + sh_nw * (j - up.ub);
         gateup_unit_t<1, LPR>(p, rt, d, d + rbH, -1, f, xq, xq_words);
-        __syncwarp();
+        release_unit(j);
         ++consumed;
-        issue_upto(up.ub + n_sh);
       }
       MOE_WSTAMP(l, 4);
     }
@@ -655,17 +796,19 @@ __global__ void __launch_bounds__(kLT, 1)
           if (e < E) sc_s[e] = __uint_as_float((uint32_t)v[i]);
         }
       }
-      __syncthreads();
+      csync();
       if (tt < T) {
         float* sc_s = rprob + (size_t)tt * E32;
         if (nsel == 1)
           topk_part<1>(sc_s, bsel, sbase, E, k, rcand + (size_t)warp * k);
         else if (nsel == 2)
           topk_part<2>(sc_s, bsel, sbase, E, k, rcand + (size_t)warp * k);
-        else
+        else if (nsel == 4)
           topk_part<4>(sc_s, bsel, sbase, E, k, rcand + (size_t)warp * k);
+        else
+          topk_part<8>(sc_s, bsel, sbase, E, k, rcand + (size_t)warp * k);
       }
-      __syncthreads();
+      csync();
       if (warp < T) {
         const int id = topk_merge(rcand + (size_t)warp * Wt * k, Wt * k, k);
         MOE_WSTAMP(l, 6);
@@ -675,30 +818,36 @@ __global__ void __launch_bounds__(kLT, 1)
         finish_routes(id, wv);
       }
     }
-    __syncthreads();
+    csync();
     MOE_STAMP(l, 4);
+    if (threadIdx.x == 0) {       // the copy warp may now issue this layer's routed rows
+      __threadfence_block();
+      *routes_known = (uint32_t)(l + 1);
+    }
     if (*gave_up) wait_ns = 0;
 #pragma unroll 1
     for (int i = threadIdx.x; i < (T * k + (p.n_shared ? T : 0)) * rows_max; i += kLT)
       part[i] = 0.0f;
-    {
-      const RowRange rr = split_rows(rt.n_slots * p.F, 1, cta, G);
-      up.n_rt = count(rr.a, rr.b);
-      up.rr_a = rr.a;
-      const int n_dn_units = (rt.n_slots + p.n_shared) * ngroups;
-      up.n_dn = warp < n_dn_units ? (n_dn_units - warp + kLW - 1) / kLW : 0;
-    }
+    plan_routes(up);
     const int ub = up.ub, n_rt = up.n_rt, rr_a = up.rr_a;
     const int n_tot = n_sh + n_rt + up.n_dn;
-    const int limit = ub + n_tot + (l + 1 < Lyr ? n_sh : 0);
-    issue_upto(limit);
+#ifdef MOE_PROFILE
+    long long pw = 0, pc = 0, pi = 0, pl = clock64();
+#endif
 
     // ---- gate/up: the routed rows as they arrive (the shared expert's were
     // computed above)
 #pragma unroll 1
     for (int j = ub + n_sh; ok && j < ub + n_sh + n_rt; ++j) {
+#ifdef MOE_PROFILE
+      long long c0 = clock64();
+#endif
       ok = wait_unit(j);
       if (!ok) break;
+#ifdef MOE_PROFILE
+      long long c1 = clock64();
+      pw += c1 - c0;
+#endif
       if (j == ub + n_sh) MOE_WSTAMP(l, 0);
       const uint8_t* d = up.myslots + (size_t)(j % kLSlots) * S.slot_bytes;
       const int lj = j - ub;
@@ -708,20 +857,30 @@ __global__ void __launch_bounds__(kLT, 1)
         gateup_unit_t<1, LPR>(p, rt, d, d + rbH, sl, f, xq, xq_words);
       else
         gateup_unit_t<MAXT, LPR>(p, rt, d, d + rbH, sl, f, xq, xq_words);
-      __syncwarp();
+      release_unit(j);
       ++consumed;
-      issue_upto(limit);
+#ifdef MOE_PROFILE
+      pc += clock64() - c1;
+#endif
     }
 
     MOE_WSTAMP(l, 1);
+#ifdef MOE_PROFILE
+    MOE_WPUT(l, 8, (uint64_t)pw);
+    MOE_WPUT(l, 9, (uint64_t)pc);
+    MOE_WPUT(l, 10, (uint64_t)pi);
+    MOE_WPUT(l, 11, (uint64_t)(clock64() - pl));
+    MOE_WPUT(l, 12, (uint64_t)n_rt);
+    pw = pc = pi = 0;
+#endif
     // ---- h of this layer: every CTA's rows written
-    __syncthreads();
+    csync();
     MOE_STAMP(l, 5);
     if (threadIdx.x == 0) {
       grid_arrive(&p.sync[kSyncH]);
       grid_wait(&p.sync[kSyncH], (uint32_t)(G * (l + 1)), wait_ns, p.status, gave_up);
     }
-    __syncthreads();
+    csync();
     MOE_STAMP(l, 6);
     if (*gave_up) wait_ns = 0;
     if (S.stage_bytes) {
@@ -740,20 +899,27 @@ __global__ void __launch_bounds__(kLT, 1)
             bulk_g2s(dst, p.h_s + (size_t)j * p.Fs, rbS, recs_bar);
       }
       // wait even after an earlier timeout: no copy of this CTA stays in flight
-      const bool landed = __syncthreads_and(mbar_wait(recs_bar, (uint32_t)(l & 1), p.status));
+      const bool landed = csync_and(mbar_wait(recs_bar, (uint32_t)(l & 1), p.status));
       ok = ok && landed;
       if (ok) quant_h<true>(p, rt, stage, recs, threadIdx.x, kLT);
     } else {
       quant_h<false>(p, rt, nullptr, recs, threadIdx.x, kLT);
     }
-    __syncthreads();
+    csync();
     MOE_STAMP(l, 7);
 
     // ---- down
 #pragma unroll 1
     for (int j = ub + n_sh + n_rt; ok && j < ub + n_tot; ++j) {
+#ifdef MOE_PROFILE
+      long long c0 = clock64();
+#endif
       ok = wait_unit(j);
       if (!ok) break;
+#ifdef MOE_PROFILE
+      long long c1 = clock64();
+      pw += c1 - c0;
+#endif
       if (j == ub + n_sh + n_rt) MOE_WSTAMP(l, 2);
       const uint8_t* d = up.myslots + (size_t)(j % kLSlots) * S.slot_bytes;
       const int u = warp + kLW * (j - ub - n_sh - n_rt);
@@ -766,12 +932,19 @@ __global__ void __launch_bounds__(kLT, 1)
         down_unit_t<1, LPR>(p, rt, d, dsl, r0, nr, recs, part, rows_max);
       else
         down_unit_t<MAXT, LPR>(p, rt, d, dsl, r0, nr, recs, part, rows_max);
-      __syncwarp();
+      release_unit(j);
       ++consumed;
-      issue_upto(limit);
+#ifdef MOE_PROFILE
+      pc += clock64() - c1;
+#endif
     }
     MOE_WSTAMP(l, 3);
-    __syncthreads();
+#ifdef MOE_PROFILE
+    MOE_WPUT(l, 13, (uint64_t)pw);
+    MOE_WPUT(l, 14, (uint64_t)pc);
+    MOE_WPUT(l, 15, (uint64_t)pi);
+#endif
+    csync();
     MOE_STAMP(l, 8);
 
     // ---- combine in the fixed order: shared expert, then routed experts ascending
@@ -787,7 +960,7 @@ __global__ void __launch_bounds__(kLT, 1)
       }
       yl[(size_t)t * H + dn.a + r] = acc;
     }
-    __syncthreads();
+    csync();
     MOE_STAMP(l, 9);
     if (threadIdx.x == 0) grid_arrive(&p.sync[kSyncY]);
     // the records and partials are read: the next layer's router rows may
@@ -802,7 +975,7 @@ __global__ void __launch_bounds__(kLT, 1)
     // A failed wait on this CTA's own copies (a 2 s limit, not reached when
     // the weights are readable) ends the layers here: the slots' copy order is
     // no longer known. The counters above were still raised for this layer.
-    if (!__syncthreads_and(ok ? 1 : 0)) break;
+    if (!csync_and(ok)) break;
 
     // ---- the next layer's units follow this layer's
     up.ub += n_tot;
@@ -810,10 +983,17 @@ __global__ void __launch_bounds__(kLT, 1)
     up.n_rt = up.rr_a = up.n_dn = 0;
   }
 
+  // ---- the copy warp stops (it has issued everything unless the layers
+  // ended early) and reports how many units it issued per warp
+  if (threadIdx.x == 0) {
+    __threadfence_block();
+    *stop = 1u;
+  }
+  __syncthreads();
   // ---- drain this warp's bulk copies still in flight (after a timeout, or
   // rows fetched ahead for a layer that did not run), then the router rows
   // fetched ahead
-  while (consumed < issued) {
+  while (consumed < (int)final_iss[warp]) {
     wait_unit(consumed);
     ++consumed;
   }
@@ -821,7 +1001,7 @@ __global__ void __launch_bounds__(kLT, 1)
     mbar_wait(rwr_bar, (uint32_t)(rwr_issued & 1), p.status);
 
   // ---- leave: the last CTA out resets the counters and moves the epoch on
-  __syncthreads();
+  csync();
   if (threadIdx.x == 0) {
     const uint32_t old = atomicAdd(&p.sync[kSyncOut], 1u);
     if (old == (uint32_t)G - 1u) {
@@ -868,7 +1048,7 @@ bool layers_resident(const void* kfn, size_t smem) {
   bool ok = false;
   if (ensure_smem_attr(kfn, smem) == cudaSuccess) {
     int blocks = 0;
-    ok = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kfn, kLT, smem) == cudaSuccess &&
+    ok = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kfn, kLTP, smem) == cudaSuccess &&
          blocks >= 1;
   }
   cudaGetLastError();
@@ -937,7 +1117,7 @@ cudaError_t launch_decode_layers(const DecodeParams& p0, const LayerTable& lt, i
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_sms);
-    cfg.blockDim = dim3(kLT);
+    cfg.blockDim = dim3(kLTP);
     cfg.dynamicSmemBytes = sm;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -993,7 +1173,7 @@ extern "C" int moe_profile_stamps(void* host, size_t bytes) {
   const size_t n = sizeof(moe::g_prof) < bytes ? sizeof(moe::g_prof) : bytes;
   return cudaMemcpyFromSymbol(host, moe::g_prof, n) == cudaSuccess ? 0 : -1;
 }
-// Per-warp stamps (uint64 [256][64][16 warps][8]).
+// Per-warp stamps (uint64 [256][64][16 warps][16]).
 extern "C" int moe_profile_warp_stamps(void* host, size_t bytes) {
   const size_t n = sizeof(moe::g_profw) < bytes ? sizeof(moe::g_profw) : bytes;
   return cudaMemcpyFromSymbol(host, moe::g_profw, n) == cudaSuccess ? 0 : -1;
