@@ -54,8 +54,12 @@ __device__ uint64_t g_prof[kProfCtas * kProfLayers * kProfPhases];
 // [5] every score seen, [6] selection done, [7] route table built (warp 0),
 // [8..11] clock64 cycles of the routed gate/up loop: waiting, computing,
 // issuing copies, the whole loop; [12] its units; [13..15] the down loop's
-// waiting, computing, issuing cycles
-constexpr int kProfW = 16;
+// waiting, computing, issuing cycles; [16] / [17] written by the copy warp's
+// lane w: the layer's route table seen, its first routed unit issued;
+// [18] / [19] / [20] clock64 cycles of a token warp's top-k (polling
+// included), of finishing its routes, of warp 0's route table build and of
+// its per-warp plans for the copy warp
+constexpr int kProfW = 22;
 __device__ uint64_t g_profw[kProfCtas * kProfLayers * 16 * kProfW];
 #define MOE_WSTAMP(l, k)                                                                      \
   do {                                                                                        \
@@ -68,6 +72,12 @@ __device__ uint64_t g_profw[kProfCtas * kProfLayers * 16 * kProfW];
     if ((threadIdx.x & 31) == 0 && (l) < kProfLayers && blockIdx.x < kProfCtas)              \
       g_profw[(((size_t)blockIdx.x * kProfLayers + (l)) * 16 + (threadIdx.x >> 5)) * kProfW + \
               (k)] = (v);                                                                     \
+  } while (0)
+#define MOE_PSTAMP(l, w, k)                                                                   \
+  do {                                                                                        \
+    if ((l) < kProfLayers && blockIdx.x < kProfCtas)                                          \
+      g_profw[(((size_t)blockIdx.x * kProfLayers + (l)) * 16 + (w)) * kProfW + (k)] =         \
+          global_timer_ns();                                                                  \
   } while (0)
 #define MOE_STAMP(l, ph)                                                                     \
   do {                                                                                       \
@@ -83,6 +93,9 @@ __device__ uint64_t g_profw[kProfCtas * kProfLayers * 16 * kProfW];
   } while (0)
 #define MOE_WPUT(l, k, v) \
   do {                    \
+  } while (0)
+#define MOE_PSTAMP(l, w, k) \
+  do {                      \
   } while (0)
 #endif
 
@@ -119,9 +132,11 @@ __host__ __device__ inline LayersSmem layers_smem(int H, int F, int Fs, int ns, 
   m.slots = align_up_dev(m.xq + (size_t)T * dqvec_words(H) * 4, 128);
   m.bars = m.slots + (size_t)kLW * kLSlots * m.slot_bytes;
   // the slots' "free" barriers, then the copy warp's words: the layer whose
-  // routes are known, the stop flag, the units issued per computing warp
+  // routes are known, the stop flag, the units issued per computing warp, the
+  // routed and down units per computing warp and the first routed row
   m.ebars = align_up_dev(m.bars + (size_t)(kLW * kLSlots + 4) * 8, 16);
-  m.recs = align_up_dev(m.ebars + (size_t)kLW * kLSlots * 8 + 8 + (size_t)kLW * 4, 128);
+  m.recs = align_up_dev(m.ebars + (size_t)kLW * kLSlots * 8 + 8 + (size_t)kLW * 4 +
+                            (size_t)kLW * 8 + 4, 128);
   const size_t recs =
       (size_t)T * k * dqvec_words(F) * 4 + (ns ? (size_t)T * dqvec_words(Fs) * 4 : 0);
   m.part = align_up_dev(m.recs + recs, 16);
@@ -466,6 +481,7 @@ __global__ void __launch_bounds__(kLTP, 1)
   volatile uint32_t* routes_known = reinterpret_cast<uint32_t*>(ebars + kLW * kLSlots);
   volatile uint32_t* stop = routes_known + 1;
   volatile uint32_t* final_iss = stop + 1;       // units the copy warp issued, per warp
+  int* plan_s = const_cast<int*>(reinterpret_cast<volatile int*>(final_iss + kLW));  // [kLW][2], rr_a
   uint32_t* recs = reinterpret_cast<uint32_t*>(smem + S.recs);
   float* part = reinterpret_cast<float*>(smem + S.part);
   uint16_t* rx = reinterpret_cast<uint16_t*>(smem + S.rx);
@@ -501,13 +517,27 @@ __global__ void __launch_bounds__(kLTP, 1)
   auto count_w = [&](int w, int a, int b) { return a + w < b ? (b - a - w + kLW - 1) / kLW : 0; };
   auto count = [&](int a, int b) { return count_w(warp, a, b); };
   // The shared expert's rows go to the warps that do not take a token's
-  // top-k (warps T..15): they compute them while the scores are exchanged.
+  // top-k (warps T..kLW-1): they compute them while the scores are exchanged.
+  // Warps on a scheduler (warp index mod 4) without a token warp come first,
+  // so that the top-k and route table, on the path to the routed copies, do
+  // not share their scheduler with these rows.
   const int sh_nw = kLW - T;
+  auto sh_rank = [&](int w) {     // w's place among the shared-row warps, -1 if none
+    if (w < T) return -1;
+    const bool a = (w & 3) >= T;
+    int r = 0;
+#pragma unroll 1
+    for (int v = T; v < kLW; ++v) {
+      const bool av = (v & 3) >= T;
+      if (a ? (av && v < w) : (av || v < w)) ++r;
+    }
+    return r;
+  };
   auto n_sh_of = [&](int w) {
-    const int sw = w - T;
+    const int sw = sh_rank(w);
     return (sw >= 0 && shr.a + sw < shr.b) ? (shr.b - shr.a - sw + sh_nw - 1) / sh_nw : 0;
   };
-  const int sh_w = warp - T;
+  const int sh_w = sh_rank(warp);
   const int n_sh = n_sh_of(warp);
   const int re0 = lr_e0(E, cta, G), re1 = lr_e0(E, cta + 1, G);
   const int ne = re1 - re0;
@@ -527,7 +557,7 @@ __global__ void __launch_bounds__(kLTP, 1)
     u.n_sh = n_sh_of(w);
     u.n_rt = u.rr_a = u.n_dn = 0;
     u.sh_a = shr.a;
-    u.sh_w = w - T;
+    u.sh_w = sh_rank(w);
     u.sh_nw = sh_nw;
     u.ngroups = ngroups;
     u.nrows_cta = nrows_cta;
@@ -536,13 +566,30 @@ __global__ void __launch_bounds__(kLTP, 1)
     return u;
   };
   // ... and its routed and down units once the route table is built
-  auto plan_routes = [&](LUnitPlan& u) {
-    const RowRange rr = split_rows(rt.n_slots * p.F, 1, cta, G);
+  auto plan_slots = [&](LUnitPlan& u, int n_slots) {
+    // split_rows(n_slots * F, 1, cta, G) in 32-bit arithmetic (n_slots * F * G
+    // < 2^32): this is on the path from the route table to the first copy
+    const uint32_t tot = (uint32_t)(n_slots * p.F);
+    const RowRange rr{(int)(tot * (uint32_t)cta / (uint32_t)G),
+                      (int)(tot * (uint32_t)(cta + 1) / (uint32_t)G)};
     u.n_rt = count_w(u.warp, rr.a, rr.b);
     u.rr_a = rr.a;
-    const int n_dn_units = (rt.n_slots + p.n_shared) * ngroups;
+    const int n_dn_units = (n_slots + p.n_shared) * ngroups;
     u.n_dn = u.warp < n_dn_units ? (n_dn_units - u.warp + kLW - 1) / kLW : 0;
   };
+  auto plan_routes = [&](LUnitPlan& u) { plan_slots(u, rt.n_slots); };
+  // One token: the in-kernel selection gives k distinct experts except in the
+  // degenerate case of NaN or -inf keys, so lane w of warp 0 keeps warp w's
+  // plan for k slots from the start.
+  int k_nrt = 0, k_ndn = 0, k_rra = 0;
+  if (MAXT == 1 && warp == 0 && lane < kLW) {
+    LUnitPlan pl;
+    pl.warp = lane;
+    plan_slots(pl, k);
+    k_nrt = pl.n_rt;
+    k_ndn = pl.n_dn;
+    k_rra = pl.rr_a;
+  }
 
   if (warp == kLW) {
     // ---- the copy warp: lane w < kLW issues computing warp w's units in
@@ -569,6 +616,9 @@ __global__ void __launch_bounds__(kLTP, 1)
                           (uint32_t)(((iss / kLSlots) + 1) & 1));
         if (!__any_sync(0xFFFFFFFFu, can)) break;
         if (can) {
+#ifdef MOE_PROFILE
+          if (known && iss == u.ub + u.n_sh) MOE_PSTAMP(lp, w, 17);
+#endif
           issue_unit_layers(p, lt, rt, u, iss);
           ++iss;
         }
@@ -577,8 +627,11 @@ __global__ void __launch_bounds__(kLTP, 1)
       if (!known) {
         if (*routes_known >= (uint32_t)(lp + 1)) {     // layer lp's route table is built
           __threadfence_block();
+          if (mine) MOE_PSTAMP(lp, w, 16);
           if (mine) {
-            plan_routes(u);
+            u.n_rt = plan_s[2 * w];
+            u.n_dn = plan_s[2 * w + 1];
+            u.rr_a = plan_s[2 * kLW];
             lim = u.ub + u.n_sh + u.n_rt + u.n_dn + (lp + 1 < Lyr ? u.n_sh : 0);
           }
           known = true;
@@ -719,6 +772,7 @@ __global__ void __launch_bounds__(kLTP, 1)
         }
       }
       csync();
+      MOE_STAMP(l, 11);
 #pragma unroll 1
       for (int i = threadIdx.x; i < ne * T; i += kLT) {
         const int el = i / T, t = i - el * T;
@@ -769,8 +823,72 @@ __global__ void __launch_bounds__(kLTP, 1)
         }
       }
       if (T > 1) bar_sync_n(1, T * 32);     // the token warps only
+      if (MAXT == 1 && warp == 0) {
+        // One token, k distinct experts (the usual case): the slots are the
+        // ids in ascending order and the plans are the ones kept above, so the
+        // copy warp may start on the routed rows before the rest of the table
+        // is built.
+        const int e = lane < k ? id : 0x7FFFFFFF;
+        int r = 0;
+        bool dup = false;
+#pragma unroll
+        for (int q = 0; q < MOE_MAX_TOP_K; ++q) {
+          const int eq = __shfl_sync(0xFFFFFFFFu, e, q);
+          if (q < k) {
+            r += (eq < e) ? 1 : 0;
+            dup = dup || (eq == e && q != lane);
+          }
+        }
+        if (!__any_sync(0xFFFFFFFFu, lane < k && dup)) {
+          if (lane < k) rt.slot_expert[r] = e;
+          if (lane < kLW) {
+            plan_s[2 * lane] = k_nrt;
+            plan_s[2 * lane + 1] = k_ndn;
+            if (lane == 0) plan_s[2 * kLW] = k_rra;
+          }
+          __syncwarp();
+          if (lane == 0) {
+            __threadfence_block();
+            *routes_known = (uint32_t)(l + 1);
+          }
+          build_route_table_warp(rt, rids, rw, k, E);    // the same slots, and the rest
+          MOE_WSTAMP(l, 7);
+          return;
+        }
+      }
       if (warp == 0) {
+#ifdef MOE_PROFILE
+        const long long c0 = clock64();
+#endif
         build_route_table_warp(rt, rids, rw, T * k, E);
+#ifdef MOE_PROFILE
+        long long c1 = clock64();
+        MOE_WPUT(l, 20, (uint64_t)(c1 - c0));
+#ifdef MOE_PROFILE_TWICE
+        build_route_table_warp(rt, rids, rw, T * k, E);     // the same table again, warm
+        const long long c2 = clock64();
+        MOE_WPUT(l, 18, (uint64_t)(c2 - c1));
+        c1 = c2;
+#endif
+#endif
+        // every computing warp's routed and down units, for the copy warp,
+        // which may then issue this layer's routed rows
+        if (lane < kLW) {
+          LUnitPlan pl;
+          pl.warp = lane;
+          plan_routes(pl);
+          plan_s[2 * lane] = pl.n_rt;
+          plan_s[2 * lane + 1] = pl.n_dn;
+          if (lane == 0) plan_s[2 * kLW] = pl.rr_a;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence_block();
+          *routes_known = (uint32_t)(l + 1);
+        }
+#ifdef MOE_PROFILE
+        MOE_WPUT(l, 21, (uint64_t)(clock64() - c1));
+#endif
         MOE_WSTAMP(l, 7);
       }
     };
@@ -779,10 +897,20 @@ __global__ void __launch_bounds__(kLTP, 1)
       if (warp < T) {
         int id;
         float wv;
+#ifdef MOE_PROFILE
+        const long long q0 = clock64();
+#endif
         layer_topk<2>(tsc + (size_t)warp * E, want, E, k, W.bias, rprob + (size_t)warp * E32, id,
                       wv, wait_ns, p.status, gave_up, l);
         MOE_WSTAMP(l, 4);
+#ifdef MOE_PROFILE
+        const long long q1 = clock64();
+#endif
         finish_routes(id, wv);
+#ifdef MOE_PROFILE
+        MOE_WPUT(l, 18, (uint64_t)(q1 - q0));
+        MOE_WPUT(l, 19, (uint64_t)(clock64() - q1));
+#endif
       }
     } else {
       if (warp < T) {
@@ -820,10 +948,6 @@ __global__ void __launch_bounds__(kLTP, 1)
     }
     csync();
     MOE_STAMP(l, 4);
-    if (threadIdx.x == 0) {       // the copy warp may now issue this layer's routed rows
-      __threadfence_block();
-      *routes_known = (uint32_t)(l + 1);
-    }
     if (*gave_up) wait_ns = 0;
 #pragma unroll 1
     for (int i = threadIdx.x; i < (T * k + (p.n_shared ? T : 0)) * rows_max; i += kLT)
@@ -1173,7 +1297,7 @@ extern "C" int moe_profile_stamps(void* host, size_t bytes) {
   const size_t n = sizeof(moe::g_prof) < bytes ? sizeof(moe::g_prof) : bytes;
   return cudaMemcpyFromSymbol(host, moe::g_prof, n) == cudaSuccess ? 0 : -1;
 }
-// Per-warp stamps (uint64 [256][64][16 warps][16]).
+// Per-warp stamps (uint64 [256][64][16 warps][22]).
 extern "C" int moe_profile_warp_stamps(void* host, size_t bytes) {
   const size_t n = sizeof(moe::g_profw) < bytes ? sizeof(moe::g_profw) : bytes;
   return cudaMemcpyFromSymbol(host, moe::g_profw, n) == cudaSuccess ? 0 : -1;
