@@ -113,19 +113,38 @@ inline int gu_blocks_max(int S, int bps, int slots_max, int P, int T, int G) {
   return tot / (10 * G) + 4 + gu_cost(T) / 10 + sh;
 }
 
+// The gate/up and down kernels run nw warps per CTA: nw - 1 compute, and the
+// last one issues every weight copy. A bulk copy is taken in by the copy
+// engine no faster than memory delivers, so the issuing thread stalls
+// meanwhile; with each computing warp issuing its own rows, that took about as
+// many cycles as its dot products. Lane w of the copy warp keeps computing
+// warp w's slots filled in the warp's unit order, each slot once the warp has
+// released its previous unit (an mbarrier arrival).
+struct CopyWarpSmem {
+  size_t ebars, stop, iss;      // slot-free barriers, stop flag, units issued per warp
+};
+__host__ __device__ inline size_t copy_warp_smem(size_t at, int nc, CopyWarpSmem& c) {
+  c.ebars = align_up_dev(at, 8);
+  c.stop = c.ebars + (size_t)nc * kGuSlots * 8;
+  c.iss = c.stop + 4;
+  return align_up_dev(c.iss + (size_t)nc * 4, 16);
+}
+
 struct GuSmem {
   size_t xq, slots, bars, cnt, total, slot_bytes;
+  CopyWarpSmem cw;
 };
 // xs: the quantised x records sit in shared memory; otherwise the kernel reads
 // them from the workspace, where quant_x_kernel wrote them. nblk: the block
 // counters a CTA needs.
 __host__ __device__ inline GuSmem gu_smem(int H, int T, int nw, bool xs, int g, int nblk) {
   GuSmem m;
+  const int nc = nw - 1;
   m.slot_bytes = align_up_dev((size_t)2 * g * (H / 32) * kBlockB, 128);
   m.xq = align_up_dev(sizeof(RouteTable), 128);
   m.slots = align_up_dev(m.xq + (xs ? (size_t)T * dqvec_words(H) * 4 : 0), 128);
-  m.bars = m.slots + (size_t)nw * kGuSlots * m.slot_bytes;
-  m.cnt = m.bars + (size_t)nw * kGuSlots * 8;
+  m.bars = m.slots + (size_t)nc * kGuSlots * m.slot_bytes;
+  m.cnt = copy_warp_smem(m.bars + (size_t)nc * kGuSlots * 8, nc, m.cw);
   m.total = m.cnt + (size_t)nblk * 4;
   return m;
 }
@@ -171,22 +190,32 @@ template <int LPR, bool XS>
 __global__ void __launch_bounds__(512, 1) gu_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int H = p.H;
-  const int nw = blockDim.x >> 5;
+  const int nw = (blockDim.x >> 5) - 1;          // computing warps; warp nw issues the copies
   const int g = row_granule_dev(H);
-  const GuSmem L = gu_smem(H, p.T, nw, XS, g, p.gu_nblk);
+  const GuSmem L = gu_smem(H, p.T, nw + 1, XS, g, p.gu_nblk);
   RouteTable& rt = *reinterpret_cast<RouteTable*>(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool copier = warp == nw;
   const int xq_words = dqvec_words(H);
   const size_t rbH = (size_t)(H / 32) * kBlockB;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* ebars = reinterpret_cast<uint64_t*>(smem + L.cw.ebars);
+  volatile uint32_t* stop = reinterpret_cast<uint32_t*>(smem + L.cw.stop);
+  volatile uint32_t* final_iss = reinterpret_cast<uint32_t*>(smem + L.cw.iss);
   uint32_t* bcnt = reinterpret_cast<uint32_t*>(smem + L.cnt);
-  uint8_t* myslots = smem + L.slots + (size_t)warp * kGuSlots * L.slot_bytes;
-  uint64_t* mybar = bars + warp * kGuSlots;
+  // the warp whose slots this thread fills (copy warp lane w) or computes
+  const int ww = copier ? (lane < nw ? lane : 0) : warp;
+  uint8_t* myslots = smem + L.slots + (size_t)ww * kGuSlots * L.slot_bytes;
+  uint64_t* mybar = bars + ww * kGuSlots;
 
   if (threadIdx.x == 0) {
 #pragma unroll 1
-    for (int i = 0; i < nw * kGuSlots; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < nw * kGuSlots; ++i) {
+      mbar_init(&bars[i], 1);
+      mbar_init(&ebars[i], 1);
+    }
     mbar_fence_init();
+    *stop = 0u;
   }
 #pragma unroll 1
   for (int i = threadIdx.x; i < p.gu_nblk; i += blockDim.x) bcnt[i] = 0u;
@@ -201,7 +230,7 @@ __global__ void __launch_bounds__(512, 1) gu_kernel(const __grid_constant__ Deco
   const int upb = 32 / g;                      // units per block
   const int n_sh_u = (sb1 - sb0) * upb;
   int rb0 = 0, n_u = n_sh_u;
-  auto count = [&](int nu) { return warp < nu ? (nu - warp + nw - 1) / nw : 0; };
+  auto count = [&](int nu) { return ww < nu ? (nu - ww + nw - 1) / nw : 0; };
   const int n_sh = count(n_sh_u);
   int n_tot = n_sh;
   int issued = 0, consumed = 0;
@@ -237,13 +266,22 @@ __global__ void __launch_bounds__(512, 1) gu_kernel(const __grid_constant__ Deco
     }
     k.u += nw;
   };
-  Cursor ci{warp, -1, 0}, cc{warp, -1, 0};        // next unit to issue, to compute
+  Cursor ci{ww, -1, 0}, cc{ww, -1, 0};            // next unit to issue, to compute
   const uint32_t ubytes = (uint32_t)(g * rbH);     // a multiple of 16
+  // the copy warp: lane w < nw issues warp w's next units, up to `limit`, each
+  // once its slot is free; true if it issued any
   auto issue_upto = [&](int limit) {
-    while (issued < limit && issued - consumed < kGuSlots) {
-      int sl, f;
-      cur_get(ci, sl, f);
-      if (lane == 0) {
+    bool any = false;
+#pragma unroll 1
+    for (;;) {
+      bool can = lane < nw && issued < limit;
+      if (can && issued >= kGuSlots)
+        can = mbar_test(&ebars[ww * kGuSlots + issued % kGuSlots],
+                        (uint32_t)(((issued / kGuSlots) + 1) & 1));
+      if (!__any_sync(0xFFFFFFFFu, can)) break;
+      if (can) {
+        int sl, f;
+        cur_get(ci, sl, f);
         const size_t row = sl < 0 ? (size_t)f : (size_t)rt.slot_expert[sl] * p.F + f;
         const int s = issued % kGuSlots;
         uint8_t* dst = myslots + (size_t)s * L.slot_bytes;
@@ -251,13 +289,15 @@ __global__ void __launch_bounds__(512, 1) gu_kernel(const __grid_constant__ Deco
         bulk_g2s_hint(dst, (sl < 0 ? p.sh_gate : p.gate) + row * rbH, ubytes, &mybar[s], pol);
         bulk_g2s_hint(dst + ubytes, (sl < 0 ? p.sh_up : p.up) + row * rbH, ubytes, &mybar[s],
                       pol);
+        cur_next(ci);
+        ++issued;
       }
-      cur_next(ci);
-      ++issued;
+      any = true;
     }
+    return any;
   };
 
-  issue_upto(n_sh);
+  if (copier) issue_upto(n_sh < kGuSlots ? n_sh : kGuSlots);
   pdl_wait();
   pdl_trigger();
   uint32_t* xq = XS ? reinterpret_cast<uint32_t*>(smem + L.xq) : p.xrec;
@@ -283,7 +323,28 @@ __global__ void __launch_bounds__(512, 1) gu_kernel(const __grid_constant__ Deco
     n_u = n_sh_u + (rb1 - rb0) * upb;
   }
   n_tot = count(n_u);
-  issue_upto(n_tot);
+  if (copier) {
+    // every unit of every computing warp, as slots free up; a stop from the
+    // computing warps (a failed wait) or a long idle spell ends it early
+    const bool mine = lane < nw;
+    uint64_t t_act = global_timer_ns();
+#pragma unroll 1
+    while (!__all_sync(0xFFFFFFFFu, !mine || issued >= n_tot) && !*stop) {
+      const uint64_t now = global_timer_ns();
+      if (issue_upto(n_tot)) {
+        t_act = now;
+      } else {
+        if (now - t_act > 2 * kWaitLimitNs) {
+          if (lane == 0 && p.status) atomicOr(p.status, MOE_STATUS_TIMEOUT);
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    if (mine) final_iss[lane] = (uint32_t)issued;
+    __syncthreads();     // the computing warps' final barrier
+    return;
+  }
 
 #pragma unroll 1
   for (int j = 0; ok && j < n_tot; ++j) {
@@ -305,18 +366,14 @@ __global__ void __launch_bounds__(512, 1) gu_kernel(const __grid_constant__ Deco
                                     xq_words);
     }
     __syncwarp();
+    if (lane == 0) mbar_arrive(&ebars[warp * kGuSlots + j % kGuSlots]);   // slot free
     ++consumed;
-    issue_upto(n_tot);
     // this warp's h stores, then its rows' arrival on the block
     __threadfence_block();
     __syncwarp();
     if (lane == 0) atomicAdd(&bcnt[blk], (uint32_t)g);
   }
-  // after a timeout: no bulk copy of this warp stays in flight
-  while (consumed < issued) {
-    mbar_wait(&mybar[consumed % kGuSlots], (uint32_t)((consumed / kGuSlots) & 1), p.status);
-    ++consumed;
-  }
+  if (!ok && lane == 0) *stop = 1u;
   // Quantise the CTA's blocks of h, block b by warp b % nw once all 32 of its
   // rows have arrived (spread evenly: the warp that happens to add the last
   // row would otherwise collect most of them and fall behind).
@@ -333,6 +390,12 @@ __global__ void __launch_bounds__(512, 1) gu_kernel(const __grid_constant__ Deco
       const int sl = rb / bps;
       quant_h_block(p, rt, sl, rb - sl * bps);
     }
+  }
+  // after a timeout: no bulk copy of this warp stays in flight
+  __syncthreads();
+  while (consumed < (int)final_iss[warp]) {
+    mbar_wait(&mybar[consumed % kGuSlots], (uint32_t)((consumed / kGuSlots) & 1), p.status);
+    ++consumed;
   }
 }
 
@@ -360,9 +423,11 @@ __host__ __device__ inline int dn_rows_per_unit(int K) {
 
 struct DnSmem {
   size_t slots, bars, total, slot_bytes;
+  CopyWarpSmem cw;
 };
 __host__ __device__ inline DnSmem dn_smem(int F, int Fs, int n_shared, int nw) {
   DnSmem m;
+  const int nc = nw - 1;
   size_t ub = (size_t)dn_rows_per_unit(F) * (F / 32) * kBlockB;
   if (n_shared) {
     const size_t us = (size_t)dn_rows_per_unit(Fs) * (Fs / 32) * kBlockB;
@@ -370,8 +435,8 @@ __host__ __device__ inline DnSmem dn_smem(int F, int Fs, int n_shared, int nw) {
   }
   m.slot_bytes = align_up_dev(ub, 128);
   m.slots = align_up_dev(sizeof(RouteTable), 128);
-  m.bars = m.slots + (size_t)nw * kGuSlots * m.slot_bytes;
-  m.total = m.bars + (size_t)nw * kGuSlots * 8;
+  m.bars = m.slots + (size_t)nc * kGuSlots * m.slot_bytes;
+  m.total = copy_warp_smem(m.bars + (size_t)nc * kGuSlots * 8, nc, m.cw);
   return m;
 }
 
@@ -379,21 +444,30 @@ template <int LPR>
 __global__ void __launch_bounds__(512, 1) dn_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int H = p.H;
-  const int nw = blockDim.x >> 5;
-  const DnSmem L = dn_smem(p.F, p.Fs, p.n_shared, nw);
+  const int nw = (blockDim.x >> 5) - 1;          // computing warps; warp nw issues the copies
+  const DnSmem L = dn_smem(p.F, p.Fs, p.n_shared, nw + 1);
   RouteTable& rt = *reinterpret_cast<RouteTable*>(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool copier = warp == nw;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
-  uint8_t* myslots = smem + L.slots + (size_t)warp * kGuSlots * L.slot_bytes;
-  uint64_t* mybar = bars + warp * kGuSlots;
+  uint64_t* ebars = reinterpret_cast<uint64_t*>(smem + L.cw.ebars);
+  volatile uint32_t* stop = reinterpret_cast<uint32_t*>(smem + L.cw.stop);
+  volatile uint32_t* final_iss = reinterpret_cast<uint32_t*>(smem + L.cw.iss);
+  const int ww = copier ? (lane < nw ? lane : 0) : warp;
+  uint8_t* myslots = smem + L.slots + (size_t)ww * kGuSlots * L.slot_bytes;
+  uint64_t* mybar = bars + ww * kGuSlots;
   const int P = p.T * p.k;
   const int ru = dn_rows_per_unit(p.F), rus = p.n_shared ? dn_rows_per_unit(p.Fs) : 32;
   const uint32_t rbK = (uint32_t)(p.F / 32 * kBlockB), rbKs = (uint32_t)(p.Fs / 32 * kBlockB);
 
   if (threadIdx.x == 0) {
 #pragma unroll 1
-    for (int i = 0; i < nw * kGuSlots; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < nw * kGuSlots; ++i) {
+      mbar_init(&bars[i], 1);
+      mbar_init(&ebars[i], 1);
+    }
     mbar_fence_init();
+    *stop = 0u;
   }
   __syncthreads();
 
@@ -402,7 +476,7 @@ __global__ void __launch_bounds__(512, 1) dn_kernel(const __grid_constant__ Deco
   const int sb0 = gu_shared_cum(S, c, G), sb1 = gu_shared_cum(S, c + 1, G);
   const int n_sh_u = (sb1 - sb0) * (32 / rus);
   int rb0 = 0, n_u = n_sh_u;
-  auto count = [&](int nu) { return warp < nu ? (nu - warp + nw - 1) / nw : 0; };
+  auto count = [&](int nu) { return ww < nu ? (nu - ww + nw - 1) / nw : 0; };
   const int n_sh = count(n_sh_u);
   int n_tot = n_sh;
   int issued = 0, consumed = 0;
@@ -437,25 +511,36 @@ __global__ void __launch_bounds__(512, 1) dn_kernel(const __grid_constant__ Deco
     }
     k.u += nw;
   };
-  Cursor ci{warp, -1, 0}, cc{warp, -1, 0};
+  Cursor ci{ww, -1, 0}, cc{ww, -1, 0};
+  // the copy warp: lane w < nw issues warp w's next units, up to `limit`, each
+  // once its slot is free; true if it issued any
   auto issue_upto = [&](int limit) {
-    while (issued < limit && issued - consumed < kGuSlots) {
-      int sl, row;
-      cur_get(ci, sl, row);
-      if (lane == 0) {
+    bool any = false;
+#pragma unroll 1
+    for (;;) {
+      bool can = lane < nw && issued < limit;
+      if (can && issued >= kGuSlots)
+        can = mbar_test(&ebars[ww * kGuSlots + issued % kGuSlots],
+                        (uint32_t)(((issued / kGuSlots) + 1) & 1));
+      if (!__any_sync(0xFFFFFFFFu, can)) break;
+      if (can) {
+        int sl, row;
+        cur_get(ci, sl, row);
         const int s = issued % kGuSlots;
         const uint8_t* src = sl < 0 ? p.sh_down + (size_t)row * rbKs
                                     : p.down + ((size_t)rt.slot_expert[sl] * H + row) * rbK;
         const uint32_t bytes = sl < 0 ? rus * rbKs : ru * rbK;    // multiples of 16
         mbar_arrive_expect_tx(&mybar[s], bytes);
         bulk_g2s_hint(myslots + (size_t)s * L.slot_bytes, src, bytes, &mybar[s], pol);
+        cur_next(ci);
+        ++issued;
       }
-      cur_next(ci);
-      ++issued;
+      any = true;
     }
+    return any;
   };
 
-  issue_upto(n_sh);
+  if (copier) issue_upto(n_sh < kGuSlots ? n_sh : kGuSlots);
   // ids and weights come from a kernel that finished before the gate/up kernel
   // passed its own dependency wait: they may be read before this one's
   if (P <= 64) {
@@ -471,7 +556,28 @@ __global__ void __launch_bounds__(512, 1) dn_kernel(const __grid_constant__ Deco
     n_u = n_sh_u + (rb1 - rb0) * (32 / ru);
   }
   n_tot = count(n_u);
-  issue_upto(n_tot);
+  if (copier) {
+    // every unit of every computing warp, as slots free up; a stop from the
+    // computing warps (a failed wait) or a long idle spell ends it early
+    const bool mine = lane < nw;
+    uint64_t t_act = global_timer_ns();
+#pragma unroll 1
+    while (!__all_sync(0xFFFFFFFFu, !mine || issued >= n_tot) && !*stop) {
+      const uint64_t now = global_timer_ns();
+      if (issue_upto(n_tot)) {
+        t_act = now;
+      } else {
+        if (now - t_act > 2 * kWaitLimitNs) {
+          if (lane == 0 && p.status) atomicOr(p.status, MOE_STATUS_TIMEOUT);
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    if (mine) final_iss[lane] = (uint32_t)issued;
+    __syncthreads();     // the computing warps' final barrier
+    return;
+  }
   pdl_wait();                  // the records come from the gate/up kernel
   pdl_trigger();
 
@@ -497,11 +603,13 @@ __global__ void __launch_bounds__(512, 1) dn_kernel(const __grid_constant__ Deco
     else
       down_rows<kGuMaxT, LPR>(d, shared ? p.Fs : p.F, shared ? rus : ru, ntok, rec_of, store);
     __syncwarp();
+    if (lane == 0) mbar_arrive(&ebars[warp * kGuSlots + j % kGuSlots]);   // slot free
     ++consumed;
-    issue_upto(n_tot);
   }
+  if (!ok && lane == 0) *stop = 1u;
   // after a timeout: no bulk copy of this warp stays in flight
-  while (consumed < issued) {
+  __syncthreads();
+  while (consumed < (int)final_iss[warp]) {
     mbar_wait(&mybar[consumed % kGuSlots], (uint32_t)((consumed / kGuSlots) & 1), p.status);
     ++consumed;
   }

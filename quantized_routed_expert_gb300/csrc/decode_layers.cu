@@ -200,17 +200,6 @@ __device__ __forceinline__ bool csync_and(bool v) {
       : "memory");
   return r != 0;
 }
-// Whether the phase of parity `parity` of an mbarrier has completed (no wait).
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 
 // What a warp needs to issue the copies of its units. Its sequence: per layer
 // its shared gate/up rows, its routed gate/up rows, its down groups; then the
