@@ -21,12 +21,14 @@
 
 namespace moe {
 
-constexpr int kFW = 16;            // warps per CTA
-constexpr int kFT = kFW * 32;      // threads per CTA
-constexpr int kFSlots = 2;         // bulk-copy slots per warp
+constexpr int kFW = 15;            // computing warps per CTA (warp 15 issues the copies)
+constexpr int kFT = kFW * 32;      // computing threads per CTA
+constexpr int kFTP = kFT + 32;     // threads per CTA: the computing warps and the copy warp
+constexpr int kFSlots = 2;         // bulk-copy slots per computing warp
+constexpr int kFBar = 2;           // named barrier of the computing warps
 
 struct FusedSmem {
-  size_t xq, slots, bars, recs, part, total, slot_bytes;
+  size_t xq, slots, bars, ebars, recs, part, total, slot_bytes;
   // router scratch (routed kernel), overlaying the records area, which is used
   // only after the h barrier
   size_t r_wr, r_x, r_part, r_keys, r_ids, r_w;
@@ -52,7 +54,12 @@ __host__ __device__ inline FusedSmem fused_smem(int H, int F, int Fs, int ns, in
   m.xq = align_up_dev(sizeof(RouteTable), 128);
   m.slots = align_up_dev(m.xq + (size_t)T * dqvec_words(H) * 4, 128);
   m.bars = m.slots + (size_t)kFW * kFSlots * m.slot_bytes;
-  m.recs = align_up_dev(m.bars + (size_t)(kFW * kFSlots + 4) * 8, 128);
+  // the slots' "free" barriers, then the copy warp's words: routes known, stop,
+  // units issued per computing warp, each warp's routed and down units and the
+  // first routed row
+  m.ebars = align_up_dev(m.bars + (size_t)(kFW * kFSlots + 4) * 8, 16);
+  m.recs = align_up_dev(m.ebars + (size_t)kFW * kFSlots * 8 + 8 + (size_t)kFW * 4 +
+                            (size_t)kFW * 8 + 4, 128);
   const size_t recs = (size_t)T * k * dqvec_words(F) * 4 + (ns ? (size_t)T * dqvec_words(Fs) * 4 : 0);
   m.part = align_up_dev(m.recs + recs, 16);
   size_t end = m.part + (size_t)(T * k + (ns ? T : 0)) * rows_max * 4;
@@ -134,7 +141,7 @@ __device__ __noinline__ void issue_unit(const DecodeParams& p, const RouteTable&
 }
 
 template <int MAXT, bool ROUTE, int LPR>
-__global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(kFTP, 1) decode_fused_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int H = p.H;
   const int rows_max = p.dn_rows_max;
@@ -153,13 +160,24 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int xq_words = dqvec_words(H);
   const int rbH = H / 32 * kBlockB;
-  uint8_t* myslots = slots + (size_t)warp * kFSlots * L.slot_bytes;
-  uint64_t* mybar = bars + warp * kFSlots;
+  uint64_t* ebars = reinterpret_cast<uint64_t*>(smem + L.ebars);     // slot freed
+  volatile uint32_t* routes_known = reinterpret_cast<uint32_t*>(ebars + kFW * kFSlots);
+  volatile uint32_t* stop = routes_known + 1;
+  volatile uint32_t* final_iss = stop + 1;
+  int* plan_s = const_cast<int*>(reinterpret_cast<volatile int*>(final_iss + kFW));  // [kFW][2], rr_a
+  // the warp whose slots this thread fills (copy warp lane w) or computes
+  const int ww = warp == kFW ? (lane < kFW ? lane : 0) : warp;
+  uint8_t* myslots = slots + (size_t)ww * kFSlots * L.slot_bytes;
+  uint64_t* mybar = bars + ww * kFSlots;
 
   if (threadIdx.x == 0) {
     #pragma unroll 1
     for (int i = 0; i < kFW * kFSlots + 3; ++i) mbar_init(&bars[i], 1);
+    #pragma unroll 1
+    for (int i = 0; i < kFW * kFSlots; ++i) mbar_init(&ebars[i], 1);
     mbar_fence_init();
+    *routes_known = 0u;
+    *stop = 0u;
   }
   __syncthreads();
 
@@ -168,20 +186,20 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
   const RowRange dn = split_rows(H, 1, blockIdx.x, gridDim.x);
   const int nrows_cta = dn.b - dn.a;
   const int ngroups = (nrows_cta + RG - 1) / RG;
-  auto count = [&](int a, int b) { return a + warp < b ? (b - a - warp + kFW - 1) / kFW : 0; };
+  auto count = [&](int a, int b) { return a + ww < b ? (b - a - ww + kFW - 1) / kFW : 0; };
   const int n_sh = count(shr.a, shr.b);
   int n_rt = 0, n_tot = n_sh;      // known once the route table exists
   RowRange rr{0, 0};
   int n_dslots = 0;
 
-  int issued = 0, consumed = 0;
+  int consumed = 0;
   bool ok = true;
   const uint64_t pol = l2_evict_first_policy();   // weights are read once per call
   UnitPlan up;
   up.myslots = myslots;
   up.slot_bytes = L.slot_bytes;
   up.mybar = mybar;
-  up.warp = warp;
+  up.warp = ww;
   up.n_sh = n_sh;
   up.n_rt = 0;
   up.sh_a = shr.a;
@@ -191,15 +209,72 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
   up.dn_a = dn.a;
   up.rg = RG;
   up.pol = pol;
-  auto issue_upto = [&](int limit) {
-    while (issued < limit && issued - consumed < kFSlots) {
-      if (lane == 0) issue_unit(p, rt, up, issued);
-      ++issued;
-    }
-  };
   auto wait_unit = [&](int j) {
     return mbar_wait(&mybar[j % kFSlots], (uint32_t)((j / kFSlots) & 1), p.status);
   };
+  auto release_unit = [&](int j) {  // the warp is done with unit j's slot
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ebars[warp * kFSlots + j % kFSlots]);
+  };
+
+  if (warp == kFW) {
+    // ---- the copy warp. A bulk copy is taken in by the copy engine no
+    // faster than memory delivers, so the issuing thread stalls meanwhile;
+    // here no computing warp ever issues a weight copy. Lane w < kFW fills
+    // computing warp w's two slots in its unit order, each slot once the warp
+    // released the unit two back, the routed and down units once the route
+    // table is built (its plan then comes from warp 0).
+    const bool mine = lane < kFW;
+    int iss = 0, lim = mine ? n_sh : 0;
+    bool known = false;
+    const uint64_t idle_ns = 2 * kWaitLimitNs + p.wait_ns;
+    uint64_t t_act = global_timer_ns();
+#pragma unroll 1
+    for (;;) {
+      bool any = false;
+#pragma unroll 1
+      for (;;) {
+        bool can = mine && iss < lim;
+        if (can && iss >= kFSlots)
+          can = mbar_test(&ebars[ww * kFSlots + iss % kFSlots],
+                          (uint32_t)(((iss / kFSlots) + 1) & 1));
+        if (!__any_sync(0xFFFFFFFFu, can)) break;
+        if (can) {
+          issue_unit(p, rt, up, iss);
+          ++iss;
+        }
+        any = true;
+      }
+      if (!known) {
+        if (*routes_known) {
+          __threadfence_block();
+          if (mine) {
+            up.n_rt = plan_s[2 * ww];
+            up.rr_a = plan_s[2 * kFW];
+            lim = n_sh + up.n_rt + plan_s[2 * ww + 1];
+          }
+          known = true;
+          any = true;
+        }
+      } else if (__all_sync(0xFFFFFFFFu, !mine || iss == lim)) {
+        break;                                   // every unit of the call issued
+      }
+      if (*stop) break;
+      const uint64_t now = global_timer_ns();
+      if (any) {
+        t_act = now;
+      } else {
+        if (now - t_act > idle_ns) {
+          if (lane == 0 && p.status) atomicOr(p.status, MOE_STATUS_TIMEOUT);
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    if (mine) final_iss[lane] = (uint32_t)iss;
+    __syncthreads();     // the computing warps' final barrier
+    return;
+  }
 
   // Router rows of this CTA's experts (constant): fetch them while the previous
   // kernel on the stream finishes.
@@ -211,8 +286,6 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
     bulk_g2s_hint(smem + L.r_wr, p.Wr + (size_t)re0 * H, bytes, rwr_bar,
                   l2_evict_first_policy());
   }
-  // Shared-expert rows do not depend on the routes: start fetching them too.
-  issue_upto(n_sh);
   pdl_wait();
   pdl_trigger();
   if (ROUTE && threadIdx.x == 0 && re1 > re0) {
@@ -266,7 +339,7 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
         }
       }
     }
-    __syncthreads();
+    bar_sync_n(kFBar, kFT);
     #pragma unroll 1
     for (int i = threadIdx.x; i < ne * p.T; i += kFT) {
       const int el = i / p.T, t = i - el * p.T;
@@ -275,10 +348,10 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
       p.scores[(size_t)t * p.E + re0 + el] = sc;
     }
     __threadfence();
-    __syncthreads();
+    bar_sync_n(kFBar, kFT);
     if (threadIdx.x == 0) atomicAdd(&p.sync[2], 1u);
   }
-  __syncthreads();
+  bar_sync_n(kFBar, kFT);
 
   // ---- routing (this CTA's experts' scores were published above)
   const int32_t* ids_src = p.ids;
@@ -298,7 +371,7 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
       }
       __threadfence();
     }
-    __syncthreads();
+    bar_sync_n(kFBar, kFT);
     // keys p + b and sigmoids p, rows padded to E32 with -inf (keys)
     float* keys_all = reinterpret_cast<float*>(smem + L.r_keys);
     const int E32 = (p.E + 31) & ~31;
@@ -313,7 +386,7 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
       keys_all[(size_t)p.T * E32 + i] = pr;
       keys_all[i] = key;
     }
-    __syncthreads();
+    bar_sync_n(kFBar, kFT);
     if (warp < p.T) {
       const int t = warp;
       float* keys = keys_all + (size_t)t * E32;
@@ -333,8 +406,25 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
     ids_src = ids_s;
     w_src = w_s;
   }
-  if (warp == 0) build_route_table_warp(rt, ids_src, w_src, p.T * p.k, p.E);
-  __syncthreads();
+  if (warp == 0) {
+    build_route_table_warp(rt, ids_src, w_src, p.T * p.k, p.E);
+    // every computing warp's routed and down units, for the copy warp (the
+    // row split of split_rows in 32-bit arithmetic: n_slots * F * G < 2^32)
+    if (lane < kFW) {
+      const uint32_t tot = (uint32_t)(rt.n_slots * p.F);
+      const int a = (int)(tot * blockIdx.x / gridDim.x), b = (int)(tot * (blockIdx.x + 1) / gridDim.x);
+      plan_s[2 * lane] = a + lane < b ? (b - a - lane + kFW - 1) / kFW : 0;
+      const int nu = (rt.n_slots + p.n_shared) * ngroups;
+      plan_s[2 * lane + 1] = lane < nu ? (nu - lane + kFW - 1) / kFW : 0;
+      if (lane == 0) plan_s[2 * kFW] = a;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();
+      *routes_known = 1u;
+    }
+  }
+  bar_sync_n(kFBar, kFT);
   if (blockIdx.x == 0 && threadIdx.x == 0 && p.status && rt.invalid)
     atomicAdd(p.status, (uint32_t)(rt.invalid < 0xFFFF ? rt.invalid : 0xFFFF));
   #pragma unroll 1
@@ -348,7 +438,6 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
   const int n_dn_units = n_dslots * ngroups;
   const int n_dn = warp < n_dn_units ? (n_dn_units - warp + kFW - 1) / kFW : 0;
   n_tot = n_sh + n_rt + n_dn;
-  issue_upto(n_tot);
 
   // the routed rows' copies are in flight: compute the shared expert's rows
   // (landed long ago) while they arrive, then the routed rows
@@ -372,13 +461,12 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
       gateup_unit_t<1, LPR>(p, rt, d, d + rbH, sl, f, xq, xq_words);
     else
       gateup_unit_t<MAXT, LPR>(p, rt, d, d + rbH, sl, f, xq, xq_words);
-    __syncwarp();
+    release_unit(j);
     ++consumed;
-    issue_upto(n_tot);
   }
 
   // ---- grid barrier: every h row of this call is in global memory
-  __syncthreads();
+  bar_sync_n(kFBar, kFT);
   if (threadIdx.x == 0) {
     __threadfence();
     atomicAdd(&p.sync[0], 1u);
@@ -392,7 +480,7 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
     }
     __threadfence();
   }
-  __syncthreads();
+  bar_sync_n(kFBar, kFT);
   // every CTA quantises all of h into its own records: staged in shared
   // memory by bulk copies when there is room, else read through L2
   if (L.stage_bytes) {
@@ -416,7 +504,7 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
   } else {
     quant_h<false>(p, rt, nullptr, recs, threadIdx.x, kFT);
   }
-  __syncthreads();
+  bar_sync_n(kFBar, kFT);
 
   #pragma unroll 1
   for (int j = n_sh + n_rt; ok && j < n_tot; ++j) {
@@ -433,11 +521,10 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
       down_unit_t<1, LPR>(p, rt, d, dsl, r0, nr, recs, part, rows_max);
     else
       down_unit_t<MAXT, LPR>(p, rt, d, dsl, r0, nr, recs, part, rows_max);
-    __syncwarp();
+    release_unit(j);
     ++consumed;
-    issue_upto(n_tot);
   }
-  __syncthreads();
+  bar_sync_n(kFBar, kFT);
 
   // ---- combine in the fixed order: shared expert, then routed experts ascending
   #pragma unroll 1
@@ -453,8 +540,15 @@ __global__ void __launch_bounds__(kFT, 1) decode_fused_kernel(const __grid_const
     p.y[(size_t)t * H + dn.a + r] = acc;
   }
 
-  // ---- after a timeout, drain this warp's bulk copies still in flight
-  while (consumed < issued) {
+  // ---- the copy warp stops (it has issued everything unless a wait failed)
+  // and reports how many units it issued per warp; after a timeout, drain
+  // this warp's bulk copies still in flight
+  if (threadIdx.x == 0) {
+    __threadfence_block();
+    *stop = 1u;
+  }
+  __syncthreads();
+  while (consumed < (int)final_iss[warp]) {
     wait_unit(consumed);
     ++consumed;
   }
@@ -508,7 +602,7 @@ bool fused_resident(const DecodeParams& p, size_t smem) {
   bool ok = false;
   if (ensure_smem_attr(k, smem) == cudaSuccess) {
     int blocks = 0;
-    ok = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k, kFT, smem) == cudaSuccess &&
+    ok = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k, kFTP, smem) == cudaSuccess &&
          blocks >= 1;
   }
   cudaGetLastError();
@@ -575,7 +669,7 @@ cudaError_t launch_decode_fused(const DecodeParams& p, int num_sms, size_t smem,
                                 cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms);
-  cfg.blockDim = dim3(kFT);
+  cfg.blockDim = dim3(kFTP);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

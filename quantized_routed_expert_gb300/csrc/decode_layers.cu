@@ -853,12 +853,7 @@ __global__ void __launch_bounds__(kLTP, 1)
 #ifdef MOE_PROFILE
         long long c1 = clock64();
         MOE_WPUT(l, 20, (uint64_t)(c1 - c0));
-#ifdef MOE_PROFILE_TWICE
-        build_route_table_warp(rt, rids, rw, T * k, E);     // the same table again, warm
-        const long long c2 = clock64();
-        MOE_WPUT(l, 18, (uint64_t)(c2 - c1));
-        c1 = c2;
-#endif
+
 #endif
         // every computing warp's routed and down units, for the copy warp,
         // which may then issue this layer's routed rows
