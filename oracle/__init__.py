@@ -27,6 +27,7 @@ _lib = None
 
 EXACT = 0
 MMA16 = 1
+MMA8 = 2     # E4M3 operands with power-of-two row / vector exponents (oracle.cpp header)
 
 
 def build(force: bool = False) -> str:
@@ -62,6 +63,11 @@ def _load():
         lib.orc_bf16_to_double.restype = c.c_double
         lib.orc_double_to_half.argtypes = [c.c_double]
         lib.orc_double_to_half.restype = c.c_uint16
+        lib.orc_e4m3_to_double.argtypes = [c.c_uint8]
+        lib.orc_e4m3_to_double.restype = c.c_double
+        lib.orc_double_to_e4m3.argtypes = [c.c_double]
+        lib.orc_double_to_e4m3.restype = c.c_uint8
+        lib.orc_dequant_rows_e4m3.argtypes = [P, c.c_int64, c.c_int, P, P]
         lib.orc_dequant_blocks.argtypes = [P, c.c_int64, c.c_int, P]
         lib.orc_sanitize.argtypes = [P, P, c.c_int64, c.c_int, P, P]
         lib.orc_route.argtypes = [c.c_int, c.c_int, c.c_int, P, P, P, c.c_int, P, P, P, P]
@@ -96,6 +102,26 @@ def bf16_to_double(bits: int) -> float:
 
 def double_to_half(v: float) -> int:
     return int(_load().orc_double_to_half(float(v)))
+
+
+def e4m3_to_double(code: int) -> float:
+    return _load().orc_e4m3_to_double(int(code) & 0xFF)
+
+
+def double_to_e4m3(v: float) -> int:
+    return int(_load().orc_double_to_e4m3(float(v)))
+
+
+def dequant_rows_e4m3(mat: np.ndarray, rows: int, K: int):
+    """Mode-2 (mma8) weights of `rows` rows of a K-input IQ4_NL matrix: float64
+    [rows][K] and each row's exponent E_m (int32 [rows])."""
+    b = np.ascontiguousarray(mat, dtype=np.uint8).reshape(-1)
+    assert b.size >= rows * (K // 32) * 18
+    out = np.empty((rows, K), np.float64)
+    ex = np.empty(rows, np.int32)
+    rc = _load().orc_dequant_rows_e4m3(_ptr(b), int(rows), int(K), _ptr(out), _ptr(ex))
+    assert rc == 0
+    return out, ex
 
 
 def max_threads() -> int:

@@ -33,6 +33,22 @@
 // (round-to-nearest-even, subnormals kept): each dequantised weight d*T[q],
 // each activation x, and each h before the down projection. It is the
 // reference for the tensor-core prefill path, whose operands are fp16.
+//
+// Mode "mma8" is the reference for the prefill path with 8-bit operands (the
+// Xolotl blog's "Prompts" passage runs its prompt contraction on 8-bit tensor
+// cores). The format taken is E4M3 of the OCP 8-bit floating point
+// specification (1 sign, 4 exponent bits with bias 7, 3 fraction bits; no
+// infinities, S.1111.111 is NaN, largest finite 448), rounded to nearest with
+// ties to even and finite overflow saturated to +-448. E4M3 spans fewer
+// binades than IQ4_NL weights or activations, so each value is rounded after
+// a power-of-two scaling that the contraction's output undoes exactly:
+//  * a weight row m (K inputs) is scaled by 2^-E_m, E_m the largest exponent
+//    of its blocks' fp16 scales d (-14 for a subnormal or zero d), so that
+//    |d*T*2^-E_m| < 254 for every weight of the row: w8 = 2^E_m e4m3(d*T*2^-E_m);
+//  * an activation vector v (a token's x, or one (token, expert) pair's h) is
+//    scaled by 2^-X, X = floor(log2 max|v|) - 6 (0 for an all-zero vector), so
+//    that its largest magnitude lies in [64, 128): v8 = 2^X e4m3(v*2^-X).
+// Everything else, as in the exact mode, is a plain double computation.
 
 #include <cmath>
 #include <cstdint>
@@ -116,6 +132,81 @@ uint16_t double_to_half(double v) {
 
 double round_to_half(double v) { return half_to_double(double_to_half(v)); }
 
+// E4M3 byte -> double, from the field layout: e = bits 6..3, f = bits 2..0;
+// e == 0: subnormal f/8 * 2^-6; else (1 + f/8) * 2^(e-7); S.1111.111 is NaN.
+double e4m3_to_double(uint8_t c) {
+  const int sgn = (c >> 7) & 1, e = (c >> 3) & 0xF, f = c & 7;
+  if (e == 0xF && f == 7) return std::numeric_limits<double>::quiet_NaN();
+  const double mag = (e == 0) ? std::ldexp(f / 8.0, -6) : std::ldexp(1.0 + f / 8.0, e - 7);
+  return sgn ? -mag : mag;
+}
+
+// double -> E4M3, round to nearest with ties to even (on the 3-bit fraction,
+// subnormals included), finite overflow saturated to +-448, NaN to 0x7F.
+uint8_t double_to_e4m3(double v) {
+  if (std::isnan(v)) return 0x7F;
+  const uint8_t sgn = std::signbit(v) ? 0x80 : 0x00;
+  double a = std::fabs(v);
+  if (a >= 448.0) return sgn | 0x7E;               // saturate (the largest finite, 1.110 x 2^8)
+  // the quantum of a's binade: 2^(e-3) for normals (e >= -6), 2^-9 below
+  int e = 0;
+  std::frexp(a, &e);                               // a = m 2^e, m in [0.5, 1)
+  int ex = e - 1;                                  // floor(log2 a) for a > 0
+  if (a == 0.0 || ex < -6) ex = -6;
+  const double q = std::ldexp(1.0, ex - 3);
+  double n = a / q;                                // exact: a power-of-two scaling
+  double r = std::floor(n);
+  const double frac = n - r;
+  if (frac > 0.5 || (frac == 0.5 && std::fmod(r, 2.0) != 0.0)) r += 1.0;
+  const double rv = r * q;                         // the rounded magnitude
+  if (rv >= 448.0) return sgn | 0x7E;
+  if (rv == 0.0) return sgn;
+  int e2 = 0;
+  std::frexp(rv, &e2);
+  int ebin = e2 - 1;                               // rv's binade after rounding
+  if (ebin < -6) {                                 // subnormal: f/8 * 2^-6
+    const int f = static_cast<int>(std::ldexp(rv, 9));
+    return sgn | static_cast<uint8_t>(f);
+  }
+  const int f = static_cast<int>(std::ldexp(rv, 3 - ebin)) - 8;
+  return sgn | static_cast<uint8_t>(((ebin + 7) << 3) | f);
+}
+double round_to_e4m3(double v) { return e4m3_to_double(double_to_e4m3(v)); }
+
+// Exponent of an fp16 scale for the row scaling: floor(log2 |d|) for a normal
+// d (its biased exponent field minus 15), -14 for a subnormal or zero d.
+int half_exponent(uint16_t dbits) {
+  const int f = (dbits >> 10) & 0x1F;
+  return f == 0 ? -14 : f - 15;
+}
+
+// The row exponent E_m: the largest exponent of the row's block scales.
+int row_exponent(const uint8_t* row, int nb) {
+  int e = -1000;
+  for (int b = 0; b < nb; ++b) {
+    const uint8_t* blk = row + static_cast<size_t>(b) * 18;
+    const int eb = half_exponent(static_cast<uint16_t>(blk[0] | (blk[1] << 8)));
+    e = eb > e ? eb : e;
+  }
+  return e;
+}
+
+// An activation vector's exponent X = floor(log2 max|v|) - 6; 0 when all zero.
+int vector_exponent(const double* v, int n) {
+  double m = 0.0;
+  for (int i = 0; i < n; ++i) m = std::fabs(v[i]) > m ? std::fabs(v[i]) : m;
+  if (!(m > 0.0) || !std::isfinite(m)) return 0;
+  int e = 0;
+  std::frexp(m, &e);
+  return (e - 1) - 6;
+}
+
+// v <- 2^X e4m3(v 2^-X) with the vector's own exponent.
+void round_vector_e4m3(double* v, int n) {
+  const int X = vector_exponent(v, n);
+  for (int i = 0; i < n; ++i) v[i] = std::ldexp(round_to_e4m3(std::ldexp(v[i], -X)), X);
+}
+
 // Dequantise one 18-byte block into 32 doubles.
 void dequant_block(const uint8_t* blk, int mode, double* w) {
   const uint16_t dbits = static_cast<uint16_t>(blk[0] | (blk[1] << 8));
@@ -129,14 +220,24 @@ void dequant_block(const uint8_t* blk, int mode, double* w) {
     for (int i = 0; i < kBlockWeights; ++i) w[i] = round_to_half(w[i]);
 }
 
+// Mode 2 dequantisation of one block of a row with exponent E.
+void dequant_block_e4m3(const uint8_t* blk, int E, double* w) {
+  dequant_block(blk, 0, w);
+  for (int i = 0; i < kBlockWeights; ++i) w[i] = std::ldexp(round_to_e4m3(std::ldexp(w[i], -E)), E);
+}
+
 // Row r of a matrix with K inputs: blocks r*K/32 ... r*K/32 + K/32 - 1.
 double row_dot(const uint8_t* mat, int r, int K, const double* v, int mode) {
   const int nb = K / kBlockWeights;
   const uint8_t* row = mat + static_cast<size_t>(r) * nb * kBlockBytes;
   double acc = 0.0;
   double w[kBlockWeights];
+  const int E = mode == 2 ? row_exponent(row, nb) : 0;
   for (int b = 0; b < nb; ++b) {
-    dequant_block(row + static_cast<size_t>(b) * kBlockBytes, mode, w);
+    if (mode == 2)
+      dequant_block_e4m3(row + static_cast<size_t>(b) * kBlockBytes, E, w);
+    else
+      dequant_block(row + static_cast<size_t>(b) * kBlockBytes, mode, w);
     for (int i = 0; i < kBlockWeights; ++i) acc += w[i] * v[b * kBlockWeights + i];
   }
   return acc;
@@ -156,6 +257,7 @@ void expert_ffn(int H, int F, const uint8_t* gate, const uint8_t* up,
     if (mode == 1) hv = round_to_half(hv);
     h[f] = hv;
   }
+  if (mode == 2) round_vector_e4m3(h.data(), F);
   for (int n = 0; n < H; ++n) o[n] = row_dot(down, n, F, h.data(), mode);
 }
 
@@ -169,6 +271,25 @@ int orc_table(int32_t* out16) {
 }
 
 double orc_half_to_double(uint16_t h) { return half_to_double(h); }
+double orc_e4m3_to_double(uint8_t c) { return e4m3_to_double(c); }
+uint8_t orc_double_to_e4m3(double v) { return double_to_e4m3(v); }
+
+// Mode-2 weights of `rows` rows of a K-input matrix, as doubles [rows][K], and
+// each row's exponent E_m (row_exp may be NULL).
+int orc_dequant_rows_e4m3(const uint8_t* mat, int64_t rows, int K, double* out,
+                          int32_t* row_exp) {
+  if (!mat || !out || rows < 0 || K <= 0 || K % 32) return -1;
+  const int nb = K / 32;
+  for (int64_t r = 0; r < rows; ++r) {
+    const uint8_t* row = mat + static_cast<size_t>(r) * nb * kBlockBytes;
+    const int E = row_exponent(row, nb);
+    if (row_exp) row_exp[r] = E;
+    for (int b = 0; b < nb; ++b)
+      dequant_block_e4m3(row + static_cast<size_t>(b) * kBlockBytes, E,
+                         out + static_cast<size_t>(r) * K + static_cast<size_t>(b) * 32);
+  }
+  return 0;
+}
 double orc_bf16_to_double(uint16_t b) { return bf16_to_double(b); }
 uint16_t orc_double_to_half(double v) { return double_to_half(v); }
 
@@ -236,11 +357,13 @@ int orc_route(int H, int E, int k, const uint16_t* Wr, const float* bias,
 int orc_expert_ffn(int H, int F, const uint8_t* gate, const uint8_t* up,
                    const uint8_t* down, const uint16_t* x, int mode, double* o) {
   if (H <= 0 || F <= 0 || H % 32 || F % 32 || !gate || !up || !down || !x || !o) return -1;
+  if (mode != 0 && mode != 1 && mode != 2) return -1;
   std::vector<double> xv(H);
   for (int h = 0; h < H; ++h) {
     xv[h] = bf16_to_double(x[h]);
     if (mode == 1) xv[h] = round_to_half(xv[h]);
   }
+  if (mode == 2) round_vector_e4m3(xv.data(), H);
   expert_ffn(H, F, gate, up, down, xv.data(), mode, o);
   return 0;
 }
@@ -258,7 +381,7 @@ int orc_moe_layer(int H, int F, int Fs, int E, int k, int n_shared,
                   int T, const int32_t* ids, const double* w, int mode, int threads,
                   double* y) {
   if (H <= 0 || F <= 0 || H % 32 || F % 32 || E <= 0 || k <= 0 || k > E || T < 0 ||
-      (n_shared != 0 && n_shared != 1) || (mode != 0 && mode != 1) || !x || !y ||
+      (n_shared != 0 && n_shared != 1) || (mode != 0 && mode != 1 && mode != 2) || !x || !y ||
       (T > 0 && (!ids || !w)))
     return -1;
   if (n_shared && (Fs <= 0 || Fs % 32 || !sh_gate || !sh_up || !sh_down)) return -1;
@@ -268,12 +391,14 @@ int orc_moe_layer(int H, int F, int Fs, int E, int k, int n_shared,
   orc_sanitize(ids, w, static_cast<int64_t>(T) * k, E, sid.data(), sw.data());
   for (size_t i = 0; i < sid.size(); ++i)
     if (!gate[sid[i]] || !up[sid[i]] || !down[sid[i]]) return -2;
-  // Activations, optionally rounded to fp16 (mode mma16).
+  // Activations, rounded to fp16 (mode mma16) or per token to E4M3 (mma8).
   std::vector<double> xv(static_cast<size_t>(T) * H);
   for (size_t i = 0; i < xv.size(); ++i) {
     xv[i] = bf16_to_double(x[i]);
     if (mode == 1) xv[i] = round_to_half(xv[i]);
   }
+  if (mode == 2)
+    for (int t = 0; t < T; ++t) round_vector_e4m3(xv.data() + static_cast<size_t>(t) * H, H);
   std::vector<double> o(static_cast<size_t>(n_pairs) * H);
   const int kk = k + n_shared;
   auto run_pair = [&](int64_t p) {

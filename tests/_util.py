@@ -67,6 +67,54 @@ def np_swiglu_expert(mats, H: int, F: int, x: np.ndarray, fp16: bool = False) ->
     return h @ Wd.T
 
 
+def torch_e4m3(v: np.ndarray) -> np.ndarray:
+    """Round values to E4M3 with PyTorch's float8_e4m3fn conversion (round to
+    nearest even); the library routine the mma8 pins check against. Values must
+    lie within +-464, where PyTorch and the saturating reading agree. PyTorch
+    converts through float32, so a float64 input is rounded twice: exact for
+    the pins' weights and activations (which are float32 values), and for h it
+    differs only for a value within a float32 ulp of an E4M3 midpoint."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(v, np.float64))
+    return t.to(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def np_row_exponents(blocks: np.ndarray, rows: int, K: int) -> np.ndarray:
+    """Largest fp16 scale exponent of each row (field - 15; -14 for field 0)."""
+    b = np.ascontiguousarray(blocks, np.uint8).reshape(rows, K // 32, 18)
+    f = ((b[:, :, 0].astype(np.int32) | (b[:, :, 1].astype(np.int32) << 8)) >> 10) & 0x1F
+    return np.where(f == 0, -14, f - 15).max(axis=1)
+
+
+def np_e4m3_rows(M: np.ndarray, E: np.ndarray) -> np.ndarray:
+    """Rows of M rounded as 2^E e4m3(M 2^-E), E per row."""
+    sc = np.ldexp(1.0, E.astype(np.int64))[:, None]
+    return torch_e4m3(M / sc) * sc
+
+
+def np_e4m3_vectors(V: np.ndarray) -> np.ndarray:
+    """Each row v of V rounded as 2^X e4m3(v 2^-X), X = floor(log2 max|v|) - 6."""
+    m = np.abs(V).max(axis=1)
+    _, e = np.frexp(m)
+    X = np.where(m > 0, e - 1 - 6, 0)
+    return np_e4m3_rows(V, X)
+
+
+def np_swiglu_expert_e4m3(mats, H: int, F: int, x: np.ndarray) -> np.ndarray:
+    """Dense SwiGLU expert with the mma8 reading's roundings, from numpy
+    (dequantisation, exponents, BLAS) and PyTorch (E4M3 rounding)."""
+    from scipy.special import expit
+    out = []
+    for m, rows, K in ((mats[0], F, H), (mats[1], F, H), (mats[2], H, F)):
+        out.append(np_e4m3_rows(np_dense(m, rows, K), np_row_exponents(m, rows, K)))
+    Wg, Wu, Wd = out
+    x8 = np_e4m3_vectors(x)
+    g = x8 @ Wg.T
+    u = x8 @ Wu.T
+    h8 = np_e4m3_vectors(g * expit(g) * u)
+    return h8 @ Wd.T
+
+
 def np_route(Wr_bits: np.ndarray, bias, x_bits: np.ndarray, k: int):
     """Keys from numpy (row by row np.dot), selection by brute force over all
     k-subsets (only for small E)."""

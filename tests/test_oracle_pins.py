@@ -1,13 +1,15 @@
 """Pins of the CPU oracle against facts fixed outside it: the printed IQ4_NL
-table, hand-built blocks, numpy's IEEE conversions, brute-force top-k, a dense
-numpy SwiGLU, the vLLM article's route-sanitiser example, and invariances."""
+table, hand-built blocks, numpy's IEEE conversions, PyTorch's E4M3 conversion,
+brute-force top-k, a dense numpy SwiGLU, the vLLM article's route-sanitiser
+example, and invariances."""
 import numpy as np
 import pytest
 
 import oracle
 import synth
-from _util import (bf16_to_f64, check_close, golden_kv, golden_table, np_dense, np_route,
-                   np_swiglu_expert)
+from _util import (bf16_to_f64, check_close, golden_kv, golden_table, np_dense,
+                   np_e4m3_rows, np_route, np_row_exponents, np_swiglu_expert,
+                   np_swiglu_expert_e4m3)
 
 
 # ---------------------------------------------------------------- table/layout
@@ -268,6 +270,118 @@ def test_mma16_is_close_to_exact():
     y16 = oracle.moe_layer(s.H, s.F, s.Fs, s.E, s.k, 1, ex, sh, x, ids, w, mode=oracle.MMA16)
     check_close(y16, ye, "mma16 vs exact", max_rel=5e-3, l2_rel=2e-3)
     assert not np.array_equal(y16, ye)
+
+
+# ---------------------------------------------------------------- mma8 (E4M3 operands)
+
+def test_e4m3_decoder_all_codes():
+    # every one of the 256 codes against PyTorch's float8_e4m3fn decoder
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_to_double(c) for c in codes])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan) and nan.sum() == 2      # 0x7F, 0xFF
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x08] == 2.0 ** -6
+
+
+def test_e4m3_encoder_round_to_nearest_even():
+    # every finite code value, every midpoint between neighbours (ties go to the
+    # even fraction), the float32 values just around each midpoint, and random
+    # values, both signs, against PyTorch's conversion (which agrees up to 464).
+    # All are float32 values: PyTorch converts a float64 through float32 first,
+    # which would round a double just below a midpoint onto it.
+    import torch
+    vals = np.array(sorted({oracle.e4m3_to_double(c) for c in range(0x7F)}))   # 0 .. 448
+    mids = ((vals[:-1] + vals[1:]) / 2).astype(np.float32)
+    near = np.concatenate([np.nextafter(mids, np.float32(0)), np.nextafter(mids, np.float32(1e9))])
+    rnd = np.random.default_rng(5).uniform(-460, 460, 4000).astype(np.float32)
+    small = np.random.default_rng(6).uniform(-2.0 ** -5, 2.0 ** -5, 2000).astype(np.float32)
+    v = np.concatenate([vals.astype(np.float32), mids, near, rnd, small, [np.float32(464.0)]])
+    v = np.concatenate([v, -v])
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.double_to_e4m3(float(x)) for x in v], np.uint8)
+    assert np.array_equal(got, ref)
+    assert oracle.double_to_e4m3(1.0625) == 0x38 and oracle.double_to_e4m3(1.1875) == 0x3A
+
+
+def test_e4m3_encoder_saturates():
+    # the saturating reading (finite overflow and infinities to +-448, NaN to NaN)
+    for v, c in ((448.0, 0x7E), (449.0, 0x7E), (480.0, 0x7E), (1e30, 0x7E),
+                 (float("inf"), 0x7E), (-1e30, 0xFE), (-float("inf"), 0xFE)):
+        assert oracle.double_to_e4m3(v) == c, v
+    assert oracle.double_to_e4m3(float("nan")) & 0x7F == 0x7F
+
+
+def test_mma8_weights_against_pytorch_rounding():
+    s = synth.Shape("t8", 256, 128, 2, 1, 2, 1)
+    g, u, d = synth.expert_mats(s, 17, 0, 1)
+    for m, rows, K in ((g, 128, 256), (d, 256, 128)):
+        w8, ex = oracle.dequant_rows_e4m3(m, rows, K)
+        assert np.array_equal(ex, np_row_exponents(m, rows, K))
+        ref = np_e4m3_rows(np_dense(m, rows, K), np_row_exponents(m, rows, K))
+        assert np.array_equal(w8, ref)
+        assert not np.array_equal(w8, np_dense(m, rows, K))           # rounding happened
+
+
+def test_mma8_single_expert_equals_dense_reference():
+    # E = 1, k = 1, no shared expert: one dense SwiGLU FFN with the mma8 roundings
+    s = synth.Shape("t", 128, 96, 1, 1, 5, 1, n_shared=0)
+    _, _, x, ex, _ = _layer_inputs(s, 11)
+    ids = np.zeros((5, 1), np.int32)
+    w = np.ones((5, 1))
+    y = oracle.moe_layer(s.H, s.F, s.F, 1, 1, 0, ex, None, x, ids, w, mode=oracle.MMA8)
+    ref = np_swiglu_expert_e4m3(ex[0], s.H, s.F, bf16_to_f64(x))
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-15 * np.abs(ref).max())
+
+
+def test_mma8_layer_equals_dense_masked_evaluation():
+    s = synth.SHAPES[0]
+    Wr, b, x, ex, sh = _layer_inputs(s, 22)
+    ids, w, _, _ = oracle.route(Wr, b, x, s.k)
+    y = oracle.moe_layer(s.H, s.F, s.Fs, s.E, s.k, 1, ex, sh, x, ids, w, mode=oracle.MMA8)
+    X = bf16_to_f64(x)
+    dense = np.stack([np_swiglu_expert_e4m3(ex[e], s.H, s.F, X) for e in range(s.E)])
+    shared = np_swiglu_expert_e4m3(sh, s.H, s.Fs, X)
+    ref = np.zeros_like(y)
+    for t in range(s.T):
+        mask = np.zeros(s.E)
+        mask[ids[t]] = w[t]
+        ref[t] = (mask[:, None] * dense[:, t, :]).sum(0) + shared[t]
+    assert np.allclose(y, ref, rtol=1e-11, atol=1e-14 * np.abs(ref).max())
+
+
+def test_mma8_exponent_steps_scale_exactly():
+    # doubling every scale of the up matrices doubles u, so h, and (the h
+    # exponent follows) y exactly; doubling every down scale doubles y exactly
+    s = synth.SHAPES[0]
+    Wr, b, x, ex, sh = _layer_inputs(s, 33)
+    ids, w, _, _ = oracle.route(Wr, b, x, s.k)
+    def run(ex_, sh_):
+        return oracle.moe_layer(s.H, s.F, s.Fs, s.E, s.k, 1, ex_, sh_, x, ids, w,
+                                mode=oracle.MMA8)
+    y = run(ex, sh)
+    def dbl(m):
+        m = m.copy()
+        dd = m[:, 0:2].copy().view("<u2")
+        m[:, 0:2] = (dd + np.uint16(0x0400)).view(np.uint8).reshape(-1, 2)
+        return m
+    y_up = run({e: (g_, dbl(u_), d_) for e, (g_, u_, d_) in ex.items()}, (sh[0], dbl(sh[1]), sh[2]))
+    y_dn = run({e: (g_, u_, dbl(d_)) for e, (g_, u_, d_) in ex.items()}, (sh[0], sh[1], dbl(sh[2])))
+    assert np.array_equal(y_up, 2.0 * y)
+    assert np.array_equal(y_dn, 2.0 * y)
+
+
+def test_mma8_is_close_to_exact():
+    # information: E4M3 operands (3 fraction bits) move y by a few percent
+    s = synth.SHAPES[0]
+    Wr, b, x, ex, sh = _layer_inputs(s, 61)
+    ids, w, _, _ = oracle.route(Wr, b, x, s.k)
+    ye = oracle.moe_layer(s.H, s.F, s.Fs, s.E, s.k, 1, ex, sh, x, ids, w, mode=oracle.EXACT)
+    y8 = oracle.moe_layer(s.H, s.F, s.Fs, s.E, s.k, 1, ex, sh, x, ids, w, mode=oracle.MMA8)
+    rel = np.linalg.norm(y8 - ye) / np.linalg.norm(ye)
+    assert 1e-3 < rel < 0.1, rel
 
 
 # ---------------------------------------------------------------- byte budget
