@@ -114,8 +114,9 @@ moe_status moe_route_topk(const moe_shape* shape, const uint16_t* router_w,
                           const float* router_bias, const uint16_t* x, int32_t T,
                           int32_t* ids, float* weights, void* stream);
 
-/* Bytes of workspace that moe_iq4nl_decode (mode 0) or
- * moe_iq4nl_prefill_grouped (mode 1) needs for up to max_tokens tokens.
+/* Bytes of workspace that moe_iq4nl_decode (mode 0),
+ * moe_iq4nl_prefill_grouped (mode 1) or moe_iq4nl_prefill_grouped_fp8
+ * (mode 2) needs for up to max_tokens tokens.
  * Returns 0 for an invalid shape, mode or max_tokens. The workspace is
  * caller-owned device memory, 256-byte aligned, and MUST be zero-filled once
  * after allocation (cudaMemset); every call leaves its counter words at zero
@@ -257,6 +258,53 @@ moe_status moe_iq4nl_prefill_grouped(const moe_shape* shape, const moe_expert_we
                                      const float* weights, float* y, void* ws,
                                      size_t ws_bytes, uint32_t* status, void* stream);
 
+/* Prefill with 8-bit operands: the same step as moe_iq4nl_prefill_grouped on
+ * the 8-bit tensor cores (tcgen05 kind::f8f6f4, fp32 accumulation), which
+ * the Xolotl engine blog ("Prompts: fast, and exact") names for its prompt
+ * contraction on the 4090. Operands are OCP E4M3 codes (bias 7, largest
+ * finite 448), rounded to nearest even with finite overflow saturated:
+ *   weights : row r of a matrix is scaled by 2^-E_r before rounding, E_r the
+ *             largest floor(log2 d) over the row's block scales d (-14 for a
+ *             zero or subnormal d), so w8 = 2^E_r e4m3(d T[q] 2^-E_r);
+ *   x       : each token's row is scaled by 2^-X, X = floor(log2 max|x|) - 6
+ *             (0 for an all-zero row), so its largest value lies in [64, 128);
+ *   h       : each (token, expert) row of SwiGLU outputs the same way, from
+ *             the row's fp32 h.
+ * The accumulators are multiplied back by 2^(E_r + X) exactly; the combine is
+ * that of moe_iq4nl_prefill_grouped. The result differs from the fp16-operand
+ * call by the E4M3 rounding (about 2^-4 relative per operand).
+ *   row_exp : device int8, the table moe_iq4nl_fp8_row_exponents wrote for
+ *             these weights (it depends on the weights only: make it once).
+ * Shape rule: hidden, ffn and ffn_shared are multiples of 256 (the operand
+ * ring carries 256 weights of a row per copy); other shapes are refused with
+ * MOE_ERR_UNSUPPORTED. ws from moe_workspace_bytes(shape, >= T, 2); the other
+ * arguments as for moe_iq4nl_prefill_grouped. */
+moe_status moe_iq4nl_prefill_grouped_fp8(const moe_shape* shape, const moe_expert_weights* w,
+                                         const int8_t* row_exp, const uint16_t* x, int32_t T,
+                                         const int32_t* ids, const float* weights, float* y,
+                                         void* ws, size_t ws_bytes, uint32_t* status,
+                                         void* stream);
+
+/* Entries (int8, one per weight row) of the row-exponent table of a shape:
+ * E*ffn (gate) + E*ffn (up) + E*hidden (down) and, with a shared expert,
+ * ffn_shared (gate) + ffn_shared (up) + hidden (down), in that order. 0 for an
+ * invalid shape. */
+int64_t moe_fp8_row_exponent_count(const moe_shape* shape);
+
+/* Write the row-exponent table (E_r above, in the order above) of a layer's
+ * weights to row_exp (device, moe_fp8_row_exponent_count bytes). */
+moe_status moe_iq4nl_fp8_row_exponents(const moe_shape* shape, const moe_expert_weights* w,
+                                       int8_t* row_exp, void* stream);
+
+/* The E4M3 weight decoder of moe_iq4nl_prefill_grouped_fp8 on its own, so
+ * that it can be checked bit for bit: rows x K weights (K a multiple of 32;
+ * rows of K/32 IQ4_NL blocks, 18 bytes each, packed) to row_exp[rows] (E_r as
+ * above) and out[rows][K], the E4M3 code of d T[q] 2^-E_r for each weight, both
+ * through the device functions the fp8 prefill runs.
+ *   mat : device, 2-byte aligned   row_exp : device   out : device, 4-byte aligned */
+moe_status moe_iq4nl_dequantize_e4m3(const void* mat, int64_t rows, int32_t K, int8_t* row_exp,
+                                     uint8_t* out, void* stream);
+
 /* Dequantise n_blocks consecutive IQ4_NL blocks (the block layout above),
  * through one of the block decoders the layer kernels use, so that each can be
  * checked bit for bit against the format's definition:
@@ -286,7 +334,8 @@ moe_status moe_sanitize_routes(const int32_t* ids, const float* weights, int64_t
 
 /* Kernel launches one call makes for this shape and token count (host, no
  * device work): call 0 = moe_route_topk, 1 = moe_iq4nl_decode,
- * 2 = moe_iq4nl_decode_routed, 3 = moe_iq4nl_prefill_grouped, and
+ * 2 = moe_iq4nl_decode_routed, 3 = moe_iq4nl_prefill_grouped,
+ * 5 = moe_iq4nl_prefill_grouped_fp8, and
  * 4 + 2*n_layers + chained = moe_iq4nl_decode_layers of n_layers layers
  * (chained 0 or 1). Returns a negative moe_status for bad arguments. */
 int32_t moe_launches_per_call(const moe_shape* shape, int32_t T, int32_t call);

@@ -40,7 +40,7 @@ STATUS_INVALID_ROUTE_MASK = 0x0000FFFF
 STATUS_TIMEOUT = 0x80000000
 MAX_DECODE_TOKENS = 16
 STATIC_SCRATCH_BYTES = 8 << 20
-DECODE, PREFILL = 0, 1
+DECODE, PREFILL, PREFILL_FP8 = 0, 1, 2
 DEQUANT_FP32, DEQUANT_FP16, DEQUANT_FP32_ONE_TOKEN = 0, 1, 2
 
 
@@ -81,6 +81,17 @@ _lib.moe_iq4nl_decode_layers.restype = ctypes.c_int
 _lib.moe_iq4nl_decode_static.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(_Weights), _P,
                                          ctypes.c_int32, _P, _P, _P, _P, _P]
 _lib.moe_iq4nl_decode_static.restype = ctypes.c_int
+_lib.moe_iq4nl_prefill_grouped_fp8.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(_Weights),
+                                               _P, _P, ctypes.c_int32, _P, _P, _P, _P,
+                                               ctypes.c_size_t, _P, _P]
+_lib.moe_iq4nl_prefill_grouped_fp8.restype = ctypes.c_int
+_lib.moe_fp8_row_exponent_count.argtypes = [ctypes.POINTER(Shape)]
+_lib.moe_fp8_row_exponent_count.restype = ctypes.c_int64
+_lib.moe_iq4nl_fp8_row_exponents.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(_Weights), _P,
+                                             _P]
+_lib.moe_iq4nl_fp8_row_exponents.restype = ctypes.c_int
+_lib.moe_iq4nl_dequantize_e4m3.argtypes = [_P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P]
+_lib.moe_iq4nl_dequantize_e4m3.restype = ctypes.c_int
 _lib.moe_iq4nl_dequantize.argtypes = [_P, ctypes.c_int64, ctypes.c_int32, _P, _P]
 _lib.moe_iq4nl_dequantize.restype = ctypes.c_int
 _lib.moe_sanitize_routes.argtypes = [_P, _P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P, _P]
@@ -97,7 +108,9 @@ _lib.moe_version.restype = ctypes.c_char_p
 
 EXPORTS = ("moe_route_topk", "moe_workspace_bytes", "moe_iq4nl_decode", "moe_iq4nl_decode_routed",
            "moe_iq4nl_decode_layers",
-           "moe_iq4nl_decode_static", "moe_iq4nl_prefill_grouped", "moe_iq4nl_dequantize", "moe_sanitize_routes",
+           "moe_iq4nl_decode_static", "moe_iq4nl_prefill_grouped", "moe_iq4nl_prefill_grouped_fp8",
+           "moe_fp8_row_exponent_count", "moe_iq4nl_fp8_row_exponents", "moe_iq4nl_dequantize_e4m3",
+           "moe_iq4nl_dequantize", "moe_sanitize_routes",
            "moe_launches_per_call", "moe_set_pdl", "moe_set_barrier_wait_ns", "moe_status_string",
            "moe_version")
 
@@ -474,6 +487,55 @@ def iq4nl_prefill_grouped(shape: Shape, w: ExpertWeights, x, ids, weights, ws, y
     """Prefill a chunk of tokens: y fp32 [T,H]."""
     return _layer(_lib.moe_iq4nl_prefill_grouped, "moe_iq4nl_prefill_grouped", shape, w, x, ids,
                   weights, y, ws, status, stream)
+
+
+def fp8_row_exponents(shape: Shape, w: ExpertWeights, out=None, stream=None):
+    """The row-exponent table of the 8-bit prefill for these weights: int8 [n]
+    (gate rows, up rows, down rows, then the shared expert's), made once per
+    set of weights."""
+    n = int(_lib.moe_fp8_row_exponent_count(ctypes.byref(shape)))
+    if n <= 0:
+        raise MoeError(MOE_ERR_INVALID_ARG, "moe_fp8_row_exponent_count")
+    keep = w.check(shape)
+    w.check_device()
+    dev = keep[0].device
+    if out is None:
+        out = torch.empty(n, dtype=torch.int8, device=dev)
+    _dev(out, torch.int8, "out", (n,))
+    _same_device(out, *keep)
+    _check(_lib.moe_iq4nl_fp8_row_exponents(ctypes.byref(shape), ctypes.byref(w.c), _ptr(out),
+                                            _stream(stream)), "moe_iq4nl_fp8_row_exponents")
+    return out
+
+
+def iq4nl_prefill_grouped_fp8(shape: Shape, w: ExpertWeights, row_exp, x, ids, weights, ws,
+                              y=None, status=None, stream=None):
+    """Prefill a chunk of tokens with E4M3 operands: y fp32 [T,H]. row_exp from
+    fp8_row_exponents(shape, w); ws from workspace(shape, T, PREFILL_FP8)."""
+    T, y = _layer_args(shape, w, x, ids, weights, y, status)
+    n = int(_lib.moe_fp8_row_exponent_count(ctypes.byref(shape)))
+    _dev(row_exp, torch.int8, "row_exp", (n,) if n > 0 else None)
+    if ws is not None:
+        _dev(ws, torch.uint8, "ws")
+    _same_device(x, row_exp, ws)
+    _check(_lib.moe_iq4nl_prefill_grouped_fp8(
+        ctypes.byref(shape), ctypes.byref(w.c), _ptr(row_exp), _ptr(x), int(T), _ptr(ids),
+        _ptr(weights), _ptr(y), _ptr(ws), int(ws.numel() if ws is not None else 0),
+        _ptr(status), _stream(stream)), "moe_iq4nl_prefill_grouped_fp8")
+    return y
+
+
+def iq4nl_dequantize_e4m3(mat, rows: int, K: int, stream=None):
+    """mat: uint8 device tensor of rows x K/32 IQ4_NL blocks -> (row exponents
+    int8 [rows], E4M3 codes uint8 [rows, K]) through the 8-bit prefill's decoder."""
+    if not isinstance(mat, torch.Tensor) or K % 32 or mat.numel() != rows * (K // 32) * 18:
+        raise ValueError("mat must hold rows x K/32 blocks of 18 bytes")
+    _dev(mat, torch.uint8, "mat")
+    row_exp = torch.empty(rows, dtype=torch.int8, device=mat.device)
+    out = torch.empty((rows, K), dtype=torch.uint8, device=mat.device)
+    _check(_lib.moe_iq4nl_dequantize_e4m3(_ptr(mat), int(rows), int(K), _ptr(row_exp), _ptr(out),
+                                          _stream(stream)), "moe_iq4nl_dequantize_e4m3")
+    return row_exp, out
 
 
 def iq4nl_dequantize(blocks, fp16: bool = False, out=None, stream=None, mode=None):

@@ -147,6 +147,10 @@ size_t moe_workspace_bytes(const moe_shape* shape, int32_t max_tokens, int32_t m
     if (max_tokens < 1 || max_tokens > moe::kPrefillMaxTokens) return 0;
     return (size_t)moe::prefill_layout(*shape, max_tokens).total;
   }
+  if (mode == 2) {
+    if (max_tokens < 1 || max_tokens > moe::kPrefillMaxTokens) return 0;
+    return (size_t)moe::prefill_layout(*shape, max_tokens, true).total;
+  }
   return 0;
 }
 
@@ -263,6 +267,57 @@ moe_status moe_iq4nl_prefill_grouped(const moe_shape* shape, const moe_expert_we
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+moe_status moe_iq4nl_prefill_grouped_fp8(const moe_shape* shape, const moe_expert_weights* w,
+                                         const int8_t* row_exp, const uint16_t* x, int32_t T,
+                                         const int32_t* ids, const float* weights, float* y,
+                                         void* ws, size_t ws_bytes, uint32_t* status,
+                                         void* stream) {
+  moe_status st = layer_args(shape, w, x, T, moe::kPrefillMaxTokens, ids, weights, y, ws, status);
+  if (st != MOE_OK || T == 0) return st;
+  if (!row_exp) return MOE_ERR_INVALID_ARG;
+  if (!moe::prefill_fp8_supported(*shape)) return MOE_ERR_UNSUPPORTED;
+  const moe::PrefillLayout L = moe::prefill_layout(*shape, T, true);
+  if (ws_bytes < (size_t)L.total) return MOE_ERR_WORKSPACE;
+  const int sms = num_sms();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  const cudaError_t e = moe::launch_prefill_fp8(*shape, *w, row_exp, x, T, ids, weights, y,
+                                                reinterpret_cast<uint8_t*>(ws), L, status, sms,
+                                                g_pdl.load() != 0,
+                                                reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int64_t moe_fp8_row_exponent_count(const moe_shape* shape) {
+  if (check_shape(shape) != MOE_OK) return 0;
+  return moe::fp8_row_exponent_count(*shape);
+}
+
+moe_status moe_iq4nl_fp8_row_exponents(const moe_shape* shape, const moe_expert_weights* w,
+                                       int8_t* row_exp, void* stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (!w || !row_exp) return MOE_ERR_INVALID_ARG;
+  st = check_weights(shape, w);
+  if (st != MOE_OK) return st;
+  const cudaError_t e = moe::launch_fp8_row_exponents(*shape, *w, row_exp,
+                                                      reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_iq4nl_dequantize_e4m3(const void* mat, int64_t rows, int32_t K, int8_t* row_exp,
+                                     uint8_t* out, void* stream) {
+  if (rows < 0 || K < 32 || K % 32) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!mat || !row_exp || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(mat, 2) || !aligned(out, 4)) return MOE_ERR_MISALIGNED;
+  const int sms = num_sms();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  const cudaError_t e = moe::launch_dequant_e4m3(mat, rows, K, row_exp, out, sms,
+                                                 reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 moe_status moe_iq4nl_dequantize(const void* blocks, int64_t n_blocks, int32_t mode,
                                 void* out, void* stream) {
   if (n_blocks < 0 || (mode != MOE_DEQUANT_FP32 && mode != MOE_DEQUANT_FP16 &&
@@ -321,6 +376,7 @@ int32_t moe_launches_per_call(const moe_shape* shape, int32_t T, int32_t call) {
     return call == 2 ? n + 1 : n;
   }
   if (call == 3) return moe::prefill_launches(*shape, T);
+  if (call == 5) return moe::prefill_fp8_supported(*shape) ? 7 : 0;
   if (call >= 6) {                           // 4 + 2 * n_layers + chained
     const int n_layers = (call - 4) / 2, chained = (call - 4) % 2;
     if (n_layers < 1 || n_layers > MOE_MAX_LAYERS || T > MOE_MAX_DECODE_TOKENS)

@@ -48,7 +48,7 @@ __device__ uint64_t g_pfprof[2 * 256 * 16 * 8];
   } while (0)
 #endif
 
-PrefillLayout prefill_layout(const moe_shape& s, int64_t T) {
+PrefillLayout prefill_layout(const moe_shape& s, int64_t T, bool fp8) {
   PrefillLayout L{};
   int64_t off = 0;
   auto take = [&](int64_t bytes) {
@@ -68,6 +68,15 @@ PrefillLayout prefill_layout(const moe_shape& s, int64_t T) {
   L.h16 = take(rows * fmax * 2);                // h in bucket order, fp16
   L.o = take(rows * H * 4);                     // expert outputs in bucket order, fp32
   L.sched = 0;
+  if (fp8) {
+    L.x8 = take(rows * H);                      // E4M3 codes of x 2^-X, bucket order
+    L.h8 = take(rows * fmax);                   // E4M3 codes of h 2^-X
+    L.h32 = take(rows * fmax * 4);              // h, fp32, bucket order
+    L.xexp = take(T * 4);                       // each token's exponent
+    L.bexp = take(rows * 4);                    // each bucket row's x exponent
+    L.hexp = take(rows * 4);                    // each bucket row's h exponent
+    L.hmax = take(rows * 4);                    // each bucket row's largest |h|
+  }
   L.total = off;
   return L;
 }
@@ -220,9 +229,19 @@ struct CombineListParams {
   int32_t* comb_row;       // [T][k+1]
   float* comb_w;           // [T][k+1]
 };
+// F8: the bucket rows are E4M3 codes of x 2^-X_t (X_t the token's exponent),
+// each row's X_t goes to bexp, and the rows' largest-|h| words are cleared for
+// the gate/up GEMM.
+struct Gather8 {
+  const int32_t* xexp_tok;   // [T]
+  int32_t* bexp;             // [rows]
+  uint32_t* hmax;            // [rows]
+  uint8_t* x8;               // [rows][H]
+};
+template <bool F8>
 __global__ void pf_gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ bucket_off,
                                  const int32_t* __restrict__ row_tok, int E, int H, __half* xs,
-                                 const CombineListParams cl) {
+                                 const CombineListParams cl, const Gather8 g8) {
   pdl_wait();
   pdl_trigger();
   {
@@ -262,6 +281,29 @@ __global__ void pf_gather_kernel(const uint16_t* __restrict__ x, const int32_t* 
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
   const int h8 = H / 8;
+  if constexpr (F8) {
+    for (int r = gw; r < rows; r += nw) {
+      const int t = row_tok[r];
+      const int X = g8.xexp_tok[t];
+      if (lane == 0) {
+        g8.bexp[r] = X;
+        g8.hmax[r] = 0u;
+      }
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+      uint2* dst = reinterpret_cast<uint2*>(g8.x8 + (size_t)r * H);
+      for (int c = lane; c < h8; c += 32) {
+        const uint4 v = src[c];
+        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+        uint32_t pk[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)      // values 2i (low half) and 2i + 1 (high half)
+          pk[i] = cvt_e4m3x2(ldexpf(__uint_as_float(in[i] & 0xFFFF0000u), -X),
+                             ldexpf(__uint_as_float(in[i] << 16), -X));
+        dst[c] = make_uint2(pk[0] | (pk[1] << 16), pk[2] | (pk[3] << 16));
+      }
+    }
+    return;
+  }
   for (int r = gw; r < rows; r += nw) {
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)row_tok[r] * H);
     uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)r * H);
@@ -276,6 +318,61 @@ __global__ void pf_gather_kernel(const uint16_t* __restrict__ x, const int32_t* 
         out[i] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
       }
       dst[c] = make_uint4(out[0], out[1], out[2], out[3]);
+    }
+  }
+}
+
+// E4M3 operands: each token's exponent X_t = floor(log2 max|x_t|) - 6, one
+// warp per token.
+__global__ void pf8_xexp_kernel(const uint16_t* __restrict__ x, int T, int H,
+                                int32_t* __restrict__ xexp) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  for (int t = gw; t < T; t += nw) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    uint32_t m = 0;
+    for (int c = lane; c < H / 8; c += 32) {
+      const uint4 v = src[c];
+      const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {   // |bf16| as fp32 bits: the order of the values
+        const uint32_t a = (in[i] << 16) & 0x7FFFFFFFu, b = in[i] & 0x7FFF0000u;
+        m = a > m ? a : m;
+        m = b > m ? b : m;
+      }
+    }
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if (lane == 0) xexp[t] = vec_exponent_bits(m);
+  }
+}
+
+// E4M3 operands: h (fp32, written by the gate/up GEMM) to E4M3 codes of
+// h 2^-X_p, X_p from the row's largest |h|, one warp per bucket row.
+__global__ void pf8_hconv_kernel(const float* __restrict__ h32, const uint32_t* __restrict__ hmax,
+                                 const int32_t* __restrict__ bucket_off, int E, int ld, int F,
+                                 int Fs, uint8_t* __restrict__ h8, int32_t* __restrict__ hexp) {
+  pdl_wait();
+  pdl_trigger();
+  const int rows = bucket_off[E + 1], n_valid = bucket_off[E];
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  for (int r = gw; r < rows; r += nw) {
+    const int X = vec_exponent_bits(hmax[r]);
+    if (lane == 0) hexp[r] = X;
+    const int K = r < n_valid ? F : Fs;
+    const float4* src = reinterpret_cast<const float4*>(h32 + (size_t)r * ld);
+    uint2* dst = reinterpret_cast<uint2*>(h8 + (size_t)r * ld);
+    for (int c = lane; c < K / 8; c += 32) {
+      const float4 a = src[2 * c], b = src[2 * c + 1];
+      const uint32_t p0 = cvt_e4m3x2(ldexpf(a.y, -X), ldexpf(a.x, -X));
+      const uint32_t p1 = cvt_e4m3x2(ldexpf(a.w, -X), ldexpf(a.z, -X));
+      const uint32_t p2 = cvt_e4m3x2(ldexpf(b.y, -X), ldexpf(b.x, -X));
+      const uint32_t p3 = cvt_e4m3x2(ldexpf(b.w, -X), ldexpf(b.z, -X));
+      dst[c] = make_uint2(p0 | (p1 << 16), p2 | (p3 << 16));
     }
   }
 }
@@ -306,6 +403,14 @@ struct GemmParams {
   float* o;              // down out: [rows][ldo]
   int ldo;
   uint32_t* status;
+  // E4M3 operands only: each weight row's exponent (routed [E][M], shared
+  // [Ms]) for a0, a1, s0, s1; the B operand's exponent per bucket row (x: its
+  // token's, h: its pair's); gate/up writes h as fp32 [rows][ldh] and each
+  // row's largest |h| (fp32 bits, by atomicMax: the same whatever the order)
+  const int8_t *e0, *e1, *se0, *se1;
+  const int32_t* bexp;
+  float* h32;
+  uint32_t* hmax;
 };
 
 // Shared memory and warp roles of the GEMM kernels. RAW: the IQ4_NL rows of the
@@ -369,10 +474,18 @@ __device__ __forceinline__ int box_index(int n) {
   return n <= 32 ? 0 : (n <= 64 ? 1 : (n <= 128 ? 2 : 3));
 }
 
-template <bool GATEUP, bool RAW>
+// F8: E4M3 operands (kind::f8f6f4). A K-step is then 128 values, the same 128
+// bytes of every row as a 64-value fp16 step, so the stages, rings and
+// barriers are the same; a raw copy (four pairs of blocks) feeds two steps.
+// Each weight row is scaled by 2^-E_row before rounding and each B row by
+// 2^-bexp; the epilogue multiplies the accumulator back by 2^(E_row + bexp).
+template <bool GATEUP, bool RAW, bool F8>
 __global__ void __launch_bounds__(GemmCfg<GATEUP, RAW>::kThreads, 1)
 pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
   using S = GemmCfg<GATEUP, RAW>;
+  static_assert(!F8 || RAW, "E4M3 operands need the raw-row ring");
+  constexpr int kTKe = F8 ? 128 : kTK;                     // K values per stage
+  constexpr int kStepsPerRaw = F8 ? 2 : S::kRawGroup;      // stages per raw copy
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -457,7 +570,7 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
       for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
         const TileInfo ti = tile_info(t);
         const int K = ti.bucket < p.E ? p.K : p.Ks;
-        for (int ks = 0; ks < K / kTK; ++ks, ++it) {
+        for (int ks = 0; ks < K / kTKe; ++ks, ++it) {
           const int s = it % S::kStages;
           if (!mbar_wait(&empty[s], ((it / S::kStages) & 1) ^ 1, p.status)) {
             t = ntiles;                          // give up; fall through to the exit barrier
@@ -465,8 +578,8 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
           }
           uint8_t* b = stages + (size_t)s * S::kStage + (GATEUP ? 2 : 1) * S::kA;
           const int bx = box_index(ti.nvalid);
-          mbar_arrive_expect_tx(&full_b[s], (uint32_t)((32 << bx) * kTK * 2));
-          tma_load_2d(b, &tmaps.m[bx], ks * kTK, ti.row0 + ti.n0, &full_b[s]);
+          mbar_arrive_expect_tx(&full_b[s], (uint32_t)((32 << bx) * 128));   // 128 B a row
+          tma_load_2d(b, &tmaps.m[bx], ks * kTKe, ti.row0 + ti.n0, &full_b[s]);
         }
       }
     }
@@ -485,7 +598,7 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
         PF_STAMP(tc, 0, global_timer_ns());
         PF_STAMP(tc, 6, (uint64_t)ti.nvalid);
         PF_STAMP(tc, 7, (uint64_t)ti.bucket);
-        for (int ks = 0; ks < K / kTK; ++ks, ++it) {
+        for (int ks = 0; ks < K / kTKe; ++ks, ++it) {
           const int s = it % S::kStages;
           const uint32_t par = (it / S::kStages) & 1;
           if (!mbar_wait(&full_a[s], par, p.status) || !mbar_wait(&full_b[s], par, p.status)) {
@@ -498,10 +611,15 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
           const uint64_t ad1 = sw128_kmajor_desc(smem_u32(st + S::kA));
           const uint64_t bd = sw128_kmajor_desc(smem_u32(st + (GATEUP ? 2 : 1) * S::kA));
 #pragma unroll
-          for (int kk = 0; kk < kTK / 16; ++kk) {
+          for (int kk = 0; kk < 4; ++kk) {          // 32 bytes of K per MMA
             const uint32_t accum = (ks > 0 || kk > 0) ? 1u : 0u;
-            tc_mma_f16(acc, ad0 + 2 * kk, bd + 2 * kk, idesc, accum);
-            if (GATEUP) tc_mma_f16(acc + kTN, ad1 + 2 * kk, bd + 2 * kk, idesc, accum);
+            if constexpr (F8) {
+              tc_mma_f8(acc, ad0 + 2 * kk, bd + 2 * kk, idesc, accum);
+              if (GATEUP) tc_mma_f8(acc + kTN, ad1 + 2 * kk, bd + 2 * kk, idesc, accum);
+            } else {
+              tc_mma_f16(acc, ad0 + 2 * kk, bd + 2 * kk, idesc, accum);
+              if (GATEUP) tc_mma_f16(acc + kTN, ad1 + 2 * kk, bd + 2 * kk, idesc, accum);
+            }
           }
           tc_commit(&empty[s]);
         }
@@ -551,7 +669,14 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
       const TileInfo ti = tile_info(t);
       const bool sh = ti.bucket >= p.E;
       const int K = sh ? p.Ks : p.K;
-      const int nks = K / kTK;
+      const int nks = K / kTKe;
+      // E4M3: the exponent of this thread's weight row
+      int erow = 0;
+      if constexpr (F8) {
+        const int8_t* et = sh ? ((GATEUP && part) ? p.se1 : p.se0)
+                              : ((GATEUP && part) ? p.e1 : p.e0);
+        erow = et[(sh ? 0 : (size_t)ti.bucket * p.M) + ti.m0 + r];
+      }
       if (warp == S::kCtl && lane == 0) PF_STAMP(tc, 2, global_timer_ns());
       // publish one dequantised K-step of this thread
       auto publish = [&](int s) {
@@ -561,16 +686,38 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
         ++it;
       };
       if constexpr (RAW) {
-        for (int g = 0; ok && g < nks / S::kRawGroup; ++g, ++itr) {
+        for (int g = 0; ok && g < nks / kStepsPerRaw; ++g, ++itr) {
           const int sr = itr % S::kRawRing;
           if (!mbar_wait(&full_raw[sr], (itr / S::kRawRing) & 1, p.status)) { ok = false; break; }
           const uint8_t* rrow = raw + (size_t)sr * S::kRawStage + (GATEUP ? part * S::kRawMat : 0) +
                                 (size_t)r * S::kRawGroup * kPairB;
 #pragma unroll
-          for (int j = 0; j < S::kRawGroup; ++j) {
+          for (int j = 0; j < kStepsPerRaw; ++j) {
             const int s = it % S::kStages;
             if (!mbar_wait(&empty[s], ((it / S::kStages) & 1) ^ 1, p.status)) { ok = false; break; }
             uint8_t* tile = stages + (size_t)s * S::kStage + (GATEUP ? part * S::kA : 0);
+            if constexpr (F8) {
+              // the step's four blocks are pairs 2j and 2j + 1 of the copy; this
+              // thread takes pair 2j + blkh: 64 codes, chunks 4 blkh .. 4 blkh + 3
+              const uint32_t* pw = reinterpret_cast<const uint32_t*>(rrow + (2 * j + blkh) * kPairB);
+              uint32_t w9[9];
+#pragma unroll
+              for (int i = 0; i < 9; ++i) w9[i] = pw[i];
+              uint32_t q0[4], q1[4], o0[8], o1[8];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) q0[i] = prmt(w9[i], w9[i + 1], 0x5432u);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) q1[i] = w9[5 + i];
+              dequant_block_e4m3(q0, (uint16_t)(w9[0] & 0xFFFFu), erow, o0);
+              dequant_block_e4m3(q1, (uint16_t)(w9[4] >> 16), erow, o1);
+              const int c0 = 4 * blkh;
+              sw128_store_chunk(tile, r, c0, make_uint4(o0[0], o0[1], o0[2], o0[3]));
+              sw128_store_chunk(tile, r, c0 + 1, make_uint4(o0[4], o0[5], o0[6], o0[7]));
+              sw128_store_chunk(tile, r, c0 + 2, make_uint4(o1[0], o1[1], o1[2], o1[3]));
+              sw128_store_chunk(tile, r, c0 + 3, make_uint4(o1[4], o1[5], o1[6], o1[7]));
+              publish(s);
+              continue;
+            }
             const uint32_t* w = reinterpret_cast<const uint32_t*>(rrow + j * kPairB + (blkh ? 16 : 0));
             uint32_t q[4];
             uint16_t dbits;
@@ -668,6 +815,12 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
       constexpr int kCols = kTN / (S::kDq / 4);
       const int ch = dw >> 2;                   // column share
       const int mrow = ti.m0 + q * 32 + lane;   // weight row of this thread
+      int eg = 0, eu = 0;                       // E4M3: the gate and up rows' exponents
+      if constexpr (F8) {
+        const size_t er = (sh ? 0 : (size_t)ti.bucket * p.M) + mrow;
+        eg = (sh ? p.se0 : p.e0)[er];
+        eu = (sh ? p.se1 : p.e1)[er];
+      }
       for (int c = 0; c < kCols; c += 32) {
         const int col = ch * kCols + c;
         if (col >= ti.nvalid) break;            // warp-uniform
@@ -678,8 +831,19 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           if (col + j < ti.nvalid) {
-            const float hv = silu_mul(__uint_as_float(g[j]), __uint_as_float(u[j]));
-            p.h[(size_t)(ti.row0 + ti.n0 + col + j) * p.ldh + mrow] = __float2half_rn(hv);
+            const size_t row = (size_t)(ti.row0 + ti.n0 + col + j);
+            if constexpr (F8) {
+              const int bx = p.bexp[row];
+              const float hv = silu_mul(ldexpf(__uint_as_float(g[j]), eg + bx),
+                                        ldexpf(__uint_as_float(u[j]), eu + bx));
+              p.h32[row * p.ldh + mrow] = hv;
+              // the row's largest |h| over this warp's 32 rows of W, then over the grid
+              const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(hv)));
+              if (lane == 0) atomicMax(&p.hmax[row], m);
+            } else {
+              const float hv = silu_mul(__uint_as_float(g[j]), __uint_as_float(u[j]));
+              p.h[row * p.ldh + mrow] = __float2half_rn(hv);
+            }
           }
         }
       }
@@ -704,6 +868,11 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
         if (warp == S::kCtl + S::kDq && lane == 0) PF_STAMP(tc, 4, global_timer_ns());
         const int mrow = ti.m0 + q * 32 + lane;
         const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * kTN);
+        int ed = 0;                               // E4M3: the down row's exponent
+        if constexpr (F8) {
+          const bool sh = ti.bucket >= p.E;
+          ed = (sh ? p.se0 : p.e0)[(sh ? 0 : (size_t)ti.bucket * p.M) + mrow];
+        }
         for (int col = 0; col < kTN; col += 32) {
           if (col >= ti.nvalid) break;            // warp-uniform
           uint32_t g[32];
@@ -711,8 +880,12 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (col + j < ti.nvalid)
-              p.o[(size_t)(ti.row0 + ti.n0 + col + j) * p.ldo + mrow] = __uint_as_float(g[j]);
+            if (col + j < ti.nvalid) {
+              const size_t row = (size_t)(ti.row0 + ti.n0 + col + j);
+              float v = __uint_as_float(g[j]);
+              if constexpr (F8) v = ldexpf(v, ed + p.bexp[row]);
+              p.o[row * p.ldo + mrow] = v;
+            }
         }
         tc_fence_before();
         __syncwarp();
@@ -772,6 +945,65 @@ __global__ void pf_combine_kernel(const float* __restrict__ o, const int32_t* __
 }
 
 // ---------------------------------------------------------------------------
+// E4M3 weight scales: each row's exponent, the largest floor(log2 d) of its
+// blocks' fp16 scales (-14 for a subnormal or zero d), one warp per row.
+struct RowExpJob {
+  const uint8_t* mat;
+  int64_t rows;
+  int K;
+  int8_t* out;
+};
+struct RowExpJobs {
+  RowExpJob j[6];
+  int n;
+};
+__global__ void pf8_row_exp_kernel(const __grid_constant__ RowExpJobs jobs) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int q = 0; q < jobs.n; ++q) {
+    const RowExpJob& J = jobs.j[q];
+    const int nb = J.K / 32;
+    for (int64_t r = gw; r < J.rows; r += nw) {
+      const uint8_t* row = J.mat + r * nb * kBlockB;
+      int e = -1000;
+      for (int b = lane; b < nb; b += 32) {
+        const uint16_t d = (uint16_t)(row[(size_t)b * kBlockB] | (row[(size_t)b * kBlockB + 1] << 8));
+        const int f = (d >> 10) & 0x1F;
+        const int eb = f == 0 ? -14 : f - 15;
+        e = eb > e ? eb : e;
+      }
+      e = __reduce_max_sync(0xFFFFFFFFu, (unsigned)(e + 1024)) - 1024;
+      if (lane == 0) J.out[r] = (int8_t)e;
+    }
+  }
+}
+
+// Each thread: one block of a row, through dequant_block_e4m3 with the row's
+// exponent (written by pf8_row_exp_kernel first).
+__global__ void pf8_dequant_kernel(const uint8_t* __restrict__ mat, int64_t rows, int K,
+                                   const int8_t* __restrict__ row_exp, uint8_t* __restrict__ out) {
+  const int nb = K / 32;
+  const int64_t n = rows * nb;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / nb;
+    const uint8_t* b = mat + i * kBlockB;
+    const uint16_t d = (uint16_t)(b[0] | (b[1] << 8));
+    uint32_t q[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+      q[w] = (uint32_t)b[2 + 4 * w] | ((uint32_t)b[3 + 4 * w] << 8) |
+             ((uint32_t)b[4 + 4 * w] << 16) | ((uint32_t)b[5 + 4 * w] << 24);
+    uint32_t c[8];
+    dequant_block_e4m3(q, d, row_exp[r], c);
+    uint32_t* o = reinterpret_cast<uint32_t*>(out + i * 32);   // 32 codes, K order
+#pragma unroll
+    for (int w = 0; w < 8; ++w) o[w] = c[w];
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Host side.
 namespace {
 
@@ -799,6 +1031,22 @@ bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, i
   cuuint32_t box[2] = {(cuuint32_t)kTK, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// E4M3 codes [rows][cols] row-major (cols bytes a row), box 128 columns x
+// box_rows rows, 128-byte swizzle.
+bool make_tmap_u8(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols};
+  cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -839,16 +1087,16 @@ cudaError_t launch_ex(Kern kernel, dim3 grid, dim3 block, size_t smem, bool pdl,
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-template <bool GATEUP, bool RAW>
+template <bool GATEUP, bool RAW, bool F8 = false>
 cudaError_t launch_gemm(int num_sms, int E, bool pdl, cudaStream_t stream, const TmapSet& tm,
                         const GemmParams& g) {
   using S = GemmCfg<GATEUP, RAW>;
   const size_t sm = S::kTotal + (size_t)(E + 2) * 8;
   const cudaError_t e =
-      ensure_smem_attr(reinterpret_cast<const void*>(pf_gemm_kernel<GATEUP, RAW>), sm);
+      ensure_smem_attr(reinterpret_cast<const void*>(pf_gemm_kernel<GATEUP, RAW, F8>), sm);
   if (e != cudaSuccess) return e;
-  return launch_ex(pf_gemm_kernel<GATEUP, RAW>, dim3(num_sms), dim3(S::kThreads), sm, pdl, stream,
-                   tm, g);
+  return launch_ex(pf_gemm_kernel<GATEUP, RAW, F8>, dim3(num_sms), dim3(S::kThreads), sm, pdl,
+                   stream, tm, g);
 }
 
 }  // namespace
@@ -887,8 +1135,8 @@ cudaError_t launch_prefill(const moe_shape& s, const moe_expert_weights& w, cons
   e = launch_ex(pf_bucket_kernel, dim3(1), dim3(kBucketThreads), bsm, pdl, stream, bp);
   if (e != cudaSuccess) return e;
   const CombineListParams cl{(const int32_t*)row_of, weights, T, k, s.n_shared, comb_row, comb_w};
-  e = launch_ex(pf_gather_kernel, dim3(num_sms * 4), dim3(256), 0, pdl, stream, x,
-                (const int32_t*)boff, (const int32_t*)row_tok, E, H, x16, cl);
+  e = launch_ex(pf_gather_kernel<false>, dim3(num_sms * 4), dim3(256), 0, pdl, stream, x,
+                (const int32_t*)boff, (const int32_t*)row_tok, E, H, x16, cl, Gather8{});
   if (e != cudaSuccess) return e;
 
   TmapSet tm_x, tm_h;
@@ -940,6 +1188,174 @@ cudaError_t launch_prefill(const moe_shape& s, const moe_expert_weights& w, cons
   g2.ldo = H;
   e = raw2 ? launch_gemm<false, true>(num_sms, E, pdl, stream, tm_h, g2)
            : launch_gemm<false, false>(num_sms, E, pdl, stream, tm_h, g2);
+  if (e != cudaSuccess) return e;
+
+  const int64_t total = (int64_t)T * (H / 4);
+  int64_t grid = (total + 255) / 256;
+  if (grid > (int64_t)num_sms * 8) grid = (int64_t)num_sms * 8;
+  return launch_ex(pf_combine_kernel, dim3((unsigned)grid), dim3(256), 0, pdl, stream,
+                   (const float*)o, (const int32_t*)comb_row, (const float*)comb_w, T, k + 1, H,
+                   y);
+}
+
+// ---------------------------------------------------------------------------
+// The prefill with E4M3 operands: the same bucketing, tiles and combine; the
+// weights' row scales come from a table made once for the weights
+// (launch_fp8_row_exponents).
+bool prefill_fp8_supported(const moe_shape& s) {
+  // the raw-row ring (reduction lengths multiples of 256) feeds the E4M3 producers
+  return prefill_supported(s) && s.hidden % 256 == 0 && s.ffn % 256 == 0 &&
+         (!s.n_shared || s.ffn_shared % 256 == 0);
+}
+
+int64_t fp8_row_exponent_count(const moe_shape& s) {
+  const int64_t E = s.n_experts, H = s.hidden, F = s.ffn;
+  const int64_t Fs = s.n_shared ? s.ffn_shared : 0;
+  return E * F * 2 + E * H + (s.n_shared ? 2 * Fs + H : 0);
+}
+
+cudaError_t launch_fp8_row_exponents(const moe_shape& s, const moe_expert_weights& w,
+                                     int8_t* out, cudaStream_t stream) {
+  const int64_t E = s.n_experts, H = s.hidden, F = s.ffn;
+  const int64_t Fs = s.n_shared ? s.ffn_shared : 0;
+  RowExpJobs jobs{};
+  int64_t off = 0;
+  auto add = [&](const void* m, int64_t rows, int K) {
+    jobs.j[jobs.n++] = RowExpJob{reinterpret_cast<const uint8_t*>(m), rows, K, out + off};
+    off += rows;
+  };
+  add(w.gate, E * F, (int)H);
+  add(w.up, E * F, (int)H);
+  add(w.down, E * H, (int)F);
+  if (s.n_shared) {
+    add(w.sh_gate, Fs, (int)H);
+    add(w.sh_up, Fs, (int)H);
+    add(w.sh_down, H, (int)Fs);
+  }
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  pf8_row_exp_kernel<<<sms * 8, 256, 0, stream>>>(jobs);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_e4m3(const void* mat, int64_t rows, int K, int8_t* row_exp,
+                                uint8_t* out, int num_sms, cudaStream_t stream) {
+  RowExpJobs jobs{};
+  jobs.j[0] = RowExpJob{reinterpret_cast<const uint8_t*>(mat), rows, K, row_exp};
+  jobs.n = 1;
+  pf8_row_exp_kernel<<<num_sms * 8, 256, 0, stream>>>(jobs);
+  int64_t grid = (rows * (K / 32) + 255) / 256;
+  if (grid > (int64_t)num_sms * 16) grid = (int64_t)num_sms * 16;
+  pf8_dequant_kernel<<<(unsigned)grid, 256, 0, stream>>>(reinterpret_cast<const uint8_t*>(mat),
+                                                        rows, K, row_exp, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_fp8(const moe_shape& s, const moe_expert_weights& w,
+                               const int8_t* row_exp, const uint16_t* x, int T,
+                               const int32_t* ids, const float* weights, float* y, uint8_t* ws,
+                               const PrefillLayout& L, uint32_t* status, int num_sms, bool pdl,
+                               cudaStream_t stream) {
+  if (!prefill_fp8_supported(s)) return cudaErrorNotSupported;
+  const int E = s.n_experts, k = s.top_k, H = s.hidden, F = s.ffn;
+  const int Fs = s.n_shared ? s.ffn_shared : 0;
+  const int fmax = F > Fs ? F : Fs;
+  const int64_t rows = (int64_t)T * k + (s.n_shared ? T : 0);
+  int32_t* boff = reinterpret_cast<int32_t*>(ws + L.counts);
+  int32_t* row_of = reinterpret_cast<int32_t*>(ws + L.offsets);
+  int32_t* row_tok = reinterpret_cast<int32_t*>(ws + L.perm);
+  int32_t* comb_row = reinterpret_cast<int32_t*>(ws + L.comb);
+  float* comb_w = reinterpret_cast<float*>(ws + L.comb + (int64_t)T * (k + 1) * 4);
+  float* o = reinterpret_cast<float*>(ws + L.o);
+  uint8_t* x8 = ws + L.x8;
+  uint8_t* h8 = ws + L.h8;
+  float* h32 = reinterpret_cast<float*>(ws + L.h32);
+  int32_t* xexp = reinterpret_cast<int32_t*>(ws + L.xexp);
+  int32_t* bexp = reinterpret_cast<int32_t*>(ws + L.bexp);
+  int32_t* hexp = reinterpret_cast<int32_t*>(ws + L.hexp);
+  uint32_t* hmax = reinterpret_cast<uint32_t*>(ws + L.hmax);
+  const int64_t EF = (int64_t)E * F, EH = (int64_t)E * H;
+  const int8_t* ex_gate = row_exp;
+  const int8_t* ex_up = row_exp + EF;
+  const int8_t* ex_down = row_exp + 2 * EF;
+  const int8_t* ex_sg = row_exp + 2 * EF + EH;
+  const int8_t* ex_su = ex_sg + Fs;
+  const int8_t* ex_sd = ex_su + Fs;
+
+  BucketParams bp{ids, T, k, E, s.n_shared, boff, row_of, row_tok, status};
+  const size_t bsm = (size_t)kBucketWarps * E * 4;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(pf_bucket_kernel), bsm);
+  if (e != cudaSuccess) return e;
+  e = launch_ex(pf_bucket_kernel, dim3(1), dim3(kBucketThreads), bsm, pdl, stream, bp);
+  if (e != cudaSuccess) return e;
+  e = launch_ex(pf8_xexp_kernel, dim3(num_sms), dim3(256), 0, pdl, stream, x, T, H, xexp);
+  if (e != cudaSuccess) return e;
+  const CombineListParams cl{(const int32_t*)row_of, weights, T, k, s.n_shared, comb_row, comb_w};
+  const Gather8 g8{(const int32_t*)xexp, bexp, hmax, x8};
+  e = launch_ex(pf_gather_kernel<true>, dim3(num_sms * 4), dim3(256), 0, pdl, stream, x,
+                (const int32_t*)boff, (const int32_t*)row_tok, E, H, (__half*)nullptr, cl, g8);
+  if (e != cudaSuccess) return e;
+
+  TmapSet tm_x, tm_h;
+  for (int b = 0; b < kNumBoxes; ++b)
+    if (!make_tmap_u8(&tm_x.m[b], x8, rows, H, 32 << b) ||
+        !make_tmap_u8(&tm_h.m[b], h8, rows, fmax, 32 << b))
+      return cudaErrorInvalidValue;
+  if (!make_raw_tmap(&tm_x.raw[0], w.gate, (int64_t)E * F, H) ||
+      !make_raw_tmap(&tm_x.raw[1], w.up, (int64_t)E * F, H) ||
+      (s.n_shared && (!make_raw_tmap(&tm_x.raw[2], w.sh_gate, Fs, H) ||
+                      !make_raw_tmap(&tm_x.raw[3], w.sh_up, Fs, H))) ||
+      !make_raw_tmap(&tm_h.raw[0], w.down, (int64_t)E * H, F) ||
+      (s.n_shared && !make_raw_tmap(&tm_h.raw[2], w.sh_down, H, Fs)))
+    return cudaErrorInvalidValue;
+  GemmParams g1{};
+  g1.E = E;
+  g1.n_shared = s.n_shared;
+  g1.M = F;
+  g1.Ms = Fs;
+  g1.K = H;
+  g1.Ks = H;
+  g1.a0 = reinterpret_cast<const uint8_t*>(w.gate);
+  g1.a1 = reinterpret_cast<const uint8_t*>(w.up);
+  g1.s0 = reinterpret_cast<const uint8_t*>(w.sh_gate);
+  g1.s1 = reinterpret_cast<const uint8_t*>(w.sh_up);
+  g1.bucket_off = boff;
+  g1.ldh = fmax;
+  g1.status = status;
+  g1.e0 = ex_gate;
+  g1.e1 = ex_up;
+  g1.se0 = ex_sg;
+  g1.se1 = ex_su;
+  g1.bexp = bexp;
+  g1.h32 = h32;
+  g1.hmax = hmax;
+  e = launch_gemm<true, true, true>(num_sms, E, pdl, stream, tm_x, g1);
+  if (e != cudaSuccess) return e;
+  e = launch_ex(pf8_hconv_kernel, dim3(num_sms * 4), dim3(256), 0, pdl, stream,
+                (const float*)h32, (const uint32_t*)hmax, (const int32_t*)boff, E, fmax, F, Fs,
+                h8, hexp);
+  if (e != cudaSuccess) return e;
+
+  GemmParams g2 = g1;
+  g2.M = H;
+  g2.Ms = H;
+  g2.K = F;
+  g2.Ks = Fs;
+  g2.a0 = reinterpret_cast<const uint8_t*>(w.down);
+  g2.a1 = nullptr;
+  g2.s0 = reinterpret_cast<const uint8_t*>(w.sh_down);
+  g2.s1 = nullptr;
+  g2.e0 = ex_down;
+  g2.e1 = nullptr;
+  g2.se0 = ex_sd;
+  g2.se1 = nullptr;
+  g2.bexp = hexp;
+  g2.h32 = nullptr;
+  g2.hmax = nullptr;
+  g2.o = o;
+  g2.ldo = H;
+  e = launch_gemm<false, true, true>(num_sms, E, pdl, stream, tm_h, g2);
   if (e != cudaSuccess) return e;
 
   const int64_t total = (int64_t)T * (H / 4);

@@ -37,6 +37,17 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint
       : "memory");
 }
 
+// The same with E4M3 A and B (kind::f8f6f4; the instruction descriptor's A and
+// B format fields hold 0, E4M3, as for fp16 above).
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -151,6 +162,74 @@ __device__ __forceinline__ void dequant_block_half(const uint32_t (&q)[4], uint1
   for (int i = 0; i < 4; ++i) offsets_to_half4(lo[i], d2, w[2 * i], w[2 * i + 1]);     // 0..15
 #pragma unroll
   for (int i = 0; i < 4; ++i) offsets_to_half4(hi[i], d2, w[8 + 2 * i], w[8 + 2 * i + 1]);  // 16..31
+}
+
+// ---------------------------------------------------------------------------
+// E4M3 (OCP 8-bit float: bias 7, largest finite 448, no infinities) operands.
+
+// Two fp32 values to two E4M3 codes, round to nearest even, finite overflow
+// saturated to +-448: the first operand goes to the upper byte.
+__device__ __forceinline__ uint16_t cvt_e4m3x2(float hi, float lo) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// 2^e as an fp32 (e in [-126, 127]).
+__device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+
+// The 16 E4M3 codes of one block's table, e4m3(d T[i] 2^-E) for the block's
+// fp16 scale d and its row's exponent E: byte i of t[j] is code 4j + i. d T is
+// exact in fp32 (11 by 7 significant bits) and the power of two is exact, so
+// each code is the round-to-nearest-even of the exact scaled weight.
+__device__ __forceinline__ void e4m3_block_table(uint16_t dbits, int E, uint32_t (&t)[4]) {
+  const float ds = __half2float(__ushort_as_half(dbits)) * exp2i(-E);
+  const float T0 = -127.f, T1 = -104.f, T2 = -83.f, T3 = -65.f, T4 = -49.f, T5 = -35.f,
+              T6 = -22.f, T7 = -10.f, T8 = 1.f, T9 = 13.f, T10 = 25.f, T11 = 38.f, T12 = 53.f,
+              T13 = 69.f, T14 = 89.f, T15 = 113.f;
+  auto pack = [&](float a, float b, float c, float d) {
+    return (uint32_t)cvt_e4m3x2(b * ds, a * ds) | ((uint32_t)cvt_e4m3x2(d * ds, c * ds) << 16);
+  };
+  t[0] = pack(T0, T1, T2, T3);
+  t[1] = pack(T4, T5, T6, T7);
+  t[2] = pack(T8, T9, T10, T11);
+  t[3] = pack(T12, T13, T14, T15);
+}
+
+// Eight codes (one index word) through a 16-byte table t (as above) to the 8
+// table bytes in K order: lo = bytes of the low nibbles of index bytes 0..3,
+// hi = of the high nibbles (the lookup of iq4_lookup8_split, on a table held
+// in registers).
+__device__ __forceinline__ void lookup16_split(uint32_t q, const uint32_t (&t)[4], uint32_t& lo,
+                                               uint32_t& hi) {
+  const uint32_t qm = q & 0x77777777u;
+  const uint32_t sel = 0x32103210u | ((q >> 1) & 0x44444444u);
+  const uint32_t r0 = prmt(prmt(t[0], t[1], qm), prmt(t[2], t[3], qm), sel);
+  const uint32_t qm1 = qm >> 16;
+  const uint32_t r1 = prmt(prmt(t[0], t[1], qm1), prmt(t[2], t[3], qm1), sel >> 16);
+  lo = prmt(r0, r1, 0x6420u);
+  hi = prmt(r0, r1, 0x7531u);
+}
+
+// One 32-weight block (its 4 index words, fp16 scale bits) of a row with
+// exponent E to its 32 E4M3 codes in K order: words 0..3 hold weights 0..15,
+// words 4..7 weights 16..31. The fp8 prefill producers call this for every
+// block they put into an A tile.
+__device__ __forceinline__ void dequant_block_e4m3(const uint32_t (&q)[4], uint16_t dbits, int E,
+                                                   uint32_t (&w)[8]) {
+  uint32_t t[4];
+  e4m3_block_table(dbits, E, t);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) lookup16_split(q[i], t, w[i], w[4 + i]);
+}
+
+// floor(log2 |v|) - 6 from an fp32 bit pattern of |v| (0 for zero), the
+// exponent that puts a vector's largest magnitude in [64, 128).
+__device__ __forceinline__ int vec_exponent_bits(uint32_t mbits) {
+  if (mbits == 0u) return 0;
+  const int f = (int)(mbits >> 23);
+  if (f == 0) return (31 - __clz(mbits)) - 149 - 6;    // subnormal: value = m 2^-149
+  return (f - 127) - 6;
 }
 
 }  // namespace moe

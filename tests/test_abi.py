@@ -63,6 +63,19 @@ def test_workspace_bytes_rules(lib):
     assert moe.workspace_bytes(odd, 1, moe.DECODE) == 0
     # 256-byte aligned regions: size is a multiple of 256
     assert moe.workspace_bytes(s, 3, moe.DECODE) % 256 == 0
+    # the 8-bit prefill keeps the fp16 layout's regions and adds its own
+    assert moe.workspace_bytes(s, 2048, moe.PREFILL_FP8) > moe.workspace_bytes(s, 2048, moe.PREFILL)
+    assert moe.workspace_bytes(s, 16385, moe.PREFILL_FP8) == 0
+
+
+def test_fp8_row_exponent_count(lib):
+    import quantized_routed_expert_gb300 as moe
+    s = moe.make_shape(3584, 1024, 64, 4)
+    n = lib.moe_fp8_row_exponent_count
+    n.restype = ctypes.c_int64
+    assert n(ctypes.byref(s)) == 2 * 64 * 1024 + 64 * 3584 + 2 * 1024 + 3584
+    bad = moe.make_shape(3584, 1024, 64, 65)
+    assert n(ctypes.byref(bad)) == 0
 
 
 def test_pdl_switch_round_trips(lib):
