@@ -60,6 +60,8 @@ def parse():
     ap.add_argument("--impl", default="libmoe", choices=["libmoe", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--fp8", action="store_true",
+                    help="prefill workload: E4M3 operands (moe_iq4nl_prefill_grouped_fp8)")
     ap.add_argument("--layers", type=int, default=None,
                     help="run only the first N layers (small profiling cases)")
     ap.add_argument("--experts", type=int, default=None,
@@ -68,7 +70,7 @@ def parse():
     a = ap.parse_args()
     # the other configurations are measured only on a default (headline) run
     a.workloads = a.workloads and a.config is None and a.layers is None and a.experts is None \
-        and a.tokens is None and not a.same_tokens
+        and a.tokens is None and not a.same_tokens and not a.fp8
     if a.config is None:
         a.config = 1
     return a
@@ -239,8 +241,10 @@ class OracleRun:
     so that generation stays outside the timed calls and repeated passes."""
 
     def __init__(self, cfg: int, T: int, layers=None, max_tokens: int = 16, threads=None,
-                 cache_bytes: float = 3e9, experts=None):
+                 cache_bytes: float = 3e9, experts=None, fp8: bool = False):
+        import oracle
         import synth
+        self.mode = oracle.MMA8 if fp8 else oracle.EXACT
         self.s, _ = workload(cfg, None, layers, experts)
         self.seed = synth.seed_of(cfg)
         self.T_full = T
@@ -282,7 +286,7 @@ class OracleRun:
             experts = {int(e): self._expert(l, int(e)) for e in np.unique(ids)}
             t0 = time.perf_counter()
             oracle.moe_layer(s.H, s.F, s.Fs, s.E, s.k, s.n_shared, experts, self.shared[l], x,
-                             ids, w, mode=oracle.EXACT, threads=self.threads)
+                             ids, w, mode=self.mode, threads=self.threads)
             spent += time.perf_counter() - t0
             done += 1
             if spent > budget_s:
@@ -290,17 +294,20 @@ class OracleRun:
         return self.T * done / s.L / spent, spent, done
 
     def describe(self, passes: int, layers: int, spent: float) -> str:
+        import oracle
+        kind = "E4M3-operand (mma8) fp64 oracle" if self.mode == oracle.MMA8 else \
+            "exact fp64 oracle"
         return (f"{self.T} of {self.T_full} token(s) of the workload, {passes} pass(es) over "
                 f"input sets, {layers} layer calls in all (a full pass is {self.s.L}; route + "
-                f"layer, exact fp64 oracle), {spent:.1f} s of oracle time; tokens/s scaled to "
+                f"layer, {kind}), {spent:.1f} s of oracle time; tokens/s scaled to "
                 f"the full {self.s.L}-layer stack")
 
 
 def oracle_baseline(cfg: int, T: int, layers=None, budget_s: float = 10.0,
-                    wall_s: float = 120.0, experts=None):
+                    wall_s: float = 120.0, experts=None, fp8: bool = False):
     """cpu_baseline: passes over the input sets until about budget_s seconds of
     oracle time (or wall_s of wall time, weight generation included)."""
-    run = OracleRun(cfg, T, layers, experts=experts)
+    run = OracleRun(cfg, T, layers, experts=experts, fp8=fp8)
     t_wall = time.perf_counter()
     toks, spent, passes, calls = 0.0, 0.0, 0, 0
     while spent < budget_s and time.perf_counter() - t_wall < wall_s:
@@ -320,7 +327,8 @@ def run_reference(args):
     if rank != 0:
         return 0
     s, T = workload(args.config, args.tokens, args.layers, args.experts)
-    run = OracleRun(args.config, T, args.layers, experts=args.experts)
+    fp8 = getattr(args, "fp8", False) and args.config == 4
+    run = OracleRun(args.config, T, args.layers, experts=args.experts, fp8=fp8)
     per = []
     for i in range(args.warmup + args.steps):
         tps, dt, done = run.one_pass(i % N_SETS, budget_s=3.0)
@@ -336,7 +344,8 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded; shapes of the pages' models)",
         "config": {"workload": s.name, "tokens_per_step": T, "layers": s.L,
-                   "sample_tokens": run.T, "input_sets": N_SETS},
+                   "sample_tokens": run.T, "input_sets": N_SETS,
+                   **({"operands": "e4m3"} if fp8 else {})},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": run.cores, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -384,6 +393,7 @@ OTHER_WORKLOADS = (
     {"config": 3, "tokens": 4, "step": "routed", "steps": 10, "warmup": 3},
     {"config": 3, "tokens": 16, "step": "routed", "steps": 10, "warmup": 3},
     {"config": 4, "tokens": None, "step": "routed", "steps": 10, "warmup": 3},
+    {"config": 4, "tokens": None, "step": "routed", "steps": 10, "warmup": 3, "fp8": True},
 )
 
 
@@ -397,6 +407,7 @@ def other_workloads(args, ctx):
         a.steps, a.warmup = w["steps"], w["warmup"]
         a.no_e2e, a.no_cpu_baseline = True, True
         a.same_tokens = bool(w.get("same_tokens", False))
+        a.fp8 = bool(w.get("fp8", False))
         a.layers, a.experts = None, None
         r = measure(a, ctx)
         torch.cuda.empty_cache()
@@ -404,6 +415,7 @@ def other_workloads(args, ctx):
         out.append({"workload": r["config"]["workload"], "tokens_per_step": r["config"]["tokens_per_step"],
                     "same_tokens": a.same_tokens,
                     "layers": r["config"]["layers"], "step_call": r["step_call"],
+                    "dtype": r["dtype"],
                     "steps": a.steps, "warmup": a.warmup,
                     "ms_per_step": r["ms_per_step"], "step_ms": r["step_ms"],
                     "value": r["value"], "unit": UNIT,
@@ -433,6 +445,7 @@ def measure(args, ctx):
     s, T = workload(args.config, args.tokens, args.layers, args.experts)
     seed = synth.seed_of(args.config)
     prefill = args.config == 4
+    fp8 = prefill and getattr(args, "fp8", False)
     shape = moe.make_shape(s.H, s.F, s.E, s.k, s.Fs, s.n_shared)
     layers = [Layer(s, seed, l, device=dev) for l in range(s.L)]
     wts = [moe.ExpertWeights(L.gate, L.up, L.down, L.sh_gate, L.sh_up, L.sh_down)
@@ -443,10 +456,17 @@ def measure(args, ctx):
     ids = torch.zeros((s.L, T, s.k), dtype=torch.int32, device=dev)
     w = torch.zeros((s.L, T, s.k), dtype=torch.float32, device=dev)
     y = torch.zeros((s.L, T, s.H), dtype=torch.float32, device=dev)
-    mode = moe.PREFILL if prefill else moe.DECODE
+    mode = (moe.PREFILL_FP8 if fp8 else moe.PREFILL) if prefill else moe.DECODE
     ws = moe.workspace(shape, T, mode, dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     layer_fn = moe.iq4nl_prefill_grouped if prefill else moe.iq4nl_decode
+    if fp8:
+        # each layer's row-exponent table, made once with the weights (not timed)
+        rexp = {id(wts[l]): moe.fp8_row_exponents(shape, wts[l]) for l in range(s.L)}
+
+        def layer_fn(shape_, w_, x_, ids_, wt_, ws_, y=None, status=None):
+            return moe.iq4nl_prefill_grouped_fp8(shape_, w_, rexp[id(w_)], x_, ids_, wt_, ws_,
+                                                 y=y, status=status)
 
     multi = (not prefill) and args.step in ("layers", "chained")
     chained = args.step == "chained"
@@ -467,7 +487,8 @@ def measure(args, ctx):
 
     if prefill:
         launches_per_layer = (moe.launches_per_call(shape, T, moe.CALL_ROUTE) +
-                              moe.launches_per_call(shape, T, moe.CALL_PREFILL))
+                              moe.launches_per_call(shape, T, moe.CALL_PREFILL_FP8 if fp8
+                                                    else moe.CALL_PREFILL))
     elif multi:
         launches_per_layer = moe.launches_per_call(
             shape, T, moe.call_decode_layers(s.L, chained)) / s.L
@@ -618,7 +639,8 @@ def measure(args, ctx):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tps, cores, desc = oracle_baseline(args.config, T, args.layers, experts=args.experts)
+        tps, cores, desc = oracle_baseline(args.config, T, args.layers, experts=args.experts,
+                                           fp8=fp8)
         cpu = {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
 
     # the dominant kernel: for the fused decode every launch of the step is the
@@ -641,13 +663,21 @@ def measure(args, ctx):
         achieved = unit_bytes / (launch_ms * 1e-3) / 1e9
         prof = profiled_traffic(PROFILE_DECODE_FUSED, T)
     else:
-        kernel = ("moe_iq4nl_prefill_grouped (bucket, gather, tcgen05 gate/up and down GEMMs, "
+        kernel = ("moe_iq4nl_prefill_grouped_fp8 (bucket, token exponents, E4M3 gather, "
+                  "tcgen05 kind::f8f6f4 gate/up GEMM, h to E4M3, down GEMM, combine), per call"
+                  if fp8 else
+                  "moe_iq4nl_prefill_grouped (bucket, gather, tcgen05 gate/up and down GEMMs, "
                   "combine), per call" if prefill else
                   "moe_iq4nl_decode (the layer without routing), per call")
         launch_ms = layer_ms
         unit_bytes = layer_bytes
         prof = None
     traffic = prof["dram_bytes_per_launch"] if prof else None
+    # the 8-bit contraction's peak: the measured bf16 rate x the nominal fp8/bf16
+    # ratio (4.5 / 2.25 PFLOP/s dense)
+    tc_peak = 2.0 * bf16 if fp8 else bf16
+    tc_kind = (peak_kind + " (cuBLAS bf16 dense x 2, the nominal E4M3/bf16 ratio)" if fp8 else
+               peak_kind + " (cuBLAS bf16 dense; kind::f16 fp16 has the same rate)")
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -655,7 +685,9 @@ def measure(args, ctx):
             "step_ms": step_stats,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": ("iq4_nl weights x int16 activations, exact int dot, f32 accumulate"
-                      if not prefill else "fp16 x fp16 -> f32 (tcgen05 kind::f16)"),
+                      if not prefill else
+                      "e4m3 x e4m3 -> f32 (tcgen05 kind::f8f6f4)" if fp8 else
+                      "fp16 x fp16 -> f32 (tcgen05 kind::f16)"),
             "data": "synthetic (seeded; shapes of the pages' models)",
             "config": {"workload": s.name, "tokens_per_step": T, "layers": s.L,
                        "input_sets": N_SETS, "graph": "one CUDA graph per step, PDL between "
@@ -663,7 +695,8 @@ def measure(args, ctx):
                        "l2": f"inputs larger than L2: {bytes_per_step / 1e9:.3f} GB of distinct "
                              "expert bytes per step vs 129 MB L2",
                        "parallelism": f"replicas x{world}",
-                       **({"same_tokens": True} if args.same_tokens else {})},
+                       **({"same_tokens": True} if args.same_tokens else {}),
+                       **({"operands": "e4m3"} if fp8 else {})},
             "hbm_gbs": step_gbs, "hbm_frac_of_measured": step_gbs / hbm,
             "bytes_per_step": bytes_per_step,
             "roofline": ({"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
@@ -672,14 +705,13 @@ def measure(args, ctx):
                           "algorithmic_bytes_per_launch": unit_bytes,
                           "traffic_source": prof["source"] if prof else None}
                          if not prefill else
-                         {"bound": "tensor", "achieved": tflops, "peak": bf16, "unit": "TFLOP/s",
-                          "frac": tflops / bf16, "traffic": traffic,
-                          "kernel": kernel,
-                          "peak_kind": peak_kind + " (cuBLAS bf16 dense; kind::f16 fp16 has the "
-                                       "same rate)",
+                         {"bound": "tensor", "achieved": tflops, "peak": tc_peak,
+                          "unit": "TFLOP/s", "frac": tflops / tc_peak, "traffic": traffic,
+                          "kernel": kernel, "peak_kind": tc_kind,
                           "avg_call_ms": layer_ms, "algorithmic_flops_per_call": flops_layer}),
             "layer_call_ms": layer_call_ms, "route_call_ms": route_ms,
-            "step_call": "moe_iq4nl_prefill_grouped after moe_route_topk" if prefill else
+            "step_call": ("moe_iq4nl_prefill_grouped_fp8 after moe_route_topk" if fp8 else
+                          "moe_iq4nl_prefill_grouped after moe_route_topk") if prefill else
                          (f"moe_iq4nl_decode_layers ({'chained' if chained else 'own inputs'},"
                           " all layers in one call)" if multi else
                           "moe_iq4nl_decode_routed (route + layer in one call)"),

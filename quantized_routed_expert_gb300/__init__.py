@@ -135,6 +135,7 @@ def status_string(status: int) -> str:
 
 
 CALL_ROUTE, CALL_DECODE, CALL_DECODE_ROUTED, CALL_PREFILL = 0, 1, 2, 3
+CALL_PREFILL_FP8 = 5
 MAX_LAYERS = 128
 
 

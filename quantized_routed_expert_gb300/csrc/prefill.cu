@@ -285,6 +285,7 @@ __global__ void pf_gather_kernel(const uint16_t* __restrict__ x, const int32_t* 
     for (int r = gw; r < rows; r += nw) {
       const int t = row_tok[r];
       const int X = g8.xexp_tok[t];
+      const float sx = pow2_of(-X);
       if (lane == 0) {
         g8.bexp[r] = X;
         g8.hmax[r] = 0u;
@@ -297,8 +298,8 @@ __global__ void pf_gather_kernel(const uint16_t* __restrict__ x, const int32_t* 
         uint32_t pk[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)      // values 2i (low half) and 2i + 1 (high half)
-          pk[i] = cvt_e4m3x2(ldexpf(__uint_as_float(in[i] & 0xFFFF0000u), -X),
-                             ldexpf(__uint_as_float(in[i] << 16), -X));
+          pk[i] = cvt_e4m3x2(pow2_scale(__uint_as_float(in[i] & 0xFFFF0000u), -X, sx),
+                             pow2_scale(__uint_as_float(in[i] << 16), -X, sx));
         dst[c] = make_uint2(pk[0] | (pk[1] << 16), pk[2] | (pk[3] << 16));
       }
     }
@@ -362,16 +363,17 @@ __global__ void pf8_hconv_kernel(const float* __restrict__ h32, const uint32_t* 
   const int nw = (gridDim.x * blockDim.x) >> 5;
   for (int r = gw; r < rows; r += nw) {
     const int X = vec_exponent_bits(hmax[r]);
+    const float sx = pow2_of(-X);
     if (lane == 0) hexp[r] = X;
     const int K = r < n_valid ? F : Fs;
     const float4* src = reinterpret_cast<const float4*>(h32 + (size_t)r * ld);
     uint2* dst = reinterpret_cast<uint2*>(h8 + (size_t)r * ld);
     for (int c = lane; c < K / 8; c += 32) {
       const float4 a = src[2 * c], b = src[2 * c + 1];
-      const uint32_t p0 = cvt_e4m3x2(ldexpf(a.y, -X), ldexpf(a.x, -X));
-      const uint32_t p1 = cvt_e4m3x2(ldexpf(a.w, -X), ldexpf(a.z, -X));
-      const uint32_t p2 = cvt_e4m3x2(ldexpf(b.y, -X), ldexpf(b.x, -X));
-      const uint32_t p3 = cvt_e4m3x2(ldexpf(b.w, -X), ldexpf(b.z, -X));
+      const uint32_t p0 = cvt_e4m3x2(pow2_scale(a.y, -X, sx), pow2_scale(a.x, -X, sx));
+      const uint32_t p1 = cvt_e4m3x2(pow2_scale(a.w, -X, sx), pow2_scale(a.z, -X, sx));
+      const uint32_t p2 = cvt_e4m3x2(pow2_scale(b.y, -X, sx), pow2_scale(b.x, -X, sx));
+      const uint32_t p3 = cvt_e4m3x2(pow2_scale(b.w, -X, sx), pow2_scale(b.z, -X, sx));
       dst[c] = make_uint2(p0 | (p1 << 16), p2 | (p3 << 16));
     }
   }
@@ -461,6 +463,14 @@ __device__ __forceinline__ void dequant_block_to_tile(const uint32_t (&q)[4], ui
 struct TileInfo {
   int bucket, m0, n0, nvalid, row0;
 };
+
+// silu(g) u in the GEMM epilogues, on the hardware exp2 and reciprocal (a few
+// fp32 ulps): h is rounded to fp16 or E4M3 right after, far coarser. For g
+// below about -87, 1 + e^-g exceeds 2^126 and the quotient is a signed zero,
+// where the exact value is below 1e-36 in magnitude.
+__device__ __forceinline__ float silu_mul_fast(float g, float u) {
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
 
 // Token tiles are loaded with the smallest of four box heights that covers
 // the tile's tokens, and the MMA runs with N = tokens rounded up to 16: with
@@ -808,42 +818,80 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
       if (warp == S::kCtl && lane == 0) PF_STAMP(tc, 3, global_timer_ns());
       if constexpr (S::kEpi == 0) {
       // epilogue: TMEM lanes of this warp's quarter, a share of the token columns
-      if (!mbar_wait(acc_full, tc & 1, p.status)) { ok = false; break; }
-      tc_fence_after();
-      if (warp == S::kCtl && lane == 0) PF_STAMP(tc, 4, global_timer_ns());
       const int q = warp & 3;
       constexpr int kCols = kTN / (S::kDq / 4);
       const int ch = dw >> 2;                   // column share
       const int mrow = ti.m0 + q * 32 + lane;   // weight row of this thread
-      int eg = 0, eu = 0;                       // E4M3: the gate and up rows' exponents
+      // E4M3: 2^(gate, up row exponents) and, in lane j, the exponent of the
+      // share's first column chunk, loaded before the accumulator wait
+      float sg = 1.f, su = 1.f;
+      int bx_next = 0;
       if constexpr (F8) {
         const size_t er = (sh ? 0 : (size_t)ti.bucket * p.M) + mrow;
-        eg = (sh ? p.se0 : p.e0)[er];
-        eu = (sh ? p.se1 : p.e1)[er];
+        sg = exp2i((sh ? p.se0 : p.e0)[er]);
+        su = exp2i((sh ? p.se1 : p.e1)[er]);
+        if (ch * kCols + lane < ti.nvalid) bx_next = p.bexp[ti.row0 + ti.n0 + ch * kCols + lane];
       }
+      if (!mbar_wait(acc_full, tc & 1, p.status)) { ok = false; break; }
+      tc_fence_after();
+      if (warp == S::kCtl && lane == 0) PF_STAMP(tc, 4, global_timer_ns());
       for (int c = 0; c < kCols; c += 32) {
         const int col = ch * kCols + c;
         if (col >= ti.nvalid) break;            // warp-uniform
         uint32_t g[32], u[32];
         tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + col, g);
         tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + kTN + col, u);
+        int bxl = bx_next;                      // E4M3: lane j: column col + j
+        if constexpr (F8) {
+          bx_next = 0;
+          if (c + 32 < kCols && col + 32 + lane < ti.nvalid)
+            bx_next = p.bexp[ti.row0 + ti.n0 + col + 32 + lane];
+        }
         tmem_ld_wait();
+        if constexpr (F8) {
+          // h = silu(g) u with g, u scaled back by 2^(row + column exponents);
+          // lane j keeps column j's largest |h| over the warp's 32 rows
+          const bool in = bxl >= -126 && bxl <= 127;
+          const float stl = pow2_of(bxl);
+          uint32_t mmax = 0;
+          if (__all_sync(0xFFFFFFFFu, in)) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (col + j < ti.nvalid) {
+                const size_t row = (size_t)(ti.row0 + ti.n0 + col + j);
+                const float st = __shfl_sync(0xFFFFFFFFu, stl, j);
+                const float hv = silu_mul_fast(__uint_as_float(g[j]) * sg * st,
+                                               __uint_as_float(u[j]) * su * st);
+                p.h32[row * p.ldh + mrow] = hv;
+                const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(hv)));
+                mmax = lane == j ? m : mmax;
+              }
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (col + j < ti.nvalid) {
+                const size_t row = (size_t)(ti.row0 + ti.n0 + col + j);
+                const int bx = __shfl_sync(0xFFFFFFFFu, bxl, j);
+                const float st = pow2_of(bx);
+                const float hv = silu_mul_fast(scale_acc(__uint_as_float(g[j]), sg, bx, st),
+                                               scale_acc(__uint_as_float(u[j]), su, bx, st));
+                p.h32[row * p.ldh + mrow] = hv;
+                const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(hv)));
+                mmax = lane == j ? m : mmax;
+              }
+            }
+          }
+          // then over the grid: one atomic per column, all lanes at once
+          if (col + lane < ti.nvalid) atomicMax(&p.hmax[ti.row0 + ti.n0 + col + lane], mmax);
+          continue;
+        }
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           if (col + j < ti.nvalid) {
             const size_t row = (size_t)(ti.row0 + ti.n0 + col + j);
-            if constexpr (F8) {
-              const int bx = p.bexp[row];
-              const float hv = silu_mul(ldexpf(__uint_as_float(g[j]), eg + bx),
-                                        ldexpf(__uint_as_float(u[j]), eu + bx));
-              p.h32[row * p.ldh + mrow] = hv;
-              // the row's largest |h| over this warp's 32 rows of W, then over the grid
-              const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(hv)));
-              if (lane == 0) atomicMax(&p.hmax[row], m);
-            } else {
-              const float hv = silu_mul(__uint_as_float(g[j]), __uint_as_float(u[j]));
-              p.h[row * p.ldh + mrow] = __float2half_rn(hv);
-            }
+            const float hv = silu_mul_fast(__uint_as_float(g[j]), __uint_as_float(u[j]));
+            p.h[row * p.ldh + mrow] = __float2half_rn(hv);
           }
         }
       }
@@ -863,16 +911,18 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
       for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tc) {
         const TileInfo ti = tile_info(t);
         const int ab = tc % S::kAcc;
+        const int mrow = ti.m0 + q * 32 + lane;
+        // E4M3: 2^(the down row's exponent), loaded before the accumulator
+        // wait; the columns' (h rows') exponents scale the combine weights
+        float sd = 1.f;
+        if constexpr (F8) {
+          const bool sh = ti.bucket >= p.E;
+          sd = exp2i((sh ? p.se0 : p.e0)[(sh ? 0 : (size_t)ti.bucket * p.M) + mrow]);
+        }
         if (!mbar_wait(&acc_full[ab], (tc / S::kAcc) & 1, p.status)) break;
         tc_fence_after();
         if (warp == S::kCtl + S::kDq && lane == 0) PF_STAMP(tc, 4, global_timer_ns());
-        const int mrow = ti.m0 + q * 32 + lane;
         const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * kTN);
-        int ed = 0;                               // E4M3: the down row's exponent
-        if constexpr (F8) {
-          const bool sh = ti.bucket >= p.E;
-          ed = (sh ? p.se0 : p.e0)[(sh ? 0 : (size_t)ti.bucket * p.M) + mrow];
-        }
         for (int col = 0; col < kTN; col += 32) {
           if (col >= ti.nvalid) break;            // warp-uniform
           uint32_t g[32];
@@ -882,9 +932,7 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
           for (int j = 0; j < 32; ++j)
             if (col + j < ti.nvalid) {
               const size_t row = (size_t)(ti.row0 + ti.n0 + col + j);
-              float v = __uint_as_float(g[j]);
-              if constexpr (F8) v = ldexpf(v, ed + p.bexp[row]);
-              p.o[row * p.ldo + mrow] = v;
+              p.o[row * p.ldo + mrow] = F8 ? __uint_as_float(g[j]) * sd : __uint_as_float(g[j]);
             }
         }
         tc_fence_before();
@@ -905,9 +953,13 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
 
 // ---------------------------------------------------------------------------
 // 4. Combine: y[t] = o[shared row] + sum over routed rows (experts ascending) w o.
+// F8: o holds the down outputs without their h row's factor 2^X (X = hexp of
+// the row); it enters through the weight, w 2^X, the same product whenever
+// w 2^X is a normal fp32 (each fp32 rounding commutes with the power of two).
+template <bool F8>
 __global__ void pf_combine_kernel(const float* __restrict__ o, const int32_t* __restrict__ comb_row,
                                   const float* __restrict__ comb_w, int T, int kk, int H,
-                                  float* __restrict__ y) {
+                                  float* __restrict__ y, const int32_t* __restrict__ hexp) {
   pdl_wait();
   pdl_trigger();
   const int h4 = H / 4;
@@ -932,7 +984,11 @@ __global__ void pf_combine_kernel(const float* __restrict__ o, const int32_t* __
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         if (r[u] < 0) break;
-        const float wv = cw[j0 + u];
+        float wv = cw[j0 + u];
+        if constexpr (F8) {
+          const int X = hexp[r[u]];
+          wv = X >= -126 ? wv * exp2i(X) : ldexpf(wv, X);
+        }
         acc.x = fmaf(wv, v[u].x, acc.x);
         acc.y = fmaf(wv, v[u].y, acc.y);
         acc.z = fmaf(wv, v[u].z, acc.z);
@@ -1193,9 +1249,9 @@ cudaError_t launch_prefill(const moe_shape& s, const moe_expert_weights& w, cons
   const int64_t total = (int64_t)T * (H / 4);
   int64_t grid = (total + 255) / 256;
   if (grid > (int64_t)num_sms * 8) grid = (int64_t)num_sms * 8;
-  return launch_ex(pf_combine_kernel, dim3((unsigned)grid), dim3(256), 0, pdl, stream,
+  return launch_ex(pf_combine_kernel<false>, dim3((unsigned)grid), dim3(256), 0, pdl, stream,
                    (const float*)o, (const int32_t*)comb_row, (const float*)comb_w, T, k + 1, H,
-                   y);
+                   y, (const int32_t*)nullptr);
 }
 
 // ---------------------------------------------------------------------------
@@ -1350,7 +1406,7 @@ cudaError_t launch_prefill_fp8(const moe_shape& s, const moe_expert_weights& w,
   g2.e1 = nullptr;
   g2.se0 = ex_sd;
   g2.se1 = nullptr;
-  g2.bexp = hexp;
+  g2.bexp = nullptr;                 // the h rows' exponents enter in the combine
   g2.h32 = nullptr;
   g2.hmax = nullptr;
   g2.o = o;
@@ -1361,9 +1417,9 @@ cudaError_t launch_prefill_fp8(const moe_shape& s, const moe_expert_weights& w,
   const int64_t total = (int64_t)T * (H / 4);
   int64_t grid = (total + 255) / 256;
   if (grid > (int64_t)num_sms * 8) grid = (int64_t)num_sms * 8;
-  return launch_ex(pf_combine_kernel, dim3((unsigned)grid), dim3(256), 0, pdl, stream,
+  return launch_ex(pf_combine_kernel<true>, dim3((unsigned)grid), dim3(256), 0, pdl, stream,
                    (const float*)o, (const int32_t*)comb_row, (const float*)comb_w, T, k + 1, H,
-                   y);
+                   y, (const int32_t*)hexp);
 }
 
 }  // namespace moe

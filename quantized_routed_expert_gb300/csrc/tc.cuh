@@ -178,6 +178,24 @@ __device__ __forceinline__ uint16_t cvt_e4m3x2(float hi, float lo) {
 // 2^e as an fp32 (e in [-126, 127]).
 __device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
 
+// v 2^a 2^b for an E4M3 accumulator v (zero, or of magnitude in [2^-18, 2^30]:
+// sums of products of E4M3 codes) and the exponents of its row (a, in
+// [-14, 15]) and token (b). v 2^a is exact and normal, so one rounding at most,
+// as in ldexpf(v, a + b), which serves when 2^b is not a normal fp32.
+// v 2^e, with s = 2^e precomputed when e is in [-126, 127] (then the product
+// is exact unless it falls below the normal range, where it rounds once, as
+// ldexpf does); ldexpf otherwise.
+__device__ __forceinline__ float pow2_scale(float v, int e, float s) {
+  return (e >= -126 && e <= 127) ? v * s : ldexpf(v, e);
+}
+__device__ __forceinline__ float pow2_of(int e) {
+  return exp2i(e < -126 ? -126 : (e > 127 ? 127 : e));
+}
+
+__device__ __forceinline__ float scale_acc(float v, float sa, int b, float sb) {
+  return (b >= -126 && b <= 127) ? (v * sa) * sb : ldexpf(v * sa, b);
+}
+
 // The 16 E4M3 codes of one block's table, e4m3(d T[i] 2^-E) for the block's
 // fp16 scale d and its row's exponent E: byte i of t[j] is code 4j + i. d T is
 // exact in fp32 (11 by 7 significant bits) and the power of two is exact, so
