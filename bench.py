@@ -663,8 +663,8 @@ def measure(args, ctx):
         achieved = unit_bytes / (launch_ms * 1e-3) / 1e9
         prof = profiled_traffic(PROFILE_DECODE_FUSED, T)
     else:
-        kernel = ("moe_iq4nl_prefill_grouped_fp8 (bucket, token exponents, E4M3 gather, "
-                  "tcgen05 kind::f8f6f4 gate/up GEMM, h to E4M3, down GEMM, combine), per call"
+        kernel = ("moe_iq4nl_prefill_grouped_fp8 (bucket, E4M3 gather, tcgen05 kind::f8f6f4 "
+                  "gate/up GEMM, h to E4M3, down GEMM, combine), per call"
                   if fp8 else
                   "moe_iq4nl_prefill_grouped (bucket, gather, tcgen05 gate/up and down GEMMs, "
                   "combine), per call" if prefill else

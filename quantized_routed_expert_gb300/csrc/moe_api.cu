@@ -376,7 +376,7 @@ int32_t moe_launches_per_call(const moe_shape* shape, int32_t T, int32_t call) {
     return call == 2 ? n + 1 : n;
   }
   if (call == 3) return moe::prefill_launches(*shape, T);
-  if (call == 5) return moe::prefill_fp8_supported(*shape) ? 7 : 0;
+  if (call == 5) return moe::prefill_fp8_supported(*shape) ? 6 : 0;
   if (call >= 6) {                           // 4 + 2 * n_layers + chained
     const int n_layers = (call - 4) / 2, chained = (call - 4) % 2;
     if (n_layers < 1 || n_layers > MOE_MAX_LAYERS || T > MOE_MAX_DECODE_TOKENS)

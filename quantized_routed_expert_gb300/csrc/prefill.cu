@@ -72,10 +72,8 @@ PrefillLayout prefill_layout(const moe_shape& s, int64_t T, bool fp8) {
     L.x8 = take(rows * H);                      // E4M3 codes of x 2^-X, bucket order
     L.h8 = take(rows * fmax);                   // E4M3 codes of h 2^-X
     L.h32 = take(rows * fmax * 4);              // h, fp32, bucket order
-    L.xexp = take(T * 4);                       // each token's exponent
     L.bexp = take(rows * 4);                    // each bucket row's x exponent
     L.hexp = take(rows * 4);                    // each bucket row's h exponent
-    L.hmax = take(rows * 4);                    // each bucket row's largest |h|
   }
   L.total = off;
   return L;
@@ -229,13 +227,12 @@ struct CombineListParams {
   int32_t* comb_row;       // [T][k+1]
   float* comb_w;           // [T][k+1]
 };
-// F8: the bucket rows are E4M3 codes of x 2^-X_t (X_t the token's exponent),
-// each row's X_t goes to bexp, and the rows' largest-|h| words are cleared for
-// the gate/up GEMM.
+// F8: the bucket rows are E4M3 codes of x 2^-X_t, X_t = floor(log2 max|x_t|)
+// - 6 (0 for a zero row), and each row's X_t goes to bexp. The row's warp finds
+// the maximum in a first pass over x_t (|bf16| bits widened to fp32 order like
+// the values); the second pass converts (its loads hit L1).
 struct Gather8 {
-  const int32_t* xexp_tok;   // [T]
   int32_t* bexp;             // [rows]
-  uint32_t* hmax;            // [rows]
   uint8_t* x8;               // [rows][H]
 };
 template <bool F8>
@@ -284,13 +281,18 @@ __global__ void pf_gather_kernel(const uint16_t* __restrict__ x, const int32_t* 
   if constexpr (F8) {
     for (int r = gw; r < rows; r += nw) {
       const int t = row_tok[r];
-      const int X = g8.xexp_tok[t];
-      const float sx = pow2_of(-X);
-      if (lane == 0) {
-        g8.bexp[r] = X;
-        g8.hmax[r] = 0u;
-      }
       const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+      uint32_t m = 0;
+      for (int c = lane; c < h8; c += 32) {
+        const uint4 v = src[c];
+        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          m = max(m, max((in[i] << 16) & 0x7FFFFFFFu, in[i] & 0x7FFF0000u));
+      }
+      const int X = vec_exponent_bits(__reduce_max_sync(0xFFFFFFFFu, m));
+      const float sx = pow2_of(-X);
+      if (lane == 0) g8.bexp[r] = X;
       uint2* dst = reinterpret_cast<uint2*>(g8.x8 + (size_t)r * H);
       for (int c = lane; c < h8; c += 32) {
         const uint4 v = src[c];
@@ -303,56 +305,31 @@ __global__ void pf_gather_kernel(const uint16_t* __restrict__ x, const int32_t* 
         dst[c] = make_uint2(pk[0] | (pk[1] << 16), pk[2] | (pk[3] << 16));
       }
     }
-    return;
-  }
-  for (int r = gw; r < rows; r += nw) {
-    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)row_tok[r] * H);
-    uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)r * H);
-    for (int c = lane; c < h8; c += 32) {
-      const uint4 v = src[c];
-      const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-      uint32_t out[4];
+  } else {
+    for (int r = gw; r < rows; r += nw) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)row_tok[r] * H);
+      uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)r * H);
+      for (int c = lane; c < h8; c += 32) {
+        const uint4 v = src[c];
+        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+        uint32_t out[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const __half lo = __float2half_rn(__uint_as_float(in[i] << 16));
-        const __half hi = __float2half_rn(__uint_as_float(in[i] & 0xFFFF0000u));
-        out[i] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
-      }
-      dst[c] = make_uint4(out[0], out[1], out[2], out[3]);
-    }
-  }
-}
-
-// E4M3 operands: each token's exponent X_t = floor(log2 max|x_t|) - 6, one
-// warp per token.
-__global__ void pf8_xexp_kernel(const uint16_t* __restrict__ x, int T, int H,
-                                int32_t* __restrict__ xexp) {
-  pdl_wait();
-  pdl_trigger();
-  const int lane = threadIdx.x & 31;
-  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int nw = (gridDim.x * blockDim.x) >> 5;
-  for (int t = gw; t < T; t += nw) {
-    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
-    uint32_t m = 0;
-    for (int c = lane; c < H / 8; c += 32) {
-      const uint4 v = src[c];
-      const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {   // |bf16| as fp32 bits: the order of the values
-        const uint32_t a = (in[i] << 16) & 0x7FFFFFFFu, b = in[i] & 0x7FFF0000u;
-        m = a > m ? a : m;
-        m = b > m ? b : m;
+        for (int i = 0; i < 4; ++i) {
+          const __half lo = __float2half_rn(__uint_as_float(in[i] << 16));
+          const __half hi = __float2half_rn(__uint_as_float(in[i] & 0xFFFF0000u));
+          out[i] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+        }
+        dst[c] = make_uint4(out[0], out[1], out[2], out[3]);
       }
     }
-    m = __reduce_max_sync(0xFFFFFFFFu, m);
-    if (lane == 0) xexp[t] = vec_exponent_bits(m);
   }
 }
 
 // E4M3 operands: h (fp32, written by the gate/up GEMM) to E4M3 codes of
-// h 2^-X_p, X_p from the row's largest |h|, one warp per bucket row.
-__global__ void pf8_hconv_kernel(const float* __restrict__ h32, const uint32_t* __restrict__ hmax,
+// h 2^-X_p, X_p from the row's largest |h|, one warp per bucket row: a first
+// pass over the row finds the largest |h| (as fp32 bits, which order like the
+// values), the second converts (its loads hit L1).
+__global__ void pf8_hconv_kernel(const float* __restrict__ h32,
                                  const int32_t* __restrict__ bucket_off, int E, int ld, int F,
                                  int Fs, uint8_t* __restrict__ h8, int32_t* __restrict__ hexp) {
   pdl_wait();
@@ -362,11 +339,17 @@ __global__ void pf8_hconv_kernel(const float* __restrict__ h32, const uint32_t* 
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
   for (int r = gw; r < rows; r += nw) {
-    const int X = vec_exponent_bits(hmax[r]);
-    const float sx = pow2_of(-X);
-    if (lane == 0) hexp[r] = X;
     const int K = r < n_valid ? F : Fs;
     const float4* src = reinterpret_cast<const float4*>(h32 + (size_t)r * ld);
+    uint32_t m = 0;
+    for (int c = lane; c < K / 4; c += 32) {
+      const float4 a = src[c];
+      m = max(m, max(max(__float_as_uint(fabsf(a.x)), __float_as_uint(fabsf(a.y))),
+                     max(__float_as_uint(fabsf(a.z)), __float_as_uint(fabsf(a.w)))));
+    }
+    const int X = vec_exponent_bits(__reduce_max_sync(0xFFFFFFFFu, m));
+    const float sx = pow2_of(-X);
+    if (lane == 0) hexp[r] = X;
     uint2* dst = reinterpret_cast<uint2*>(h8 + (size_t)r * ld);
     for (int c = lane; c < K / 8; c += 32) {
       const float4 a = src[2 * c], b = src[2 * c + 1];
@@ -406,13 +389,11 @@ struct GemmParams {
   int ldo;
   uint32_t* status;
   // E4M3 operands only: each weight row's exponent (routed [E][M], shared
-  // [Ms]) for a0, a1, s0, s1; the B operand's exponent per bucket row (x: its
-  // token's, h: its pair's); gate/up writes h as fp32 [rows][ldh] and each
-  // row's largest |h| (fp32 bits, by atomicMax: the same whatever the order)
+  // [Ms]) for a0, a1, s0, s1; gate/up: x's exponent per bucket row (its
+  // token's), and h written as fp32 [rows][ldh]
   const int8_t *e0, *e1, *se0, *se1;
   const int32_t* bexp;
   float* h32;
-  uint32_t* hmax;
 };
 
 // Shared memory and warp roles of the GEMM kernels. RAW: the IQ4_NL rows of the
@@ -849,22 +830,17 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
         }
         tmem_ld_wait();
         if constexpr (F8) {
-          // h = silu(g) u with g, u scaled back by 2^(row + column exponents);
-          // lane j keeps column j's largest |h| over the warp's 32 rows
+          // h = silu(g) u with g, u scaled back by 2^(row + column exponents)
           const bool in = bxl >= -126 && bxl <= 127;
           const float stl = pow2_of(bxl);
-          uint32_t mmax = 0;
           if (__all_sync(0xFFFFFFFFu, in)) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               if (col + j < ti.nvalid) {
                 const size_t row = (size_t)(ti.row0 + ti.n0 + col + j);
                 const float st = __shfl_sync(0xFFFFFFFFu, stl, j);
-                const float hv = silu_mul_fast(__uint_as_float(g[j]) * sg * st,
-                                               __uint_as_float(u[j]) * su * st);
-                p.h32[row * p.ldh + mrow] = hv;
-                const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(hv)));
-                mmax = lane == j ? m : mmax;
+                p.h32[row * p.ldh + mrow] = silu_mul_fast(__uint_as_float(g[j]) * sg * st,
+                                                          __uint_as_float(u[j]) * su * st);
               }
             }
           } else {
@@ -874,24 +850,20 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
                 const size_t row = (size_t)(ti.row0 + ti.n0 + col + j);
                 const int bx = __shfl_sync(0xFFFFFFFFu, bxl, j);
                 const float st = pow2_of(bx);
-                const float hv = silu_mul_fast(scale_acc(__uint_as_float(g[j]), sg, bx, st),
-                                               scale_acc(__uint_as_float(u[j]), su, bx, st));
-                p.h32[row * p.ldh + mrow] = hv;
-                const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(hv)));
-                mmax = lane == j ? m : mmax;
+                p.h32[row * p.ldh + mrow] =
+                    silu_mul_fast(scale_acc(__uint_as_float(g[j]), sg, bx, st),
+                                  scale_acc(__uint_as_float(u[j]), su, bx, st));
               }
             }
           }
-          // then over the grid: one atomic per column, all lanes at once
-          if (col + lane < ti.nvalid) atomicMax(&p.hmax[ti.row0 + ti.n0 + col + lane], mmax);
-          continue;
-        }
+        } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (col + j < ti.nvalid) {
-            const size_t row = (size_t)(ti.row0 + ti.n0 + col + j);
-            const float hv = silu_mul_fast(__uint_as_float(g[j]), __uint_as_float(u[j]));
-            p.h[row * p.ldh + mrow] = __float2half_rn(hv);
+          for (int j = 0; j < 32; ++j) {
+            if (col + j < ti.nvalid) {
+              const size_t row = (size_t)(ti.row0 + ti.n0 + col + j);
+              const float hv = silu_mul_fast(__uint_as_float(g[j]), __uint_as_float(u[j]));
+              p.h[row * p.ldh + mrow] = __float2half_rn(hv);
+            }
           }
         }
       }
@@ -1327,10 +1299,8 @@ cudaError_t launch_prefill_fp8(const moe_shape& s, const moe_expert_weights& w,
   uint8_t* x8 = ws + L.x8;
   uint8_t* h8 = ws + L.h8;
   float* h32 = reinterpret_cast<float*>(ws + L.h32);
-  int32_t* xexp = reinterpret_cast<int32_t*>(ws + L.xexp);
   int32_t* bexp = reinterpret_cast<int32_t*>(ws + L.bexp);
   int32_t* hexp = reinterpret_cast<int32_t*>(ws + L.hexp);
-  uint32_t* hmax = reinterpret_cast<uint32_t*>(ws + L.hmax);
   const int64_t EF = (int64_t)E * F, EH = (int64_t)E * H;
   const int8_t* ex_gate = row_exp;
   const int8_t* ex_up = row_exp + EF;
@@ -1345,10 +1315,8 @@ cudaError_t launch_prefill_fp8(const moe_shape& s, const moe_expert_weights& w,
   if (e != cudaSuccess) return e;
   e = launch_ex(pf_bucket_kernel, dim3(1), dim3(kBucketThreads), bsm, pdl, stream, bp);
   if (e != cudaSuccess) return e;
-  e = launch_ex(pf8_xexp_kernel, dim3(num_sms), dim3(256), 0, pdl, stream, x, T, H, xexp);
-  if (e != cudaSuccess) return e;
   const CombineListParams cl{(const int32_t*)row_of, weights, T, k, s.n_shared, comb_row, comb_w};
-  const Gather8 g8{(const int32_t*)xexp, bexp, hmax, x8};
+  const Gather8 g8{bexp, x8};
   e = launch_ex(pf_gather_kernel<true>, dim3(num_sms * 4), dim3(256), 0, pdl, stream, x,
                 (const int32_t*)boff, (const int32_t*)row_tok, E, H, (__half*)nullptr, cl, g8);
   if (e != cudaSuccess) return e;
@@ -1385,11 +1353,10 @@ cudaError_t launch_prefill_fp8(const moe_shape& s, const moe_expert_weights& w,
   g1.se1 = ex_su;
   g1.bexp = bexp;
   g1.h32 = h32;
-  g1.hmax = hmax;
   e = launch_gemm<true, true, true>(num_sms, E, pdl, stream, tm_x, g1);
   if (e != cudaSuccess) return e;
   e = launch_ex(pf8_hconv_kernel, dim3(num_sms * 4), dim3(256), 0, pdl, stream,
-                (const float*)h32, (const uint32_t*)hmax, (const int32_t*)boff, E, fmax, F, Fs,
+                (const float*)h32, (const int32_t*)boff, E, fmax, F, Fs,
                 h8, hexp);
   if (e != cudaSuccess) return e;
 
@@ -1408,7 +1375,6 @@ cudaError_t launch_prefill_fp8(const moe_shape& s, const moe_expert_weights& w,
   g2.se1 = nullptr;
   g2.bexp = nullptr;                 // the h rows' exponents enter in the combine
   g2.h32 = nullptr;
-  g2.hmax = nullptr;
   g2.o = o;
   g2.ldo = H;
   e = launch_gemm<false, true, true>(num_sms, E, pdl, stream, tm_h, g2);

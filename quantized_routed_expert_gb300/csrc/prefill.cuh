@@ -13,7 +13,7 @@ constexpr int kPrefillMaxTokens = 16384;
 struct PrefillLayout {
   int64_t counts, offsets, perm, comb, x16, h16, o, sched, total;  // byte offsets
   // E4M3 operands only (fp8 layout): codes of x and h, h as fp32, exponents
-  int64_t x8, h8, h32, xexp, bexp, hexp, hmax;
+  int64_t x8, h8, h32, bexp, hexp;
 };
 
 // fp8: the layout of the E4M3-operand prefill (adds the regions above).

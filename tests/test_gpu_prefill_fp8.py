@@ -274,4 +274,4 @@ def test_prefill_fp8_argument_errors():
             z.numel(), None, None), "fp8")
     assert e.value.status == moe.MOE_ERR_UNSUPPORTED
     assert moe.launches_per_call(s0, 4, 5) == 0
-    assert moe.launches_per_call(shape, 4, 5) == 7
+    assert moe.launches_per_call(shape, 4, 5) == 6
