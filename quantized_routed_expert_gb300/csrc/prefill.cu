@@ -228,9 +228,10 @@ struct CombineListParams {
   float* comb_w;           // [T][k+1]
 };
 // F8: the bucket rows are E4M3 codes of x 2^-X_t, X_t = floor(log2 max|x_t|)
-// - 6 (0 for a zero row), and each row's X_t goes to bexp. The row's warp finds
-// the maximum in a first pass over x_t (|bf16| bits widened to fp32 order like
-// the values); the second pass converts (its loads hit L1).
+// - 6 (0 for a zero row), in the E4M3 block order of K (e4m3_block_pos_value),
+// and each row's X_t goes to bexp. The row's warp finds the maximum in a first
+// pass over x_t (|bf16| bits widened to fp32 order like the values); the
+// second pass converts (its loads hit L1).
 struct Gather8 {
   int32_t* bexp;             // [rows]
   uint8_t* x8;               // [rows][H]
@@ -293,15 +294,20 @@ __global__ void pf_gather_kernel(const uint16_t* __restrict__ x, const int32_t* 
       const int X = vec_exponent_bits(__reduce_max_sync(0xFFFFFFFFu, m));
       const float sx = pow2_of(-X);
       if (lane == 0) g8.bexp[r] = X;
+      // positions 8c .. 8c + 7 of the E4M3 block order: values 4j .. 4j + 3
+      // and 4j + 16 .. 4j + 19 of block c / 4 (j = c % 4), interleaved
+      const uint2* src2 = reinterpret_cast<const uint2*>(x + (size_t)t * H);
       uint2* dst = reinterpret_cast<uint2*>(g8.x8 + (size_t)r * H);
       for (int c = lane; c < h8; c += 32) {
-        const uint4 v = src[c];
-        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+        const int v0 = (c >> 2) * 32 + (c & 3) * 4;
+        const uint2 a = src2[v0 / 4], b = src2[(v0 + 16) / 4];
+        const uint32_t lo[4] = {a.x << 16, a.x & 0xFFFF0000u, a.y << 16, a.y & 0xFFFF0000u};
+        const uint32_t hi[4] = {b.x << 16, b.x & 0xFFFF0000u, b.y << 16, b.y & 0xFFFF0000u};
         uint32_t pk[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)      // values 2i (low half) and 2i + 1 (high half)
-          pk[i] = cvt_e4m3x2(pow2_scale(__uint_as_float(in[i] & 0xFFFF0000u), -X, sx),
-                             pow2_scale(__uint_as_float(in[i] << 16), -X, sx));
+        for (int i = 0; i < 4; ++i)      // values 4j + i (low byte) and 4j + 16 + i
+          pk[i] = cvt_e4m3x2(pow2_scale(__uint_as_float(hi[i]), -X, sx),
+                             pow2_scale(__uint_as_float(lo[i]), -X, sx));
         dst[c] = make_uint2(pk[0] | (pk[1] << 16), pk[2] | (pk[3] << 16));
       }
     }
@@ -326,7 +332,8 @@ __global__ void pf_gather_kernel(const uint16_t* __restrict__ x, const int32_t* 
 }
 
 // E4M3 operands: h (fp32, written by the gate/up GEMM) to E4M3 codes of
-// h 2^-X_p, X_p from the row's largest |h|, one warp per bucket row: a first
+// h 2^-X_p in the E4M3 block order of K, X_p from the row's largest |h|, one
+// warp per bucket row: a first
 // pass over the row finds the largest |h| (as fp32 bits, which order like the
 // values), the second converts (its loads hit L1).
 __global__ void pf8_hconv_kernel(const float* __restrict__ h32,
@@ -352,11 +359,13 @@ __global__ void pf8_hconv_kernel(const float* __restrict__ h32,
     if (lane == 0) hexp[r] = X;
     uint2* dst = reinterpret_cast<uint2*>(h8 + (size_t)r * ld);
     for (int c = lane; c < K / 8; c += 32) {
-      const float4 a = src[2 * c], b = src[2 * c + 1];
-      const uint32_t p0 = cvt_e4m3x2(pow2_scale(a.y, -X, sx), pow2_scale(a.x, -X, sx));
-      const uint32_t p1 = cvt_e4m3x2(pow2_scale(a.w, -X, sx), pow2_scale(a.z, -X, sx));
-      const uint32_t p2 = cvt_e4m3x2(pow2_scale(b.y, -X, sx), pow2_scale(b.x, -X, sx));
-      const uint32_t p3 = cvt_e4m3x2(pow2_scale(b.w, -X, sx), pow2_scale(b.z, -X, sx));
+      // the E4M3 block order: values 4j + i and 4j + 16 + i of block c / 4
+      const int v0 = (c >> 2) * 32 + (c & 3) * 4;
+      const float4 a = src[v0 / 4], b = src[(v0 + 16) / 4];
+      const uint32_t p0 = cvt_e4m3x2(pow2_scale(b.x, -X, sx), pow2_scale(a.x, -X, sx));
+      const uint32_t p1 = cvt_e4m3x2(pow2_scale(b.y, -X, sx), pow2_scale(a.y, -X, sx));
+      const uint32_t p2 = cvt_e4m3x2(pow2_scale(b.z, -X, sx), pow2_scale(a.z, -X, sx));
+      const uint32_t p3 = cvt_e4m3x2(pow2_scale(b.w, -X, sx), pow2_scale(a.w, -X, sx));
       dst[c] = make_uint2(p0 | (p1 << 16), p2 | (p3 << 16));
     }
   }
@@ -1008,7 +1017,8 @@ __global__ void pf8_row_exp_kernel(const __grid_constant__ RowExpJobs jobs) {
 }
 
 // Each thread: one block of a row, through dequant_block_e4m3 with the row's
-// exponent (written by pf8_row_exp_kernel first).
+// exponent (written by pf8_row_exp_kernel first); its codes are written back in
+// K order.
 __global__ void pf8_dequant_kernel(const uint8_t* __restrict__ mat, int64_t rows, int K,
                                    const int8_t* __restrict__ row_exp, uint8_t* __restrict__ out) {
   const int nb = K / 32;
@@ -1025,9 +1035,9 @@ __global__ void pf8_dequant_kernel(const uint8_t* __restrict__ mat, int64_t rows
              ((uint32_t)b[4 + 4 * w] << 16) | ((uint32_t)b[5 + 4 * w] << 24);
     uint32_t c[8];
     dequant_block_e4m3(q, d, row_exp[r], c);
-    uint32_t* o = reinterpret_cast<uint32_t*>(out + i * 32);   // 32 codes, K order
+    uint8_t* o = out + i * 32;                 // 32 codes, back in K order
 #pragma unroll
-    for (int w = 0; w < 8; ++w) o[w] = c[w];
+    for (int p = 0; p < 32; ++p) o[e4m3_block_pos_value(p)] = (uint8_t)(c[p >> 2] >> (8 * (p & 3)));
   }
 }
 

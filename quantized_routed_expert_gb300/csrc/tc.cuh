@@ -214,31 +214,38 @@ __device__ __forceinline__ void e4m3_block_table(uint16_t dbits, int E, uint32_t
   t[3] = pack(T12, T13, T14, T15);
 }
 
-// Eight codes (one index word) through a 16-byte table t (as above) to the 8
-// table bytes in K order: lo = bytes of the low nibbles of index bytes 0..3,
-// hi = of the high nibbles (the lookup of iq4_lookup8_split, on a table held
-// in registers).
-__device__ __forceinline__ void lookup16_split(uint32_t q, const uint32_t (&t)[4], uint32_t& lo,
-                                               uint32_t& hi) {
+// Eight codes (one index word) through a 16-byte table t (as above), in the
+// order of the word's nibbles: r0 = codes of index byte 0's low and high
+// nibble, then byte 1's, r1 = the same for bytes 2 and 3 (three prmt per four
+// codes, on a table held in registers).
+__device__ __forceinline__ void lookup16_nibbles(uint32_t q, const uint32_t (&t)[4], uint32_t& r0,
+                                                 uint32_t& r1) {
   const uint32_t qm = q & 0x77777777u;
   const uint32_t sel = 0x32103210u | ((q >> 1) & 0x44444444u);
-  const uint32_t r0 = prmt(prmt(t[0], t[1], qm), prmt(t[2], t[3], qm), sel);
+  r0 = prmt(prmt(t[0], t[1], qm), prmt(t[2], t[3], qm), sel);
   const uint32_t qm1 = qm >> 16;
-  const uint32_t r1 = prmt(prmt(t[0], t[1], qm1), prmt(t[2], t[3], qm1), sel >> 16);
-  lo = prmt(r0, r1, 0x6420u);
-  hi = prmt(r0, r1, 0x7531u);
+  r1 = prmt(prmt(t[0], t[1], qm1), prmt(t[2], t[3], qm1), sel >> 16);
+}
+
+// The E4M3 operands' order of K inside each 32-value block: position p holds
+// value 4 (p / 8) + (p / 2) % 4 + 16 (p % 2), i.e. values j and j + 16 side by
+// side, the order in which a block's index bytes hold them (low nibble j, high
+// nibble j + 16). A and B of the contraction share it, so the sums are the
+// same; the weight producers then store the lookups as they come out.
+__host__ __device__ constexpr int e4m3_block_pos_value(int p) {
+  return 4 * (p >> 3) + ((p >> 1) & 3) + 16 * (p & 1);
 }
 
 // One 32-weight block (its 4 index words, fp16 scale bits) of a row with
-// exponent E to its 32 E4M3 codes in K order: words 0..3 hold weights 0..15,
-// words 4..7 weights 16..31. The fp8 prefill producers call this for every
-// block they put into an A tile.
+// exponent E to its 32 E4M3 codes in the block order above: byte p of
+// w[p / 4]. The fp8 prefill producers call this for every block they put into
+// an A tile.
 __device__ __forceinline__ void dequant_block_e4m3(const uint32_t (&q)[4], uint16_t dbits, int E,
                                                    uint32_t (&w)[8]) {
   uint32_t t[4];
   e4m3_block_table(dbits, E, t);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) lookup16_split(q[i], t, w[i], w[4 + i]);
+  for (int i = 0; i < 4; ++i) lookup16_nibbles(q[i], t, w[2 * i], w[2 * i + 1]);
 }
 
 // floor(log2 |v|) - 6 from an fp32 bit pattern of |v| (0 for zero), the
