@@ -807,59 +807,63 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
       if (!ok) break;
       if (warp == S::kCtl && lane == 0) PF_STAMP(tc, 3, global_timer_ns());
       if constexpr (S::kEpi == 0) {
-      // epilogue: TMEM lanes of this warp's quarter, a share of the token columns
+      // epilogue: TMEM lanes of this warp's quarter; the tile's token columns
+      // in units of 8, dealt round-robin to the warps of the quarter, so that
+      // a tile of few tokens still spreads over all the dequantising warps
+      constexpr int kShares = S::kDq / 4;       // warps per TMEM lane quarter
       const int q = warp & 3;
-      constexpr int kCols = kTN / (S::kDq / 4);
-      const int ch = dw >> 2;                   // column share
+      const int ch = dw >> 2;                   // this warp's units: ch, ch + kShares, ...
       const int mrow = ti.m0 + q * 32 + lane;   // weight row of this thread
-      // E4M3: 2^(gate, up row exponents) and, in lane j, the exponent of the
-      // share's first column chunk, loaded before the accumulator wait
+      const int nunits = (ti.nvalid + 7) >> 3;
+      const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+      // E4M3: 2^(gate, up row exponents); the exponents of this warp's
+      // columns, lane l holding column l % 8 of unit ch + 4 (l / 8) (bxa) and
+      // of unit ch + 16 + 4 (l / 8) (bxb), loaded before the accumulator wait
       float sg = 1.f, su = 1.f;
-      int bx_next = 0;
+      int bxa = 0, bxb = 0;
       if constexpr (F8) {
+        static_assert(kShares == 4, "the exponent prefetch below deals units over four warps");
         const size_t er = (sh ? 0 : (size_t)ti.bucket * p.M) + mrow;
         sg = exp2i((sh ? p.se0 : p.e0)[er]);
         su = exp2i((sh ? p.se1 : p.e1)[er]);
-        if (ch * kCols + lane < ti.nvalid) bx_next = p.bexp[ti.row0 + ti.n0 + ch * kCols + lane];
+        const int ca = (ch + 4 * (lane >> 3)) * 8 + (lane & 7);
+        if (ca < ti.nvalid) bxa = p.bexp[ti.row0 + ti.n0 + ca];
+        if (ca + 128 < ti.nvalid) bxb = p.bexp[ti.row0 + ti.n0 + ca + 128];
       }
       if (!mbar_wait(acc_full, tc & 1, p.status)) { ok = false; break; }
       tc_fence_after();
       if (warp == S::kCtl && lane == 0) PF_STAMP(tc, 4, global_timer_ns());
-      for (int c = 0; c < kCols; c += 32) {
-        const int col = ch * kCols + c;
-        if (col >= ti.nvalid) break;            // warp-uniform
-        uint32_t g[32], u[32];
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + col, g);
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + kTN + col, u);
-        int bxl = bx_next;                      // E4M3: lane j: column col + j
-        if constexpr (F8) {
-          bx_next = 0;
-          if (c + 32 < kCols && col + 32 + lane < ti.nvalid)
-            bx_next = p.bexp[ti.row0 + ti.n0 + col + 32 + lane];
-        }
+#pragma unroll 1
+      for (int i = 0; i < (kTN / 8) / kShares; ++i) {
+        const int unit = ch + kShares * i;
+        if (unit >= nunits) break;              // warp-uniform
+        const int col = unit * 8;
+        uint32_t g[8], u[8];
+        tmem_ld8(tq + col, g);
+        tmem_ld8(tq + kTN + col, u);
         tmem_ld_wait();
+        const size_t row0 = (size_t)(ti.row0 + ti.n0 + col);
         if constexpr (F8) {
-          // h = silu(g) u with g, u scaled back by 2^(row + column exponents)
-          const bool in = bxl >= -126 && bxl <= 127;
-          const float stl = pow2_of(bxl);
-          if (__all_sync(0xFFFFFFFFu, in)) {
+          // h = silu(g) u with g, u scaled back by 2^(row + column exponents);
+          // lanes 0..7 (and their copies) get the unit's eight exponents
+          const int bx8 = __shfl_sync(0xFFFFFFFFu, i < 4 ? bxa : bxb, ((i & 3) << 3) + (lane & 7));
+          const float st8 = pow2_of(bx8);
+          if (__all_sync(0xFFFFFFFFu, bx8 >= -126 && bx8 <= 127)) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < 8; ++j) {
               if (col + j < ti.nvalid) {
-                const size_t row = (size_t)(ti.row0 + ti.n0 + col + j);
-                const float st = __shfl_sync(0xFFFFFFFFu, stl, j);
-                p.h32[row * p.ldh + mrow] = silu_mul_fast(__uint_as_float(g[j]) * sg * st,
-                                                          __uint_as_float(u[j]) * su * st);
+                const float st = __shfl_sync(0xFFFFFFFFu, st8, j);
+                p.h32[(row0 + j) * p.ldh + mrow] = silu_mul_fast(__uint_as_float(g[j]) * sg * st,
+                                                                 __uint_as_float(u[j]) * su * st);
               }
             }
           } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < 8; ++j) {
               if (col + j < ti.nvalid) {
-                const size_t row = (size_t)(ti.row0 + ti.n0 + col + j);
-                const int bx = __shfl_sync(0xFFFFFFFFu, bxl, j);
+                const int bx = __shfl_sync(0xFFFFFFFFu, bx8, j);
                 const float st = pow2_of(bx);
-                p.h32[row * p.ldh + mrow] =
+                p.h32[(row0 + j) * p.ldh + mrow] =
                     silu_mul_fast(scale_acc(__uint_as_float(g[j]), sg, bx, st),
                                   scale_acc(__uint_as_float(u[j]), su, bx, st));
               }
@@ -867,11 +871,10 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
           }
         } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
+          for (int j = 0; j < 8; ++j) {
             if (col + j < ti.nvalid) {
-              const size_t row = (size_t)(ti.row0 + ti.n0 + col + j);
               const float hv = silu_mul_fast(__uint_as_float(g[j]), __uint_as_float(u[j]));
-              p.h[row * p.ldh + mrow] = __float2half_rn(hv);
+              p.h[(row0 + j) * p.ldh + mrow] = __float2half_rn(hv);
             }
           }
         }
