@@ -270,9 +270,13 @@ moe_status moe_iq4nl_prefill_grouped(const moe_shape* shape, const moe_expert_we
  *             (0 for an all-zero row), so its largest value lies in [64, 128);
  *   h       : each (token, expert) row of SwiGLU outputs the same way, from
  *             the row's fp32 h.
- * The accumulators are multiplied back by 2^(E_r + X) exactly; the combine is
+ * The fp32 accumulators are multiplied back by the powers of two: the weight
+ * row's and x's in the contractions' epilogues, h's through the combine weight
+ * (w 2^X, the same product while w 2^X is a normal fp32); the combine order is
  * that of moe_iq4nl_prefill_grouped. The result differs from the fp16-operand
- * call by the E4M3 rounding (about 2^-4 relative per operand).
+ * call by the E4M3 rounding (about 2^-4 relative per operand). Inside each
+ * 32-value block both operands keep K in the order of the IQ4_NL index bytes
+ * (values j and j + 16 side by side); the sums do not depend on it.
  *   row_exp : device int8, the table moe_iq4nl_fp8_row_exponents wrote for
  *             these weights (it depends on the weights only: make it once).
  * Shape rule: hidden, ffn and ffn_shared are multiples of 256 (the operand

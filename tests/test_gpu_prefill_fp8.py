@@ -209,6 +209,43 @@ def test_prefill_fp8_full_chunk_sampled_tokens():
     assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
 
 
+def test_prefill_fp8_largest_chunk_sampled_tokens():
+    # the largest chunk the call takes (16384 tokens), Xing shape: bucketing,
+    # tile schedule, token exponents and h conversion at their maximum
+    moe = lib()
+    s = synth.SHAPES[4]
+    L = layer_of(4, 2)
+    T = 16384
+    shape = moe_shape(s)
+    assert moe.workspace_bytes(shape, T, moe.PREFILL_FP8) > 0
+    assert moe.workspace_bytes(shape, T + 1, moe.PREFILL_FP8) == 0
+    x_host = synth.x_rows(L.seed, 2, s.H, T)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ids, w, y = run_prefill_fp8(L, x_host, status=status)
+    assert int(status.item()) == 0
+    rows = np.random.default_rng(1).choice(T, 10, replace=False)
+    rows = np.sort(np.concatenate([rows, [0, T - 1]]))
+    check_close(y[rows], oracle_rows(L, x_host, ids, w, rows), "prefill fp8 T=16384 sampled")
+
+
+def test_prefill_fp8_empty_chunk():
+    # T = 0: nothing to do, nothing launched, y untouched
+    moe = lib()
+    L = layer_of(SMALL, 0, seed=3)
+    s = L.shape
+    shape = moe_shape(s)
+    wts = weights_of(L)
+    rexp = moe.fp8_row_exponents(shape, wts)
+    x = torch.zeros((0, s.H), dtype=torch.bfloat16, device=DEV)
+    ids = torch.zeros((0, s.k), dtype=torch.int32, device=DEV)
+    w = torch.zeros((0, s.k), dtype=torch.float32, device=DEV)
+    y = moe.iq4nl_prefill_grouped_fp8(shape, wts, rexp, x, ids, w,
+                                      moe.workspace(shape, 1, moe.PREFILL_FP8, DEV))
+    torch.cuda.synchronize()
+    assert tuple(y.shape) == (0, s.H)
+    assert moe.launches_per_call(shape, 0, 5) == 0
+
+
 @pytest.mark.parametrize("H,F,E,k,T,ns", [
     (256, 256, 1, 1, 3, 0),        # one expert, no shared expert
     (256, 512, 16, 4, 300, 1),     # four 128-row weight tiles, ragged token tiles
