@@ -333,12 +333,18 @@ __global__ void pf_gather_kernel(const uint16_t* __restrict__ x, const int32_t* 
 
 // E4M3 operands: h (fp32, written by the gate/up GEMM) to E4M3 codes of
 // h 2^-X_p in the E4M3 block order of K, X_p from the row's largest |h|, one
-// warp per bucket row: a first
+// warp per bucket row. The down outputs then lack the factor 2^X_p: the row's
+// combine weight w (its token's slot in the combine list) becomes w 2^X_p, the
+// same product as scaling the outputs whenever w 2^X_p is a normal fp32 (each
+// fp32 rounding commutes with a power of two). A first
 // pass over the row finds the largest |h| (as fp32 bits, which order like the
 // values), the second converts (its loads hit L1).
 __global__ void pf8_hconv_kernel(const float* __restrict__ h32,
                                  const int32_t* __restrict__ bucket_off, int E, int ld, int F,
-                                 int Fs, uint8_t* __restrict__ h8, int32_t* __restrict__ hexp) {
+                                 int Fs, uint8_t* __restrict__ h8, int32_t* __restrict__ hexp,
+                                 const int32_t* __restrict__ row_tok,
+                                 const int32_t* __restrict__ comb_row, float* __restrict__ comb_w,
+                                 int kk) {
   pdl_wait();
   pdl_trigger();
   const int rows = bucket_off[E + 1], n_valid = bucket_off[E];
@@ -357,6 +363,13 @@ __global__ void pf8_hconv_kernel(const float* __restrict__ h32,
     const int X = vec_exponent_bits(__reduce_max_sync(0xFFFFFFFFu, m));
     const float sx = pow2_of(-X);
     if (lane == 0) hexp[r] = X;
+    if (lane < kk) {                           // this row's slot in its token's list
+      const size_t slot = (size_t)row_tok[r] * kk + lane;
+      if (comb_row[slot] == r) {
+        const float w = comb_w[slot];
+        comb_w[slot] = X >= -126 ? w * exp2i(X) : ldexpf(w, X);
+      }
+    }
     uint2* dst = reinterpret_cast<uint2*>(h8 + (size_t)r * ld);
     for (int c = lane; c < K / 8; c += 32) {
       // the E4M3 block order: values 4j + i and 4j + 16 + i of block c / 4
@@ -937,13 +950,9 @@ pf_gemm_kernel(const __grid_constant__ TmapSet tmaps, const GemmParams p) {
 
 // ---------------------------------------------------------------------------
 // 4. Combine: y[t] = o[shared row] + sum over routed rows (experts ascending) w o.
-// F8: o holds the down outputs without their h row's factor 2^X (X = hexp of
-// the row); it enters through the weight, w 2^X, the same product whenever
-// w 2^X is a normal fp32 (each fp32 rounding commutes with the power of two).
-template <bool F8>
 __global__ void pf_combine_kernel(const float* __restrict__ o, const int32_t* __restrict__ comb_row,
                                   const float* __restrict__ comb_w, int T, int kk, int H,
-                                  float* __restrict__ y, const int32_t* __restrict__ hexp) {
+                                  float* __restrict__ y) {
   pdl_wait();
   pdl_trigger();
   const int h4 = H / 4;
@@ -968,11 +977,7 @@ __global__ void pf_combine_kernel(const float* __restrict__ o, const int32_t* __
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         if (r[u] < 0) break;
-        float wv = cw[j0 + u];
-        if constexpr (F8) {
-          const int X = hexp[r[u]];
-          wv = X >= -126 ? wv * exp2i(X) : ldexpf(wv, X);
-        }
+        const float wv = cw[j0 + u];
         acc.x = fmaf(wv, v[u].x, acc.x);
         acc.y = fmaf(wv, v[u].y, acc.y);
         acc.z = fmaf(wv, v[u].z, acc.z);
@@ -1234,9 +1239,9 @@ cudaError_t launch_prefill(const moe_shape& s, const moe_expert_weights& w, cons
   const int64_t total = (int64_t)T * (H / 4);
   int64_t grid = (total + 255) / 256;
   if (grid > (int64_t)num_sms * 8) grid = (int64_t)num_sms * 8;
-  return launch_ex(pf_combine_kernel<false>, dim3((unsigned)grid), dim3(256), 0, pdl, stream,
+  return launch_ex(pf_combine_kernel, dim3((unsigned)grid), dim3(256), 0, pdl, stream,
                    (const float*)o, (const int32_t*)comb_row, (const float*)comb_w, T, k + 1, H,
-                   y, (const int32_t*)nullptr);
+                   y);
 }
 
 // ---------------------------------------------------------------------------
@@ -1370,7 +1375,7 @@ cudaError_t launch_prefill_fp8(const moe_shape& s, const moe_expert_weights& w,
   if (e != cudaSuccess) return e;
   e = launch_ex(pf8_hconv_kernel, dim3(num_sms * 4), dim3(256), 0, pdl, stream,
                 (const float*)h32, (const int32_t*)boff, E, fmax, F, Fs,
-                h8, hexp);
+                h8, hexp, (const int32_t*)row_tok, (const int32_t*)comb_row, comb_w, k + 1);
   if (e != cudaSuccess) return e;
 
   GemmParams g2 = g1;
@@ -1396,9 +1401,9 @@ cudaError_t launch_prefill_fp8(const moe_shape& s, const moe_expert_weights& w,
   const int64_t total = (int64_t)T * (H / 4);
   int64_t grid = (total + 255) / 256;
   if (grid > (int64_t)num_sms * 8) grid = (int64_t)num_sms * 8;
-  return launch_ex(pf_combine_kernel<true>, dim3((unsigned)grid), dim3(256), 0, pdl, stream,
+  return launch_ex(pf_combine_kernel, dim3((unsigned)grid), dim3(256), 0, pdl, stream,
                    (const float*)o, (const int32_t*)comb_row, (const float*)comb_w, T, k + 1, H,
-                   y, (const int32_t*)hexp);
+                   y);
 }
 
 }  // namespace moe
