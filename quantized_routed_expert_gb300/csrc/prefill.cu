@@ -229,16 +229,16 @@ struct CombineListParams {
 };
 // F8: the bucket rows are E4M3 codes of x 2^-X_t, X_t = floor(log2 max|x_t|)
 // - 6 (0 for a zero row), in the E4M3 block order of K (e4m3_block_pos_value),
-// and each row's X_t goes to bexp. The row's warp finds the maximum in a first
-// pass over x_t (|bf16| bits widened to fp32 order like the values); the
-// second pass converts (its loads hit L1).
+// and each row's X_t goes to bexp. The token's warp finds the maximum in a
+// first pass over x_t (|bf16| bits widened to fp32 order like the values); the
+// second pass converts (its loads hit L1) and writes every row of the token.
 struct Gather8 {
   int32_t* bexp;             // [rows]
   uint8_t* x8;               // [rows][H]
 };
 template <bool F8>
 __global__ void pf_gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ bucket_off,
-                                 const int32_t* __restrict__ row_tok, int E, int H, __half* xs,
+                                 int E, int H, __half* xs,
                                  const CombineListParams cl, const Gather8 g8) {
   pdl_wait();
   pdl_trigger();
@@ -274,14 +274,20 @@ __global__ void pf_gather_kernel(const uint16_t* __restrict__ x, const int32_t* 
       }
     }
   }
-  const int rows = bucket_off[E + 1];
+  // one warp per token: its x row is read once and written to each of its
+  // bucket rows (lane j < k: the row of slot j, -1 for an invalid pair; lane k:
+  // the shared expert's row)
+  const int n_valid = bucket_off[E];
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
   const int h8 = H / 8;
-  if constexpr (F8) {
-    for (int r = gw; r < rows; r += nw) {
-      const int t = row_tok[r];
+  for (int t = gw; t < cl.T; t += nw) {
+    int myrow = -1;
+    if (lane < cl.k) myrow = cl.row_of[(size_t)t * cl.k + lane];
+    else if (lane == cl.k && cl.n_shared) myrow = n_valid + t;
+    const uint32_t have = __ballot_sync(0xFFFFFFFFu, myrow >= 0);
+    if constexpr (F8) {
       const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
       uint32_t m = 0;
       for (int c = lane; c < h8; c += 32) {
@@ -293,11 +299,10 @@ __global__ void pf_gather_kernel(const uint16_t* __restrict__ x, const int32_t* 
       }
       const int X = vec_exponent_bits(__reduce_max_sync(0xFFFFFFFFu, m));
       const float sx = pow2_of(-X);
-      if (lane == 0) g8.bexp[r] = X;
+      if (myrow >= 0) g8.bexp[myrow] = X;
       // positions 8c .. 8c + 7 of the E4M3 block order: values 4j .. 4j + 3
       // and 4j + 16 .. 4j + 19 of block c / 4 (j = c % 4), interleaved
       const uint2* src2 = reinterpret_cast<const uint2*>(x + (size_t)t * H);
-      uint2* dst = reinterpret_cast<uint2*>(g8.x8 + (size_t)r * H);
       for (int c = lane; c < h8; c += 32) {
         const int v0 = (c >> 2) * 32 + (c & 3) * 4;
         const uint2 a = src2[v0 / 4], b = src2[(v0 + 16) / 4];
@@ -308,13 +313,14 @@ __global__ void pf_gather_kernel(const uint16_t* __restrict__ x, const int32_t* 
         for (int i = 0; i < 4; ++i)      // values 4j + i (low byte) and 4j + 16 + i
           pk[i] = cvt_e4m3x2(pow2_scale(__uint_as_float(hi[i]), -X, sx),
                              pow2_scale(__uint_as_float(lo[i]), -X, sx));
-        dst[c] = make_uint2(pk[0] | (pk[1] << 16), pk[2] | (pk[3] << 16));
+        const uint2 v = make_uint2(pk[0] | (pk[1] << 16), pk[2] | (pk[3] << 16));
+        for (uint32_t rem = have; rem; rem &= rem - 1) {
+          const int r = __shfl_sync(0xFFFFFFFFu, myrow, __ffs(rem) - 1);
+          reinterpret_cast<uint2*>(g8.x8 + (size_t)r * H)[c] = v;
+        }
       }
-    }
-  } else {
-    for (int r = gw; r < rows; r += nw) {
-      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)row_tok[r] * H);
-      uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)r * H);
+    } else {
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
       for (int c = lane; c < h8; c += 32) {
         const uint4 v = src[c];
         const uint32_t in[4] = {v.x, v.y, v.z, v.w};
@@ -325,7 +331,11 @@ __global__ void pf_gather_kernel(const uint16_t* __restrict__ x, const int32_t* 
           const __half hi = __float2half_rn(__uint_as_float(in[i] & 0xFFFF0000u));
           out[i] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
         }
-        dst[c] = make_uint4(out[0], out[1], out[2], out[3]);
+        const uint4 o = make_uint4(out[0], out[1], out[2], out[3]);
+        for (uint32_t rem = have; rem; rem &= rem - 1) {
+          const int r = __shfl_sync(0xFFFFFFFFu, myrow, __ffs(rem) - 1);
+          reinterpret_cast<uint4*>(xs + (size_t)r * H)[c] = o;
+        }
       }
     }
   }
@@ -1182,7 +1192,7 @@ cudaError_t launch_prefill(const moe_shape& s, const moe_expert_weights& w, cons
   if (e != cudaSuccess) return e;
   const CombineListParams cl{(const int32_t*)row_of, weights, T, k, s.n_shared, comb_row, comb_w};
   e = launch_ex(pf_gather_kernel<false>, dim3(num_sms * 4), dim3(256), 0, pdl, stream, x,
-                (const int32_t*)boff, (const int32_t*)row_tok, E, H, x16, cl, Gather8{});
+                (const int32_t*)boff, E, H, x16, cl, Gather8{});
   if (e != cudaSuccess) return e;
 
   TmapSet tm_x, tm_h;
@@ -1336,7 +1346,7 @@ cudaError_t launch_prefill_fp8(const moe_shape& s, const moe_expert_weights& w,
   const CombineListParams cl{(const int32_t*)row_of, weights, T, k, s.n_shared, comb_row, comb_w};
   const Gather8 g8{bexp, x8};
   e = launch_ex(pf_gather_kernel<true>, dim3(num_sms * 4), dim3(256), 0, pdl, stream, x,
-                (const int32_t*)boff, (const int32_t*)row_tok, E, H, (__half*)nullptr, cl, g8);
+                (const int32_t*)boff, E, H, (__half*)nullptr, cl, g8);
   if (e != cudaSuccess) return e;
 
   TmapSet tm_x, tm_h;
