@@ -513,9 +513,10 @@ def iq4nl_prefill_grouped_fp8(shape: Shape, w: ExpertWeights, row_exp, x, ids, w
                               y=None, status=None, stream=None):
     """Prefill a chunk of tokens with E4M3 operands: y fp32 [T,H]. row_exp from
     fp8_row_exponents(shape, w); ws from workspace(shape, T, PREFILL_FP8)."""
-    T, y = _layer_args(shape, w, x, ids, weights, y, status)
     n = int(_lib.moe_fp8_row_exponent_count(ctypes.byref(shape)))
-    _dev(row_exp, torch.int8, "row_exp", (n,) if n > 0 else None)
+    _meta(row_exp, torch.int8, "row_exp", (n,) if n > 0 else None)
+    T, y = _layer_args(shape, w, x, ids, weights, y, status)
+    _on_cuda(row_exp, "row_exp")
     if ws is not None:
         _dev(ws, torch.uint8, "ws")
     _same_device(x, row_exp, ws)

@@ -113,3 +113,28 @@ def test_dequantize_arguments_are_checked(moe):
         moe.iq4nl_dequantize(torch.zeros(35, dtype=torch.uint8))
     with pytest.raises(ValueError, match="CUDA device"):
         moe.iq4nl_dequantize(torch.zeros(36, dtype=torch.uint8))
+
+
+def test_fp8_prefill_arguments_are_checked(moe):
+    s, x, ids, w, y = _args(moe)
+    wt = moe.ExpertWeights(**_weights(moe, s))
+    ws = torch.zeros(1 << 20, dtype=torch.uint8)
+    n = 2 * 8 * 128 + 8 * 256 + 2 * 128 + 256       # gate, up, down rows; shared ones
+    good = torch.zeros(n, dtype=torch.int8)
+    with pytest.raises(TypeError, match="row_exp"):
+        moe.iq4nl_prefill_grouped_fp8(s, wt, good.float(), x, ids, w, ws, y=y)
+    with pytest.raises(ValueError, match="row_exp"):
+        moe.iq4nl_prefill_grouped_fp8(s, wt, good[:-1], x, ids, w, ws, y=y)
+    with pytest.raises(ValueError, match="x"):
+        moe.iq4nl_prefill_grouped_fp8(s, wt, good, torch.zeros((2, 255), dtype=torch.bfloat16),
+                                      ids, w, ws, y=y)
+    with pytest.raises(ValueError, match="CUDA device"):
+        moe.iq4nl_prefill_grouped_fp8(s, wt, good, x, ids, w, ws, y=y)
+    with pytest.raises(ValueError, match="CUDA device"):
+        moe.fp8_row_exponents(s, wt)
+    with pytest.raises(ValueError, match="18 bytes"):
+        moe.iq4nl_dequantize_e4m3(torch.zeros(36, dtype=torch.uint8), 1, 48)
+    with pytest.raises(ValueError, match="18 bytes"):
+        moe.iq4nl_dequantize_e4m3(torch.zeros(35, dtype=torch.uint8), 1, 64)
+    with pytest.raises(ValueError, match="CUDA device"):
+        moe.iq4nl_dequantize_e4m3(torch.zeros(36, dtype=torch.uint8), 1, 64)
