@@ -68,3 +68,18 @@ def test_traffic_is_quoted_only_for_the_profiled_sources(tmp_path, monkeypatch):
     with open(root / files[0], "a") as f:
         f.write("\n// edited\n")
     assert bench.profiled_traffic("p.json", 1, files, 38) is None
+
+
+def test_fp8_prefill_option(monkeypatch):
+    # --fp8 selects the E4M3 prefill call for the prefill workload and, like
+    # any non-default run, leaves the workloads block out; a default run
+    # measures the prefill chunk with both operand types
+    import sys
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--config", "4", "--fp8"])
+    a = bench.parse()
+    assert a.fp8 and a.config == 4 and not a.workloads
+    monkeypatch.setattr(sys, "argv", ["bench.py"])
+    a = bench.parse()
+    assert not a.fp8 and a.workloads and a.config == 1
+    prefill = [w for w in bench.OTHER_WORKLOADS if w["config"] == 4]
+    assert sorted(bool(w.get("fp8")) for w in prefill) == [False, True]
