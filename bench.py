@@ -149,15 +149,46 @@ FUSED_DECODE_SOURCES = ("quantized_routed_expert_gb300/csrc/decode_fused.cu",) +
 LAYERS_DECODE_SOURCES = ("quantized_routed_expert_gb300/csrc/decode_layers.cu",) + _DECODE_COMMON
 
 
+def code_only(text: str) -> str:
+    """C, C++ or CUDA source without its comments, whitespace runs collapsed to
+    one space (string and character literals are kept as written)."""
+    import re
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return re.sub(r"\s+", " ", "".join(out)).strip()
+
+
 def sources_digest(files=FUSED_DECODE_SOURCES) -> str:
     """Digest of the sources a kernel is built and launched from; a profile's
-    counters apply only to the sources they were taken on."""
+    counters apply only to the sources they were taken on. C/CUDA files enter
+    as their code (comments and layout do not change what is compiled); the
+    build script enters whole."""
     import hashlib
     h = hashlib.sha256()
     for rel in files:
         h.update(rel.encode())
         with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+            data = f.read()
+        if rel.endswith((".cu", ".cuh", ".h", ".cpp")):
+            data = code_only(data.decode("utf-8")).encode("utf-8")
+        h.update(data)
     return h.hexdigest()[:16]
 
 

@@ -65,9 +65,19 @@ def test_traffic_is_quoted_only_for_the_profiled_sources(tmp_path, monkeypatch):
     assert bench.profiled_traffic("p.json", 2, files, 38) is None
     assert bench.profiled_traffic("p.json", 1, files, 4) is None
     assert bench.profiled_traffic("missing.json", 1, files) is None
+    # a comment or the layout of a C/CUDA source does not change what is
+    # compiled: the counters still apply; any change of code voids them
     with open(root / files[0], "a") as f:
-        f.write("\n// edited\n")
+        f.write("\n// a note\n/* and\n   another */\n\n")
+    assert bench.profiled_traffic("p.json", 1, files, 38) == got
+    with open(root / files[0], "a") as f:
+        f.write("\nstatic int edited_since_capture;\n")
     assert bench.profiled_traffic("p.json", 1, files, 38) is None
+
+
+def test_code_only_keeps_literals():
+    src = 'int a = 1; // c\n/* b */ const char* s = "x // y /* z */"; char q = \'\\\'\';\n'
+    assert bench.code_only(src) == 'int a = 1; const char* s = "x // y /* z */"; char q = \'\\\'\';'
 
 
 def test_fp8_prefill_option(monkeypatch):
