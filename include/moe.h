@@ -259,10 +259,11 @@ moe_status moe_iq4nl_prefill_grouped(const moe_shape* shape, const moe_expert_we
                                      size_t ws_bytes, uint32_t* status, void* stream);
 
 /* Prefill with 8-bit operands: the same step as moe_iq4nl_prefill_grouped on
- * the 8-bit tensor cores (tcgen05 kind::f8f6f4, fp32 accumulation), which
- * the Xolotl engine blog ("Prompts: fast, and exact") names for its prompt
- * contraction on the 4090. Operands are OCP E4M3 codes (bias 7, largest
- * finite 448), rounded to nearest even with finite overflow saturated:
+ * 8-bit tensor cores (tcgen05 kind::f8f6f4, fp32 accumulation). The Xolotl
+ * engine blog ("Prompts: fast, and exact") runs its prompt contraction on the
+ * 4090's int8 tensor cores; on this GPU the 8-bit tensor format with a fast
+ * rate is floating point, so the operands here are OCP E4M3 codes (bias 7,
+ * largest finite 448), rounded to nearest even with finite overflow saturated:
  *   weights : row r of a matrix is scaled by 2^-E_r before rounding, E_r the
  *             largest floor(log2 d) over the row's block scales d (-14 for a
  *             zero or subnormal d), so w8 = 2^E_r e4m3(d T[q] 2^-E_r);

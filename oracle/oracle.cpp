@@ -35,8 +35,10 @@
 // reference for the tensor-core prefill path, whose operands are fp16.
 //
 // Mode "mma8" is the reference for the prefill path with 8-bit operands (the
-// Xolotl blog's "Prompts" passage runs its prompt contraction on 8-bit tensor
-// cores). The format taken is E4M3 of the OCP 8-bit floating point
+// Xolotl blog's "Prompts" passage runs its prompt contraction on the 4090's
+// int8 tensor cores; the 8-bit format taken here is floating point, the one
+// whose tensor rate is fast on the target GPU). The format is E4M3 of the OCP
+// 8-bit floating point
 // specification (1 sign, 4 exponent bits with bias 7, 3 fraction bits; no
 // infinities, S.1111.111 is NaN, largest finite 448), rounded to nearest with
 // ties to even and finite overflow saturated to +-448. E4M3 spans fewer
