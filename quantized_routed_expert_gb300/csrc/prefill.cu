@@ -73,7 +73,8 @@ PrefillLayout prefill_layout(const moe_shape& s, int64_t T, bool fp8) {
     L.h8 = take(rows * fmax);                   // E4M3 codes of h 2^-X
     L.h32 = take(rows * fmax * 4);              // h, fp32, bucket order
     L.bexp = take(rows * 4);                    // each bucket row's x exponent
-    L.hexp = take(rows * 4);                    // each bucket row's h exponent
+    L.hexp = take(rows * 4);                    // each bucket row's h exponent (it enters the
+                                                // combine weights; kept for inspection)
   }
   L.total = off;
   return L;
