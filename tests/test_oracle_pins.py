@@ -336,8 +336,13 @@ def test_mma8_single_expert_equals_dense_reference():
     assert np.allclose(y, ref, rtol=1e-12, atol=1e-15 * np.abs(ref).max())
 
 
-def test_mma8_layer_equals_dense_masked_evaluation():
-    s = synth.SHAPES[0]
+@pytest.mark.parametrize("s", [synth.SHAPES[0],
+                               synth.Shape("sw", 256, 128, 8, 2, 4, 1, Fs=384),
+                               synth.Shape("sn", 256, 384, 8, 2, 4, 1, Fs=128)],
+                         ids=["tiny", "shared-wider", "shared-narrower"])
+def test_mma8_layer_equals_dense_masked_evaluation(s):
+    # also with a shared expert of another width than the routed ones (its h
+    # row gets its own exponent)
     Wr, b, x, ex, sh = _layer_inputs(s, 22)
     ids, w, _, _ = oracle.route(Wr, b, x, s.k)
     y = oracle.moe_layer(s.H, s.F, s.Fs, s.E, s.k, 1, ex, sh, x, ids, w, mode=oracle.MMA8)
